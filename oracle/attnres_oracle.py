@@ -1,0 +1,303 @@
+"""Plain, slow, fp64 CPU oracle for Attention Residuals (AttnRes) residual aggregation.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports, calls or links this file:
+only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` use it.
+It shares no code, header, table or helper with the CUDA library; both sides only share the
+seeded input generators in ``synth/``.
+
+Everything here is the *direct* definition written out in float64 numpy, with no blocking,
+fusion or reordering: the two-phase schedule is exact in real arithmetic (page 1 "Attention
+Residuals 阅读补充", section "静态 Query 与两阶段计算", the merge identity; page 2 "Attention
+Residuals" note, §10), so the oracle for every phase is the plain softmax over the sources the
+definition names.  Vectorising over tokens is not a reordering: depth attention never mixes
+tokens (page 2 §7: "only aggregates along depth"; page 5 "ML 研究者的三层基本功", system layer,
+sequence sharding).
+
+Pages cited (titles as they appear on the pages):
+  page 1  "Attention Residuals 阅读补充" (chlience.com reading notes)
+  page 2  "Attention Residuals" (papers.chlience.com note on arXiv 2603.15031)
+  page 3  CSDN/gitcode overview article of the AttnRes report
+  page 4  "Kimi K3 模型结构（4）：深度维度，Attention Residuals"
+
+Readings of points the pages leave open (each is also listed in the design notes):
+  * phase 1 returns the *normalised* partial output o_A / l_A plus m_A and a true
+    log-sum-exp lse_A = m_A + ln l_A (page 2 §10 calls l both an exp-sum and a log-sum-exp;
+    page 3 section 4.2 says "max, log-sum-exp");
+  * the first sublayer of a block has no partial-sum source at all (page 2 §8, V_first);
+  * eps sits inside the square root, added to the mean square (page 1, definition of r_eps);
+  * the key-norm gain gamma belongs to the target sublayer l (page 1, "Full AttnRes" cost
+    section: one query vector and one set of RMSNorm gains per layer);
+  * no 1/sqrt(d) scale and no temperature (page 2 §7);
+  * the norm fused after the merge is the input RMSNorm of sublayer l, y = RMSNorm_in(h)
+    (page 3 section 4.2 kernel fusion; page 1 "回到 AttnRes", f(z) = F(RMSNorm(z)));
+  * the final output aggregates the embedding and all complete blocks with one extra
+    pseudo-query w_{L+1} (page 2 §8, last sentence of the block definition).
+
+Parity status: every function below is pinned by ``tests/test_oracle_pins.py`` (closed forms,
+invariants, special cases, brute force) and by ``tests/test_oracle_mutations.py`` (planted
+mistakes that the pins must catch).  No function here is "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+F64 = np.float64
+
+
+def _f64(x):
+    return np.asarray(x, dtype=F64)
+
+
+# ---------------------------------------------------------------------------------------------
+# RMSNorm (page 1, section "RMSNorm 的数学原理")
+# ---------------------------------------------------------------------------------------------
+def rms(x, eps: float):
+    """r_eps(x) = sqrt( (1/d) * sum_k x_k^2 + eps ), over the last axis (the d features of one
+    token).  Page 1, "RMSNorm 的数学原理", definition of the root mean square with eps."""
+    x = _f64(x)
+    d = x.shape[-1]
+    return np.sqrt(np.sum(x * x, axis=-1) / d + eps)
+
+
+def rmsnorm(x, gamma, eps: float):
+    """RMSNorm(x) = gamma ⊙ x / r_eps(x).  ``gamma=None`` stands for all ones.
+    Page 1, "RMSNorm 的数学原理", the normalisation with the learnable per-feature gain."""
+    x = _f64(x)
+    y = x / rms(x, eps)[..., None]
+    if gamma is not None:
+        y = y * _f64(gamma)
+    return y
+
+
+# ---------------------------------------------------------------------------------------------
+# Depth attention for one target sublayer (page 2 §7, Full AttnRes equations)
+# ---------------------------------------------------------------------------------------------
+def depth_logits(sources, w, gamma_key, eps: float):
+    """z_i = w^T RMSNorm(v_i) for every source i.
+
+    sources: [n, T, d] (source-major), w: [d], gamma_key: [d] or None.  Returns z: [n, T].
+    Page 2 §7: the keys are the RMS-normalised sources, the query is the static w_l, no scale.
+    """
+    keys = rmsnorm(sources, gamma_key, eps)            # [n, T, d]
+    return np.sum(keys * _f64(w), axis=-1)             # [n, T]
+
+
+def depth_softmax(z):
+    """alpha_i = exp(z_i) / sum_j exp(z_j) over the source axis (axis 0).  The max is taken
+    out first only to keep exp in range; it cancels exactly.  Page 2 §7."""
+    z = _f64(z)
+    e = np.exp(z - np.max(z, axis=0, keepdims=True))
+    return e / np.sum(e, axis=0, keepdims=True)
+
+
+def aggregate(sources, w, gamma_key, eps: float):
+    """h = sum_i alpha_i v_i with alpha = softmax_i(w^T RMSNorm(v_i)).
+
+    The values are the raw sources (not normalised).  Page 2 §7 (the h_l equation); page 1
+    "回到 AttnRes" (the a_{t+1,s} kernel).  Returns (h [T,d], alpha [n,T], z [n,T]).
+    """
+    src = _f64(sources)
+    z = depth_logits(src, w, gamma_key, eps)
+    alpha = depth_softmax(z)
+    h = np.sum(alpha[..., None] * src, axis=0)
+    return h, alpha, z
+
+
+def partition_stats(sources, w, gamma_key, eps: float):
+    """Softmax statistics of one source partition X (page 1, two-phase section; page 2 §10):
+
+        m_X = max_i z_i,   l_X = sum_i exp(z_i - m_X),   o_X = sum_i exp(z_i - m_X) v_i.
+
+    Returned as phase 1 hands them over (reading of the l / log-sum-exp naming clash):
+    (o_X / l_X  [T,d],  m_X [T],  lse_X = m_X + ln l_X [T],  alpha_X = e / l_X [n,T]).
+    """
+    src = _f64(sources)
+    z = depth_logits(src, w, gamma_key, eps)
+    m = np.max(z, axis=0)
+    e = np.exp(z - m)
+    ell = np.sum(e, axis=0)
+    o = np.sum(e[..., None] * src, axis=0) / ell[..., None]
+    return o, m, m + np.log(ell), e / ell
+
+
+def sublayer_input(sources, w, gamma_key, eps_key: float, gamma_in, eps_in: float):
+    """The input of sublayer l: h_l by depth attention, then its input RMSNorm y_l.
+
+    Returns (h [T,d], y [T,d], alpha [n,T]).  Page 2 §7 for h; page 1 "回到 AttnRes"
+    (f(z) = F(RMSNorm(z))) for y.
+    """
+    h, alpha, _ = aggregate(sources, w, gamma_key, eps_key)
+    y = rmsnorm(h, gamma_in, eps_in)
+    return h, y, alpha
+
+
+def phase1(reps, W, G_key, eps: float):
+    """What phase 1 of one block returns, by the definition: for each of the S queries of the
+    block, the softmax statistics over the partition A = {b_0 .. b_{n-1}} (page 2 §10 step 1;
+    page 1 two-phase section, step 1).
+
+    reps: [n, T, d]; W: [S, d]; G_key: [S, d] or None.
+    Returns o [S,T,d], m [S,T], lse [S,T], alpha [S,T,n].
+    """
+    reps = _f64(reps)
+    S = np.shape(W)[0]
+    outs = []
+    for s in range(S):
+        g = None if G_key is None else _f64(G_key)[s]
+        outs.append(partition_stats(reps, _f64(W)[s], g, eps))
+    o = np.stack([x[0] for x in outs])
+    m = np.stack([x[1] for x in outs])
+    lse = np.stack([x[2] for x in outs])
+    alpha = np.stack([np.moveaxis(x[3], 0, -1) for x in outs])
+    return o, m, lse, alpha
+
+
+# ---------------------------------------------------------------------------------------------
+# Block AttnRes depth walk (page 2 §8; page 3 section 3.2; page 4 block structure)
+# ---------------------------------------------------------------------------------------------
+def block_of(l: int, S: int):
+    """Sublayer l (1-based) sits in block n = ceil(l / S) at position i = l - (n-1) S.
+    Block boundaries fall at multiples of S; the last block may be shorter (page 4: K3 has
+    seven full blocks and a shorter tail)."""
+    n = (l - 1) // S + 1
+    return n, l - (n - 1) * S
+
+
+def block_sources(completed, partial):
+    """Sources of a sublayer in block n (page 2 §8, V_first / V_later):
+    [b_0, ..., b_{n-1}] and, from the second sublayer of the block on, the partial b_n^{i-1}.
+    ``partial=None`` is the first sublayer: the partial is absent, not a zero source."""
+    srcs = [_f64(b) for b in completed]
+    if partial is not None:
+        srcs.append(_f64(partial))
+    return np.stack(srcs)
+
+
+@dataclass
+class BlockWalk:
+    """Everything the direct-definition walk produces, for parity and pins."""
+    h: list = field(default_factory=list)          # h_l [T,d] for l = 1..L
+    y: list = field(default_factory=list)          # y_l = RMSNorm_in(h_l)
+    alpha: list = field(default_factory=list)      # alpha over the sources of l, [n_l, T]
+    n_sources: list = field(default_factory=list)  # number of sources scored by sublayer l
+    partials: list = field(default_factory=list)   # b_n^{i-1} used by l (None when i = 1)
+    closed: list = field(default_factory=list)     # b_n = b_n^{S_n} for every block n
+    final: np.ndarray | None = None                # final aggregation over b_0 .. b_N
+    final_alpha: np.ndarray | None = None
+
+
+def block_attnres_walk(b0, given_blocks, v, S: int, W, G_key, G_in, w_final, g_final,
+                       eps_key: float, eps_in: float, consistent: bool = False) -> BlockWalk:
+    """Walk L sublayers of Block AttnRes by the direct definition.
+
+    b0: embedding b_0 [T,d].  v: [L, T, d], v[l-1] stands in for f_l(h_l), the output of
+    sublayer l.  given_blocks: completed block representations b_1 .. b_N ([N,T,d]) used as
+    sources when ``consistent`` is False (the synthetic workloads give them directly);
+    when ``consistent`` is True every completed block is the sum of its own sublayer outputs,
+    b_n = sum_{j in B_n} v_j, as page 2 §8 defines it.  W, G_key, G_in: [L, d] (None = ones
+    for the gains).  w_final / g_final: the extra pseudo-query of the final aggregation.
+
+    Within block n: b_n^0 = 0, b_n^i = b_n^{i-1} + v_{(n,i)}  (page 2 §8).
+    """
+    v = _f64(v)
+    L = v.shape[0]
+    N = (L + S - 1) // S
+    out = BlockWalk()
+    completed = [_f64(b0)]
+    partial = None
+    for l in range(1, L + 1):
+        n, i = block_of(l, S)
+        srcs = block_sources(completed, partial if i >= 2 else None)
+        gk = None if G_key is None else _f64(G_key)[l - 1]
+        gi = None if G_in is None else _f64(G_in)[l - 1]
+        h, y, alpha = sublayer_input(srcs, _f64(W)[l - 1], gk, eps_key, gi, eps_in)
+        out.h.append(h)
+        out.y.append(y)
+        out.alpha.append(alpha)
+        out.n_sources.append(srcs.shape[0])
+        out.partials.append(None if i == 1 else partial)
+        # partial-sum update with this sublayer's output
+        partial = v[l - 1].copy() if i == 1 else partial + v[l - 1]
+        block_len = min(S, L - (n - 1) * S)
+        if i == block_len:                      # block n closes
+            out.closed.append(partial)
+            completed.append(partial if consistent else _f64(given_blocks[n - 1]))
+            partial = None
+    assert len(completed) == N + 1
+    fin, fin_alpha, _ = aggregate(np.stack(completed), w_final, g_final, eps_key)
+    out.final, out.final_alpha = fin, fin_alpha
+    return out
+
+
+def block_score_count(L: int, S: int) -> int:
+    """Number of (source, target) logits the block walk computes, counted from the source
+    lists above (first sublayer of block n: n sources, later ones n + 1), plus the final
+    aggregation over N + 1 sources."""
+    total = 0
+    for l in range(1, L + 1):
+        n, i = block_of(l, S)
+        total += n if i == 1 else n + 1
+    N = (L + S - 1) // S
+    return total + N + 1
+
+
+# ---------------------------------------------------------------------------------------------
+# Full AttnRes depth walk (page 2 §7)
+# ---------------------------------------------------------------------------------------------
+def full_attnres_walk(v0, v, W, G_key, G_in, w_final, g_final, eps_key: float, eps_in: float):
+    """Full AttnRes: v_0 = h_1 (embedding), v_i = f_i(h_i); sublayer l reads v_0 .. v_{l-1}.
+
+    v: [L, T, d] with v[i-1] = v_i.  The final aggregation reads v_0 .. v_L.
+    Returns a BlockWalk with one 'block' per sublayer (closed = v_l).
+    """
+    v = _f64(v)
+    L = v.shape[0]
+    out = BlockWalk()
+    hist = [_f64(v0)]
+    for l in range(1, L + 1):
+        srcs = np.stack(hist)
+        gk = None if G_key is None else _f64(G_key)[l - 1]
+        gi = None if G_in is None else _f64(G_in)[l - 1]
+        h, y, alpha = sublayer_input(srcs, _f64(W)[l - 1], gk, eps_key, gi, eps_in)
+        out.h.append(h)
+        out.y.append(y)
+        out.alpha.append(alpha)
+        out.n_sources.append(len(hist))
+        out.partials.append(None)
+        out.closed.append(v[l - 1])
+        hist.append(v[l - 1])
+    fin, fin_alpha, _ = aggregate(np.stack(hist), w_final, g_final, eps_key)
+    out.final, out.final_alpha = fin, fin_alpha
+    return out
+
+
+# ---------------------------------------------------------------------------------------------
+# Reference values for one phase-2 call and one partial update, on given inputs
+# ---------------------------------------------------------------------------------------------
+def phase2_reference(reps, partial_prev, v_prev, w, gamma_key, eps_key, gamma_in, eps_in):
+    """What the sublayer input is by definition when the block's completed sources are
+    ``reps`` [n,T,d] and the partial source is b^{i-1} = partial_prev + v_prev (either may be
+    None; both None is the first sublayer of the block, which has no partial source).
+
+    Returns (h, y, alpha [n(+1), T], p) with p the partial source used (None if absent).
+    """
+    if partial_prev is None and v_prev is None:
+        p = None
+    elif partial_prev is None:
+        p = _f64(v_prev)
+    elif v_prev is None:
+        p = _f64(partial_prev)
+    else:
+        p = _f64(partial_prev) + _f64(v_prev)
+    srcs = block_sources(list(_f64(reps)), p)
+    h, y, alpha = sublayer_input(srcs, w, gamma_key, eps_key, gamma_in, eps_in)
+    return h, y, alpha, p
+
+
+def logsumexp_bruteforce(z_row) -> float:
+    """ln sum_i exp(z_i) for a short list, with math.fsum over math.exp: a slow scalar
+    cross-check of the vectorised statistics (used only on tiny inputs)."""
+    return math.log(math.fsum(math.exp(float(zi)) for zi in z_row))

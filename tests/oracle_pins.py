@@ -1,0 +1,393 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Each ``pin_*`` takes the oracle module and raises AssertionError when the oracle disagrees
+with a closed form, an invariant, a special case that reduces to a textbook or library
+routine, or a brute-force enumeration.  ``test_oracle_pins.py`` runs them on the real oracle;
+``test_oracle_mutations.py`` plants plausible mistakes in a copy of the oracle and checks that
+some pin fails for each.  Pages are cited by title and section:
+
+  page 1  "Attention Residuals 阅读补充"
+  page 2  "Attention Residuals" (note on arXiv 2603.15031)
+"""
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+
+RNG_SEED = 1234
+
+
+def _rng(k=0):
+    return np.random.default_rng(RNG_SEED + k)
+
+
+def _close(a, b, tol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    err = float(np.max(np.abs(a - b))) if a.size else 0.0
+    assert err <= tol, f"{what}: max |diff| = {err:.3e} > {tol:.1e}"
+
+
+# --- RMSNorm (page 1, "RMSNorm 的数学原理") --------------------------------------------------
+def pin_rms_moments(O):
+    """m_2 = sigma^2 + mu^2 (page 1, "二阶原点矩与方差"): r_0(x)^2 equals numpy's variance plus
+    squared mean; with eps, r_eps^2 = m_2 + eps."""
+    r = _rng(1)
+    for d in (1, 3, 128, 7168):
+        x = r.normal(0.7, 2.0, size=(5, d))
+        m2 = np.var(x, axis=-1) + np.mean(x, axis=-1) ** 2
+        _close(O.rms(x, 0.0) ** 2, m2, 1e-12 * max(1.0, m2.max()), f"r_0^2 vs var+mean^2 d={d}")
+        _close(O.rms(x, 0.25) ** 2, m2 + 0.25, 1e-12 * max(1.0, m2.max()), "r_eps^2 = m2 + eps")
+
+
+def pin_rmsnorm_sphere(O):
+    """At gamma = 1, eps = 0 the normalised vector has length sqrt(d) and mean square 1
+    (page 1, "从均方根到欧氏范数")."""
+    r = _rng(2)
+    for d in (2, 17, 128, 2048):
+        x = r.normal(0.3, 3.0, size=(7, d))
+        y = O.rmsnorm(x, None, 0.0)
+        _close(np.linalg.norm(y, axis=-1), np.full(7, math.sqrt(d)), 1e-10 * math.sqrt(d),
+               f"|RMSNorm(x)| = sqrt(d), d={d}")
+        _close(np.mean(y * y, axis=-1), np.ones(7), 1e-12, "mean square 1")
+
+
+def pin_rmsnorm_eps_length(O):
+    """With eps > 0, |x~|^2 = d |x|^2 / (|x|^2 + d eps) < d (page 1, "ε 与 γ 改变了什么")."""
+    r = _rng(3)
+    d = 64
+    x = r.normal(0.0, 0.1, size=(9, d))
+    for eps in (1e-3, 0.01, 0.5):
+        y = O.rmsnorm(x, None, eps)
+        n2 = np.sum(x * x, axis=-1)
+        _close(np.sum(y * y, axis=-1), d * n2 / (n2 + d * eps), 1e-10 * d, f"eps length {eps}")
+
+
+def pin_rmsnorm_scale_sign(O):
+    """RMSNorm(a x) = RMSNorm(x) for a > 0 and = -RMSNorm(x) for a < 0 at eps = 0; with
+    eps > 0 the identity is only approximate (page 1, "尺度变化与平移")."""
+    r = _rng(4)
+    x = r.normal(0.0, 1.0, size=(4, 96))
+    g = r.normal(1.0, 0.3, size=96)
+    base = O.rmsnorm(x, g, 0.0)
+    for a in (1e-3, 0.5, 3.0, 1e4):
+        _close(O.rmsnorm(a * x, g, 0.0), base, 1e-11, f"scale invariance a={a}")
+        _close(O.rmsnorm(-a * x, g, 0.0), -base, 1e-11, f"sign flip a={-a}")
+    # eps > 0 breaks exact invariance when a^2 m2 is comparable to eps
+    diff = np.max(np.abs(O.rmsnorm(1e-3 * x, g, 1e-6) - O.rmsnorm(x, g, 1e-6)))
+    assert diff > 1e-3, "eps must enter the scale (page 1: approximate for eps > 0)"
+
+
+def pin_rmsnorm_shift(O):
+    """A shift x + c 1 changes m_2 to m_2 + 2 c mu + c^2 (page 1, "尺度变化与平移")."""
+    r = _rng(5)
+    x = r.normal(0.4, 1.5, size=(6, 50))
+    mu = np.mean(x, axis=-1)
+    m2 = O.rms(x, 0.0) ** 2
+    for c in (-2.0, 0.3, 5.0):
+        _close(O.rms(x + c, 0.0) ** 2, m2 + 2 * c * mu + c * c, 1e-10 * (1 + c * c), f"shift {c}")
+
+
+def pin_rmsnorm_basis_gamma(O):
+    """Closed form on a scaled basis vector: RMSNorm(c e_k; gamma) = sign(c) gamma_k sqrt(d)
+    e_k at eps = 0 (page 1 definition; gamma acts per feature)."""
+    d = 12
+    g = np.linspace(0.5, 2.0, d)
+    for k, c in ((0, 3.0), (5, -0.25), (11, 7e3)):
+        x = np.zeros(d)
+        x[k] = c
+        want = np.zeros(d)
+        want[k] = math.copysign(1.0, c) * g[k] * math.sqrt(d)
+        _close(O.rmsnorm(x, g, 0.0), want, 1e-12 * math.sqrt(d), f"basis k={k}")
+
+
+# --- depth softmax (page 2 §7) ---------------------------------------------------------------
+def _sources(r, n, T, d, shift=True):
+    v = r.normal(0.0, 1.0, size=(n, T, d)) * np.sqrt(np.arange(1, n + 1))[:, None, None]
+    if shift:
+        v = v + r.normal(0.0, 0.5, size=(n, T, 1))
+    return v
+
+
+def pin_softmax_simplex(O):
+    """alpha > 0 and sum_i alpha_i = 1 for every token (page 2 §7), also with large logits."""
+    r = _rng(6)
+    v = _sources(r, 7, 11, 40)
+    for scale in (1.0, 30.0):
+        w = r.normal(0.0, scale / math.sqrt(40), size=40)
+        _, alpha, _ = O.aggregate(v, w, None, 1e-6)
+        assert alpha.shape == (7, 11)
+        assert np.all(alpha > 0.0), "weights must be positive"
+        _close(alpha.sum(axis=0), np.ones(11), 1e-13, "weights sum to 1")
+
+
+def pin_zero_query_mean(O):
+    """Zero pseudo-queries give the uniform mean of the sources (page 2 §7, zero init)."""
+    r = _rng(7)
+    v = _sources(r, 5, 9, 33)
+    for g in (None, r.normal(1.0, 0.2, size=33)):
+        h, alpha, _ = O.aggregate(v, np.zeros(33), g, 1e-6)
+        _close(alpha, np.full((5, 9), 0.2), 1e-14, "uniform weights")
+        _close(h, v.mean(axis=0), 1e-12, "h = mean of sources")
+
+
+def pin_convex_bound(O):
+    """|h_l| <= max_i |v_i| (page 2 §7, convex-combination bound)."""
+    r = _rng(8)
+    v = _sources(r, 6, 20, 24)
+    w = r.normal(0.0, 2.0, size=24)
+    h, _, _ = O.aggregate(v, w, None, 1e-6)
+    assert np.all(np.linalg.norm(h, axis=-1) <= np.linalg.norm(v, axis=-1).max(axis=0) + 1e-12)
+
+
+def rational_case(O, gamma):
+    """Sources on distinct scaled basis vectors, queries chosen so z_j = ln p_j exactly:
+    then alpha_j = p_j / sum p and h[k_j] = c_j p_j / sum p.  Returns (got, want) pairs."""
+    d = 8
+    ks = [1, 6, 3, 4]
+    cs = [2.5, -0.75, 40.0, -3.0]
+    ps = [1.0, 2.0, 3.0, 4.0]
+    T = 1
+    v = np.zeros((4, T, d))
+    for j, (k, c) in enumerate(zip(ks, cs)):
+        v[j, 0, k] = c
+    g = np.ones(d) if gamma is None else gamma
+    w = np.zeros(d)
+    for k, c, p in zip(ks, cs, ps):
+        w[k] = math.log(p) / (math.copysign(1.0, c) * math.sqrt(d) * g[k])
+    h, alpha, z = O.aggregate(v, w, gamma, 0.0)
+    tot = sum(ps)
+    want_alpha = np.array(ps)[:, None] / tot
+    want_h = np.zeros((T, d))
+    for k, c, p in zip(ks, cs, ps):
+        want_h[0, k] = c * p / tot
+    return (z, np.log(np.array(ps))[:, None]), (alpha, want_alpha), (h, want_h)
+
+
+def pin_rational_case(O):
+    """Exact closed form (see rational_case); also with a non-uniform key gain."""
+    for gamma in (None, np.linspace(0.5, 1.5, 8)):
+        (z, zw), (a, aw), (h, hw) = rational_case(O, gamma)
+        _close(z, zw, 1e-12, "z = ln p")
+        _close(a, aw, 1e-13, "alpha = p / sum p")
+        _close(h, hw, 1e-11, "h = sum alpha v")
+
+
+def pin_one_hot_limit(O):
+    """A query aligned with source j's normalised direction and scaled up drives alpha_j -> 1
+    and h -> v_j (limit of the softmax)."""
+    r = _rng(9)
+    v = _sources(r, 4, 1, 64)
+    j = 2
+    u = O.rmsnorm(v[j, 0], None, 0.0) / math.sqrt(64)
+    h, alpha, _ = O.aggregate(v, 400.0 * u, None, 0.0)
+    assert alpha[j, 0] > 1 - 1e-9, f"alpha_j = {alpha[j, 0]}"
+    _close(h[0], v[j, 0], 1e-6 * np.abs(v[j, 0]).max(), "h -> v_j")
+
+
+def pin_scale_invariance_weights(O):
+    """Scaling one source by a > 0 leaves every weight unchanged at eps = 0, because the key
+    is RMS-normalised while the value is not (page 1, "回到 AttnRes")."""
+    r = _rng(10)
+    v = _sources(r, 5, 6, 30)
+    w = r.normal(0.0, 0.5, size=30)
+    h0, a0, _ = O.aggregate(v, w, None, 0.0)
+    for a in (0.01, 9.0):
+        v2 = v.copy()
+        v2[3] *= a
+        h1, a1, _ = O.aggregate(v2, w, None, 0.0)
+        _close(a1, a0, 1e-13, f"weights invariant, a={a}")
+        _close(h1, h0 + (a - 1.0) * a0[3][:, None] * v[3], 1e-10 * a, "h shifts by source 3 only")
+
+
+# --- two-phase statistics and merge (page 1 two-phase section; page 2 §10) --------------------
+def pin_partition_merge(O):
+    """Merging the statistics of any split A | B with the pages' formula
+        h = (e^{m_A-m} o_A + e^{m_B-m} o_B) / (e^{m_A-m} l_A + e^{m_B-m} l_B)
+    (o unnormalised) equals the direct softmax over A u B.  Brute force over every split of
+    n = 5 sources."""
+    r = _rng(11)
+    n, T, d = 5, 4, 16
+    v = _sources(r, n, T, d)
+    w = r.normal(0.0, 1.0, size=d)
+    g = r.normal(1.0, 0.1, size=d)
+    h_direct, a_direct, _ = O.aggregate(v, w, g, 1e-6)
+    for k in range(1, n):
+        for A in itertools.combinations(range(n), k):
+            B = [i for i in range(n) if i not in A]
+            oA, mA, lseA, aA = O.partition_stats(v[list(A)], w, g, 1e-6)
+            oB, mB, lseB, aB = O.partition_stats(v[B], w, g, 1e-6)
+            lA, lB = np.exp(lseA - mA), np.exp(lseB - mB)     # exp-sums from the lse
+            m = np.maximum(mA, mB)
+            ca, cb = np.exp(mA - m) * lA, np.exp(mB - m) * lB
+            h = (ca[:, None] * oA + cb[:, None] * oB) / (ca + cb)[:, None]
+            _close(h, h_direct, 1e-12, f"merge split {A}")
+            _close(aA * (ca / (ca + cb)), a_direct[list(A)], 1e-13, "merged weights A")
+            _close(aB * (cb / (ca + cb)), a_direct[B], 1e-13, "merged weights B")
+
+
+def pin_lse_bruteforce(O):
+    """lse = ln sum exp z by a scalar fsum loop, and 0 <= lse - m <= ln n."""
+    r = _rng(12)
+    n, T, d = 6, 5, 10
+    v = _sources(r, n, T, d)
+    w = r.normal(0.0, 2.0, size=d)
+    o, m, lse, alpha = O.partition_stats(v, w, None, 1e-6)
+    z = O.depth_logits(v, w, None, 1e-6)
+    for t in range(T):
+        assert abs(lse[t] - O.logsumexp_bruteforce(z[:, t])) < 1e-12
+        assert abs(m[t] - max(z[:, t])) == 0.0
+    assert np.all(lse - m >= 0.0) and np.all(lse - m <= math.log(n) + 1e-15)
+    # partition statistics over the full set reproduce the direct aggregation
+    h, a2, _ = O.aggregate(v, w, None, 1e-6)
+    _close(o, h, 1e-12, "o_A over all sources = h")
+    _close(alpha, a2, 1e-14, "alpha_A over all sources = alpha")
+
+
+def pin_phase1_per_query(O):
+    """phase1() returns, per query s, the partition statistics of that query alone, with
+    alpha laid out [S, T, n] (checked against a single-query partition_stats call and the
+    rational closed form placed at query 2)."""
+    r = _rng(13)
+    n, T, d, S = 4, 1, 8, 3
+    (_, _), (_, aw), (_, hw) = rational_case(O, None)
+    v = np.zeros((n, T, d))
+    for j, (k, c) in enumerate(zip([1, 6, 3, 4], [2.5, -0.75, 40.0, -3.0])):
+        v[j, 0, k] = c
+    W = r.normal(0.0, 1.0, size=(S, d))
+    W[2] = 0.0
+    for k, c, p in zip([1, 6, 3, 4], [2.5, -0.75, 40.0, -3.0], [1.0, 2.0, 3.0, 4.0]):
+        W[2, k] = math.log(p) / (math.copysign(1.0, c) * math.sqrt(d))
+    o, m, lse, alpha = O.phase1(v, W, None, 0.0)
+    assert o.shape == (S, T, d) and m.shape == (S, T) and alpha.shape == (S, T, n)
+    _close(o[2], hw, 1e-11, "phase1 o for the rational query")
+    _close(alpha[2, 0], aw[:, 0], 1e-13, "phase1 alpha layout [S,T,n]")
+    _close(lse[2], [math.log(10.0)], 1e-12, "lse = ln sum p")
+
+
+# --- block structure (page 2 §8) -------------------------------------------------------------
+def _walk_inputs(r, L, T, d, n_given):
+    b0 = r.normal(0.0, 1.0, size=(T, d)) + r.normal(0.0, 0.5, size=(T, 1))
+    v = r.normal(0.0, 1.0, size=(L, T, d))
+    given = r.normal(0.0, 2.0, size=(n_given, T, d))
+    W = r.normal(0.0, 1.0 / math.sqrt(d), size=(L, d)) * 8.0
+    Gk = r.normal(1.0, 0.1, size=(L, d))
+    Gi = r.normal(1.0, 0.1, size=(L, d))
+    wf = r.normal(0.0, 1.0, size=d)
+    gf = r.normal(1.0, 0.1, size=d)
+    return b0, v, given, W, Gk, Gi, wf, gf
+
+
+def pin_block_equals_full(O):
+    """N = L (one sublayer per block) recovers Full AttnRes exactly (page 2 §8, the two
+    extremes): the block walk and the full walk build their source lists differently."""
+    r = _rng(14)
+    L, T, d = 6, 5, 16
+    b0, v, given, W, Gk, Gi, wf, gf = _walk_inputs(r, L, T, d, L)
+    blk = O.block_attnres_walk(b0, given, v, 1, W, Gk, Gi, wf, gf, 1e-6, 1e-6, consistent=True)
+    full = O.full_attnres_walk(b0, v, W, Gk, Gi, wf, gf, 1e-6, 1e-6)
+    for l in range(L):
+        _close(blk.h[l], full.h[l], 1e-12, f"h_{l+1}")
+        _close(blk.y[l], full.y[l], 1e-12, f"y_{l+1}")
+        assert blk.n_sources[l] == full.n_sources[l] == l + 1
+    _close(blk.final, full.final, 1e-12, "final aggregation")
+
+
+def pin_single_block_standard_residual(O):
+    """N = 1 with zero queries and eps = 0: every sublayer averages the embedding and the
+    partial sum, and after the input RMSNorm this equals RMSNorm of the standard residual
+    stream h_l = h_1 + sum_{i<l} f_i(h_i) (page 2 §6 unrolled residual; page 2 §8 'N = 1';
+    page 1 "回到 AttnRes", a positive overall scale is cancelled by the next RMSNorm)."""
+    r = _rng(15)
+    L, T, d = 5, 3, 20
+    b0, v, given, _, _, Gi, wf, gf = _walk_inputs(r, L, T, d, 1)
+    W = np.zeros((L, d))
+    walk = O.block_attnres_walk(b0, given, v, L, W, None, Gi, wf, gf, 0.0, 0.0, consistent=True)
+    stream = b0.copy()
+    for l in range(L):
+        ref = O.rmsnorm(stream, Gi[l], 0.0)
+        _close(walk.y[l], ref, 1e-11, f"standard residual at l={l+1}")
+        want_n = 1 if l == 0 else 2
+        assert walk.n_sources[l] == want_n, "embedding + partial (none for the first sublayer)"
+        stream = stream + v[l]
+
+
+def pin_full_zero_init(O):
+    """Full AttnRes with all w_l = 0: h_l = (1/l)(h_1 + sum_{i<l} v_i) (page 2 §7)."""
+    r = _rng(16)
+    L, T, d = 5, 4, 12
+    v0 = r.normal(size=(T, d))
+    v = r.normal(size=(L, T, d))
+    W = np.zeros((L, d))
+    walk = O.full_attnres_walk(v0, v, W, None, None, np.zeros(d), None, 1e-6, 1e-6)
+    acc = v0.copy()
+    for l in range(1, L + 1):
+        _close(walk.h[l - 1], acc / l, 1e-12, f"h_{l} = mean")
+        acc = acc + v[l - 1]
+    _close(walk.final, acc / (L + 1), 1e-12, "final = mean of all")
+
+
+def pin_block_score_count(O):
+    """The number of logits of the block walk matches page 2 §8's count
+    sum_{n=1}^{N} [n + (S-1)(n+1)] (plus the final aggregation's N + 1), and each sublayer
+    scores n sources (first of the block) or n + 1 (later ones)."""
+    for L, S in ((8, 4), (12, 3), (186 - 18, 24), (6, 1)):
+        N = L // S
+        want = sum(n + (S - 1) * (n + 1) for n in range(1, N + 1)) + N + 1
+        assert O.block_score_count(L, S) == want, (L, S)
+    r = _rng(17)
+    L, S, T, d = 7, 3, 2, 8
+    b0, v, given, W, Gk, Gi, wf, gf = _walk_inputs(r, L, T, d, 3)
+    walk = O.block_attnres_walk(b0, given, v, S, W, Gk, Gi, wf, gf, 1e-6, 1e-6)
+    want_counts = [1, 2, 2, 2, 3, 3, 3]          # blocks of 3, 3, 1 sublayers
+    assert walk.n_sources == want_counts, walk.n_sources
+    assert len(walk.closed) == 3
+
+
+def pin_partials_and_given(O):
+    """Inside block n the partial source of position i is the sum of the block's earlier
+    outputs (b_n^0 = 0 means no source at i = 1); with ``consistent=False`` the completed
+    blocks are the given tensors (page 2 §8 definitions)."""
+    r = _rng(18)
+    L, S, T, d = 6, 3, 2, 8
+    b0, v, given, W, Gk, Gi, wf, gf = _walk_inputs(r, L, T, d, 2)
+    walk = O.block_attnres_walk(b0, given, v, S, W, Gk, Gi, wf, gf, 1e-6, 1e-6)
+    assert walk.partials[0] is None and walk.partials[3] is None
+    _close(walk.partials[1], v[0], 0.0, "b_1^1 = v_1")
+    _close(walk.partials[2], v[0] + v[1], 1e-15, "b_1^2")
+    _close(walk.partials[5], v[3] + v[4], 1e-15, "b_2^2")
+    # sublayer 4 (block 2, first) sees [b_0, given b_1] only
+    h4, _, _ = O.aggregate(np.stack([b0, given[0]]), W[3], Gk[3], 1e-6)
+    _close(walk.h[3], h4, 1e-13, "block 2 first sublayer uses the given b_1")
+    fin, _, _ = O.aggregate(np.stack([b0, given[0], given[1]]), wf, gf, 1e-6)
+    _close(walk.final, fin, 1e-13, "final aggregation over b_0 .. b_N")
+
+
+def pin_input_norm(O):
+    """y = RMSNorm_in(h): length sqrt(d) at gamma_in = 1, eps_in = 0, and parallel to h."""
+    r = _rng(19)
+    v = _sources(r, 3, 4, 32)
+    h, y, _ = O.sublayer_input(v, r.normal(size=32), None, 1e-6, None, 0.0)
+    _close(np.linalg.norm(y, axis=-1), np.full(4, math.sqrt(32)), 1e-11, "|y| = sqrt(d)")
+    cos = np.sum(h * y, axis=-1) / (np.linalg.norm(h, axis=-1) * np.linalg.norm(y, axis=-1))
+    _close(cos, np.ones(4), 1e-12, "y parallel to h")
+
+
+def pin_phase2_reference(O):
+    """phase2_reference forms the partial as partial_prev + v_prev, and with neither it is the
+    first sublayer (no partial source; page 2 §8, V_first)."""
+    r = _rng(20)
+    reps = _sources(r, 3, 4, 16)
+    pp, vp = r.normal(size=(4, 16)), r.normal(size=(4, 16))
+    w = r.normal(size=16)
+    h, _, a, p = O.phase2_reference(reps, pp, vp, w, None, 1e-6, None, 1e-6)
+    _close(p, pp + vp, 1e-15, "partial = prev + v")
+    h2, _, _ = O.aggregate(np.concatenate([reps, (pp + vp)[None]]), w, None, 1e-6)
+    _close(h, h2, 1e-13, "four sources")
+    h1, _, a1, p1 = O.phase2_reference(reps, None, None, w, None, 1e-6, None, 1e-6)
+    assert p1 is None and a1.shape[0] == 3
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,75 @@
+"""The cost model against the numbers the pages print (tests/golden/pages_numbers.txt), and
+the per-kernel byte counts against hand counts.  CPU only."""
+import os
+
+import pytest
+
+from depth_wise_softmax_block_b300 import cost as C
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden", "pages_numbers.txt")
+MiB, GiB = 2 ** 20, 2 ** 30
+
+
+def _load():
+    rows = {}
+    for line in open(GOLD, encoding="utf-8"):
+        if not line.strip() or line.startswith("#"):
+            continue
+        key, val, tol, _cite = [x.strip() for x in line.split("|", 3)]
+        rows[key] = (float(val), float(tol))
+    return rows
+
+
+COMPUTED = {
+    "n_pairs_L122": lambda: C.n_pairs(122),
+    "full_fwd_gflop_L122_d7168": lambda: C.full_fwd_flops_per_token(122, 7168) / 1e9,
+    "params_2Ld_million": lambda: 2 * 122 * 7168 / 1e6,
+    "full_train_gflop_L122": lambda: 3 * C.full_fwd_flops_per_token(122, 7168) / 1e9,
+    "full_history_GB_T32K_L128": lambda: C.full_history_bytes(1, 32768, 128, 7168) / 1e9,
+    "full_history_GB_8way": lambda: C.full_history_bytes(1, 32768, 128, 7168) / 8 / 1e9,
+    "decode_depth_state_MiB": lambda: 123 * 7168 * 2 / MiB,
+    "hidden_state_MiB_M4096": lambda: 4096 * 7168 * 2 / MiB,
+    "full_history_GiB_123": lambda: 123 * (4096 * 7168 * 2) / GiB,
+    "block_history_MiB_8": lambda: 8 * 4096 * 7168 * 2 / MiB,
+    "block_history_MiB_9": lambda: 9 * 4096 * 7168 * 2 / MiB,
+    "block_cache_GB_128K_N8": lambda: C.block_cache_bytes(1, 8, 131072, 7168) / 1e9,
+    "block_cache_GB_P8": lambda: C.block_cache_bytes(1, 8, 131072, 7168, P=8) / 1e9,
+    "block_cache_GB_P8_chunk16K_max": lambda: C.block_cache_bytes(1, 8, 16384, 7168, P=8) / 1e9,
+    "io_standard_d": lambda: C.io_per_layer_standard(1),
+    "io_full_two_phase_d": lambda: C.io_per_layer_full_two_phase(16, 8, 1),
+    "io_block_two_phase_d": lambda: C.io_per_layer_block_two_phase(16, 8, 1),
+    "io_mhc_d_coeff": lambda: C.io_per_layer_mhc(4, 1000) // 1000,
+    "io_mhc_scalar": lambda: C.io_per_layer_mhc(4, 1000) % 1000,
+    "pp_comm_naive_P4_V2": lambda: C.pp_comm_naive(4, 2),
+    "pp_comm_cached_P4_V2": lambda: C.pp_comm_cached(4, 2),
+}
+
+
+@pytest.mark.parametrize("key", sorted(COMPUTED))
+def test_pages_numbers(key):
+    val, tol = _load()[key]
+    got = COMPUTED[key]()
+    if key.endswith("_max"):
+        assert got < val
+    elif tol == 0:
+        assert got == val
+    else:
+        assert abs(got - val) <= tol * abs(val), (key, got, val)
+
+
+def test_every_golden_row_checked():
+    assert set(_load()) == set(COMPUTED)
+
+
+def test_kernel_bytes_hand_counts():
+    d, E = 7168, 2
+    assert C.phase1_bytes(9, 24, d, E) == 33 * d * E + 96
+    assert C.phase2_bytes(d, E, False, False) == 2 * d * E
+    assert C.phase2_bytes(d, E, True, False) == 3 * d * E + 4
+    assert C.phase2_bytes(d, E, True, True) == 5 * d * E + 4
+    st = C.block_step_bytes(9, 24, d, E, final_sources=10)
+    assert st.phase1 == 33 * d * E + 4 * 24          # o and lse; m is not written
+    assert st.phase2 == 2 * d * E + (3 * d * E + 4) + 22 * (5 * d * E + 4)
+    assert st.close == 3 * d * E
+    assert st.final == 11 * d * E
+    assert C.phase1_flops(9, 24, d) == 2 * (2 * 24 * 9 * d + 9 * d)

@@ -1,0 +1,113 @@
+"""Plant plausible mistakes in the oracle (on the CPU, in a patched copy of its functions)
+and check that at least one pin catches each.  This is what makes the pins worth trusting:
+a dropped term, a wrong sign, a wrong axis or a transposed operand must not pass."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle.attnres_oracle as O
+import oracle_pins
+
+
+def _rms_sum(x, eps):                       # forgets the 1/d of the mean
+    x = np.asarray(x, np.float64)
+    return np.sqrt(np.sum(x * x, axis=-1) + eps)
+
+
+def _rms_no_eps(x, eps):                    # drops eps
+    x = np.asarray(x, np.float64)
+    return np.sqrt(np.mean(x * x, axis=-1))
+
+
+def _rms_centered(x, eps):                  # LayerNorm-style variance instead of m_2
+    x = np.asarray(x, np.float64)
+    return np.sqrt(np.var(x, axis=-1) + eps)
+
+
+def _softmax_neg(z):                        # wrong sign in the exponent
+    z = np.asarray(z, np.float64)
+    e = np.exp(-(z - np.min(z, axis=0, keepdims=True)))
+    return e / e.sum(axis=0, keepdims=True)
+
+
+def _softmax_wrong_axis(z):                 # normalises over tokens instead of sources
+    z = np.asarray(z, np.float64)
+    e = np.exp(z - np.max(z, axis=-1, keepdims=True))
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def _logits_scaled(sources, w, gamma_key, eps):   # adds a 1/sqrt(d) scale the pages do not have
+    keys = O.rmsnorm(sources, gamma_key, eps)
+    return np.sum(keys * np.asarray(w, np.float64), axis=-1) / math.sqrt(np.shape(sources)[-1])
+
+
+def _logits_raw_keys(sources, w, gamma_key, eps):  # forgets the key RMSNorm
+    src = np.asarray(sources, np.float64)
+    g = 1.0 if gamma_key is None else np.asarray(gamma_key, np.float64)
+    return np.sum(src * g * np.asarray(w, np.float64), axis=-1)
+
+
+def _logits_gamma_on_query_index_reversed(sources, w, gamma_key, eps):  # transposed gain
+    keys = O.rmsnorm(sources, None if gamma_key is None else np.asarray(gamma_key)[::-1], eps)
+    return np.sum(keys * np.asarray(w, np.float64), axis=-1)
+
+
+def _aggregate_normed_values(sources, w, gamma_key, eps):  # uses keys as values
+    src = np.asarray(sources, np.float64)
+    z = O.depth_logits(src, w, gamma_key, eps)
+    alpha = O.depth_softmax(z)
+    return np.sum(alpha[..., None] * O.rmsnorm(src, None, eps), axis=0), alpha, z
+
+
+def _partition_lse_no_max(sources, w, gamma_key, eps):  # returns ln l instead of m + ln l
+    o, m, lse, a = _ORIG_PARTITION(sources, w, gamma_key, eps)
+    return o, m, lse - m, a
+
+
+def _partition_unnormalised(sources, w, gamma_key, eps):  # forgets to divide o by l
+    o, m, lse, a = _ORIG_PARTITION(sources, w, gamma_key, eps)
+    return o * np.exp(lse - m)[..., None], m, lse, a
+
+
+def _block_sources_zero_partial(completed, partial):  # a zero source at the first sublayer
+    srcs = [np.asarray(b, np.float64) for b in completed]
+    srcs.append(np.zeros_like(srcs[0]) if partial is None else np.asarray(partial, np.float64))
+    return np.stack(srcs)
+
+
+def _block_of_off_by_one(l, S):             # blocks start one sublayer late
+    n = l // S + 1
+    return n, l - (n - 1) * S + 1
+
+
+_ORIG_PARTITION = O.partition_stats
+
+MUTATIONS = {
+    "rms_sum_not_mean": ("rms", _rms_sum),
+    "rms_drops_eps": ("rms", _rms_no_eps),
+    "rms_centered": ("rms", _rms_centered),
+    "softmax_sign": ("depth_softmax", _softmax_neg),
+    "softmax_axis": ("depth_softmax", _softmax_wrong_axis),
+    "logit_scale": ("depth_logits", _logits_scaled),
+    "no_key_norm": ("depth_logits", _logits_raw_keys),
+    "gain_transposed": ("depth_logits", _logits_gamma_on_query_index_reversed),
+    "normed_values": ("aggregate", _aggregate_normed_values),
+    "lse_without_max": ("partition_stats", _partition_lse_no_max),
+    "o_unnormalised": ("partition_stats", _partition_unnormalised),
+    "zero_partial_source": ("block_sources", _block_sources_zero_partial),
+    "block_index_off_by_one": ("block_of", _block_of_off_by_one),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_mutation(name, monkeypatch):
+    attr, bad = MUTATIONS[name]
+    monkeypatch.setattr(O, attr, bad)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(O)
+        except Exception as e:  # noqa: BLE001 - any failure counts as caught
+            caught.append((pin.__name__, type(e).__name__))
+    assert caught, f"no pin caught the planted mistake {name}"
