@@ -1,0 +1,426 @@
+"""Benchmark of the Block AttnRes aggregation hot path on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-e2e]
+
+Workload (one step): long-context chunked prefill, 131072 tokens in 8 chunks of 16384,
+d = 7168, bf16 storage with fp32 arithmetic, a resident block-representation cache
+[10, 131072, 7168] whose slots 0..8 are the embedding and 8 completed blocks.  For every
+chunk the step runs the whole hot path:
+  query prep (u = w ⊙ gamma_key, once per step), phase 1 over the 9 sources for the block's
+  24 queries, 24 phase-2 merges (fused partial update and input RMSNorm), the block close
+  into slot 9, and the final aggregation over the 10 slots.
+Inputs are synthetic (seeded); every launch streams >= 235 MB, far more than the 126 MB L2,
+so no flush is needed between steps.
+
+Prints one JSON line.  ``value`` is tokens/s over all ranks (each rank runs its own step on its
+own GPU: tokens are independent, no collective on the data path, weak scaling).  The
+reference arm (``--impl reference``) times the fp64 CPU oracle on a bounded token sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from depth_wise_softmax_block_b300 import cost as C  # noqa: E402
+from synth import inputs as I  # noqa: E402
+
+METRIC = "AttnRes tokens/s per block and achieved HBM GB/s (% of B300 peak), 1 GPU"
+CSRC = os.path.join(ROOT, "depth_wise_softmax_block_b300", "csrc")
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        h.update(f.encode())
+        h.update(open(os.path.join(CSRC, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return float(j["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+# --------------------------------------------------------------------------------------------
+class LongContextStep:
+    """The bench step.  Allocates everything once; ``run()`` allocates nothing."""
+
+    def __init__(self, wl: I.Workload, dev, timer=None):
+        from depth_wise_softmax_block_b300 import attnres_query_prep
+        from depth_wise_softmax_block_b300.schedule import BlockRunner
+        self.wl, self.dev = wl, dev
+        self.n = 9                                   # embedding + 8 completed blocks
+        T, d, S, ch = wl.T, wl.d, wl.S, wl.chunk
+        self.nchunks = T // ch
+        assert self.nchunks * ch == T
+        self.reps = torch.empty((self.n + 1, T, d), dtype=torch.bfloat16, device=dev)
+        for j in range(self.n):
+            I.fill_block_rep(self.reps[j], j, wl.seed)
+        self.reps[self.n].zero_()                    # slot 9 receives the closed block
+        self.vbuf = I.make_outputs(wl, 1, S, dev, T=ch)   # stand-ins for f_i, shared by chunks
+        self.P = I.block_params(wl, dev)
+        self.U = torch.empty_like(self.P.W)
+        self.uf = torch.empty((1, d), device=dev)
+        self.out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+        self.timer = timer
+        self.runner = BlockRunner(ch, d, S, torch.bfloat16, dev, timer=timer)
+        self._prep = attnres_query_prep
+
+    def chunk_views(self, c):
+        sl = slice(c * self.wl.chunk, (c + 1) * self.wl.chunk)
+        return (self.reps[:self.n, sl], self.reps[self.n, sl], self.reps[:self.n + 1, sl],
+                self.out[sl])
+
+    def prep(self):
+        from depth_wise_softmax_block_b300.schedule import _call
+        _call(self.timer, "query_prep", self._prep, self.P.W, self.P.G_key, self.U)
+        _call(self.timer, "query_prep", self._prep, self.P.w_final.view(1, -1),
+              self.P.g_final.view(1, -1), self.uf)
+
+    def sublayer(self, i, y):
+        """Stand-in for the sublayer f_i: returns the synthetic output v_i."""
+        return self.vbuf[i - 1]
+
+    def run_chunk(self, c, on_call=None):
+        from depth_wise_softmax_block_b300.schedule import final_aggregation
+        reps_c, close_c, all_c, out_c = self.chunk_views(c)
+        self.runner.run_block(reps_c, self.U, self.P.G_in, self.sublayer, close_c, self.wl.eps,
+                              self.wl.eps, on_call=on_call)
+        final_aggregation(all_c, self.uf[0], out_c, self.wl.eps, timer=self.timer)
+
+    def run(self):
+        self.prep()
+        for c in range(self.nchunks):
+            self.run_chunk(c)
+
+    # algorithmic bytes, per step, per kernel kind
+    def bytes_per_launch(self):
+        d, E, ch, S, n = self.wl.d, 2, self.wl.chunk, self.wl.S, self.n
+        return {
+            "phase1": C.phase1_bytes(n, S, d, E) * ch,
+            "phase2_first": C.phase2_bytes(d, E, False, False) * ch,
+            "phase2": C.phase2_bytes(d, E, True, False) * ch,
+            "phase2_fused": C.phase2_bytes(d, E, True, True) * ch,
+            "close": C.partial_update_bytes(d, E) * ch,
+            "final": C.phase1_bytes(n + 1, 1, d, E, with_lse=False) * ch,
+        }
+
+    def launches_per_step(self):
+        return 2 + self.nchunks * (1 + self.wl.S + 1 + 1)
+
+    def step_bytes(self):
+        per_tok = C.block_step_bytes(self.n, self.wl.S, self.wl.d, 2, self.n + 1).total
+        return per_tok * self.wl.T
+
+
+# --------------------------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of the SM clock and throttle reasons."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------------------------
+def oracle_sample(wl: I.Workload, k: int, seed_offset: int = 0):
+    """Host inputs of a k-token sample of the long-context block (CPU-generated)."""
+    n, d, S = 9, wl.d, wl.S
+    T = k
+    reps = torch.empty((n, T, d), dtype=torch.bfloat16)
+    for j in range(n):
+        I.fill_block_rep(reps[j], j, wl.seed + 1000 + seed_offset)
+    v = I.make_outputs(wl, 1, S, "cpu", T=T)
+    P = I.block_params(wl, "cpu")
+    f = lambda t: t.float().numpy().astype("float64")  # noqa: E731
+    return (f(reps), f(v), f(P.W), f(P.G_key), f(P.G_in), f(P.w_final), f(P.g_final))
+
+
+def time_oracle(wl: I.Workload, k: int, seed_offset: int = 0):
+    """Run the fp64 oracle (as it stands) over a k-token sample of one block; seconds."""
+    from threadpoolctl import threadpool_limits
+    import oracle.attnres_oracle as O
+    args = oracle_sample(wl, k, seed_offset)
+    with threadpool_limits(limits=1):
+        t0 = time.perf_counter()
+        O.single_block(args[0], args[1], args[2], args[3], args[4], args[5], args[6], wl.eps,
+                       wl.eps)
+        return time.perf_counter() - t0
+
+
+# --------------------------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reference_arm(args, world, rank):
+    """The fp64 oracle on the host cores, on a bounded sample of the same workload."""
+    if rank != 0:
+        return None
+    wl = I.LONGCTX_PREFILL_BF16
+    k = args.ref_tokens
+    for w in range(args.warmup):
+        time_oracle(wl, k, w)
+    secs = [time_oracle(wl, k, 100 + s) for s in range(args.steps)]
+    step = sum(secs) / len(secs)
+    val = k / step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "tokens_per_step": k, "d": wl.d, "sources": 9,
+                   "S": wl.S},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{k} tokens of one 24-sublayer block over 9 sources + "
+                                   "final aggregation, fp64 numpy, 1 thread"},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def traffic_for(kernel: str):
+    """dram bytes per launch from a committed ncu summary, if it matches the current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    j = json.load(open(p))
+    e = j.get(kernel)
+    if not e or e.get("csrc_hash") != csrc_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+def run_e2e(step: LongContextStep, iters: int):
+    """The same step through the public API from pinned HOST buffers: per step, copy the
+    block-representation cache (slots 0..8), the sublayer stand-ins and the parameters to the
+    device, run, and read the final output back."""
+    wl = step.wl
+    h_reps = torch.empty(step.reps[:step.n].shape, dtype=torch.bfloat16, pin_memory=True)
+    h_v = torch.empty(step.vbuf.shape, dtype=torch.bfloat16, pin_memory=True)
+    params = [step.P.W, step.P.G_key, step.P.G_in, step.P.w_final, step.P.g_final]
+    h_params = [torch.empty(p.shape, dtype=p.dtype, pin_memory=True) for p in params]
+    h_out = torch.empty(step.out.shape, dtype=torch.bfloat16, pin_memory=True)
+    h_reps.copy_(step.reps[:step.n])
+    h_v.copy_(step.vbuf)
+    for h, p in zip(h_params, params):
+        h.copy_(p)
+    torch.cuda.synchronize()
+    h2d = h_reps.numel() * 2 + h_v.numel() * 2 + sum(h.numel() * 4 for h in h_params)
+    d2h = h_out.numel() * 2
+
+    def one():
+        for h, p in zip(h_params, params):
+            p.copy_(h, non_blocking=True)
+        step.vbuf.copy_(h_v, non_blocking=True)
+        ch = wl.chunk
+        for c in range(step.nchunks):
+            sl = slice(c * ch, (c + 1) * ch)
+            for j in range(step.n):
+                step.reps[j, sl].copy_(h_reps[j, sl], non_blocking=True)
+            if c == 0:
+                step.prep()
+            step.run_chunk(c)
+            h_out[sl].copy_(step.out[sl], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    one()
+    t0 = time.perf_counter()
+    for _ in range(iters):
+        one()
+    el = (time.perf_counter() - t0) / iters
+    return {"value": wl.T / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": el * 1e3}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--cpu-tokens", type=int, default=64)
+    ap.add_argument("--ref-tokens", type=int, default=16)
+    args = ap.parse_args(argv)
+    world, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        line = reference_arm(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+
+    assert torch.cuda.is_available(), "the bench needs a CUDA device"
+    assert world == args.gpus or world == 1, "--gpus must match the launcher's world size"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from depth_wise_softmax_block_b300 import build as B
+    from depth_wise_softmax_block_b300.schedule import KernelTimer
+    B.build()
+    wl = I.LONGCTX_PREFILL_BF16
+    timer = KernelTimer()
+    step = LongContextStep(wl, dev, timer=timer)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    timer.clear()
+
+    barrier(world)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        start.record()
+        for _ in range(args.steps):
+            step.run()
+        end.record()
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = start.elapsed_time(end) / args.steps
+    ms = reduce_max(ms, world)
+    tokens = wl.T * world
+    value = tokens / (ms / 1e3)
+
+    # per-kernel live durations (events on the launching stream, inside the timed region)
+    tot = timer.totals_ms()
+    bpl = step.bytes_per_launch()
+    per_kernel = {}
+    for k, (t_ms, cnt) in tot.items():
+        avg = t_ms / cnt
+        e = {"launches_per_step": cnt // args.steps, "avg_ms": avg,
+             "share_of_step": t_ms / args.steps / ms}
+        if k in bpl:
+            e["achieved_gbs"] = bpl[k] / (avg / 1e3) / 1e9
+        per_kernel[k] = e
+    dom = max((k for k in per_kernel if k in bpl), key=lambda k: tot[k][0])
+    peak, peak_kind = peaks()
+    ach = per_kernel[dom]["achieved_gbs"]
+    step_gbs = step.step_bytes() / (ms / 1e3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "tokens": wl.T, "chunk": wl.chunk, "d": wl.d,
+                   "sources": step.n, "S": wl.S, "accumulate": "f32",
+                   "l2": "no flush: every launch streams >= 235 MB (> 126 MB L2)",
+                   "parallelism": f"replicas x{world} (tokens independent)"},
+        "achieved_gbs_step": step_gbs, "frac_of_peak_step": step_gbs / peak,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak,
+                     "peak_source": peak_kind, "unit": "GB/s", "frac": ach / peak,
+                     "traffic": traffic_for(dom)},
+        "kernels": per_kernel,
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": clk.summary(),
+    }
+    del timer
+    step.timer = None
+    step.runner.timer = None
+    if not args.no_e2e and rank == 0:
+        line["e2e"] = run_e2e(step, args.e2e_steps)
+    if rank == 0:
+        secs = time_oracle(wl, args.cpu_tokens)
+        line["cpu_baseline"] = {"value": args.cpu_tokens / secs, "unit": "tokens/s", "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"{args.cpu_tokens} tokens of one 24-sublayer block "
+                                          "over 9 sources + final aggregation, fp64 numpy, "
+                                          f"1 thread, {secs:.1f} s"}
+        print(json.dumps(line), flush=True)
+    barrier(world)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,155 @@
+"""B300 (sm_103a) Attention Residuals aggregation: Python binding of ``libattnres.so``.
+
+The functions below carry the names of the C entry points in ``include/attnres.h`` and do
+argument marshalling only (shapes, strides, dtypes, the current CUDA stream); every step of
+the computation runs in the library's CUDA kernels.  PyTorch provides device memory and
+streams.  There is no CPU fallback: if the library is missing or a call fails, an exception
+is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattnres.so")
+
+F32, BF16 = 0, 1
+STATUS = {0: "ATTNRES_OK", 1: "ATTNRES_ERR_INVALID_ARG", 2: "ATTNRES_ERR_UNSUPPORTED",
+          3: "ATTNRES_ERR_MISALIGNED", 4: "ATTNRES_ERR_CUDA"}
+
+# C signatures (argument types, in order) of every exported symbol of include/attnres.h.
+_P, _I, _I64, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+SIGNATURES = {
+    "attnres_abi_version": ([], _I),
+    "attnres_status_string": ([_I], ctypes.c_char_p),
+    "attnres_last_cuda_error": ([], ctypes.c_char_p),
+    "attnres_query_prep": ([_P, _P, _P, _I, _I, _P], _I),
+    "attnres_phase1": ([_P, _I64, _I, _I64, _I, _I, _P, _I, _F, _P, _P, _P, _P, _P], _I),
+    "attnres_phase2_merge": ([_P, _P, _P, _P, _P, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _P],
+                             _I),
+    "attnres_partial_update": ([_P, _P, _P, _I64, _I, _I, _P], _I),
+    "attnres_full_reference_path": ([_P, _I, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _P], _I),
+}
+
+
+class AttnResError(RuntimeError):
+    """A library call returned a non-OK status."""
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded ``libattnres.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -m depth_wise_softmax_block_b300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        msg = STATUS.get(status, str(status))
+        if status == 4:
+            msg += ": " + library().attnres_last_cuda_error().decode()
+        raise AttnResError(f"{what} failed: {msg}")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _io(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _rows(t: torch.Tensor, T: int, d: int, name: str):
+    if t is None:
+        return
+    if tuple(t.shape[-2:]) != (T, d) or t.stride(-1) != 1 or t.stride(-2) != d:
+        raise ValueError(f"{name}: expected rows of shape [{T}, {d}] with row stride {d}")
+
+
+def attnres_query_prep(w, gamma_key, u_out, stream=None):
+    """u = w ⊙ gamma_key (query with the key-norm gain folded in), [rows, d] fp32."""
+    rows, d = w.shape
+    _check(library().attnres_query_prep(_ptr(w), _ptr(gamma_key), _ptr(u_out), rows, d,
+                                        _stream(stream)), "attnres_query_prep")
+    return u_out
+
+
+def attnres_phase1(reps, u, o_out, m_out=None, lse_out=None, alpha_out=None, eps=1e-6,
+                   stream=None):
+    """Phase 1 over ``reps`` [n, T, d] (any source stride, rows of stride d) for the S queries
+    ``u`` [S, d]; writes o [S, T, d] and the optional statistics."""
+    n, T, d = reps.shape
+    S = u.shape[0]
+    _rows(reps[0], T, d, "reps")
+    if tuple(o_out.shape) != (S, T, d) or not o_out.is_contiguous():
+        raise ValueError("o_out must be a contiguous [S, T, d] tensor")
+    src_stride = reps.stride(0) if n > 1 else T * d
+    _check(library().attnres_phase1(_ptr(reps), src_stride, n, T, d, _io(reps), _ptr(u), S,
+                                    eps, _ptr(o_out), _ptr(m_out), _ptr(lse_out),
+                                    _ptr(alpha_out), _stream(stream)), "attnres_phase1")
+    return o_out
+
+
+def attnres_phase2_merge(o_l, lse_l, partial, v_prev, partial_out, u_l, gamma_in, y_out,
+                         h_out=None, alpha_p_out=None, eps_key=1e-6, eps_in=1e-6, stream=None):
+    """Phase 2 for one sublayer: merge the partial-sum source (partial + v_prev) into the
+    phase-1 result and apply the input RMSNorm.  Tensors are [T, d]."""
+    T, d = o_l.shape
+    for name, t in (("o_l", o_l), ("partial", partial), ("v_prev", v_prev),
+                    ("partial_out", partial_out), ("y_out", y_out), ("h_out", h_out)):
+        _rows(t, T, d, name)
+    _check(library().attnres_phase2_merge(
+        _ptr(o_l), _ptr(lse_l), _ptr(partial), _ptr(v_prev), _ptr(partial_out), T, d, _io(o_l),
+        _ptr(u_l), eps_key, _ptr(gamma_in), eps_in, _ptr(h_out), _ptr(y_out), _ptr(alpha_p_out),
+        _stream(stream)), "attnres_phase2_merge")
+    return y_out
+
+
+def attnres_partial_update(partial, v, out, stream=None):
+    """out = partial + v (partial-sum update / block close)."""
+    T, d = partial.shape
+    for name, t in (("partial", partial), ("v", v), ("out", out)):
+        _rows(t, T, d, name)
+    _check(library().attnres_partial_update(_ptr(partial), _ptr(v), _ptr(out), T, d,
+                                            _io(partial), _stream(stream)),
+           "attnres_partial_update")
+    return out
+
+
+def attnres_full_reference_path(srcs, u_l, gamma_in, h_out=None, y_out=None, alpha_out=None,
+                                eps_key=1e-6, eps_in=1e-6, stream=None):
+    """Direct single-pass aggregation over the list of [T, d] source tensors ``srcs``."""
+    T, d = srcs[0].shape
+    for t in srcs:
+        _rows(t, T, d, "srcs[j]")
+    arr = (ctypes.c_void_p * len(srcs))(*[t.data_ptr() for t in srcs])
+    _check(library().attnres_full_reference_path(
+        arr, len(srcs), T, d, _io(srcs[0]), _ptr(u_l), eps_key, _ptr(gamma_in), eps_in,
+        _ptr(h_out), _ptr(y_out), _ptr(alpha_out), _stream(stream)),
+        "attnres_full_reference_path")
+    return h_out if y_out is None else y_out

@@ -1,0 +1,154 @@
+// The C ABI of include/attnres.h: host-side argument validation, then dispatch to the
+// kernels.  Nothing is launched unless every check passes; no exception crosses the ABI.
+#include <stdint.h>
+#include <string.h>
+
+#include <string>
+
+#include "../../include/attnres.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_last_cuda_error;
+
+using attnres::IO;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool opt_aligned16(const void* p) { return p == nullptr || aligned16(p); }
+bool valid_io(attnres_dtype io) { return io == ATTNRES_F32 || io == ATTNRES_BF16; }
+
+attnres_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return ATTNRES_OK;
+  g_last_cuda_error = cudaGetErrorString(e);
+  return ATTNRES_ERR_CUDA;
+}
+
+// Shared checks on T and d.
+attnres_status check_shape(int64_t T, int d) {
+  if (T < 0 || d <= 0) return ATTNRES_ERR_INVALID_ARG;
+  if (d % 8 != 0) return ATTNRES_ERR_INVALID_ARG;
+  if (d > ATTNRES_MAX_D) return ATTNRES_ERR_UNSUPPORTED;
+  if (T > INT32_MAX) return ATTNRES_ERR_UNSUPPORTED;  // one CTA (or tile) per row in x
+  return ATTNRES_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attnres_abi_version(void) { return ATTNRES_ABI_VERSION; }
+
+const char* attnres_status_string(attnres_status s) {
+  switch (s) {
+    case ATTNRES_OK: return "ATTNRES_OK";
+    case ATTNRES_ERR_INVALID_ARG: return "ATTNRES_ERR_INVALID_ARG";
+    case ATTNRES_ERR_UNSUPPORTED: return "ATTNRES_ERR_UNSUPPORTED";
+    case ATTNRES_ERR_MISALIGNED: return "ATTNRES_ERR_MISALIGNED";
+    case ATTNRES_ERR_CUDA: return "ATTNRES_ERR_CUDA";
+  }
+  return "ATTNRES_ERR_UNKNOWN";
+}
+
+const char* attnres_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+attnres_status attnres_query_prep(const float* w, const float* gamma_key, float* u_out, int rows,
+                                  int d, void* stream) {
+  if (w == nullptr || u_out == nullptr || rows < 0) return ATTNRES_ERR_INVALID_ARG;
+  const attnres_status sh = check_shape(rows, d);
+  if (sh != ATTNRES_OK) return sh;
+  if (!aligned16(w) || !aligned16(u_out) || !opt_aligned16(gamma_key))
+    return ATTNRES_ERR_MISALIGNED;
+  return cuda_status(attnres::launch_query_prep(w, gamma_key, u_out,
+                                                static_cast<int64_t>(rows) * d,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, int64_t T, int d,
+                              attnres_dtype io, const float* u, int S, float eps, void* o_out,
+                              float* m_out, float* lse_out, float* alpha_out, void* stream) {
+  if (reps == nullptr || u == nullptr || o_out == nullptr || !valid_io(io))
+    return ATTNRES_ERR_INVALID_ARG;
+  const attnres_status sh = check_shape(T, d);
+  if (sh != ATTNRES_OK) return sh;
+  if (n_src < 1 || S < 1 || !(eps >= 0.f)) return ATTNRES_ERR_INVALID_ARG;
+  if (n_src > ATTNRES_MAX_SOURCES || S > ATTNRES_MAX_QUERIES) return ATTNRES_ERR_UNSUPPORTED;
+  if (n_src > 1 && src_stride < T * d) return ATTNRES_ERR_INVALID_ARG;
+  if (src_stride < 0) return ATTNRES_ERR_INVALID_ARG;
+  if (!attnres::phase1_supported(n_src, S)) return ATTNRES_ERR_UNSUPPORTED;
+  if (!aligned16(reps) || !aligned16(u) || !aligned16(o_out) || src_stride % 8 != 0)
+    return ATTNRES_ERR_MISALIGNED;
+  attnres::Phase1Args a{reps, src_stride, n_src, T, d, u, S, eps, o_out, m_out, lse_out, alpha_out};
+  return cuda_status(attnres::launch_phase1(static_cast<IO>(io), a,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+attnres_status attnres_phase2_merge(const void* o_l, const float* lse_l, const void* partial,
+                                    const void* v_prev, void* partial_out, int64_t T, int d,
+                                    attnres_dtype io, const float* u_l, float eps_key,
+                                    const float* gamma_in, float eps_in, void* h_out, void* y_out,
+                                    float* alpha_p_out, void* stream) {
+  if (o_l == nullptr || y_out == nullptr || !valid_io(io)) return ATTNRES_ERR_INVALID_ARG;
+  const attnres_status sh = check_shape(T, d);
+  if (sh != ATTNRES_OK) return sh;
+  const bool has_p = partial != nullptr || v_prev != nullptr;
+  if (has_p && (lse_l == nullptr || u_l == nullptr)) return ATTNRES_ERR_INVALID_ARG;
+  if (partial_out != nullptr && !has_p) return ATTNRES_ERR_INVALID_ARG;
+  if (!(eps_key >= 0.f) || !(eps_in >= 0.f)) return ATTNRES_ERR_INVALID_ARG;
+  if (!aligned16(o_l) || !aligned16(y_out) || !opt_aligned16(partial) || !opt_aligned16(v_prev) ||
+      !opt_aligned16(partial_out) || !opt_aligned16(u_l) || !opt_aligned16(gamma_in) ||
+      !opt_aligned16(h_out))
+    return ATTNRES_ERR_MISALIGNED;
+  attnres::Phase2Args a{o_l, lse_l, partial, v_prev, partial_out, T, d, u_l, eps_key, gamma_in,
+                        eps_in, h_out, y_out, alpha_p_out};
+  return cuda_status(attnres::launch_phase2(static_cast<IO>(io), a,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+attnres_status attnres_partial_update(const void* partial, const void* v, void* out, int64_t T,
+                                      int d, attnres_dtype io, void* stream) {
+  if (partial == nullptr || v == nullptr || out == nullptr || !valid_io(io))
+    return ATTNRES_ERR_INVALID_ARG;
+  const attnres_status sh = check_shape(T, d);
+  if (sh != ATTNRES_OK) return sh;
+  if (!aligned16(partial) || !aligned16(v) || !aligned16(out)) return ATTNRES_ERR_MISALIGNED;
+  return cuda_status(attnres::launch_partial_update(static_cast<IO>(io), partial, v, out, T * d,
+                                                    static_cast<cudaStream_t>(stream)));
+}
+
+attnres_status attnres_full_reference_path(const void* const* srcs, int n_src, int64_t T, int d,
+                                           attnres_dtype io, const float* u_l, float eps_key,
+                                           const float* gamma_in, float eps_in, void* h_out,
+                                           void* y_out, float* alpha_out, void* stream) {
+  if (srcs == nullptr || u_l == nullptr || !valid_io(io)) return ATTNRES_ERR_INVALID_ARG;
+  if (h_out == nullptr && y_out == nullptr) return ATTNRES_ERR_INVALID_ARG;
+  const attnres_status sh = check_shape(T, d);
+  if (sh != ATTNRES_OK) return sh;
+  if (n_src < 1) return ATTNRES_ERR_INVALID_ARG;
+  if (n_src > ATTNRES_MAX_SOURCES) return ATTNRES_ERR_UNSUPPORTED;
+  if (!(eps_key >= 0.f) || !(eps_in >= 0.f)) return ATTNRES_ERR_INVALID_ARG;
+  attnres::FullArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int j = 0; j < n_src; ++j) {
+    if (srcs[j] == nullptr) return ATTNRES_ERR_INVALID_ARG;
+    if (!aligned16(srcs[j])) return ATTNRES_ERR_MISALIGNED;
+    a.srcs[j] = srcs[j];
+  }
+  if (!aligned16(u_l) || !opt_aligned16(gamma_in) || !opt_aligned16(h_out) ||
+      !opt_aligned16(y_out))
+    return ATTNRES_ERR_MISALIGNED;
+  a.n = n_src;
+  a.T = T;
+  a.d = d;
+  a.u = u_l;
+  a.eps_key = eps_key;
+  a.gamma_in = gamma_in;
+  a.eps_in = eps_in;
+  a.h = h_out;
+  a.y = y_out;
+  a.alpha = alpha_out;
+  return cuda_status(attnres::launch_full(static_cast<IO>(io), a,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,138 @@
+// Device helpers shared by the AttnRes kernels: 16-byte vector I/O, bf16 <-> fp32
+// conversion, cp.async staging and block reductions.  sm_103a only.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attnres {
+
+using bf16 = __nv_bfloat16;
+
+// Elements per 16-byte vector.
+template <typename T> struct Vec;
+template <> struct Vec<float> { static constexpr int N = 4; };
+template <> struct Vec<bf16> { static constexpr int N = 8; };
+
+// ---- global memory ------------------------------------------------------------------------
+// Streaming load of data read once by this kernel (no L1 allocation).
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_global(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// ---- conversions -------------------------------------------------------------------------
+// bf16 is the top half of an fp32: widening is a shift (low element) or a mask (high).
+__device__ __forceinline__ void unpack(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void unpack(const uint4& v, float (&f)[4]) {
+  f[0] = __uint_as_float(v.x);
+  f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z);
+  f[3] = __uint_as_float(v.w);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint4 pack(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+__device__ __forceinline__ uint4 pack(const float (&f)[4]) {
+  return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                    __float_as_uint(f[3]));
+}
+
+// Eight consecutive elements starting at a 16-byte aligned address (generic or shared).
+template <typename T> __device__ __forceinline__ void load8(const void* p, float (&f)[8]);
+template <> __device__ __forceinline__ void load8<bf16>(const void* p, float (&f)[8]) {
+  unpack(*reinterpret_cast<const uint4*>(p), f);
+}
+template <> __device__ __forceinline__ void load8<float>(const void* p, float (&f)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+template <typename T> __device__ __forceinline__ void store8(void* p, const float (&f)[8]);
+template <> __device__ __forceinline__ void store8<bf16>(void* p, const float (&f)[8]) {
+  st_global(p, pack(f));
+}
+template <> __device__ __forceinline__ void store8<float>(void* p, const float (&f)[8]) {
+  st_global(p, make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3])));
+  st_global(static_cast<char*>(p) + 16,
+            make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]),
+                       __float_as_uint(f[7])));
+}
+
+// ---- cp.async (global -> shared, 16 bytes, zero-filled when !valid) ------------------------
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  const int bytes = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---- reductions ------------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Sum of two values over the whole CTA; every thread gets the totals.  `scratch` holds at
+// least 2 * 33 floats of shared memory and is reused across calls (the trailing barrier
+// protects it).
+__device__ __forceinline__ void block_sum2(float& a, float& b, float* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+  a = warp_sum(a);
+  b = warp_sum(b);
+  if (lane == 0) {
+    scratch[warp] = a;
+    scratch[33 + warp] = b;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float x = lane < nw ? scratch[lane] : 0.f;
+    float y = lane < nw ? scratch[33 + lane] : 0.f;
+    x = warp_sum(x);
+    y = warp_sum(y);
+    if (lane == 0) {
+      scratch[32] = x;
+      scratch[65] = y;
+    }
+  }
+  __syncthreads();
+  a = scratch[32];
+  b = scratch[65];
+  __syncthreads();
+}
+
+}  // namespace attnres

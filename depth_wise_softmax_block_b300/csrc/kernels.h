@@ -1,0 +1,71 @@
+// Internal launch interface between the C ABI (attnres_abi.cu) and the kernels.
+// Arguments arrive here already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attnres {
+
+enum class IO { F32 = 0, BF16 = 1 };
+
+struct Phase1Args {
+  const void* reps;
+  int64_t src_stride;  // elements between sources
+  int n;               // sources
+  int64_t T;
+  int d;
+  const float* u;      // [S, d]
+  int S;
+  float eps;
+  void* o;             // [S, T, d]
+  float* m;            // [S, T] or null
+  float* lse;          // [S, T] or null
+  float* alpha;        // [S, T, n] or null
+};
+
+struct Phase2Args {
+  const void* o;
+  const float* lse;
+  const void* partial;
+  const void* v_prev;
+  void* partial_out;
+  int64_t T;
+  int d;
+  const float* u;
+  float eps_key;
+  const float* gamma_in;
+  float eps_in;
+  void* h;
+  void* y;
+  float* alpha_p;
+};
+
+constexpr int kMaxSources = 64;
+
+struct FullArgs {
+  const void* srcs[kMaxSources];
+  int n;
+  int64_t T;
+  int d;
+  const float* u;
+  float eps_key;
+  const float* gamma_in;
+  float eps_in;
+  void* h;
+  void* y;
+  float* alpha;
+};
+
+// Each launcher returns cudaSuccess or the launch error.
+cudaError_t launch_phase1(IO io, const Phase1Args& a, cudaStream_t s);
+// Returns false when the (n, S) combination does not fit the phase-1 kernel.
+bool phase1_supported(int n, int S);
+cudaError_t launch_phase2(IO io, const Phase2Args& a, cudaStream_t s);
+cudaError_t launch_full(IO io, const FullArgs& a, cudaStream_t s);
+cudaError_t launch_partial_update(IO io, const void* a, const void* b, void* out, int64_t n_elems,
+                                  cudaStream_t s);
+cudaError_t launch_query_prep(const float* w, const float* g, float* u, int64_t n_elems,
+                              cudaStream_t s);
+
+}  // namespace attnres

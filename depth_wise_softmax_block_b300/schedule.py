@@ -1,0 +1,129 @@
+"""Block AttnRes schedule on the GPU, driven through the C ABI.
+
+One block of S sublayers (page "Attention Residuals" note, §8 block definition and §10
+two-phase schedule):
+
+  1. phase 1: the block's S queries against the n completed sources b_0 .. b_{n-1};
+  2. for i = 1 .. S, phase 2 merges the partial source b^{i-1} and writes the sublayer input
+     y_i = RMSNorm_in(h_i).  The partial is built inside phase 2 from the previous sublayer's
+     output: b^1 = v_1 needs no write, b^{i-1} = b^{i-2} + v_{i-1} is written in place;
+  3. the block closes with b^S = b^{S-1} + v_S (the new completed source).
+
+Sublayer outputs v_i come from a caller-supplied function of y_i (the model's attention or
+MLP), which is where a real model would run f_i; the synthetic workloads hand back stand-ins.
+All buffers are allocated once by the caller-facing ``BlockRunner`` so a step allocates
+nothing.
+"""
+from __future__ import annotations
+
+from typing import Callable, Optional
+
+import torch
+
+from . import (attnres_full_reference_path, attnres_partial_update, attnres_phase1,
+               attnres_phase2_merge)
+
+
+class KernelTimer:
+    """CUDA events around each launch, on the current (launching) stream, grouped by kind.
+    Durations are read after the caller synchronises."""
+
+    def __init__(self):
+        self.events = {}
+
+    def wrap(self, kind: str, fn, *args, **kw):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        r = fn(*args, **kw)
+        b.record()
+        self.events.setdefault(kind, []).append((a, b))
+        return r
+
+    def totals_ms(self):
+        return {k: (sum(a.elapsed_time(b) for a, b in v), len(v)) for k, v in self.events.items()}
+
+    def clear(self):
+        self.events.clear()
+
+
+def _call(timer, kind, fn, *args, **kw):
+    return fn(*args, **kw) if timer is None else timer.wrap(kind, fn, *args, **kw)
+
+
+class BlockRunner:
+    """Work buffers for blocks of up to ``S_max`` sublayers over ``T`` tokens."""
+
+    def __init__(self, T: int, d: int, S_max: int, dtype, device, keep_y: bool = False,
+                 timer: Optional[KernelTimer] = None):
+        self.timer = timer
+        self.T, self.d, self.S_max = T, d, S_max
+        self.o = torch.empty((S_max, T, d), dtype=dtype, device=device)
+        self.lse = torch.empty((S_max, T), dtype=torch.float32, device=device)
+        self.partial = torch.empty((T, d), dtype=dtype, device=device)
+        self.keep_y = keep_y
+        n_y = S_max if keep_y else 1
+        self.y = torch.empty((n_y, T, d), dtype=dtype, device=device)
+
+    def y_buffer(self, i: int) -> torch.Tensor:
+        return self.y[i - 1] if self.keep_y else self.y[0]
+
+    def run_block(self, reps: torch.Tensor, U: torch.Tensor, G_in: Optional[torch.Tensor],
+                  sublayer: Callable[[int, torch.Tensor], torch.Tensor], close_out: torch.Tensor,
+                  eps_key: float = 1e-6, eps_in: float = 1e-6,
+                  on_call: Optional[Callable] = None) -> None:
+        """Run one block.
+
+        reps: [n, T, d] completed sources (any source stride); U: [S, d] folded queries;
+        G_in: [S, d] input-norm gains or None; sublayer(i, y_i) -> v_i ([T, d], 1-based i);
+        close_out: [T, d] receives b^S.  ``on_call(i, kind, args)`` is invoked before each
+        phase-2 call (tests use it to snapshot the exact inputs).
+        """
+        S = U.shape[0]
+        assert S <= self.S_max
+        o, lse = self.o[:S], self.lse[:S]
+        tm = self.timer
+        _call(tm, "phase1", attnres_phase1, reps, U, o, lse_out=lse, eps=eps_key)
+        v_prev = None       # v_{i-1}
+        part = None         # tensor holding b^{i-2} (None while it is zero)
+        for i in range(1, S + 1):
+            y = self.y_buffer(i)
+            g = None if G_in is None else G_in[i - 1]
+            if i == 1:
+                args = dict(partial=None, v_prev=None, partial_out=None)
+            elif i == 2:
+                args = dict(partial=v_prev, v_prev=None, partial_out=None)   # b^1 = v_1
+            else:
+                args = dict(partial=part, v_prev=v_prev, partial_out=self.partial)
+            if on_call is not None:
+                on_call(i, args)
+            kind = "phase2_first" if i == 1 else ("phase2" if i == 2 else "phase2_fused")
+            _call(tm, kind, attnres_phase2_merge, o[i - 1], lse[i - 1], args["partial"],
+                  args["v_prev"], args["partial_out"], U[i - 1], g, y, eps_key=eps_key,
+                  eps_in=eps_in)
+            # b^{i-1} now lives in args["partial"] (i == 2) or self.partial (i >= 3)
+            if i == 2:
+                part = v_prev
+            elif i >= 3:
+                part = self.partial
+            v_prev = sublayer(i, y)
+        # close: b^S = b^{S-1} + v_S  (b^{S-1} = v_1 when S == 2; b^1 = v_1 when S == 1)
+        if S == 1:
+            close_out.copy_(v_prev)
+        else:
+            _call(tm, "close", attnres_partial_update, part, v_prev, close_out)
+
+
+def final_aggregation(reps: torch.Tensor, u_final: torch.Tensor, out: torch.Tensor,
+                      eps: float = 1e-6, timer: Optional[KernelTimer] = None) -> torch.Tensor:
+    """Final output over b_0 .. b_N: phase 1 with the single extra pseudo-query."""
+    _call(timer, "final", attnres_phase1, reps, u_final.view(1, -1), out.view(1, *out.shape),
+          eps=eps)
+    return out
+
+
+def full_attnres_sublayer(history, u_l, g_in, y_out, h_out=None, alpha_out=None,
+                          eps_key: float = 1e-6, eps_in: float = 1e-6):
+    """Full AttnRes input of one sublayer over the explicit history v_0 .. v_{l-1}."""
+    return attnres_full_reference_path(list(history), u_l, g_in, h_out=h_out, y_out=y_out,
+                                       alpha_out=alpha_out, eps_key=eps_key, eps_in=eps_in)

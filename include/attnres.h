@@ -1,0 +1,162 @@
+/*
+ * attnres.h -- C ABI of the B300 (sm_103a) Attention Residuals (AttnRes) aggregation library.
+ *
+ * Before each sublayer l, every token replaces the fixed residual sum with softmax attention
+ * over depth.  A static per-sublayer pseudo-query w_l scores each source v as
+ * z = w_l . RMSNorm(v), and the sublayer input is h_l = sum_i softmax_i(z) v_i.
+ * ("Attention Residuals" note on arXiv 2603.15031, §7 Full AttnRes; §8 Block AttnRes.)
+ *
+ * Block AttnRes sources of sublayer l in block n at position i: the embedding b_0, the
+ * completed blocks b_1 .. b_{n-1}, and from i = 2 on the partial sum b_n^{i-1} (§8).
+ * The library runs the two-phase schedule (§10; "Attention Residuals 阅读补充", section
+ * "静态 Query 与两阶段计算"):
+ *   phase 1  scores all S queries of a block against the completed sources in one pass and
+ *            returns the normalised partial output plus (max, log-sum-exp);
+ *   phase 2  runs sublayer by sublayer, merges the partial-sum source by online softmax and
+ *            applies the sublayer's input RMSNorm in the same kernel.
+ *
+ * Conventions for every entry point
+ *   - Memory: every pointer is caller-owned.  "device" pointers must point to memory of the
+ *     current CUDA device; the library allocates nothing and keeps no state between calls.
+ *   - Layout: a [T, d] tensor is T rows of d contiguous elements (row stride d).
+ *   - dtype: ATTNRES_F32 stores float, ATTNRES_BF16 stores bfloat16 (round to nearest even);
+ *     arithmetic is fp32 in both cases.  Statistics (m, lse, alpha) are always fp32.
+ *   - Alignment: every device pointer must be 16-byte aligned and d a multiple of 8, so that
+ *     every row starts on a 16-byte boundary; otherwise ATTNRES_ERR_MISALIGNED /
+ *     ATTNRES_ERR_INVALID_ARG is returned and nothing is launched.
+ *   - Asynchrony: work is queued on `stream` (a cudaStream_t passed as void*, NULL = legacy
+ *     default stream).  No entry point synchronises.  Launch errors are reported as
+ *     ATTNRES_ERR_CUDA (the CUDA error string is available from attnres_last_cuda_error()).
+ *   - Errors: arguments are validated on the host before anything is launched; on any error
+ *     no kernel runs and the outputs are untouched.  No exception crosses the ABI.
+ *   - Aliasing: outputs must not overlap inputs, except where an entry point says so.
+ */
+#ifndef ATTNRES_H_
+#define ATTNRES_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTNRES_OK = 0,
+  ATTNRES_ERR_INVALID_ARG = 1,   /* null required pointer, non-positive size, bad enum     */
+  ATTNRES_ERR_UNSUPPORTED = 2,   /* sizes beyond the limits below                          */
+  ATTNRES_ERR_MISALIGNED = 3,    /* a device pointer or stride breaks 16-byte alignment    */
+  ATTNRES_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed            */
+} attnres_status;
+
+typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype;
+
+/* Limits (checked; larger values return ATTNRES_ERR_UNSUPPORTED). */
+#define ATTNRES_MAX_SOURCES 64     /* sources per call (phase 1 and the full path)          */
+#define ATTNRES_MAX_QUERIES 64     /* queries S per phase-1 call                             */
+#define ATTNRES_MAX_D 16384        /* hidden size (a row stays in registers)               */
+
+/* ABI version of this header; attnres_abi_version() returns the library's. */
+#define ATTNRES_ABI_VERSION 1
+int attnres_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* attnres_status_string(attnres_status status);
+
+/* Message of the last CUDA error seen by this thread's calls ("" if none). */
+const char* attnres_last_cuda_error(void);
+
+/*
+ * Query preparation (row a0): u = w ⊙ gamma_key, row by row.
+ * The key of a source is RMSNorm(v) = gamma_key ⊙ v / r(v) and the logit is w . RMSNorm(v)
+ * ("Attention Residuals" §7; "Attention Residuals 阅读补充", RMSNorm definition), so
+ * w . RMSNorm(v) = (w ⊙ gamma_key) . v / r(v).  The gain belongs to the target sublayer
+ * (one query and one set of key-norm gains per sublayer), so the product is a per-sublayer
+ * parameter: compute it once and pass u to the calls below.
+ *   w          device, fp32 [rows, d]
+ *   gamma_key  device, fp32 [rows, d], or NULL for all-ones gains (u = w)
+ *   u_out      device, fp32 [rows, d]; may alias w (in place)
+ */
+attnres_status attnres_query_prep(const float* w, const float* gamma_key, float* u_out,
+                                  int rows, int d, void* stream);
+
+/*
+ * Phase 1 (rows a1-a4): the S queries of one block against the n completed sources,
+ * one pass over the sources ("Attention Residuals" §10, step 1).
+ * For every token t and query s, with r_j = sqrt(mean_k b_j[t,k]^2 + eps) and
+ * z_j = u_s . b_j[t] / r_j:
+ *     m[s,t]   = max_j z_j
+ *     lse[s,t] = m + ln sum_j exp(z_j - m)
+ *     o[s,t,:] = sum_j exp(z_j - lse) b_j[t,:]           (normalised partial output)
+ *     alpha[s,t,j] = exp(z_j - lse)
+ *   reps        device [n_src][T][d] (io dtype): source j, token t at
+ *               reps + j*src_stride + t*d elements.  src_stride >= T*d, a multiple of 8.
+ *   u           device fp32 [S, d]: the block's queries with key gains folded in
+ *               (attnres_query_prep)
+ *   o_out       device [S][T][d] (io dtype), required
+ *   m_out, lse_out  device fp32 [S][T], each optional (NULL = not written)
+ *   alpha_out   device fp32 [S][T][n_src], optional
+ * Limits: 1 <= n_src <= 64, 1 <= S <= 64, n_src * S small enough for one CTA
+ * (n_src <= 36 when S > 24); otherwise ATTNRES_ERR_UNSUPPORTED.
+ * With S = 1 and the final pseudo-query this is also the final aggregation over
+ * b_0 .. b_N (row a10).
+ */
+attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, int64_t T,
+                              int d, attnres_dtype io, const float* u, int S, float eps,
+                              void* o_out, float* m_out, float* lse_out, float* alpha_out,
+                              void* stream);
+
+/*
+ * Phase 2 merge (rows a5-a8): one sublayer l of the block ("Attention Residuals" §10,
+ * step 2; "Attention Residuals 阅读补充", the merge of two partitions).
+ * The partial-sum source is p = partial + v_prev (a missing term counts as zero), rounded to
+ * the io dtype; with both NULL there is no partial source (first sublayer of the block,
+ * b_n^0 = 0 is not a source).  With r = sqrt(mean p^2 + eps_key), z_p = u_l . p / r,
+ * M = max(lse_l, z_p), a = exp(lse_l - M), c = exp(z_p - M):
+ *     h = (a o_l + c p) / (a + c)            (h = o_l when there is no partial source)
+ *     y = gamma_in ⊙ h / sqrt(mean h^2 + eps_in)
+ *   o_l          device [T, d] (io dtype): phase-1 output row block of this sublayer
+ *   lse_l        device fp32 [T]; required when there is a partial source
+ *   partial      device [T, d] (io dtype) or NULL: b_n^{i-2} (or b_n^{i-1} if v_prev is NULL)
+ *   v_prev       device [T, d] (io dtype) or NULL: output of the previous sublayer
+ *   partial_out  device [T, d] or NULL: receives p (the fused partial-sum update
+ *                b^{i-1} = b^{i-2} + v_{i-1}); may alias `partial`
+ *   u_l          device fp32 [d]: query of sublayer l with its key gain folded in
+ *   gamma_in     device fp32 [d] or NULL (all ones): input-norm gain of sublayer l
+ *   h_out        device [T, d] or NULL;  y_out device [T, d], required
+ *   alpha_p_out  device fp32 [T] or NULL: weight of the partial source, c / (a + c)
+ */
+attnres_status attnres_phase2_merge(const void* o_l, const float* lse_l, const void* partial,
+                                    const void* v_prev, void* partial_out, int64_t T, int d,
+                                    attnres_dtype io, const float* u_l, float eps_key,
+                                    const float* gamma_in, float eps_in, void* h_out,
+                                    void* y_out, float* alpha_p_out, void* stream);
+
+/*
+ * Partial-sum update / block close (rows a8-a9): out = partial + v, elementwise, rounded to
+ * the io dtype ("Attention Residuals" §8: b_n^i = b_n^{i-1} + f_i(h_i); the closed partial
+ * b_n^S becomes the next source).  `out` may alias `partial`.
+ */
+attnres_status attnres_partial_update(const void* partial, const void* v, void* out,
+                                      int64_t T, int d, attnres_dtype io, void* stream);
+
+/*
+ * Direct (single-pass, not two-phase) aggregation of one sublayer over an explicit list of
+ * sources: the plain Full AttnRes step ("Attention Residuals" §7), which is also the
+ * comparison point of the two-phase path.  Computes the same h and y as phase 2 would over
+ * the union of the sources.
+ *   srcs        HOST array of n_src device pointers, each [T, d] (io dtype)
+ *   u_l         device fp32 [d]; gamma_in device fp32 [d] or NULL
+ *   h_out       device [T, d] or NULL; y_out device [T, d] or NULL (at least one required)
+ *   alpha_out   device fp32 [T][n_src] or NULL
+ * Limits: 1 <= n_src <= 64.
+ */
+attnres_status attnres_full_reference_path(const void* const* srcs, int n_src, int64_t T,
+                                           int d, attnres_dtype io, const float* u_l,
+                                           float eps_key, const float* gamma_in,
+                                           float eps_in, void* h_out, void* y_out,
+                                           float* alpha_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ATTNRES_H_ */

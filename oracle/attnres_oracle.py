@@ -301,3 +301,31 @@ def logsumexp_bruteforce(z_row) -> float:
     """ln sum_i exp(z_i) for a short list, with math.fsum over math.exp: a slow scalar
     cross-check of the vectorised statistics (used only on tiny inputs)."""
     return math.log(math.fsum(math.exp(float(zi)) for zi in z_row))
+
+
+def single_block(completed, v, W, G_key, G_in, w_final, g_final, eps_key: float,
+                 eps_in: float) -> BlockWalk:
+    """One block over the given completed sources b_0 .. b_{n-1} ([n, T, d]): sublayer i
+    (1-based) reads the completed sources plus the partial b^{i-1} for i >= 2 (page 2 §8),
+    the block closes with b^S = sum of its outputs, and the final aggregation reads
+    b_0 .. b_{n-1}, b^S with the extra query (page 2 §8, last sentence).
+    v: [S, T, d]; W, G_key, G_in: [S, d] (None = ones for the gains)."""
+    completed = [_f64(b) for b in completed]
+    v = _f64(v)
+    out = BlockWalk()
+    partial = None
+    for i in range(1, v.shape[0] + 1):
+        srcs = block_sources(completed, partial)
+        gk = None if G_key is None else _f64(G_key)[i - 1]
+        gi = None if G_in is None else _f64(G_in)[i - 1]
+        h, y, alpha = sublayer_input(srcs, _f64(W)[i - 1], gk, eps_key, gi, eps_in)
+        out.h.append(h)
+        out.y.append(y)
+        out.alpha.append(alpha)
+        out.n_sources.append(srcs.shape[0])
+        out.partials.append(partial)
+        partial = v[i - 1].copy() if partial is None else partial + v[i - 1]
+    out.closed.append(partial)
+    fin, fin_alpha, _ = aggregate(np.stack(completed + [partial]), w_final, g_final, eps_key)
+    out.final, out.final_alpha = fin, fin_alpha
+    return out

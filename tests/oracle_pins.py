@@ -390,4 +390,19 @@ def pin_phase2_reference(O):
     assert p1 is None and a1.shape[0] == 3
 
 
+def pin_single_block_matches_walk(O):
+    """The one-block function over given sources equals the depth walk's first block when
+    the given source is the embedding alone (two code paths build the same source lists)."""
+    r = _rng(21)
+    L, T, d = 5, 3, 16
+    b0, v, given, W, Gk, Gi, wf, gf = _walk_inputs(r, L, T, d, 1)
+    walk = O.block_attnres_walk(b0, given, v, L, W, Gk, Gi, wf, gf, 1e-6, 1e-6, consistent=True)
+    one = O.single_block(b0[None], v, W, Gk, Gi, wf, gf, 1e-6, 1e-6)
+    for l in range(L):
+        _close(one.y[l], walk.y[l], 1e-13, f"y_{l+1}")
+        assert one.n_sources[l] == walk.n_sources[l]
+    _close(one.closed[0], v.sum(axis=0), 1e-12, "closed block = sum of outputs")
+    _close(one.final, walk.final, 1e-13, "final aggregation")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,126 @@
+"""The C-ABI library on the host, without a GPU: it builds for sm_103a, loads, exports every
+symbol include/attnres.h declares, and rejects bad arguments before launching anything.
+
+Every call here either fails validation or has T = 0 (nothing to launch), so no CUDA call is
+made and no device memory is touched; the fake pointers are never dereferenced."""
+import os
+import re
+
+import pytest
+
+import depth_wise_softmax_block_b300 as ar
+from depth_wise_softmax_block_b300 import build as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "attnres.h")
+OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
+P = 0x7F0000000000          # a 16-byte aligned fake address (never dereferenced)
+PM = P + 8                  # misaligned
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return ar.library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(attnres_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_symbols_exported(lib):
+    names = declared_symbols()
+    assert "attnres_phase1" in names and "attnres_phase2_merge" in names
+    assert "attnres_full_reference_path" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in attnres.h but not exported"
+    assert set(names) == set(ar.SIGNATURES), "binding signatures must cover the header"
+
+
+def test_version_and_strings(lib):
+    assert lib.attnres_abi_version() == 1
+    for code, name in ar.STATUS.items():
+        assert lib.attnres_status_string(code).decode() == name
+    assert lib.attnres_status_string(99).decode() == "ATTNRES_ERR_UNKNOWN"
+
+
+def p1(lib, reps=P, stride=1024 * 64, n=2, T=0, d=64, io=1, u=P, S=4, eps=1e-6, o=P):
+    return lib.attnres_phase1(reps, stride, n, T, d, io, u, S, eps, o, None, None, None, None)
+
+
+def test_phase1_validation(lib):
+    assert p1(lib) == OK                                  # T = 0: nothing to do
+    assert p1(lib, reps=None) == INVALID
+    assert p1(lib, u=None) == INVALID
+    assert p1(lib, o=None) == INVALID
+    assert p1(lib, io=7) == INVALID
+    assert p1(lib, d=60) == INVALID                       # d % 8
+    assert p1(lib, d=0) == INVALID
+    assert p1(lib, T=-1) == INVALID
+    assert p1(lib, n=0) == INVALID
+    assert p1(lib, S=0) == INVALID
+    assert p1(lib, eps=-1.0) == INVALID
+    assert p1(lib, eps=float("nan")) == INVALID
+    assert p1(lib, n=65) == UNSUPPORTED
+    assert p1(lib, S=65) == UNSUPPORTED
+    assert p1(lib, n=37, S=64) == UNSUPPORTED              # one CTA cannot hold the tile
+    assert p1(lib, n=36, S=64) == OK
+    assert p1(lib, n=64, S=24) == OK
+    assert p1(lib, d=16384 + 8) == UNSUPPORTED
+    assert p1(lib, T=10, stride=8) == INVALID              # sources would overlap
+    assert p1(lib, reps=PM) == MISALIGNED
+    assert p1(lib, u=PM) == MISALIGNED
+    assert p1(lib, o=PM) == MISALIGNED
+    assert p1(lib, stride=1024 * 64 + 4) == MISALIGNED     # source 1 would start misaligned
+
+
+def p2(lib, o=P, lse=P, part=None, v=None, pout=None, T=0, d=64, io=1, u=P, g=None, y=P, h=None):
+    return lib.attnres_phase2_merge(o, lse, part, v, pout, T, d, io, u, 1e-6, g, 1e-6, h, y, None,
+                                    None)
+
+
+def test_phase2_validation(lib):
+    assert p2(lib) == OK
+    assert p2(lib, part=P, v=P, pout=P) == OK
+    assert p2(lib, o=None) == INVALID
+    assert p2(lib, y=None) == INVALID
+    assert p2(lib, part=P, lse=None) == INVALID           # a partial source needs lse
+    assert p2(lib, v=P, u=None) == INVALID                # ... and the query
+    assert p2(lib, pout=P) == INVALID                     # nothing to write without a partial
+    assert p2(lib, d=12) == INVALID
+    assert p2(lib, io=2) == INVALID
+    assert p2(lib, o=PM) == MISALIGNED
+    assert p2(lib, part=PM) == MISALIGNED
+    assert p2(lib, v=P, g=PM) == MISALIGNED
+    assert p2(lib, h=PM) == MISALIGNED
+
+
+def test_full_and_update_validation(lib):
+    import ctypes
+    arr = (ctypes.c_void_p * 3)(P, P + 4096, P + 8192)
+    f = lib.attnres_full_reference_path
+    assert f(arr, 3, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None) == OK
+    assert f(None, 3, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None) == INVALID
+    assert f(arr, 0, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None) == INVALID
+    assert f(arr, 65, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None) == UNSUPPORTED
+    assert f(arr, 3, 0, 64, 1, P, 1e-6, None, 1e-6, None, None, None, None) == INVALID
+    bad = (ctypes.c_void_p * 2)(P, PM)
+    assert f(bad, 2, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None) == MISALIGNED
+    nul = (ctypes.c_void_p * 2)(P, None)
+    assert f(nul, 2, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None) == INVALID
+    up = lib.attnres_partial_update
+    assert up(P, P, P, 0, 64, 1, None) == OK
+    assert up(None, P, P, 0, 64, 1, None) == INVALID
+    assert up(P, P, PM, 0, 64, 1, None) == MISALIGNED
+    assert up(P, P, P, 0, 63, 1, None) == INVALID
+    qp = lib.attnres_query_prep
+    assert qp(P, None, P, 0, 64, None) == OK
+    assert qp(None, None, P, 0, 64, None) == INVALID
+    assert qp(P, PM, P, 0, 64, None) == MISALIGNED
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(ar, "_lib", None)
+    monkeypatch.setattr(ar, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        ar.library()

@@ -1,0 +1,246 @@
+"""GPU kernels (through the C ABI) against the fp64 oracle, element by element, on seeded
+inputs at sizes that span several tiles and a ragged tail.  Tolerances: parity_util.TOL."""
+import numpy as np
+import pytest
+import torch
+
+import depth_wise_softmax_block_b300 as ar
+from depth_wise_softmax_block_b300 import build as B
+import oracle.attnres_oracle as O
+from parity_util import TOL, check_close, check_outputs, to64
+from synth import inputs as I
+
+pytestmark = pytest.mark.gpu
+EPS = 1e-6
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    B.build()
+    ar.library()
+    return torch.device("cuda:0")
+
+
+def _dt(name):
+    return torch.float32 if name == "f32" else torch.bfloat16
+
+
+def make_reps(n, T, d, dtype, dev, seed, scale=1.0):
+    reps = torch.empty((n, T, d), dtype=dtype, device=dev)
+    for j in range(n):
+        I.fill_block_rep(reps[j], j, seed)
+    if scale != 1.0:
+        reps = (reps.float() * scale).to(dtype)
+    return reps
+
+
+def make_queries(S, d, dev, seed, jitter=0.02, scale=1.0, zero=False):
+    W = I.queries(S, d, seed, "w", dev, zero=zero) * scale
+    G = I.gains(S, d, jitter, seed, "g", dev)
+    U = torch.empty_like(W)
+    ar.attnres_query_prep(W, G, U)
+    return W, G, U
+
+
+def run_phase1(reps, U):
+    n, T, d = reps.shape
+    S = U.shape[0]
+    o = torch.empty((S, T, d), dtype=reps.dtype, device=reps.device)
+    m = torch.empty((S, T), dtype=torch.float32, device=reps.device)
+    lse = torch.empty_like(m)
+    alpha = torch.empty((S, T, n), dtype=torch.float32, device=reps.device)
+    ar.attnres_phase1(reps, U, o, m, lse, alpha, eps=EPS)
+    torch.cuda.synchronize()
+    return o, m, lse, alpha
+
+
+P1_CASES = [
+    # n, S, T, d, dtype
+    (1, 4, 64, 128, "f32"),
+    (2, 4, 64, 128, "f32"),
+    (3, 1, 64, 128, "f32"),
+    (1, 1, 1, 8, "f32"),            # smallest shape
+    (4, 64, 19, 256, "f32"),        # S at its maximum, ragged T
+    (9, 24, 37, 7168, "bf16"),      # the long-context block shape, ragged T
+    (9, 24, 100, 512, "bf16"),
+    (5, 18, 50, 2048, "bf16"),      # a tail block (S = 18)
+    (8, 24, 16, 200, "bf16"),       # d not a multiple of the 64-column stage
+    (10, 1, 33, 7168, "bf16"),      # final aggregation over 10 sources
+    (55, 1, 20, 2048, "bf16"),      # Full-AttnRes final aggregation (55 sources)
+    (64, 1, 9, 64, "bf16"),         # n at its maximum
+    (36, 64, 5, 64, "bf16"),        # largest n with S = 64
+    (7, 5, 23, 96, "f32"),
+]
+
+
+@pytest.mark.parametrize("n,S,T,d,dt", P1_CASES)
+def test_phase1_matches_oracle(dev, n, S, T, d, dt):
+    seed = 1000 + n * 7 + S
+    reps = make_reps(n, T, d, _dt(dt), dev, seed)
+    W, G, U = make_queries(S, d, dev, seed)
+    o, m, lse, alpha = run_phase1(reps, U)
+    oo, om, olse, oalpha = O.phase1(to64(reps), to64(W), to64(G), EPS)
+    tol = TOL[dt]
+    check_outputs(o, oo, dt, "o")
+    check_close(m, om, tol["stat"], "m")
+    check_close(lse, olse, tol["stat"], "lse")
+    check_close(alpha, oalpha, tol["weight"], "alpha")
+
+
+def test_phase1_chunk_view(dev):
+    """A token chunk of a larger cache: source stride != T*d and an offset base pointer."""
+    n, Ttot, d, S = 9, 300, 512, 24
+    reps_all = make_reps(n, Ttot, d, torch.bfloat16, dev, 77)
+    W, G, U = make_queries(S, d, dev, 77)
+    view = reps_all[:, 128:245]
+    o, m, lse, alpha = run_phase1(view, U)
+    oo, om, olse, oalpha = O.phase1(to64(view), to64(W), to64(G), EPS)
+    check_outputs(o, oo, "bf16", "o (chunk view)")
+    check_close(lse, olse, 1e-3, "lse (chunk view)")
+
+
+def test_phase1_zero_queries_give_mean(dev):
+    n, T, d, S = 6, 40, 256, 8
+    reps = make_reps(n, T, d, torch.float32, dev, 5)
+    W, G, U = make_queries(S, d, dev, 5, zero=True)
+    o, m, lse, alpha = run_phase1(reps, U)
+    check_close(alpha, np.full((S, T, n), 1.0 / n), 1e-6, "uniform weights")
+    mean = to64(reps).mean(axis=0)
+    check_outputs(o, np.broadcast_to(mean, (S, T, d)), "f32", "o = mean")
+    check_close(lse, np.full((S, T), np.log(n)), 1e-5, "lse = ln n")
+
+
+def test_phase1_extreme_logits(dev):
+    """Large queries push the softmax towards one-hot; max subtraction keeps it finite."""
+    n, T, d, S = 9, 24, 512, 24
+    reps = make_reps(n, T, d, torch.bfloat16, dev, 9)
+    W, G, U = make_queries(S, d, dev, 9, scale=60.0)
+    o, m, lse, alpha = run_phase1(reps, U)
+    oo, om, olse, oalpha = O.phase1(to64(reps), to64(W), to64(G), EPS)
+    assert float(to64(alpha).max()) > 0.999
+    check_outputs(o, oo, "bf16", "o (near one-hot)")
+    check_close(alpha, oalpha, 1e-3, "alpha (near one-hot)")
+    check_close(lse, olse, 2e-3 * max(1.0, float(np.abs(olse).max()) / 100), "lse")
+
+
+def test_phase1_deterministic(dev):
+    reps = make_reps(9, 50, 1024, torch.bfloat16, dev, 3)
+    _, _, U = make_queries(24, 1024, dev, 3)
+    a = run_phase1(reps, U)
+    b = run_phase1(reps, U)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+P2_MODES = ["first", "partial_only", "vprev_only", "fused", "fused_inplace"]
+
+
+@pytest.mark.parametrize("mode", P2_MODES)
+@pytest.mark.parametrize("n,T,d,dt", [(2, 64, 128, "f32"), (9, 45, 7168, "bf16"),
+                                       (3, 17, 2048, "bf16"), (1, 5, 8, "f32")])
+def test_phase2_matches_oracle(dev, mode, n, T, d, dt):
+    seed = 2000 + n + d
+    dtype = _dt(dt)
+    reps = make_reps(n, T, d, dtype, dev, seed)
+    W, G, U = make_queries(1, d, dev, seed)
+    o, m, lse, _ = run_phase1(reps, U)
+    G_in = I.gains(1, d, 0.05, seed, "gin", dev)[0]
+    part = I.normal((T, d), 1.5, seed, "part", dev, dtype)
+    vprev = I.normal((T, d), 1.0, seed, "vprev", dev, dtype)
+    partial = part if mode in ("partial_only", "fused", "fused_inplace") else None
+    v_prev = vprev if mode in ("vprev_only", "fused", "fused_inplace") else None
+    part_in = to64(part)
+    if mode == "fused":
+        pout = torch.empty_like(part)
+    elif mode == "fused_inplace":
+        pout = part
+    else:
+        pout = None
+    y = torch.empty((T, d), dtype=dtype, device=dev)
+    h = torch.empty_like(y)
+    ap = torch.empty((T,), dtype=torch.float32, device=dev)
+    has_p = partial is not None or v_prev is not None
+    ar.attnres_phase2_merge(o[0], lse[0], partial, v_prev, pout, U[0], G_in, y, h_out=h,
+                            alpha_p_out=ap if has_p else None, eps_key=EPS, eps_in=EPS)
+    torch.cuda.synchronize()
+    h_o, y_o, a_o, p_o = O.phase2_reference(
+        to64(reps), None if partial is None else part_in,
+        None if v_prev is None else to64(vprev), to64(W[0]), to64(G[0]), EPS, to64(G_in), EPS)
+    check_outputs(h, h_o, dt, "h")
+    check_outputs(y, y_o, dt, "y")
+    if has_p:
+        check_close(ap, a_o[-1], TOL[dt]["weight"], "weight of the partial source")
+    if pout is not None:   # the fused update is exactly round(partial + v_prev)
+        want = (torch.from_numpy(part_in).float() + vprev.float().cpu()).to(dtype)
+        assert torch.equal(pout.cpu(), want)
+
+
+@pytest.mark.parametrize("n,T,d,dt", [(3, 64, 128, "f32"), (12, 40, 2048, "bf16"),
+                                       (55, 9, 2048, "bf16"), (1, 3, 7168, "bf16"),
+                                       (64, 4, 64, "f32")])
+def test_full_path_matches_oracle(dev, n, T, d, dt):
+    seed = 3000 + n
+    dtype = _dt(dt)
+    srcs = [I.normal((T, d), 1.0 + 0.05 * j, seed, f"v{j}", dev, dtype) for j in range(n)]
+    W, G, U = make_queries(1, d, dev, seed)
+    G_in = I.gains(1, d, 0.05, seed, "gin", dev)[0]
+    y = torch.empty((T, d), dtype=dtype, device=dev)
+    h = torch.empty_like(y)
+    alpha = torch.empty((T, n), dtype=torch.float32, device=dev)
+    ar.attnres_full_reference_path(srcs, U[0], G_in, h_out=h, y_out=y, alpha_out=alpha,
+                                   eps_key=EPS, eps_in=EPS)
+    torch.cuda.synchronize()
+    src64 = np.stack([to64(s) for s in srcs])
+    h_o, y_o, a_o = O.sublayer_input(src64, to64(W[0]), to64(G[0]), EPS, to64(G_in), EPS)
+    check_outputs(h, h_o, dt, "h")
+    check_outputs(y, y_o, dt, "y")
+    check_close(alpha, a_o.T, TOL[dt]["weight"], "alpha")
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_partial_update_exact(dev, dt):
+    dtype = _dt(dt)
+    a = I.normal((333, 1024), 2.0, 1, "a", dev, dtype)
+    b = I.normal((333, 1024), 1.0, 1, "b", dev, dtype)
+    out = torch.empty_like(a)
+    ar.attnres_partial_update(a, b, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), (a.float().cpu() + b.float().cpu()).to(dtype))
+
+
+def test_query_prep_exact(dev):
+    W = I.queries(24, 7168, 4, "w", dev)
+    G = I.gains(24, 7168, 0.02, 4, "g", dev)
+    U = torch.empty_like(W)
+    ar.attnres_query_prep(W, G, U)
+    U2 = W.clone()
+    ar.attnres_query_prep(U2, None, U2)          # gamma NULL: copy, in place
+    torch.cuda.synchronize()
+    assert torch.equal(U.cpu(), W.cpu() * G.cpu())
+    assert torch.equal(U2.cpu(), W.cpu())
+
+
+def test_empty_T_is_a_noop(dev):
+    reps = torch.empty((3, 0, 64), dtype=torch.bfloat16, device=dev)
+    U = torch.zeros((2, 64), device=dev)
+    o = torch.empty((2, 0, 64), dtype=torch.bfloat16, device=dev)
+    ar.attnres_phase1(reps, U, o)
+    torch.cuda.synchronize()
+
+
+def test_scale_invariance_on_gpu(dev):
+    """At eps = 0, scaling a source by a > 0 leaves every weight unchanged (RMS-normalised
+    keys, raw values) -- checked on the GPU kernels directly."""
+    n, T, d, S = 4, 30, 256, 6
+    reps = make_reps(n, T, d, torch.float32, dev, 11)
+    _, _, U = make_queries(S, d, dev, 11)
+    base = torch.empty((S, T, n), device=dev)
+    o = torch.empty((S, T, d), device=dev)
+    ar.attnres_phase1(reps, U, o, alpha_out=base, eps=0.0)
+    reps2 = reps.clone()
+    reps2[2] *= 7.0
+    scaled = torch.empty_like(base)
+    ar.attnres_phase1(reps2, U, o, alpha_out=scaled, eps=0.0)
+    torch.cuda.synchronize()
+    check_close(scaled, base, 2e-6, "weights under source scaling")

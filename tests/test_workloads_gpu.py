@@ -1,0 +1,190 @@
+"""The five workloads on the GPU against the oracle.
+
+  tiny_block_f32       every element of every sublayer, Block walk vs the oracle walk
+                       (given and consistent block sums), plus the zero-query model
+  prefill_chunk_bf16   T = 16384, d = 7168, 186 sublayers: per-call parity on sampled rows
+  full_attnres_bf16    T = 8192, d = 2048, 54 sublayers: the direct path per sublayer, and
+                       the Block path with one sublayer per block equal to it (N = L)
+  decode_bf16          T = 256, d = 7168, 186 sublayers: per-call parity on sampled rows
+  longctx_prefill_bf16 the bench step (8 chunks of 16384 tokens over a [10, 131072, 7168]
+                       cache) in the launch configuration the bench times, sampled rows
+"""
+import numpy as np
+import pytest
+import torch
+
+import depth_wise_softmax_block_b300 as ar
+from depth_wise_softmax_block_b300 import build as B
+from depth_wise_softmax_block_b300.schedule import BlockRunner, final_aggregation
+import oracle.attnres_oracle as O
+from parity_util import TOL, check_close, check_outputs, sample_rows, to64
+from synth import inputs as I
+from walk_util import run_checked_block
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    B.build()
+    ar.library()
+    return torch.device("cuda:0")
+
+
+def folded(P, dev):
+    U = torch.empty_like(P.W)
+    ar.attnres_query_prep(P.W, P.G_key, U)
+    uf = torch.empty_like(P.w_final)
+    ar.attnres_query_prep(P.w_final.view(1, -1), P.g_final.view(1, -1), uf.view(1, -1))
+    return U, uf
+
+
+def gpu_block_walk(wl, reps, v, P, U, uf, dev, consistent=False):
+    """The whole depth on the GPU.  reps: [N+1, T, d] (slot 0 = b_0, given blocks after);
+    v: [L, T, d].  Returns (ys [L, T, d], final [T, d], closed blocks)."""
+    T, d, L, S = wl.T, wl.d, wl.L, wl.S
+    N = wl.n_blocks
+    runner = BlockRunner(T, d, S, wl.torch_dtype, dev, keep_y=True)
+    ys = torch.empty((L, T, d), dtype=wl.torch_dtype, device=dev)
+    src = reps.clone()
+    closed = torch.empty((N, T, d), dtype=wl.torch_dtype, device=dev)
+    for n in range(1, N + 1):
+        l0 = (n - 1) * S
+        Sn = min(S, L - l0)
+
+        def sublayer(i, y, l0=l0):
+            ys[l0 + i - 1].copy_(y)
+            return v[l0 + i - 1]
+
+        runner.run_block(src[:n], U[l0:l0 + Sn], P.G_in[l0:l0 + Sn], sublayer, closed[n - 1])
+        if consistent:
+            src[n].copy_(closed[n - 1])
+    fin = torch.empty((T, d), dtype=wl.torch_dtype, device=dev)
+    final_aggregation(src[:N + 1], uf, fin)
+    torch.cuda.synchronize()
+    return ys, fin, closed
+
+
+@pytest.mark.parametrize("zero", [False, True])
+@pytest.mark.parametrize("consistent", [False, True])
+def test_tiny_block_f32_every_element(dev, zero, consistent):
+    wl = I.TINY_BLOCK_F32
+    N = wl.n_blocks
+    reps = I.make_reps(wl, N + 1, dev)
+    v = I.make_outputs(wl, 1, wl.L, dev)
+    P = I.block_params(wl, dev, zero_queries=zero)
+    U, uf = folded(P, dev)
+    ys, fin, closed = gpu_block_walk(wl, reps, v, P, U, uf, dev, consistent)
+    ow = O.block_attnres_walk(to64(reps[0]), to64(reps[1:]), to64(v), wl.S, to64(P.W),
+                              to64(P.G_key), to64(P.G_in), to64(P.w_final), to64(P.g_final),
+                              wl.eps, wl.eps, consistent=consistent)
+    for l in range(wl.L):
+        check_outputs(ys[l], ow.y[l], "f32", f"y_{l + 1}")
+    for n in range(N):
+        check_outputs(closed[n], ow.closed[n], "f32", f"b_{n + 1}")
+    check_outputs(fin, ow.final, "f32", "final aggregation")
+
+
+def _block_walk_checked(wl, dev, rows_k, report):
+    T, d, L, S = wl.T, wl.d, wl.L, wl.S
+    N = wl.n_blocks
+    rows = sample_rows(T, rows_k, seed=wl.seed)
+    reps = I.make_reps(wl, N + 1, dev)
+    P = I.block_params(wl, dev)
+    U, uf = folded(P, dev)
+    runner = BlockRunner(T, d, S, wl.torch_dtype, dev)
+    vbuf = torch.empty((S, T, d), dtype=wl.torch_dtype, device=dev)
+    close = torch.empty((T, d), dtype=wl.torch_dtype, device=dev)
+    for n in range(1, N + 1):
+        l0 = (n - 1) * S
+        Sn = min(S, L - l0)
+        for i in range(Sn):
+            I.fill_sublayer_output(vbuf[i], l0 + i + 1, wl.seed)
+        run_checked_block(runner, reps[:n], U[l0:l0 + Sn], P.W[l0:l0 + Sn],
+                          P.G_key[l0:l0 + Sn], P.G_in[l0:l0 + Sn], vbuf[:Sn], close, "bf16",
+                          rows, report=report)
+    fin = torch.empty((T, d), dtype=wl.torch_dtype, device=dev)
+    final_aggregation(reps[:N + 1], uf, fin)
+    torch.cuda.synchronize()
+    want, _, _ = O.aggregate(to64(reps[:N + 1, rows]), to64(P.w_final), to64(P.g_final), wl.eps)
+    check_outputs(fin[rows], want, "bf16", "final aggregation", report)
+
+
+def test_prefill_chunk_bf16_sampled(dev):
+    report = {}
+    _block_walk_checked(I.PREFILL_CHUNK_BF16, dev, 40, report)
+    assert len([k for k in report if k.startswith("y_")]) > 0
+    print("max |err|/RMS over calls:", max(report.values()))
+
+
+def test_decode_bf16_sampled(dev):
+    report = {}
+    _block_walk_checked(I.DECODE_BF16, dev, 24, report)
+    print("max |err|/RMS over calls:", max(report.values()))
+
+
+def test_full_attnres_bf16(dev):
+    wl = I.FULL_INTERP_BF16
+    T, d, L = wl.T, wl.d, wl.L
+    rows = sample_rows(T, 32, seed=wl.seed)
+    hist = torch.empty((L + 1, T, d), dtype=torch.bfloat16, device=dev)
+    I.fill_sublayer_output(hist[0], 0, wl.seed, 0.0)               # v_0 ~ N(0, 1)
+    for l in range(1, L + 1):
+        I.fill_sublayer_output(hist[l], l, wl.seed, wl.v_growth)    # v_l ~ N(0,1)(1 + 0.05 l)
+    P = I.block_params(wl, dev)
+    U, uf = folded(P, dev)
+    y_full = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    h_full = torch.empty_like(y_full)
+    o = torch.empty((1, T, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((1, T), device=dev)
+    y_blk = torch.empty_like(y_full)
+    h64 = to64(hist[:, rows])
+    for l in range(1, L + 1):
+        srcs = [hist[j] for j in range(l)]
+        ar.attnres_full_reference_path(srcs, U[l - 1], P.G_in[l - 1], h_out=h_full, y_out=y_full)
+        # Block AttnRes with one sublayer per block: phase 1 over the same l sources, then
+        # phase 2 without a partial source
+        ar.attnres_phase1(hist[:l], U[l - 1:l], o, lse_out=lse)
+        ar.attnres_phase2_merge(o[0], lse[0], None, None, None, U[l - 1], P.G_in[l - 1], y_blk)
+        if l in (1, 2, 9, 27, 54) or l % 13 == 0:
+            _, y_o, _ = O.sublayer_input(h64[:l], to64(P.W[l - 1]), to64(P.G_key[l - 1]), wl.eps,
+                                         to64(P.G_in[l - 1]), wl.eps)
+            check_outputs(y_full[rows], y_o, "bf16", f"full y_{l}")
+            check_outputs(y_blk[rows], y_o, "bf16", f"block(N=L) y_{l}")
+        # the two GPU paths agree everywhere within the bf16 tolerance
+        check_outputs(y_blk, y_full, "bf16", f"block(N=L) vs full, l={l}")
+    fin = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    final_aggregation(hist, uf, fin)
+    torch.cuda.synchronize()
+    want, _, _ = O.aggregate(h64, to64(P.w_final), to64(P.g_final), wl.eps)
+    check_outputs(fin[rows], want, "bf16", "final aggregation (55 sources)")
+
+
+def test_longctx_prefill_bench_step_sampled(dev):
+    """The exact step the bench times, checked on sampled rows of every chunk."""
+    import bench
+    from depth_wise_softmax_block_b300.schedule import final_aggregation
+    wl = I.LONGCTX_PREFILL_BF16
+    st = bench.LongContextStep(wl, dev)
+    rows = sample_rows(wl.chunk, 12, seed=1)
+    report = {}
+    st.prep()
+    for c in range(st.nchunks):
+        reps_c, close_c, all_c, out_c = st.chunk_views(c)
+        rep = {}
+        run_checked_block(st.runner, reps_c, st.U, st.P.W, st.P.G_key, st.P.G_in, st.vbuf,
+                          close_c, "bf16", rows, wl.eps, rep)
+        final_aggregation(all_c, st.uf[0], out_c, wl.eps)
+        torch.cuda.synchronize()
+        want, _, _ = O.aggregate(to64(all_c[:, rows]), to64(st.P.w_final), to64(st.P.g_final),
+                                 wl.eps)
+        check_outputs(out_c[rows], want, "bf16", f"final chunk {c}", rep)
+        report.update({f"{k} chunk {c}": v for k, v in rep.items()})
+    assert len(report) == st.nchunks * (wl.S + 1)
+    # the timed step itself (no hooks) reproduces the checked outputs bit for bit
+    ref = st.out.clone()
+    st.run()
+    torch.cuda.synchronize()
+    assert torch.equal(st.out, ref)
+    print("max |err|/RMS over calls:", max(report.values()))
