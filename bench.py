@@ -203,14 +203,12 @@ def oracle_sample(wl: I.Workload, k: int, seed_offset: int = 0):
 
 def time_oracle(wl: I.Workload, k: int, seed_offset: int = 0):
     """Run the fp64 oracle (as it stands) over a k-token sample of one block; seconds."""
-    from threadpoolctl import threadpool_limits
     import oracle.attnres_oracle as O
     args = oracle_sample(wl, k, seed_offset)
-    with threadpool_limits(limits=1):
-        t0 = time.perf_counter()
-        O.single_block(args[0], args[1], args[2], args[3], args[4], args[5], args[6], wl.eps,
-                       wl.eps)
-        return time.perf_counter() - t0
+    t0 = time.perf_counter()     # elementwise numpy and reductions only: one thread
+    O.single_block(args[0], args[1], args[2], args[3], args[4], args[5], args[6], wl.eps,
+                   wl.eps)
+    return time.perf_counter() - t0
 
 
 # --------------------------------------------------------------------------------------------
@@ -332,6 +330,9 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--cpu-tokens", type=int, default=64)
     ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the token count (profiling a smaller case)")
+    ap.add_argument("--chunk", type=int, default=0, help="override the chunk size")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
 
@@ -349,6 +350,12 @@ def main(argv=None):
     from depth_wise_softmax_block_b300.schedule import KernelTimer
     B.build()
     wl = I.LONGCTX_PREFILL_BF16
+    if args.tokens or args.chunk:
+        import dataclasses
+        T = args.tokens or wl.T
+        ch = args.chunk or min(wl.chunk, T)
+        wl = dataclasses.replace(wl, T=T, chunk=ch,
+                                 name=f"longctx_prefill_bf16_T{T}_chunk{ch}_d7168_S24_n9")
     timer = KernelTimer()
     step = LongContextStep(wl, dev, timer=timer)
     for _ in range(args.warmup):

@@ -54,9 +54,11 @@ const char* attnres_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
 
 attnres_status attnres_query_prep(const float* w, const float* gamma_key, float* u_out, int rows,
                                   int d, void* stream) {
-  if (w == nullptr || u_out == nullptr || rows < 0) return ATTNRES_ERR_INVALID_ARG;
+  if (rows < 0) return ATTNRES_ERR_INVALID_ARG;
   const attnres_status sh = check_shape(rows, d);
   if (sh != ATTNRES_OK) return sh;
+  if (rows == 0) return ATTNRES_OK;
+  if (w == nullptr || u_out == nullptr) return ATTNRES_ERR_INVALID_ARG;
   if (!aligned16(w) || !aligned16(u_out) || !opt_aligned16(gamma_key))
     return ATTNRES_ERR_MISALIGNED;
   return cuda_status(attnres::launch_query_prep(w, gamma_key, u_out,
@@ -67,15 +69,16 @@ attnres_status attnres_query_prep(const float* w, const float* gamma_key, float*
 attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, int64_t T, int d,
                               attnres_dtype io, const float* u, int S, float eps, void* o_out,
                               float* m_out, float* lse_out, float* alpha_out, void* stream) {
-  if (reps == nullptr || u == nullptr || o_out == nullptr || !valid_io(io))
-    return ATTNRES_ERR_INVALID_ARG;
+  if (!valid_io(io)) return ATTNRES_ERR_INVALID_ARG;
   const attnres_status sh = check_shape(T, d);
   if (sh != ATTNRES_OK) return sh;
   if (n_src < 1 || S < 1 || !(eps >= 0.f)) return ATTNRES_ERR_INVALID_ARG;
   if (n_src > ATTNRES_MAX_SOURCES || S > ATTNRES_MAX_QUERIES) return ATTNRES_ERR_UNSUPPORTED;
+  if (!attnres::phase1_supported(n_src, S)) return ATTNRES_ERR_UNSUPPORTED;
+  if (T == 0) return ATTNRES_OK;
+  if (reps == nullptr || u == nullptr || o_out == nullptr) return ATTNRES_ERR_INVALID_ARG;
   if (n_src > 1 && src_stride < T * d) return ATTNRES_ERR_INVALID_ARG;
   if (src_stride < 0) return ATTNRES_ERR_INVALID_ARG;
-  if (!attnres::phase1_supported(n_src, S)) return ATTNRES_ERR_UNSUPPORTED;
   if (!aligned16(reps) || !aligned16(u) || !aligned16(o_out) || src_stride % 8 != 0)
     return ATTNRES_ERR_MISALIGNED;
   attnres::Phase1Args a{reps, src_stride, n_src, T, d, u, S, eps, o_out, m_out, lse_out, alpha_out};
@@ -88,9 +91,12 @@ attnres_status attnres_phase2_merge(const void* o_l, const float* lse_l, const v
                                     attnres_dtype io, const float* u_l, float eps_key,
                                     const float* gamma_in, float eps_in, void* h_out, void* y_out,
                                     float* alpha_p_out, void* stream) {
-  if (o_l == nullptr || y_out == nullptr || !valid_io(io)) return ATTNRES_ERR_INVALID_ARG;
+  if (!valid_io(io)) return ATTNRES_ERR_INVALID_ARG;
   const attnres_status sh = check_shape(T, d);
   if (sh != ATTNRES_OK) return sh;
+  if (!(eps_key >= 0.f) || !(eps_in >= 0.f)) return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (o_l == nullptr || y_out == nullptr) return ATTNRES_ERR_INVALID_ARG;
   const bool has_p = partial != nullptr || v_prev != nullptr;
   if (has_p && (lse_l == nullptr || u_l == nullptr)) return ATTNRES_ERR_INVALID_ARG;
   if (partial_out != nullptr && !has_p) return ATTNRES_ERR_INVALID_ARG;
@@ -107,10 +113,11 @@ attnres_status attnres_phase2_merge(const void* o_l, const float* lse_l, const v
 
 attnres_status attnres_partial_update(const void* partial, const void* v, void* out, int64_t T,
                                       int d, attnres_dtype io, void* stream) {
-  if (partial == nullptr || v == nullptr || out == nullptr || !valid_io(io))
-    return ATTNRES_ERR_INVALID_ARG;
+  if (!valid_io(io)) return ATTNRES_ERR_INVALID_ARG;
   const attnres_status sh = check_shape(T, d);
   if (sh != ATTNRES_OK) return sh;
+  if (T == 0) return ATTNRES_OK;
+  if (partial == nullptr || v == nullptr || out == nullptr) return ATTNRES_ERR_INVALID_ARG;
   if (!aligned16(partial) || !aligned16(v) || !aligned16(out)) return ATTNRES_ERR_MISALIGNED;
   return cuda_status(attnres::launch_partial_update(static_cast<IO>(io), partial, v, out, T * d,
                                                     static_cast<cudaStream_t>(stream)));
@@ -120,13 +127,15 @@ attnres_status attnres_full_reference_path(const void* const* srcs, int n_src, i
                                            attnres_dtype io, const float* u_l, float eps_key,
                                            const float* gamma_in, float eps_in, void* h_out,
                                            void* y_out, float* alpha_out, void* stream) {
-  if (srcs == nullptr || u_l == nullptr || !valid_io(io)) return ATTNRES_ERR_INVALID_ARG;
-  if (h_out == nullptr && y_out == nullptr) return ATTNRES_ERR_INVALID_ARG;
+  if (!valid_io(io)) return ATTNRES_ERR_INVALID_ARG;
   const attnres_status sh = check_shape(T, d);
   if (sh != ATTNRES_OK) return sh;
   if (n_src < 1) return ATTNRES_ERR_INVALID_ARG;
   if (n_src > ATTNRES_MAX_SOURCES) return ATTNRES_ERR_UNSUPPORTED;
   if (!(eps_key >= 0.f) || !(eps_in >= 0.f)) return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (srcs == nullptr || u_l == nullptr) return ATTNRES_ERR_INVALID_ARG;
+  if (h_out == nullptr && y_out == nullptr) return ATTNRES_ERR_INVALID_ARG;
   attnres::FullArgs a;
   memset(&a, 0, sizeof(a));
   for (int j = 0; j < n_src; ++j) {

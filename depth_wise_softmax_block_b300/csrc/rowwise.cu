@@ -63,10 +63,11 @@ __global__ void __launch_bounds__(kRowThreads) phase2_kernel(const Phase2Args a)
 #pragma unroll
           for (int e = 0; e < VE; ++e) x[e] += y[e];
         }
-        // The partial source is the stored (io-typed) tensor: round once, use the rounded value.
-        const uint4 pr = pack(x);
-        if (a.partial_out) st_global(static_cast<T*>(a.partial_out) + base + v * VE, pr);
-        unpack(pr, p[k]);
+        // The source is the exact fp32 sum; only the stored copy for the next sublayer is
+        // rounded to the io type.
+        if (a.partial_out) st_global(static_cast<T*>(a.partial_out) + base + v * VE, pack(x));
+#pragma unroll
+        for (int e = 0; e < VE; ++e) p[k][e] = x[e];
         const float4* u4 = reinterpret_cast<const float4*>(a.u + v * VE);
 #pragma unroll
         for (int e = 0; e < VE; e += 4) {

@@ -108,9 +108,9 @@ attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, i
 /*
  * Phase 2 merge (rows a5-a8): one sublayer l of the block ("Attention Residuals" §10,
  * step 2; "Attention Residuals 阅读补充", the merge of two partitions).
- * The partial-sum source is p = partial + v_prev (a missing term counts as zero), rounded to
- * the io dtype; with both NULL there is no partial source (first sublayer of the block,
- * b_n^0 = 0 is not a source).  With r = sqrt(mean p^2 + eps_key), z_p = u_l . p / r,
+ * The partial-sum source is p = partial + v_prev (a missing term counts as zero), summed in
+ * fp32 and used unrounded; with both NULL there is no partial source (first sublayer of the
+ * block, b_n^0 = 0 is not a source).  With r = sqrt(mean p^2 + eps_key), z_p = u_l . p / r,
  * M = max(lse_l, z_p), a = exp(lse_l - M), c = exp(z_p - M):
  *     h = (a o_l + c p) / (a + c)            (h = o_l when there is no partial source)
  *     y = gamma_in ⊙ h / sqrt(mean h^2 + eps_in)
@@ -118,8 +118,8 @@ attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, i
  *   lse_l        device fp32 [T]; required when there is a partial source
  *   partial      device [T, d] (io dtype) or NULL: b_n^{i-2} (or b_n^{i-1} if v_prev is NULL)
  *   v_prev       device [T, d] (io dtype) or NULL: output of the previous sublayer
- *   partial_out  device [T, d] or NULL: receives p (the fused partial-sum update
- *                b^{i-1} = b^{i-2} + v_{i-1}); may alias `partial`
+ *   partial_out  device [T, d] or NULL: receives p rounded to the io dtype (the fused
+ *                partial-sum update b^{i-1} = b^{i-2} + v_{i-1}); may alias `partial`
  *   u_l          device fp32 [d]: query of sublayer l with its key gain folded in
  *   gamma_in     device fp32 [d] or NULL (all ones): input-norm gain of sublayer l
  *   h_out        device [T, d] or NULL;  y_out device [T, d], required

@@ -329,3 +329,30 @@ def single_block(completed, v, W, G_key, G_in, w_final, g_final, eps_key: float,
     fin, fin_alpha, _ = aggregate(np.stack(completed + [partial]), w_final, g_final, eps_key)
     out.final, out.final_alpha = fin, fin_alpha
     return out
+
+
+def merge_reference(o_A, lse_A, p, w, gamma_key, eps_key: float, gamma_in, eps_in: float):
+    """Phase 2 of one sublayer on the inputs it receives: the statistics of partition A as
+    phase 1 hands them over (normalised o_A [T,d], lse_A [T]) and the partial source p [T,d]
+    (partition B = {p}, or None when the block has no partial yet).
+
+    The pages merge two partitions X in {A, B} from (m_X, l_X, o_X unnormalised) with the
+    common max m (page 1 two-phase section; page 2 §10).  A normalised o_A with its
+    log-sum-exp carries the same information: e^{m_A - m} o_A,unnorm = e^{lse_A - m} o_A and
+    e^{m_A - m} l_A = e^{lse_A - m}.  Partition B has m_B = z_p, l_B = 1, o_B = p, so
+        M = max(lse_A, z_p),  h = (e^{lse_A - M} o_A + e^{z_p - M} p) / (e^{lse_A - M} + e^{z_p - M}).
+    Returns (h, y = RMSNorm_in(h), weight of p)."""
+    o_A = _f64(o_A)
+    lse_A = _f64(lse_A)
+    if p is None:
+        h = o_A
+        a_p = np.zeros(o_A.shape[:-1])
+    else:
+        p = _f64(p)
+        z = depth_logits(p[None], w, gamma_key, eps_key)[0]
+        M = np.maximum(lse_A, z)
+        ca = np.exp(lse_A - M)
+        cb = np.exp(z - M)
+        h = (ca[..., None] * o_A + cb[..., None] * p) / (ca + cb)[..., None]
+        a_p = cb / (ca + cb)
+    return h, rmsnorm(h, gamma_in, eps_in), a_p

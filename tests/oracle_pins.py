@@ -405,4 +405,27 @@ def pin_single_block_matches_walk(O):
     _close(one.final, walk.final, 1e-13, "final aggregation")
 
 
+def pin_merge_reference(O):
+    """Phase 2 by the merge formula, fed phase 1's statistics of A, equals the direct
+    softmax over A plus the partial source (brute force over several A and p), and without a
+    partial it returns o_A itself."""
+    r = _rng(22)
+    n, T, d = 4, 6, 24
+    A = _sources(r, n, T, d)
+    w = r.normal(0.0, 0.5, size=d)
+    gk = r.normal(1.0, 0.1, size=d)
+    gi = r.normal(1.0, 0.1, size=d)
+    o, m, lse, _ = O.partition_stats(A, w, gk, 1e-6)
+    for scale in (0.1, 1.0, 10.0):
+        p = r.normal(0.0, scale, size=(T, d))
+        h, y, ap = O.merge_reference(o, lse, p, w, gk, 1e-6, gi, 1e-6)
+        h2, y2, a2 = O.sublayer_input(np.concatenate([A, p[None]]), w, gk, 1e-6, gi, 1e-6)
+        _close(h, h2, 1e-12 * scale, f"merge = direct, scale {scale}")
+        _close(y, y2, 1e-11, "y")
+        _close(ap, a2[-1], 1e-13, "weight of the partial")
+    h0, y0, a0 = O.merge_reference(o, lse, None, w, gk, 1e-6, gi, 1e-6)
+    _close(h0, o, 0.0, "no partial: h = o_A")
+    assert np.all(a0 == 0.0)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

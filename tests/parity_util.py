@@ -26,9 +26,9 @@ TOL = {
 
 
 def to64(t) -> np.ndarray:
-    if isinstance(t, np.ndarray):
-        return t.astype(np.float64)
-    return t.detach().float().cpu().numpy().astype(np.float64)
+    if isinstance(t, torch.Tensor):
+        return t.detach().float().cpu().numpy().astype(np.float64)
+    return np.asarray(t, dtype=np.float64)
 
 
 def ulp_bf16(x: np.ndarray) -> np.ndarray:
@@ -54,6 +54,37 @@ def check_outputs(got, want, dtype: str, what: str, report: dict | None = None):
         report[what] = rel
     assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; "
                            f"max |err|/RMS = {rel:.3e} (RMS {rms:.3e})")
+    return rel
+
+
+def check_two_phase(got, y_direct, o_A, w_A, r_h, gamma_in, dtype: str, what: str,
+                    report: dict | None = None):
+    """End-to-end check of a phase-2 output against the direct (one-softmax) definition.
+
+    Besides the per-call tolerance, the two-phase composition carries the storage rounding of
+    the phase-1 output o_A (bf16 when the I/O is bf16): |delta o_i| <= ulp(o_i) / 2 enters h
+    with the weight w_A of partition A, and y = gamma h / r(h) turns it into
+        |delta y_i| <= w_A (|gamma_i| |delta o_i| + |y_i| RMS(delta o)) / r(h)
+    (the second term bounds the change of r(h) by Cauchy-Schwarz).  A full ulp is used for
+    the half-ulp rounding as margin.  In fp32 mode the term is below 1e-6 and is dropped."""
+    g, w = to64(got), to64(y_direct)
+    tol = TOL[dtype]
+    rms = float(np.sqrt(np.mean(w * w)))
+    bound = tol["out_rel"] * rms
+    if dtype == "bf16":
+        uo = ulp_bf16(to64(o_A))
+        gam = np.ones(w.shape[-1]) if gamma_in is None else np.abs(to64(gamma_in))
+        wa = to64(w_A)[..., None]
+        rh = to64(r_h)[..., None]
+        rms_uo = np.sqrt(np.mean(uo * uo, axis=-1, keepdims=True))
+        bound = bound + ulp_bf16(w) + wa * (gam * uo + np.abs(w) * rms_uo) / rh
+    err = np.abs(g - w)
+    rel = float(err.max() / rms) if err.size else 0.0
+    if report is not None:
+        report[what] = rel
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} elements beyond the "
+                           f"two-phase bound; max |err|/RMS = {rel:.3e}")
     return rel
 
 

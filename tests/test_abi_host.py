@@ -1,8 +1,9 @@
 """The C-ABI library on the host, without a GPU: it builds for sm_103a, loads, exports every
 symbol include/attnres.h declares, and rejects bad arguments before launching anything.
 
-Every call here either fails validation or has T = 0 (nothing to launch), so no CUDA call is
-made and no device memory is touched; the fake pointers are never dereferenced."""
+Every call here either has T = 0 (nothing to launch; pointers may then be NULL) or fails
+validation, which happens before any launch: no CUDA call is made and the fake pointers are
+never dereferenced.  ``err()`` asserts that a call with T > 0 returned an error."""
 import os
 import re
 
@@ -15,6 +16,12 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "at
 OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
 P = 0x7F0000000000          # a 16-byte aligned fake address (never dereferenced)
 PM = P + 8                  # misaligned
+
+
+def err(status):
+    """A call with T > 0 must have failed validation (it would otherwise launch)."""
+    assert status != OK
+    return status
 
 
 @pytest.fixture(scope="module")
@@ -50,9 +57,10 @@ def p1(lib, reps=P, stride=1024 * 64, n=2, T=0, d=64, io=1, u=P, S=4, eps=1e-6, 
 
 def test_phase1_validation(lib):
     assert p1(lib) == OK                                  # T = 0: nothing to do
-    assert p1(lib, reps=None) == INVALID
-    assert p1(lib, u=None) == INVALID
-    assert p1(lib, o=None) == INVALID
+    assert p1(lib, reps=None, u=None, o=None) == OK       # ... and pointers may be NULL
+    assert err(p1(lib, T=4, reps=None)) == INVALID
+    assert err(p1(lib, T=4, u=None)) == INVALID
+    assert err(p1(lib, T=4, o=None)) == INVALID
     assert p1(lib, io=7) == INVALID
     assert p1(lib, d=60) == INVALID                       # d % 8
     assert p1(lib, d=0) == INVALID
@@ -67,11 +75,11 @@ def test_phase1_validation(lib):
     assert p1(lib, n=36, S=64) == OK
     assert p1(lib, n=64, S=24) == OK
     assert p1(lib, d=16384 + 8) == UNSUPPORTED
-    assert p1(lib, T=10, stride=8) == INVALID              # sources would overlap
-    assert p1(lib, reps=PM) == MISALIGNED
-    assert p1(lib, u=PM) == MISALIGNED
-    assert p1(lib, o=PM) == MISALIGNED
-    assert p1(lib, stride=1024 * 64 + 4) == MISALIGNED     # source 1 would start misaligned
+    assert err(p1(lib, T=10, stride=8)) == INVALID         # sources would overlap
+    assert err(p1(lib, T=4, reps=PM)) == MISALIGNED
+    assert err(p1(lib, T=4, u=PM)) == MISALIGNED
+    assert err(p1(lib, T=4, o=PM)) == MISALIGNED
+    assert err(p1(lib, T=4, stride=1024 * 64 + 4)) == MISALIGNED  # source 1 misaligned
 
 
 def p2(lib, o=P, lse=P, part=None, v=None, pout=None, T=0, d=64, io=1, u=P, g=None, y=P, h=None):
@@ -81,18 +89,19 @@ def p2(lib, o=P, lse=P, part=None, v=None, pout=None, T=0, d=64, io=1, u=P, g=No
 
 def test_phase2_validation(lib):
     assert p2(lib) == OK
+    assert p2(lib, o=None, y=None, u=None, lse=None) == OK
     assert p2(lib, part=P, v=P, pout=P) == OK
-    assert p2(lib, o=None) == INVALID
-    assert p2(lib, y=None) == INVALID
-    assert p2(lib, part=P, lse=None) == INVALID           # a partial source needs lse
-    assert p2(lib, v=P, u=None) == INVALID                # ... and the query
-    assert p2(lib, pout=P) == INVALID                     # nothing to write without a partial
+    assert err(p2(lib, T=4, o=None)) == INVALID
+    assert err(p2(lib, T=4, y=None)) == INVALID
+    assert err(p2(lib, T=4, part=P, lse=None)) == INVALID  # a partial source needs lse
+    assert err(p2(lib, T=4, v=P, u=None)) == INVALID       # ... and the query
+    assert err(p2(lib, T=4, pout=P)) == INVALID            # nothing to write without a partial
     assert p2(lib, d=12) == INVALID
     assert p2(lib, io=2) == INVALID
-    assert p2(lib, o=PM) == MISALIGNED
-    assert p2(lib, part=PM) == MISALIGNED
-    assert p2(lib, v=P, g=PM) == MISALIGNED
-    assert p2(lib, h=PM) == MISALIGNED
+    assert err(p2(lib, T=4, o=PM)) == MISALIGNED
+    assert err(p2(lib, T=4, part=PM)) == MISALIGNED
+    assert err(p2(lib, T=4, v=P, g=PM)) == MISALIGNED
+    assert err(p2(lib, T=4, h=PM)) == MISALIGNED
 
 
 def test_full_and_update_validation(lib):
@@ -100,23 +109,23 @@ def test_full_and_update_validation(lib):
     arr = (ctypes.c_void_p * 3)(P, P + 4096, P + 8192)
     f = lib.attnres_full_reference_path
     assert f(arr, 3, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None) == OK
-    assert f(None, 3, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None) == INVALID
+    assert err(f(None, 3, 4, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None)) == INVALID
     assert f(arr, 0, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None) == INVALID
     assert f(arr, 65, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None) == UNSUPPORTED
-    assert f(arr, 3, 0, 64, 1, P, 1e-6, None, 1e-6, None, None, None, None) == INVALID
+    assert err(f(arr, 3, 4, 64, 1, P, 1e-6, None, 1e-6, None, None, None, None)) == INVALID
     bad = (ctypes.c_void_p * 2)(P, PM)
-    assert f(bad, 2, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None) == MISALIGNED
+    assert err(f(bad, 2, 4, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None)) == MISALIGNED
     nul = (ctypes.c_void_p * 2)(P, None)
-    assert f(nul, 2, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None) == INVALID
+    assert err(f(nul, 2, 4, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None)) == INVALID
     up = lib.attnres_partial_update
     assert up(P, P, P, 0, 64, 1, None) == OK
-    assert up(None, P, P, 0, 64, 1, None) == INVALID
-    assert up(P, P, PM, 0, 64, 1, None) == MISALIGNED
+    assert err(up(None, P, P, 4, 64, 1, None)) == INVALID
+    assert err(up(P, P, PM, 4, 64, 1, None)) == MISALIGNED
     assert up(P, P, P, 0, 63, 1, None) == INVALID
     qp = lib.attnres_query_prep
     assert qp(P, None, P, 0, 64, None) == OK
-    assert qp(None, None, P, 0, 64, None) == INVALID
-    assert qp(P, PM, P, 0, 64, None) == MISALIGNED
+    assert err(qp(None, None, P, 4, 64, None)) == INVALID
+    assert err(qp(P, PM, P, 4, 64, None)) == MISALIGNED
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

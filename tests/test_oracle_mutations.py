@@ -81,7 +81,14 @@ def _block_of_off_by_one(l, S):             # blocks start one sublayer late
     return n, l - (n - 1) * S + 1
 
 
+def _merge_ignores_lse(o_A, lse_A, p, w, gamma_key, eps_key, gamma_in, eps_in):  # drops e^{lse}
+    h, y, a = _ORIG_MERGE(o_A, np.zeros_like(np.asarray(lse_A, np.float64)), p, w, gamma_key,
+                          eps_key, gamma_in, eps_in)
+    return h, y, a
+
+
 _ORIG_PARTITION = O.partition_stats
+_ORIG_MERGE = O.merge_reference
 
 MUTATIONS = {
     "rms_sum_not_mean": ("rms", _rms_sum),
@@ -97,6 +104,7 @@ MUTATIONS = {
     "o_unnormalised": ("partition_stats", _partition_unnormalised),
     "zero_partial_source": ("block_sources", _block_sources_zero_partial),
     "block_index_off_by_one": ("block_of", _block_of_off_by_one),
+    "merge_ignores_lse": ("merge_reference", _merge_ignores_lse),
 }
 
 

@@ -7,7 +7,7 @@ import torch
 import depth_wise_softmax_block_b300 as ar
 from depth_wise_softmax_block_b300 import build as B
 import oracle.attnres_oracle as O
-from parity_util import TOL, check_close, check_outputs, to64
+from parity_util import TOL, check_close, check_outputs, check_two_phase, to64
 from synth import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -164,13 +164,25 @@ def test_phase2_matches_oracle(dev, mode, n, T, d, dt):
     ar.attnres_phase2_merge(o[0], lse[0], partial, v_prev, pout, U[0], G_in, y, h_out=h,
                             alpha_p_out=ap if has_p else None, eps_key=EPS, eps_in=EPS)
     torch.cuda.synchronize()
-    h_o, y_o, a_o, p_o = O.phase2_reference(
+    p_exact = None
+    if has_p:
+        p_exact = (part_in if partial is not None else 0.0) + \
+                  (to64(vprev) if v_prev is not None else 0.0)
+    # per call: the oracle gets exactly what the call received (o_l, lse_l, partial, v_prev)
+    h_m, y_m, a_m = O.merge_reference(to64(o[0]), to64(lse[0]), p_exact, to64(W[0]),
+                                      to64(G[0]), EPS, to64(G_in), EPS)
+    check_outputs(h, h_m, dt, "h (per call)")
+    check_outputs(y, y_m, dt, "y (per call)")
+    if has_p:
+        check_close(ap, a_m, TOL[dt]["weight"], "weight of the partial source")
+    # end to end: phase 1 + phase 2 against the direct softmax over all the sources
+    h_o, y_o, a_o, _ = O.phase2_reference(
         to64(reps), None if partial is None else part_in,
         None if v_prev is None else to64(vprev), to64(W[0]), to64(G[0]), EPS, to64(G_in), EPS)
-    check_outputs(h, h_o, dt, "h")
-    check_outputs(y, y_o, dt, "y")
-    if has_p:
-        check_close(ap, a_o[-1], TOL[dt]["weight"], "weight of the partial source")
+    oA, _, _, _ = O.phase1(to64(reps), to64(W[:1]), to64(G[:1]), EPS)
+    wA = 1.0 - (a_o[-1] if has_p else 0.0)
+    rh = O.rms(h_o, EPS)
+    check_two_phase(y, y_o, oA[0], wA, rh, to64(G_in), dt, "y (two-phase vs direct)")
     if pout is not None:   # the fused update is exactly round(partial + v_prev)
         want = (torch.from_numpy(part_in).float() + vprev.float().cpu()).to(dtype)
         assert torch.equal(pout.cpu(), want)
