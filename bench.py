@@ -268,7 +268,7 @@ def reference_arm(args, world, rank):
 
 def traffic_for(kernel: str):
     """dram bytes per launch from a committed ncu summary, if it matches the current source."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    p = os.path.join(ROOT, "profiles", "dram_traffic_longctx_T4096.json")
     if not os.path.exists(p):
         return None
     j = json.load(open(p))
