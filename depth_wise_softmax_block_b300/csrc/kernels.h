@@ -54,7 +54,9 @@ struct FullArgs {
   float eps_in;
   void* h;
   void* y;
-  float* alpha;
+  float* alpha;     // [T][n] or null
+  float* m;         // [T] or null: max logit
+  float* lse;       // [T] or null: log-sum-exp of the logits
 };
 
 // Each launcher returns cudaSuccess or the launch error.

@@ -6,13 +6,19 @@
 // One CTA owns a tile of TT tokens and runs two sweeps over the hidden dimension d:
 //   sweep 1  streams the tile's source rows [n][TT][64 columns] and the query slice [S][64]
 //            through a 3-stage cp.async pipeline in shared memory.  Each warp takes one
-//            8-column octet of every stage; each lane accumulates the logits numerators
-//            u_s . b_j[t] of (NS sources x NQ queries) of one token plus the sums of squares.
-//   reduce   partial sums of the 8 warps are added in a fixed order (deterministic), then
-//            one thread per (token, query) forms r_j, z_j, m, lse and alpha.
-//   sweep 2  streams the same source rows again and writes o[s,t,:] = sum_j alpha_j b_j[t,:]
-//            with 16-byte coalesced stores.
-// Arithmetic is fp32 throughout; o is rounded once to the I/O type.
+//            8-column octet of every stage; each lane accumulates the logit numerators
+//            u_s . b_j[t] of (NS sources x NQ queries) of one token and the sums of squares,
+//            with packed fp32 FMAs over column pairs (even and odd columns are summed
+//            separately and added at the end).
+//   reduce   the 8 warps' partial sums are added in a fixed order (deterministic), then one
+//            thread per (token, query) forms r_j, z_j, m, lse and alpha.
+//   sweep 2  streams the same source rows again (from L2 when they are still there) and
+//            writes o[s,t,:] = sum_j alpha_j b_j[t,:] with 16-byte streaming stores.
+// Arithmetic is fp32 throughout; o is rounded once to the I/O type.  A single query (S = 1,
+// the final aggregation) has no logits to share across queries and runs on the row-wise
+// single-pass kernel instead.
+#include <string.h>
+
 #include <algorithm>
 
 #include "common.cuh"
@@ -44,12 +50,11 @@ inline int next_pow2(int x) {
 }
 inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-// Register-tile shape (NS sources x NQ queries per lane) for a given S.
+// Register-tile shape (NS sources x NQ queries per lane) for S >= 2.
 inline void tile_shape(int S, int& NS, int& NQ) {
-  if (S == 1) { NS = 16; NQ = 1; }
-  else if (S <= 4) { NS = 9; NQ = 4; }
+  if (S <= 4) { NS = 9; NQ = 4; }
   else if (S <= 24) { NS = 9; NQ = 6; }
-  else { NS = 9; NQ = 8; }
+  else { NS = 4; NQ = 8; }
 }
 
 bool make_plan(int n, int S, int E, P1Plan& p) {
@@ -69,10 +74,46 @@ bool make_plan(int n, int S, int E, P1Plan& p) {
     const int area0 = std::max(kStages * p.stageBytes, kThreads * p.RS * 4);
     p.offDots = align_up(area0, 16);
     p.offAlpha = align_up(p.offDots + p.TT * n * (S + 1) * 4, 16);
-    p.smem = p.offAlpha + p.TT * n * p.QG * 8 * 4;
+    p.smem = p.offAlpha + p.TT * n * p.QG * NQ * 2 * 4;
     if (p.smem <= kMaxSmem) return true;
   }
   return false;
+}
+
+// Streaming (evict-first) store of the phase-1 output, which phase 2 reads once much later.
+__device__ __forceinline__ void st_stream(void* p, uint4 v) {
+  __stcs(reinterpret_cast<uint4*>(p), v);
+}
+
+// Eight consecutive elements as four (even, odd) column pairs.
+template <typename T> __device__ __forceinline__ void load_pairs(const void* p, float2 (&f)[4]);
+template <> __device__ __forceinline__ void load_pairs<bf16>(const void* p, float2 (&f)[4]) {
+  const uint4 v = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+}
+template <> __device__ __forceinline__ void load_pairs<float>(const void* p, float2 (&f)[4]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  f[0] = make_float2(a.x, a.y);
+  f[1] = make_float2(a.z, a.w);
+  f[2] = make_float2(b.x, b.y);
+  f[3] = make_float2(b.z, b.w);
+}
+
+template <typename T> __device__ __forceinline__ void store_pairs(void* p, const float2 (&f)[4]);
+template <> __device__ __forceinline__ void store_pairs<bf16>(void* p, const float2 (&f)[4]) {
+  st_stream(p, make_uint4(pack_bf16x2(f[0].x, f[0].y), pack_bf16x2(f[1].x, f[1].y),
+                          pack_bf16x2(f[2].x, f[2].y), pack_bf16x2(f[3].x, f[3].y)));
+}
+template <> __device__ __forceinline__ void store_pairs<float>(void* p, const float2 (&f)[4]) {
+  st_stream(p, make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y),
+                          __float_as_uint(f[1].x), __float_as_uint(f[1].y)));
+  st_stream(static_cast<char*>(p) + 16,
+            make_uint4(__float_as_uint(f[2].x), __float_as_uint(f[2].y),
+                       __float_as_uint(f[3].x), __float_as_uint(f[3].y)));
 }
 
 template <typename IOT, int NS, int NQ>
@@ -117,18 +158,18 @@ phase1_kernel(const Phase1Args a, const P1Plan pl) {
     }
   };
 
-  // ---------------- sweep 1: logits numerators and sums of squares ----------------
+  // ---------------- sweep 1: logit numerators and sums of squares ----------------
   const bool active1 = lane < TT * SG * QG;
   const int g = lane % QG;
   const int sg = (lane / QG) % SG;
   const int tl = lane / (QG * SG);
-  float acc[NS][NQ];
-  float ss[NS];
+  float2 acc[NS][NQ];
+  float2 ss[NS];
 #pragma unroll
   for (int jj = 0; jj < NS; ++jj) {
-    ss[jj] = 0.f;
+    ss[jj] = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int qq = 0; qq < NQ; ++qq) acc[jj][qq] = 0.f;
+    for (int qq = 0; qq < NQ; ++qq) acc[jj][qq] = make_float2(0.f, 0.f);
   }
 
 #pragma unroll
@@ -144,14 +185,14 @@ phase1_kernel(const Phase1Args a, const P1Plan pl) {
     if (active1) {
       const unsigned char* st = smem + (c % kStages) * pl.stageBytes;
       const unsigned char* ut = st + pl.bBytes + g * kUnit + warp * 32;
-      float uv[NQ][8];
+      float2 uv[NQ][4];
 #pragma unroll
       for (int qq = 0; qq < NQ; ++qq) {
         if (g * NQ + qq < S) {  // padded queries of the last group read nothing
-          load8<float>(ut + (g * NQ + qq) * pl.uRowB, uv[qq]);
+          load_pairs<float>(ut + (g * NQ + qq) * pl.uRowB, uv[qq]);
         } else {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) uv[qq][k] = 0.f;
+          for (int i = 0; i < 4; ++i) uv[qq][i] = make_float2(0.f, 0.f);
         }
       }
       const unsigned char* bt = st + tl * pl.rowB + warp * 8 * E;
@@ -159,15 +200,14 @@ phase1_kernel(const Phase1Args a, const P1Plan pl) {
       for (int jj = 0; jj < NS; ++jj) {
         const int j = sg * NS + jj;
         if (j < n) {
-          float bv[8];
-          load8<IOT>(bt + j * TT * pl.rowB, bv);
+          float2 bv[4];
+          load_pairs<IOT>(bt + j * TT * pl.rowB, bv);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) ss[jj] = fmaf(bv[k], bv[k], ss[jj]);
+          for (int i = 0; i < 4; ++i) ss[jj] = __ffma2_rn(bv[i], bv[i], ss[jj]);
 #pragma unroll
-          for (int qq = 0; qq < NQ; ++qq) {
+          for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int k = 0; k < 8; ++k) acc[jj][qq] = fmaf(uv[qq][k], bv[k], acc[jj][qq]);
-          }
+            for (int qq = 0; qq < NQ; ++qq) acc[jj][qq] = __ffma2_rn(uv[qq][i], bv[i], acc[jj][qq]);
         }
       }
     }
@@ -182,8 +222,8 @@ phase1_kernel(const Phase1Args a, const P1Plan pl) {
 #pragma unroll
     for (int jj = 0; jj < NS; ++jj) {
 #pragma unroll
-      for (int qq = 0; qq < NQ; ++qq) r[jj * NQ + qq] = acc[jj][qq];
-      r[NS * NQ + jj] = ss[jj];
+      for (int qq = 0; qq < NQ; ++qq) r[jj * NQ + qq] = acc[jj][qq].x + acc[jj][qq].y;
+      r[NS * NQ + jj] = ss[jj].x + ss[jj].y;
     }
   }
   __syncthreads();
@@ -209,7 +249,8 @@ phase1_kernel(const Phase1Args a, const P1Plan pl) {
   }
 
   // ---------------- softmax statistics, one thread per (token, query) ----------------
-  float* alph = reinterpret_cast<float*>(smem + pl.offAlpha);  // [TT][n][QG][8]
+  // alpha is stored twice, (a, a), so sweep 2 reads ready-made pairs: [TT][n][QG][NQ][2]
+  float* alph = reinterpret_cast<float*>(smem + pl.offAlpha);
   const float fd = static_cast<float>(d);
   for (int i = tid; i < TT * S; i += kThreads) {
     const int t = i / S, s = i % S;
@@ -229,7 +270,9 @@ phase1_kernel(const Phase1Args a, const P1Plan pl) {
     for (int j = 0; j < n; ++j) {
       const float z = dt[j * S1 + s] / sqrtf(dt[j * S1 + S] / fd + a.eps);
       const float al = expf(z - m) / l;
-      alph[((t * n + j) * QG + s / NQ) * 8 + s % NQ] = al;
+      float* ap = alph + (((t * n + j) * QG + s / NQ) * NQ + s % NQ) * 2;
+      ap[0] = al;
+      ap[1] = al;
       if (a.alpha != nullptr && tok < T) a.alpha[(static_cast<int64_t>(s) * T + tok) * n + j] = al;
     }
     if (tok < T) {
@@ -250,27 +293,35 @@ phase1_kernel(const Phase1Args a, const P1Plan pl) {
     cp_async_commit();
     if (active2) {
       const unsigned char* bt = smem + (c % kStages) * pl.stageBytes + t2 * pl.rowB + kg * 8 * E;
-      const float* at = alph + (t2 * n * QG + g2) * 8;
-      float acc2[NQ][8];
+      const float* at = alph + (t2 * n * QG + g2) * NQ * 2;
+      float2 acc2[NQ][4];
 #pragma unroll
       for (int qq = 0; qq < NQ; ++qq)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) acc2[qq][k] = 0.f;
+        for (int i = 0; i < 4; ++i) acc2[qq][i] = make_float2(0.f, 0.f);
       for (int j = 0; j < n; ++j) {
-        float bv[8], al[8];
-        load8<IOT>(bt + j * TT * pl.rowB, bv);
-        load8<float>(at + j * QG * 8, al);
+        float2 bv[4];
+        load_pairs<IOT>(bt + j * TT * pl.rowB, bv);
+        float2 al[NQ];
+        const float4* ap = reinterpret_cast<const float4*>(at + j * QG * NQ * 2);
+#pragma unroll
+        for (int h = 0; h < NQ / 2; ++h) {
+          const float4 f = ap[h];
+          al[2 * h] = make_float2(f.x, f.y);
+          al[2 * h + 1] = make_float2(f.z, f.w);
+        }
 #pragma unroll
         for (int qq = 0; qq < NQ; ++qq)
 #pragma unroll
-          for (int k = 0; k < 8; ++k) acc2[qq][k] = fmaf(al[qq], bv[k], acc2[qq][k]);
+          for (int i = 0; i < 4; ++i) acc2[qq][i] = __ffma2_rn(al[qq], bv[i], acc2[qq][i]);
       }
       const int k = c * KC + kg * 8;
       if (tok2 < T && k < d) {
 #pragma unroll
         for (int qq = 0; qq < NQ; ++qq) {
           const int q = g2 * NQ + qq;
-          if (q < S) store8<IOT>(o + ((static_cast<int64_t>(q) * T + tok2) * d + k) * E, acc2[qq]);
+          if (q < S)
+            store_pairs<IOT>(o + ((static_cast<int64_t>(q) * T + tok2) * d + k) * E, acc2[qq]);
         }
       }
     }
@@ -294,21 +345,38 @@ cudaError_t launch_io(const Phase1Args& a, cudaStream_t s) {
   if (!make_plan(a.n, a.S, sizeof(T), pl)) return cudaErrorInvalidValue;
   int NS, NQ;
   tile_shape(a.S, NS, NQ);
-  if (NQ == 1) return launch_t<T, 16, 1>(a, pl, s);
   if (NQ == 4) return launch_t<T, 9, 4>(a, pl, s);
   if (NQ == 6) return launch_t<T, 9, 6>(a, pl, s);
-  return launch_t<T, 9, 8>(a, pl, s);
+  return launch_t<T, 4, 8>(a, pl, s);
 }
 
 }  // namespace
 
 bool phase1_supported(int n, int S) {
+  if (S == 1) return n >= 1 && n <= kMaxSources;
   P1Plan pl;
   return make_plan(n, S, 4, pl) && make_plan(n, S, 2, pl);
 }
 
 cudaError_t launch_phase1(IO io, const Phase1Args& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
+  if (a.S == 1) {  // one query: the row-wise single-pass kernel, sources at base + j * stride
+    FullArgs f;
+    memset(&f, 0, sizeof(f));
+    const int64_t E = io == IO::BF16 ? 2 : 4;
+    for (int j = 0; j < a.n; ++j)
+      f.srcs[j] = static_cast<const char*>(a.reps) + j * a.src_stride * E;
+    f.n = a.n;
+    f.T = a.T;
+    f.d = a.d;
+    f.u = a.u;
+    f.eps_key = a.eps;
+    f.h = a.o;
+    f.alpha = a.alpha;
+    f.m = a.m;
+    f.lse = a.lse;
+    return launch_full(io, f, s);
+  }
   return io == IO::BF16 ? launch_io<bf16>(a, s) : launch_io<float>(a, s);
 }
 

@@ -19,10 +19,11 @@
 namespace attnres {
 namespace {
 
-constexpr int kRowThreads = 256;  // at most one CTA of 256 threads per row
+constexpr int kRowThreads = 256;    // full path: at most 256 threads per row
+constexpr int kMergeThreads = 512;  // phase 2: at most 512 threads per row (fewer registers)
 
 template <typename T, int VPT>
-__global__ void __launch_bounds__(kRowThreads) phase2_kernel(const Phase2Args a) {
+__global__ void __launch_bounds__(kMergeThreads) phase2_kernel(const Phase2Args a) {
   constexpr int VE = Vec<T>::N;
   __shared__ float scratch[66];
   const int64_t row = blockIdx.x;
@@ -221,11 +222,20 @@ __global__ void __launch_bounds__(kRowThreads) full_kernel(const FullArgs a) {
       acc[k][e] *= rl;
       ssh = fmaf(acc[k][e], acc[k][e], ssh);
     }
-  block_sum2(ssh, unused, scratch);  // its barriers also publish zs[]
-  const float inv = 1.f / sqrtf(ssh / fd + a.eps_in);
+  float inv = 0.f;
+  if (a.y != nullptr) {  // uniform over the CTA
+    block_sum2(ssh, unused, scratch);  // its barriers also publish zs[]
+    inv = 1.f / sqrtf(ssh / fd + a.eps_in);
+  } else {
+    __syncthreads();  // publish zs[]
+  }
 
+  const float lse = mrun + logf(lrun);
+  if (threadIdx.x == 0) {
+    if (a.m != nullptr) a.m[row] = mrun;
+    if (a.lse != nullptr) a.lse[row] = lse;
+  }
   if (a.alpha != nullptr) {
-    const float lse = mrun + logf(lrun);
     for (int j = threadIdx.x; j < a.n; j += blockDim.x)
       a.alpha[row * a.n + j] = expf(zs[j] - lse);
   }
@@ -286,16 +296,16 @@ __global__ void prep_kernel(const float* w, const float* g, float* u, int64_t n4
 }
 
 // Vectors per thread and threads per CTA for a row of nv 16-byte vectors.
-inline void row_geometry(int nv, int& vpt, int& threads) {
+inline void row_geometry(int nv, int& vpt, int& threads, int max_threads = kRowThreads) {
   vpt = 1;
-  while ((nv + vpt - 1) / vpt > kRowThreads) vpt *= 2;
+  while ((nv + vpt - 1) / vpt > max_threads) vpt *= 2;
   threads = ((nv + vpt - 1) / vpt + 31) / 32 * 32;
 }
 
 template <typename T>
 cudaError_t phase2_io(const Phase2Args& a, cudaStream_t s) {
   int vpt, threads;
-  row_geometry(a.d / Vec<T>::N, vpt, threads);
+  row_geometry(a.d / Vec<T>::N, vpt, threads, kMergeThreads);
   const unsigned grid = static_cast<unsigned>(a.T);
   switch (vpt) {
     case 1: phase2_kernel<T, 1><<<grid, threads, 0, s>>>(a); break;

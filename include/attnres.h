@@ -95,8 +95,8 @@ attnres_status attnres_query_prep(const float* w, const float* gamma_key, float*
  *   o_out       device [S][T][d] (io dtype), required
  *   m_out, lse_out  device fp32 [S][T], each optional (NULL = not written)
  *   alpha_out   device fp32 [S][T][n_src], optional
- * Limits: 1 <= n_src <= 64, 1 <= S <= 64, n_src * S small enough for one CTA
- * (n_src <= 36 when S > 24); otherwise ATTNRES_ERR_UNSUPPORTED.
+ * Limits: 1 <= n_src <= 64, 1 <= S <= 64, and n_src <= 16 when S > 24 (the per-token tile
+ * must fit one CTA); otherwise ATTNRES_ERR_UNSUPPORTED.
  * With S = 1 and the final pseudo-query this is also the final aggregation over
  * b_0 .. b_N (row a10).
  */

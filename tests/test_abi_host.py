@@ -71,8 +71,9 @@ def test_phase1_validation(lib):
     assert p1(lib, eps=float("nan")) == INVALID
     assert p1(lib, n=65) == UNSUPPORTED
     assert p1(lib, S=65) == UNSUPPORTED
-    assert p1(lib, n=37, S=64) == UNSUPPORTED              # one CTA cannot hold the tile
-    assert p1(lib, n=36, S=64) == OK
+    assert p1(lib, n=17, S=64) == UNSUPPORTED              # one CTA cannot hold the tile
+    assert p1(lib, n=16, S=64) == OK
+    assert p1(lib, n=64, S=1) == OK
     assert p1(lib, n=64, S=24) == OK
     assert p1(lib, d=16384 + 8) == UNSUPPORTED
     assert err(p1(lib, T=10, stride=8)) == INVALID         # sources would overlap

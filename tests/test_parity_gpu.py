@@ -69,7 +69,9 @@ P1_CASES = [
     (10, 1, 33, 7168, "bf16"),      # final aggregation over 10 sources
     (55, 1, 20, 2048, "bf16"),      # Full-AttnRes final aggregation (55 sources)
     (64, 1, 9, 64, "bf16"),         # n at its maximum
-    (36, 64, 5, 64, "bf16"),        # largest n with S = 64
+    (16, 64, 5, 64, "bf16"),        # largest n with S = 64
+    (64, 2, 11, 64, "bf16"),        # n at its maximum with two queries
+    (2, 2, 70, 136, "f32"),
     (7, 5, 23, 96, "f32"),
 ]
 
