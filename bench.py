@@ -296,20 +296,36 @@ def run_e2e(step: LongContextStep, iters: int):
     h2d = h_reps.numel() * 2 + h_v.numel() * 2 + sum(h.numel() * 4 for h in h_params)
     d2h = h_out.numel() * 2
 
+    # Copies overlap the kernels: host-to-device on one stream, device-to-host on another,
+    # the kernels on the current stream; events order each chunk's copies and compute.
+    compute = torch.cuda.current_stream()
+    up = torch.cuda.Stream()
+    down = torch.cuda.Stream()
+
     def one():
-        for h, p in zip(h_params, params):
-            p.copy_(h, non_blocking=True)
-        step.vbuf.copy_(h_v, non_blocking=True)
+        with torch.cuda.stream(up):
+            for h, p in zip(h_params, params):
+                p.copy_(h, non_blocking=True)
+            step.vbuf.copy_(h_v, non_blocking=True)
         ch = wl.chunk
         for c in range(step.nchunks):
             sl = slice(c * ch, (c + 1) * ch)
-            for j in range(step.n):
-                step.reps[j, sl].copy_(h_reps[j, sl], non_blocking=True)
+            with torch.cuda.stream(up):
+                for j in range(step.n):
+                    step.reps[j, sl].copy_(h_reps[j, sl], non_blocking=True)
+                landed = torch.cuda.Event()
+                landed.record(up)
+            compute.wait_event(landed)
             if c == 0:
                 step.prep()
             step.run_chunk(c)
-            h_out[sl].copy_(step.out[sl], non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+            done = torch.cuda.Event()
+            done.record(compute)
+            with torch.cuda.stream(down):
+                down.wait_event(done)
+                h_out[sl].copy_(step.out[sl], non_blocking=True)
+        for s in (up, compute, down):
+            s.synchronize()
 
     one()
     t0 = time.perf_counter()
@@ -328,8 +344,10 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=2)
-    ap.add_argument("--cpu-tokens", type=int, default=64)
-    ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--cpu-tokens", type=int, default=512,
+                    help="oracle sample for cpu_baseline (about 10 s of one core)")
+    ap.add_argument("--ref-tokens", type=int, default=64,
+                    help="oracle sample per step of the reference arm (about 1 s)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the token count (profiling a smaller case)")
     ap.add_argument("--chunk", type=int, default=0, help="override the chunk size")

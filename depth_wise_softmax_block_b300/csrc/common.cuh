@@ -135,4 +135,31 @@ __device__ __forceinline__ void block_sum2(float& a, float& b, float* scratch) {
   __syncthreads();
 }
 
+// Sum of N values over the whole CTA with one set of barriers; every thread gets the totals.
+// `scratch` holds at least N * 33 floats of shared memory.
+template <int N>
+__device__ __forceinline__ void block_sum_n(float (&v)[N], float* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int i = 0; i < N; ++i) v[i] = warp_sum(v[i]);
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) scratch[i * 33 + warp] = v[i];
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      float x = lane < nw ? scratch[i * 33 + lane] : 0.f;
+      x = warp_sum(x);
+      if (lane == 0) scratch[i * 33 + 32] = x;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < N; ++i) v[i] = scratch[i * 33 + 32];
+  __syncthreads();
+}
+
 }  // namespace attnres

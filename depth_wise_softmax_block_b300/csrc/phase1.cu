@@ -36,6 +36,7 @@ constexpr int kMaxSmem = 227 * 1024;
 
 struct P1Plan {
   int SG, QG, TT;       // source groups, query groups, tokens per CTA
+  int ttShift;          // log2(TT): TT is a power of two
   int rowB, uRowB;      // bytes per staged (source, token) row / query row
   int bBytes, stageBytes;
   int RS;               // floats per thread in the cross-warp reduction buffer (odd)
@@ -75,6 +76,8 @@ bool make_plan(int n, int S, int E, P1Plan& p) {
     p.offDots = align_up(area0, 16);
     p.offAlpha = align_up(p.offDots + p.TT * n * (S + 1) * 4, 16);
     p.smem = p.offAlpha + p.TT * n * p.QG * NQ * 2 * 4;
+    p.ttShift = 0;
+    while ((1 << p.ttShift) < p.TT) ++p.ttShift;
     if (p.smem <= kMaxSmem) return true;
   }
   return false;
@@ -136,8 +139,8 @@ phase1_kernel(const Phase1Args a, const P1Plan pl) {
     const int k0 = c * KC;
     const int nb = n * TT * UPR;
     for (int i = tid; i < nb; i += kThreads) {
-      const int unit = i % UPR, row = i / UPR;  // row = j * TT + t
-      const int t = row % TT, j = row / TT;
+      const int unit = i % UPR, row = i / UPR;  // row = j * TT + t (TT a power of two)
+      const int t = row & (TT - 1), j = row >> pl.ttShift;
       const int k = k0 + unit * (kUnit / E);
       const bool ok = (t0 + t < T) && (k < d);
       const char* src =
