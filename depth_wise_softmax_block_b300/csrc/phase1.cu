@@ -205,12 +205,13 @@ phase1_kernel(const Phase1Args a, const P1Plan pl) {
         if (j < n) {
           float2 bv[4];
           load_pairs<IOT>(bt + j * TT * pl.rowB, bv);
+          // the sum-of-squares chain is spread between independent dot-product updates
 #pragma unroll
-          for (int i = 0; i < 4; ++i) ss[jj] = __ffma2_rn(bv[i], bv[i], ss[jj]);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
+          for (int i = 0; i < 4; ++i) {
+            ss[jj] = __ffma2_rn(bv[i], bv[i], ss[jj]);
 #pragma unroll
             for (int qq = 0; qq < NQ; ++qq) acc[jj][qq] = __ffma2_rn(uv[qq][i], bv[i], acc[jj][qq]);
+          }
         }
       }
     }
@@ -302,16 +303,29 @@ phase1_kernel(const Phase1Args a, const P1Plan pl) {
       for (int qq = 0; qq < NQ; ++qq)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc2[qq][i] = make_float2(0.f, 0.f);
+      // The next source's octet and alpha pairs are read from shared memory while the
+      // current source is accumulated (the trip count n is a runtime value).
+      float2 bv[4], bn[4];
+      float4 af[NQ / 2], an[NQ / 2];
+      load_pairs<IOT>(bt, bn);
+#pragma unroll
+      for (int h = 0; h < NQ / 2; ++h) an[h] = reinterpret_cast<const float4*>(at)[h];
       for (int j = 0; j < n; ++j) {
-        float2 bv[4];
-        load_pairs<IOT>(bt + j * TT * pl.rowB, bv);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) bv[i] = bn[i];
+#pragma unroll
+        for (int h = 0; h < NQ / 2; ++h) af[h] = an[h];
+        if (j + 1 < n) {
+          load_pairs<IOT>(bt + (j + 1) * TT * pl.rowB, bn);
+          const float4* ap = reinterpret_cast<const float4*>(at + (j + 1) * QG * NQ * 2);
+#pragma unroll
+          for (int h = 0; h < NQ / 2; ++h) an[h] = ap[h];
+        }
         float2 al[NQ];
-        const float4* ap = reinterpret_cast<const float4*>(at + j * QG * NQ * 2);
 #pragma unroll
         for (int h = 0; h < NQ / 2; ++h) {
-          const float4 f = ap[h];
-          al[2 * h] = make_float2(f.x, f.y);
-          al[2 * h + 1] = make_float2(f.z, f.w);
+          al[2 * h] = make_float2(af[h].x, af[h].y);
+          al[2 * h + 1] = make_float2(af[h].z, af[h].w);
         }
 #pragma unroll
         for (int qq = 0; qq < NQ; ++qq)

@@ -141,12 +141,12 @@ __global__ void __launch_bounds__(kMergeThreads) phase2_kernel(const Phase2Args 
   }
 }
 
-// Sources are taken G at a time: every load of a group is in flight at once, and one CTA
-// reduction returns the group's G sums of squares and G dot products.
-template <typename T, int VPT, int G>
+// Online softmax over the sources, one source per step, with the rows of the next two sources
+// already in flight (two register buffers; the source loop is unrolled by two).
+template <typename T, int VPT>
 __global__ void __launch_bounds__(kRowThreads) full_kernel(const FullArgs a) {
   constexpr int VE = Vec<T>::N;
-  __shared__ float scratch[2 * G * 33];
+  __shared__ float scratch[66];
   __shared__ float zs[kMaxSources];
   const int64_t row = blockIdx.x;
   const int nv = a.d / VE;
@@ -160,76 +160,63 @@ __global__ void __launch_bounds__(kRowThreads) full_kernel(const FullArgs a) {
     for (int e = 0; e < VE; ++e) acc[k][e] = 0.f;
   float mrun = -INFINITY, lrun = 0.f;
 
-  for (int j0 = 0; j0 < a.n; j0 += G) {
-    uint4 raw[G][VPT];
+  auto load = [&](uint4 (&r)[VPT], int j) {
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-#pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        const int v = threadIdx.x + k * blockDim.x;
-        raw[g][k] = make_uint4(0u, 0u, 0u, 0u);  // zeros are bf16 and fp32 zeros
-        if (j0 + g < a.n && v < nv)
-          raw[g][k] = ld_stream(static_cast<const T*>(a.srcs[j0 + g]) + base + v * VE);
-      }
+    for (int k = 0; k < VPT; ++k) {
+      const int v = threadIdx.x + k * blockDim.x;
+      r[k] = make_uint4(0u, 0u, 0u, 0u);  // zeros are bf16 and fp32 zeros
+      if (v < nv) r[k] = ld_stream(static_cast<const T*>(a.srcs[j]) + base + v * VE);
     }
-    float red[2 * G];  // [sum of squares of source g, dot of source g]
+  };
+  // Score source j (held in x), then fold it into the running max, sum and accumulator.
+  auto fold = [&](const float (&x)[VPT][VE], int j) {
+    float ss = 0.f, dot = 0.f;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float ss = 0.f, dot = 0.f;
+    for (int k = 0; k < VPT; ++k) {
+      const int v = threadIdx.x + k * blockDim.x;
+      if (v < nv) {
+        const float4* u4 = reinterpret_cast<const float4*>(a.u + v * VE);
 #pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        const int v = threadIdx.x + k * blockDim.x;
-        if (v < nv) {
-          float x[VE];
-          unpack(raw[g][k], x);
-          const float4* u4 = reinterpret_cast<const float4*>(a.u + v * VE);
-#pragma unroll
-          for (int e = 0; e < VE; e += 4) {
-            const float4 uu = __ldg(u4 + e / 4);
-            dot = fmaf(uu.x, x[e], dot);
-            dot = fmaf(uu.y, x[e + 1], dot);
-            dot = fmaf(uu.z, x[e + 2], dot);
-            dot = fmaf(uu.w, x[e + 3], dot);
-          }
-#pragma unroll
-          for (int e = 0; e < VE; ++e) ss = fmaf(x[e], x[e], ss);
+        for (int e = 0; e < VE; e += 4) {
+          const float4 uu = __ldg(u4 + e / 4);
+          dot = fmaf(uu.x, x[k][e], dot);
+          dot = fmaf(uu.y, x[k][e + 1], dot);
+          dot = fmaf(uu.z, x[k][e + 2], dot);
+          dot = fmaf(uu.w, x[k][e + 3], dot);
         }
-      }
-      red[2 * g] = ss;
-      red[2 * g + 1] = dot;
-    }
-    block_sum_n<2 * G>(red, scratch);
-    float z[G];
-    float mnew = mrun;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      z[g] = red[2 * g + 1] / sqrtf(red[2 * g] / fd + a.eps_key);
-      if (j0 + g < a.n) {
-        mnew = fmaxf(mnew, z[g]);
-        if (threadIdx.x == 0) zs[j0 + g] = z[g];
+        for (int e = 0; e < VE; ++e) ss = fmaf(x[k][e], x[k][e], ss);
       }
     }
-    const float sc = expf(mrun - mnew);  // 0 for the first group (mrun = -inf)
-    lrun *= sc;
+    block_sum2(ss, dot, scratch);
+    const float z = dot / sqrtf(ss / fd + a.eps_key);
+    if (threadIdx.x == 0) zs[j] = z;
+    const float mnew = fmaxf(mrun, z);
+    const float sc = expf(mrun - mnew);  // 0 for the first source (mrun = -inf)
+    const float ez = expf(z - mnew);
+    lrun = lrun * sc + ez;
+    mrun = mnew;
 #pragma unroll
     for (int k = 0; k < VPT; ++k)
 #pragma unroll
-      for (int e = 0; e < VE; ++e) acc[k][e] *= sc;
+      for (int e = 0; e < VE; ++e) acc[k][e] = fmaf(acc[k][e], sc, ez * x[k][e]);
+  };
+
+  uint4 bufA[VPT], bufB[VPT];
+  load(bufA, 0);
+  if (a.n > 1) load(bufB, 1);
+  for (int j = 0; j < a.n; j += 2) {
+    float x[VPT][VE];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      if (j0 + g < a.n) {
-        const float ez = expf(z[g] - mnew);
-        lrun += ez;
+    for (int k = 0; k < VPT; ++k) unpack(bufA[k], x[k]);
+    if (j + 2 < a.n) load(bufA, j + 2);
+    fold(x, j);
+    if (j + 1 < a.n) {  // uniform over the CTA
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-          float x[VE];
-          unpack(raw[g][k], x);
-#pragma unroll
-          for (int e = 0; e < VE; ++e) acc[k][e] = fmaf(ez, x[e], acc[k][e]);
-        }
-      }
+      for (int k = 0; k < VPT; ++k) unpack(bufB[k], x[k]);
+      if (j + 3 < a.n) load(bufB, j + 3);
+      fold(x, j + 1);
     }
-    mrun = mnew;
   }
 
   const float rl = 1.f / lrun;
@@ -342,13 +329,12 @@ cudaError_t full_io(const FullArgs& a, cudaStream_t s) {
   int vpt, threads;
   row_geometry(a.d / Vec<T>::N, vpt, threads);
   const unsigned grid = static_cast<unsigned>(a.T);
-  // G sources per group: G * vpt 16-byte loads in flight per thread (at most 16)
   switch (vpt) {
-    case 1: full_kernel<T, 1, 4><<<grid, threads, 0, s>>>(a); break;
-    case 2: full_kernel<T, 2, 4><<<grid, threads, 0, s>>>(a); break;
-    case 4: full_kernel<T, 4, 4><<<grid, threads, 0, s>>>(a); break;
-    case 8: full_kernel<T, 8, 2><<<grid, threads, 0, s>>>(a); break;
-    case 16: full_kernel<T, 16, 1><<<grid, threads, 0, s>>>(a); break;
+    case 1: full_kernel<T, 1><<<grid, threads, 0, s>>>(a); break;
+    case 2: full_kernel<T, 2><<<grid, threads, 0, s>>>(a); break;
+    case 4: full_kernel<T, 4><<<grid, threads, 0, s>>>(a); break;
+    case 8: full_kernel<T, 8><<<grid, threads, 0, s>>>(a); break;
+    case 16: full_kernel<T, 16><<<grid, threads, 0, s>>>(a); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
