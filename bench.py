@@ -392,6 +392,8 @@ def main(argv=None):
         end.record()
         torch.cuda.synchronize()
     barrier(world)
+    from depth_wise_softmax_block_b300 import attnres_poll_device_errors
+    attnres_poll_device_errors()      # raises if a kernel's bounded wait gave up
     ms = start.elapsed_time(end) / args.steps
     ms = reduce_max(ms, world)
     tokens = wl.T * world

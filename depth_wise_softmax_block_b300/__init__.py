@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libattnres.so")
 
 F32, BF16 = 0, 1
 STATUS = {0: "ATTNRES_OK", 1: "ATTNRES_ERR_INVALID_ARG", 2: "ATTNRES_ERR_UNSUPPORTED",
-          3: "ATTNRES_ERR_MISALIGNED", 4: "ATTNRES_ERR_CUDA"}
+          3: "ATTNRES_ERR_MISALIGNED", 4: "ATTNRES_ERR_CUDA", 5: "ATTNRES_ERR_TIMEOUT"}
 
 # C signatures (argument types, in order) of every exported symbol of include/attnres.h.
 _P, _I, _I64, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
@@ -26,6 +26,7 @@ SIGNATURES = {
     "attnres_abi_version": ([], _I),
     "attnres_status_string": ([_I], ctypes.c_char_p),
     "attnres_last_cuda_error": ([], ctypes.c_char_p),
+    "attnres_poll_device_errors": ([], _I),
     "attnres_query_prep": ([_P, _P, _P, _I, _I, _P], _I),
     "attnres_phase1": ([_P, _I64, _I, _I64, _I, _I, _P, _I, _F, _P, _P, _P, _P, _P], _I),
     "attnres_phase2_merge": ([_P, _P, _P, _P, _P, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _P],
@@ -89,6 +90,11 @@ def _rows(t: torch.Tensor, T: int, d: int, name: str):
         return
     if tuple(t.shape[-2:]) != (T, d) or t.stride(-1) != 1 or t.stride(-2) != d:
         raise ValueError(f"{name}: expected rows of shape [{T}, {d}] with row stride {d}")
+
+
+def attnres_poll_device_errors():
+    """Raise if a kernel's bounded wait gave up since the previous poll (synchronises)."""
+    _check(library().attnres_poll_device_errors(), "attnres_poll_device_errors")
 
 
 def attnres_query_prep(w, gamma_key, u_out, stream=None):

@@ -46,11 +46,23 @@ const char* attnres_status_string(attnres_status s) {
     case ATTNRES_ERR_UNSUPPORTED: return "ATTNRES_ERR_UNSUPPORTED";
     case ATTNRES_ERR_MISALIGNED: return "ATTNRES_ERR_MISALIGNED";
     case ATTNRES_ERR_CUDA: return "ATTNRES_ERR_CUDA";
+    case ATTNRES_ERR_TIMEOUT: return "ATTNRES_ERR_TIMEOUT";
   }
   return "ATTNRES_ERR_UNKNOWN";
 }
 
 const char* attnres_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+attnres_status attnres_poll_device_errors(void) {
+  const unsigned int n1 = attnres::phase1_poll_timeouts();
+  const unsigned int n2 = attnres::phase1_tc_poll_timeouts();
+  const unsigned int n = (n1 == 0xffffffffu || n2 == 0xffffffffu) ? 0xffffffffu : n1 + n2;
+  if (n == 0xffffffffu) {
+    g_last_cuda_error = "could not read the device wait-timeout counter";
+    return ATTNRES_ERR_CUDA;
+  }
+  return n == 0 ? ATTNRES_OK : ATTNRES_ERR_TIMEOUT;
+}
 
 attnres_status attnres_query_prep(const float* w, const float* gamma_key, float* u_out, int rows,
                                   int d, void* stream) {

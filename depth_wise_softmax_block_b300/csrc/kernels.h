@@ -2,6 +2,7 @@
 // Arguments arrive here already validated.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (type only)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -69,5 +70,20 @@ cudaError_t launch_partial_update(IO io, const void* a, const void* b, void* out
                                   cudaStream_t s);
 cudaError_t launch_query_prep(const float* w, const float* g, float* u, int64_t n_elems,
                               cudaStream_t s);
+// Tensor-copy descriptors (tmap.cu).  Sources: dims (column, token, source) of a [n][T][d]
+// tensor whose sources are src_stride elements apart, box (box_k, box_t, n), 128-byte swizzle.
+// Queries: dims (column, query) of an fp32 [S][d] tensor, box (32, S), 128-byte swizzle.
+cudaError_t encode_source_map(CUtensorMap* map, const void* reps, int64_t src_stride, int n,
+                              int64_t T, int d, int E, int box_k, int box_t);
+cudaError_t encode_query_map(CUtensorMap* map, const float* u, int S, int d);
+
+// Tensor-core phase 1 (phase1_tc.cu): bf16 I/O, 2 <= S <= 24, n <= 16.
+bool phase1_tc_supported(int n, int S);
+cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s);
+unsigned int phase1_tc_poll_timeouts();
+
+// Number of bounded waits in the phase-1 kernel that gave up since the last call (read and
+// cleared; synchronous).  0xffffffff if the device word could not be read.
+unsigned int phase1_poll_timeouts();
 
 }  // namespace attnres

@@ -3,45 +3,51 @@
 // "Attention Residuals 阅读补充", section "静态 Query 与两阶段计算": stacking the static
 // queries turns S matrix-vector products into one pass over the history).
 //
-// One CTA owns a tile of TT tokens and runs two sweeps over the hidden dimension d:
-//   sweep 1  streams the tile's source rows [n][TT][64 columns] and the query slice [S][64]
-//            through a 3-stage cp.async pipeline in shared memory.  Each warp takes one
-//            8-column octet of every stage; each lane accumulates the logit numerators
-//            u_s . b_j[t] of (NS sources x NQ queries) of one token and the sums of squares,
-//            with packed fp32 FMAs over column pairs (even and odd columns are summed
-//            separately and added at the end).
-//   reduce   the 8 warps' partial sums are added in a fixed order (deterministic), then one
-//            thread per (token, query) forms r_j, z_j, m, lse and alpha.
-//   sweep 2  streams the same source rows again (from L2 when they are still there) and
-//            writes o[s,t,:] = sum_j alpha_j b_j[t,:] with 16-byte streaming stores.
-// Arithmetic is fp32 throughout; o is rounded once to the I/O type.  A single query (S = 1,
-// the final aggregation) has no logits to share across queries and runs on the row-wise
-// single-pass kernel instead.
+// One CTA of 8 warps owns a tile of TT tokens.  Thread 0 streams the tile through a ring of
+// shared-memory stages with tensor (TMA) copies: a stage is the 128-byte column slice
+// (64 bf16 or 32 fp32 columns) of all n x TT source rows, plus, during the first sweep, the
+// same columns of the S queries.  Copies use the 128-byte swizzle, so 16-byte reads of eight
+// different rows hit eight different bank groups.  The warps run:
+//   sweep 1  each warp takes one 16-byte column chunk of every stage; each lane accumulates
+//            the logit numerators u_s . b_j[t] of (NS sources x NQ queries) of one token and
+//            the sums of squares, with packed fp32 FMAs over column pairs;
+//   reduce   the 8 warps' partial sums are added in a fixed order (deterministic); then
+//            r_j, z_j = u_s . b_j / r_j, m, lse and alpha for every (token, query);
+//   sweep 2  the same source rows stream through the ring again (its first stages are already
+//            in flight while the reduction runs) and o[s,t,:] = sum_j alpha_j b_j[t,:] is
+//            written with 16-byte streaming stores.
+// Stage hand-off uses "full" (copy landed) and "empty" (all warps done) mbarriers;
+// every wait is bounded (tma.cuh).  Arithmetic is fp32; o is rounded once to the I/O type.
+// A single query (S = 1, the final aggregation) has nothing to share across queries and runs
+// on the row-wise single-pass kernel instead.
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tma.cuh"
 
 namespace attnres {
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int KC = 64;        // columns per pipeline stage (one 8-column octet per warp)
-constexpr int kStages = 3;
-constexpr int kUnit = 16;     // cp.async granule in bytes
 constexpr int kMaxSmem = 227 * 1024;
+constexpr int kMaxStages = 8;
+constexpr int kRow = 128;                     // bytes per staged row (one swizzle span)
 
 struct P1Plan {
   int SG, QG, TT;       // source groups, query groups, tokens per CTA
-  int ttShift;          // log2(TT): TT is a power of two
-  int rowB, uRowB;      // bytes per staged (source, token) row / query row
-  int bBytes, stageBytes;
-  int RS;               // floats per thread in the cross-warp reduction buffer (odd)
-  int offDots, offAlpha;
-  int smem;
+  int KC;               // columns per stage (kRow bytes of a row)
+  int nUBox;            // query boxes per stage (32 fp32 columns each)
+  int bBytes, bSpan;    // bytes of the source box as copied / rounded up to 1024
+  int uBox, uSpan;      // bytes of one query box as copied / rounded up to 1024
+  int stageBytes, ST;   // bytes per stage, number of stages
+  int RS;               // floats per thread in the cross-warp reduction (odd)
+  int offRed, offDots, offBar;
+  int smem;             // dynamic shared memory to request (includes 1024 alignment slack)
 };
 
 inline int next_pow2(int x) {
@@ -64,21 +70,27 @@ bool make_plan(int n, int S, int E, P1Plan& p) {
   p.SG = next_pow2((n + NS - 1) / NS);
   p.QG = next_pow2((S + NQ - 1) / NQ);
   if (p.SG * p.QG > 32) return false;
-  p.rowB = KC * E + 16;
-  p.uRowB = KC * 4 + 16;
+  p.KC = kRow / E;
+  p.nUBox = p.KC * 4 / kRow;
   p.RS = NS * NQ + NS;
   if ((p.RS & 1) == 0) p.RS += 1;
+  p.uBox = S * kRow;
+  p.uSpan = align_up(p.uBox, 1024);
   for (p.TT = 32 / (p.SG * p.QG); p.TT >= 1; p.TT /= 2) {
-    p.bBytes = n * p.TT * p.rowB;
-    const int uBytes = S * p.uRowB + p.QG * kUnit;
-    p.stageBytes = align_up(p.bBytes + uBytes, 128);
-    const int area0 = std::max(kStages * p.stageBytes, kThreads * p.RS * 4);
-    p.offDots = align_up(area0, 16);
-    p.offAlpha = align_up(p.offDots + p.TT * n * (S + 1) * 4, 16);
-    p.smem = p.offAlpha + p.TT * n * p.QG * NQ * 2 * 4;
-    p.ttShift = 0;
-    while ((1 << p.ttShift) < p.TT) ++p.ttShift;
-    if (p.smem <= kMaxSmem) return true;
+    p.bBytes = n * p.TT * kRow;
+    p.bSpan = align_up(p.bBytes, 1024);
+    p.stageBytes = p.bSpan + p.nUBox * p.uSpan;
+    const int red = std::max(kThreads * p.RS * 4, p.TT * n * p.QG * NQ * 2 * 4);
+    const int dots = p.TT * n * (S + 1) * 4;
+    const int fixed = align_up(red, 16) + align_up(dots, 16) + (2 * kMaxStages + 2) * 8;
+    const int room = kMaxSmem - 1024 - fixed;
+    p.ST = std::min(kMaxStages, room / p.stageBytes);
+    if (p.ST < 2) continue;
+    p.offRed = p.ST * p.stageBytes;
+    p.offDots = p.offRed + align_up(red, 16);
+    p.offBar = p.offDots + align_up(dots, 16);
+    p.smem = 1024 + p.offBar + (2 * p.ST + 2) * 8;
+    return true;
   }
   return false;
 }
@@ -88,75 +100,107 @@ __device__ __forceinline__ void st_stream(void* p, uint4 v) {
   __stcs(reinterpret_cast<uint4*>(p), v);
 }
 
-// Eight consecutive elements as four (even, odd) column pairs.
-template <typename T> __device__ __forceinline__ void load_pairs(const void* p, float2 (&f)[4]);
-template <> __device__ __forceinline__ void load_pairs<bf16>(const void* p, float2 (&f)[4]) {
-  const uint4 v = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+// One 16-byte chunk as (even, odd) column pairs: 4 pairs of bf16, 2 pairs of fp32.
+template <typename T> struct Chunk;
+template <> struct Chunk<bf16> {
+  static constexpr int PR = 4;
+  static __device__ __forceinline__ void load(const void* p, float2 (&f)[PR]) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
-}
-template <> __device__ __forceinline__ void load_pairs<float>(const void* p, float2 (&f)[4]) {
-  const float4 a = reinterpret_cast<const float4*>(p)[0];
-  const float4 b = reinterpret_cast<const float4*>(p)[1];
-  f[0] = make_float2(a.x, a.y);
-  f[1] = make_float2(a.z, a.w);
-  f[2] = make_float2(b.x, b.y);
-  f[3] = make_float2(b.z, b.w);
-}
-
-template <typename T> __device__ __forceinline__ void store_pairs(void* p, const float2 (&f)[4]);
-template <> __device__ __forceinline__ void store_pairs<bf16>(void* p, const float2 (&f)[4]) {
-  st_stream(p, make_uint4(pack_bf16x2(f[0].x, f[0].y), pack_bf16x2(f[1].x, f[1].y),
-                          pack_bf16x2(f[2].x, f[2].y), pack_bf16x2(f[3].x, f[3].y)));
-}
-template <> __device__ __forceinline__ void store_pairs<float>(void* p, const float2 (&f)[4]) {
-  st_stream(p, make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y),
-                          __float_as_uint(f[1].x), __float_as_uint(f[1].y)));
-  st_stream(static_cast<char*>(p) + 16,
-            make_uint4(__float_as_uint(f[2].x), __float_as_uint(f[2].y),
-                       __float_as_uint(f[3].x), __float_as_uint(f[3].y)));
-}
+    for (int i = 0; i < 4; ++i)
+      f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+  }
+  static __device__ __forceinline__ void store(void* p, const float2 (&f)[PR]) {
+    st_stream(p, make_uint4(pack_bf16x2(f[0].x, f[0].y), pack_bf16x2(f[1].x, f[1].y),
+                            pack_bf16x2(f[2].x, f[2].y), pack_bf16x2(f[3].x, f[3].y)));
+  }
+};
+template <> struct Chunk<float> {
+  static constexpr int PR = 2;
+  static __device__ __forceinline__ void load(const void* p, float2 (&f)[PR]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    f[0] = make_float2(a.x, a.y);
+    f[1] = make_float2(a.z, a.w);
+  }
+  static __device__ __forceinline__ void store(void* p, const float2 (&f)[PR]) {
+    st_stream(p, make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y),
+                            __float_as_uint(f[1].x), __float_as_uint(f[1].y)));
+  }
+};
 
 template <typename IOT, int NS, int NQ>
 __global__ void __launch_bounds__(kThreads, 1)
-phase1_kernel(const Phase1Args a, const P1Plan pl) {
-  extern __shared__ __align__(128) unsigned char smem[];
+phase1_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_u,
+              const Phase1Args a, const P1Plan pl) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   constexpr int E = sizeof(IOT);
-  constexpr int UPR = KC * E / kUnit;  // 16-byte units per staged source row
+  constexpr int VE = 16 / E;                 // elements per 16-byte chunk
+  constexpr int PR = Chunk<IOT>::PR;         // column pairs per chunk
+  constexpr int NUC = VE / 4;                // 16-byte query chunks per column chunk
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = a.n, S = a.S, d = a.d;
-  const int TT = pl.TT, QG = pl.QG, SG = pl.SG;
+  const int TT = pl.TT, QG = pl.QG, SG = pl.SG, ST = pl.ST, KC = pl.KC;
   const int64_t T = a.T;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * TT;
-  const int nchunks = (d + KC - 1) / KC;
-  const char* reps = static_cast<const char*>(a.reps);
+  const int nch = (d + KC - 1) / KC;
 
-  // Stage chunk c (columns c*KC ..) into pipeline slot `slot`; zero-fill past T and d.
-  auto issue = [&](int c, int slot, bool with_u) {
-    unsigned char* st = smem + slot * pl.stageBytes;
-    const int k0 = c * KC;
-    const int nb = n * TT * UPR;
-    for (int i = tid; i < nb; i += kThreads) {
-      const int unit = i % UPR, row = i / UPR;  // row = j * TT + t (TT a power of two)
-      const int t = row & (TT - 1), j = row >> pl.ttShift;
-      const int k = k0 + unit * (kUnit / E);
-      const bool ok = (t0 + t < T) && (k < d);
-      const char* src =
-          ok ? reps + (static_cast<int64_t>(j) * a.src_stride + (t0 + t) * d + k) * E : reps;
-      cp_async16(st + row * pl.rowB + unit * kUnit, src, ok);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.offBar);
+  uint64_t* empty = full + ST;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + ST);
+
+  if (tid == 0) {
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
     }
-    if (with_u) {
-      unsigned char* ut = st + pl.bBytes;
-      const int nu = S * (KC * 4 / kUnit);
-      for (int i = tid; i < nu; i += kThreads) {
-        const int unit = i % (KC * 4 / kUnit), q = i / (KC * 4 / kUnit);
-        const int k = k0 + unit * 4;
-        const bool ok = k < d;
-        const float* src = ok ? a.u + static_cast<int64_t>(q) * d + k : a.u;
-        // query groups are offset by one granule so the QG groups hit distinct banks
-        cp_async16(ut + q * pl.uRowB + (q / NQ) * kUnit + unit * kUnit, src, ok);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  // The ring runs 2 * nch iterations: sweep 1 (sources + queries), then sweep 2 (sources).
+  // Thread 0 issues the copies: the first ST iterations up front, then, at every iteration,
+  // the refill of the slot used one iteration earlier once all warps have released it.
+  const int total = 2 * nch;
+  auto issue = [&](int i) {
+    const int slot = i % ST;
+    const bool first = i < nch;
+    const int c = first ? i : i - nch;
+    unsigned char* st = smem + slot * pl.stageBytes;
+    mbar_arrive_expect_tx(&full[slot], pl.bBytes + (first ? pl.nUBox * pl.uBox : 0));
+    tma_load_3d(st, &tm_b, c * KC, static_cast<int>(t0), 0, &full[slot]);
+    if (first) {
+      for (int h = 0; h < pl.nUBox; ++h)
+        tma_load_2d(st + pl.bSpan + h * pl.uSpan, &tm_u, c * KC + 32 * h, 0, &full[slot]);
+    }
+  };
+  int issued = 0;  // meaningful in thread 0 only
+  if (tid == 0) {
+    tma_prefetch_map(&tm_b);
+    tma_prefetch_map(&tm_u);
+    issued = ST < total ? ST : total;
+    for (int i = 0; i < issued; ++i) issue(i);
+  }
+
+  int it = 0;  // ring position, shared by both sweeps
+  auto acquire = [&](int slot) {
+    if (!*abort_flag && !mbar_wait(&full[slot], (it / ST) & 1)) *abort_flag = 1;
+  };
+  auto release = [&](int slot) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    if (warp == 0) {  // the whole warp waits, lane 0 issues
+      const int prev = it - 1;
+      if (prev >= 0 && prev + ST < total) {
+        const int ps = prev % ST;
+        if (!*abort_flag && !mbar_wait(&empty[ps], (prev / ST) & 1)) *abort_flag = 1;
+        __syncwarp();
+        if (lane == 0 && !*abort_flag) {
+          issue(prev + ST);
+          issued = prev + ST + 1;
+        }
       }
     }
   };
@@ -166,6 +210,19 @@ phase1_kernel(const Phase1Args a, const P1Plan pl) {
   const int g = lane % QG;
   const int sg = (lane / QG) % SG;
   const int tl = lane / (QG * SG);
+  int boff[NS];
+#pragma unroll
+  for (int jj = 0; jj < NS; ++jj) boff[jj] = sw128((sg * NS + jj) * TT + tl, warp);
+  int uoff[NQ][NUC];
+#pragma unroll
+  for (int qq = 0; qq < NQ; ++qq) {
+    const int q = g * NQ + qq;
+#pragma unroll
+    for (int h = 0; h < NUC; ++h)  // bf16: chunks 2(w%4), 2(w%4)+1 of box w/4; fp32: chunk w
+      uoff[qq][h] = pl.bSpan + (NUC == 2 ? (warp >> 2) * pl.uSpan : 0) +
+                    sw128(q, NUC == 2 ? 2 * (warp & 3) + h : warp);
+  }
+
   float2 acc[NS][NQ];
   float2 ss[NS];
 #pragma unroll
@@ -175,39 +232,33 @@ phase1_kernel(const Phase1Args a, const P1Plan pl) {
     for (int qq = 0; qq < NQ; ++qq) acc[jj][qq] = make_float2(0.f, 0.f);
   }
 
-#pragma unroll
-  for (int c = 0; c < kStages - 1; ++c) {
-    if (c < nchunks) issue(c, c, true);
-    cp_async_commit();
-  }
-  for (int c = 0; c < nchunks; ++c) {
-    cp_async_wait<kStages - 2>();
-    __syncthreads();
-    if (c + kStages - 1 < nchunks) issue(c + kStages - 1, (c + kStages - 1) % kStages, true);
-    cp_async_commit();
+  for (int c = 0; c < nch; ++c, ++it) {
+    const int slot = it % ST;
+    acquire(slot);
     if (active1) {
-      const unsigned char* st = smem + (c % kStages) * pl.stageBytes;
-      const unsigned char* ut = st + pl.bBytes + g * kUnit + warp * 32;
-      float2 uv[NQ][4];
+      const unsigned char* st = smem + slot * pl.stageBytes;
+      float2 uv[NQ][PR];
 #pragma unroll
       for (int qq = 0; qq < NQ; ++qq) {
         if (g * NQ + qq < S) {  // padded queries of the last group read nothing
-          load_pairs<float>(ut + (g * NQ + qq) * pl.uRowB, uv[qq]);
+#pragma unroll
+          for (int h = 0; h < NUC; ++h) {
+            const float4 x = *reinterpret_cast<const float4*>(st + uoff[qq][h]);
+            uv[qq][2 * h] = make_float2(x.x, x.y);
+            uv[qq][2 * h + 1] = make_float2(x.z, x.w);
+          }
         } else {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) uv[qq][i] = make_float2(0.f, 0.f);
+          for (int i = 0; i < PR; ++i) uv[qq][i] = make_float2(0.f, 0.f);
         }
       }
-      const unsigned char* bt = st + tl * pl.rowB + warp * 8 * E;
 #pragma unroll
       for (int jj = 0; jj < NS; ++jj) {
-        const int j = sg * NS + jj;
-        if (j < n) {
-          float2 bv[4];
-          load_pairs<IOT>(bt + j * TT * pl.rowB, bv);
-          // the sum-of-squares chain is spread between independent dot-product updates
+        if (sg * NS + jj < n) {
+          float2 bv[PR];
+          Chunk<IOT>::load(st + boff[jj], bv);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < PR; ++i) {
             ss[jj] = __ffma2_rn(bv[i], bv[i], ss[jj]);
 #pragma unroll
             for (int qq = 0; qq < NQ; ++qq) acc[jj][qq] = __ffma2_rn(uv[qq][i], bv[i], acc[jj][qq]);
@@ -215,12 +266,11 @@ phase1_kernel(const Phase1Args a, const P1Plan pl) {
         }
       }
     }
+    release(slot);
   }
-  cp_async_wait<0>();
-  __syncthreads();
 
   // ---------------- reduce the 8 warps' partial sums (fixed order) ----------------
-  float* red = reinterpret_cast<float*>(smem);  // reuses the pipeline slots
+  float* red = reinterpret_cast<float*>(smem + pl.offRed);
   if (active1) {
     float* r = red + tid * pl.RS;
 #pragma unroll
@@ -244,36 +294,30 @@ phase1_kernel(const Phase1Args a, const P1Plan pl) {
     dots[i] = sum;
   }
   __syncthreads();
-
-  // The pipeline slots are free again: start staging sweep 2 while the softmax runs.
-#pragma unroll
-  for (int c = 0; c < kStages - 1; ++c) {
-    if (c < nchunks) issue(c, c, false);
-    cp_async_commit();
+  // 1 / r_j in place of the sum of squares
+  const float fd = static_cast<float>(d);
+  for (int i = tid; i < TT * n; i += kThreads) {
+    float* p = dots + i * S1 + S;
+    *p = 1.f / sqrtf(*p / fd + a.eps);
   }
+  __syncthreads();
 
   // ---------------- softmax statistics, one thread per (token, query) ----------------
-  // alpha is stored twice, (a, a), so sweep 2 reads ready-made pairs: [TT][n][QG][NQ][2]
-  float* alph = reinterpret_cast<float*>(smem + pl.offAlpha);
-  const float fd = static_cast<float>(d);
+  // alpha is stored twice, (a, a), so sweep 2 reads ready-made pairs: [TT][n][QG][NQ][2].
+  // It reuses the reduction buffer, which is dead once `dots` is complete.
+  float* alph = red;
   for (int i = tid; i < TT * S; i += kThreads) {
     const int t = i / S, s = i % S;
     const int64_t tok = t0 + t;
     const float* dt = dots + t * n * S1;
     float m = -INFINITY;
-    for (int j = 0; j < n; ++j) {
-      const float z = dt[j * S1 + s] / sqrtf(dt[j * S1 + S] / fd + a.eps);
-      m = fmaxf(m, z);
-    }
+    for (int j = 0; j < n; ++j) m = fmaxf(m, dt[j * S1 + s] * dt[j * S1 + S]);
     float l = 0.f;
-    for (int j = 0; j < n; ++j) {
-      const float z = dt[j * S1 + s] / sqrtf(dt[j * S1 + S] / fd + a.eps);
-      l += expf(z - m);
-    }
+    for (int j = 0; j < n; ++j) l += expf(dt[j * S1 + s] * dt[j * S1 + S] - m);
     const float lse = m + logf(l);
+    const float rl = 1.f / l;
     for (int j = 0; j < n; ++j) {
-      const float z = dt[j * S1 + s] / sqrtf(dt[j * S1 + S] / fd + a.eps);
-      const float al = expf(z - m) / l;
+      const float al = expf(dt[j * S1 + s] * dt[j * S1 + S] - m) * rl;
       float* ap = alph + (((t * n + j) * QG + s / NQ) * NQ + s % NQ) * 2;
       ap[0] = al;
       ap[1] = al;
@@ -284,39 +328,38 @@ phase1_kernel(const Phase1Args a, const P1Plan pl) {
       if (a.lse != nullptr) a.lse[static_cast<int64_t>(s) * T + tok] = lse;
     }
   }
+  __syncthreads();
 
   // ---------------- sweep 2: o[s,t,:] = sum_j alpha[s,t,j] b_j[t,:] ----------------
   const bool active2 = tid < TT * QG * 8;
-  const int kg = tid % 8, g2 = (tid / 8) % QG, t2 = tid / (8 * QG);
+  const int kg = tid & 7, g2 = (tid >> 3) % QG, t2 = tid / (8 * QG);
   const int64_t tok2 = t0 + t2;
+  const float* at = alph + (t2 * n * QG + g2) * NQ * 2;
   char* o = static_cast<char*>(a.o);
-  for (int c = 0; c < nchunks; ++c) {
-    cp_async_wait<kStages - 2>();
-    __syncthreads();  // also orders the softmax's alpha writes before the first use
-    if (c + kStages - 1 < nchunks) issue(c + kStages - 1, (c + kStages - 1) % kStages, false);
-    cp_async_commit();
+  for (int c = 0; c < nch; ++c, ++it) {
+    const int slot = it % ST;
+    acquire(slot);
     if (active2) {
-      const unsigned char* bt = smem + (c % kStages) * pl.stageBytes + t2 * pl.rowB + kg * 8 * E;
-      const float* at = alph + (t2 * n * QG + g2) * NQ * 2;
-      float2 acc2[NQ][4];
+      const unsigned char* st = smem + slot * pl.stageBytes;
+      float2 acc2[NQ][PR];
 #pragma unroll
       for (int qq = 0; qq < NQ; ++qq)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc2[qq][i] = make_float2(0.f, 0.f);
-      // The next source's octet and alpha pairs are read from shared memory while the
+        for (int i = 0; i < PR; ++i) acc2[qq][i] = make_float2(0.f, 0.f);
+      // The next source's chunk and alpha pairs are read from shared memory while the
       // current source is accumulated (the trip count n is a runtime value).
-      float2 bv[4], bn[4];
+      float2 bv[PR], bn[PR];
       float4 af[NQ / 2], an[NQ / 2];
-      load_pairs<IOT>(bt, bn);
+      Chunk<IOT>::load(st + sw128(t2, kg), bn);
 #pragma unroll
       for (int h = 0; h < NQ / 2; ++h) an[h] = reinterpret_cast<const float4*>(at)[h];
       for (int j = 0; j < n; ++j) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) bv[i] = bn[i];
+        for (int i = 0; i < PR; ++i) bv[i] = bn[i];
 #pragma unroll
         for (int h = 0; h < NQ / 2; ++h) af[h] = an[h];
         if (j + 1 < n) {
-          load_pairs<IOT>(bt + (j + 1) * TT * pl.rowB, bn);
+          Chunk<IOT>::load(st + sw128((j + 1) * TT + t2, kg), bn);
           const float4* ap = reinterpret_cast<const float4*>(at + (j + 1) * QG * NQ * 2);
 #pragma unroll
           for (int h = 0; h < NQ / 2; ++h) an[h] = ap[h];
@@ -330,29 +373,43 @@ phase1_kernel(const Phase1Args a, const P1Plan pl) {
 #pragma unroll
         for (int qq = 0; qq < NQ; ++qq)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) acc2[qq][i] = __ffma2_rn(al[qq], bv[i], acc2[qq][i]);
+          for (int i = 0; i < PR; ++i) acc2[qq][i] = __ffma2_rn(al[qq], bv[i], acc2[qq][i]);
       }
-      const int k = c * KC + kg * 8;
+      const int k = c * KC + kg * VE;
       if (tok2 < T && k < d) {
 #pragma unroll
         for (int qq = 0; qq < NQ; ++qq) {
           const int q = g2 * NQ + qq;
           if (q < S)
-            store_pairs<IOT>(o + ((static_cast<int64_t>(q) * T + tok2) * d + k) * E, acc2[qq]);
+            Chunk<IOT>::store(o + ((static_cast<int64_t>(q) * T + tok2) * d + k) * E, acc2[qq]);
         }
       }
     }
+    release(slot);
   }
-  cp_async_wait<0>();
+  // Drain: the last copy issued into every slot has landed before the CTA may exit (only
+  // an aborted run can leave one in flight).
+  if (tid == 0) {
+    for (int s = 0; s < ST && s < issued; ++s) {
+      const int last = issued - 1 - ((issued - 1 - s) % ST);
+      mbar_wait(&full[s], (last / ST) & 1);
+    }
+  }
 }
 
+// ---------------------------------- host side ----------------------------------
 template <typename T, int NS, int NQ>
 cudaError_t launch_t(const Phase1Args& a, const P1Plan& pl, cudaStream_t s) {
+  CUtensorMap mb, mu;
+  cudaError_t e = encode_source_map(&mb, a.reps, a.src_stride, a.n, a.T, a.d, sizeof(T), pl.KC,
+                                    pl.TT);
+  if (e == cudaSuccess) e = encode_query_map(&mu, a.u, a.S, a.d);
+  if (e != cudaSuccess) return e;
   auto kern = phase1_kernel<T, NS, NQ>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
   if (e != cudaSuccess) return e;
   const int64_t blocks = (a.T + pl.TT - 1) / pl.TT;
-  kern<<<static_cast<unsigned>(blocks), kThreads, pl.smem, s>>>(a, pl);
+  kern<<<static_cast<unsigned>(blocks), kThreads, pl.smem, s>>>(mb, mu, a, pl);
   return cudaGetLastError();
 }
 
@@ -394,7 +451,22 @@ cudaError_t launch_phase1(IO io, const Phase1Args& a, cudaStream_t s) {
     f.lse = a.lse;
     return launch_full(io, f, s);
   }
+  if (io == IO::BF16 && phase1_tc_supported(a.n, a.S)) {
+    // ATTNRES_PHASE1_PATH=cuda_cores keeps the logits on the CUDA cores (comparison runs)
+    const char* path = getenv("ATTNRES_PHASE1_PATH");
+    if (path == nullptr || strcmp(path, "cuda_cores") != 0) return launch_phase1_tc(a, s);
+  }
   return io == IO::BF16 ? launch_io<bf16>(a, s) : launch_io<float>(a, s);
+}
+
+unsigned int phase1_poll_timeouts() {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_wait_timeouts, sizeof(v)) != cudaSuccess) return 0xffffffffu;
+  if (v != 0) {
+    const unsigned int z = 0;
+    cudaMemcpyToSymbol(g_wait_timeouts, &z, sizeof(z));
+  }
+  return v;
 }
 
 }  // namespace attnres

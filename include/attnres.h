@@ -45,7 +45,8 @@ typedef enum {
   ATTNRES_ERR_INVALID_ARG = 1,   /* null required pointer, non-positive size, bad enum     */
   ATTNRES_ERR_UNSUPPORTED = 2,   /* sizes beyond the limits below                          */
   ATTNRES_ERR_MISALIGNED = 3,    /* a device pointer or stride breaks 16-byte alignment    */
-  ATTNRES_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed            */
+  ATTNRES_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed            */
+  ATTNRES_ERR_TIMEOUT = 5        /* a kernel's bounded wait for its own copies gave up     */
 } attnres_status;
 
 typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype;
@@ -64,6 +65,17 @@ const char* attnres_status_string(attnres_status status);
 
 /* Message of the last CUDA error seen by this thread's calls ("" if none). */
 const char* attnres_last_cuda_error(void);
+
+/*
+ * Device-side error poll.  The phase-1 kernel stages its tiles with asynchronous tensor copies
+ * and waits for them on shared-memory barriers; every such wait is bounded.  A wait that gives
+ * up (a copy that never lands) makes the kernel finish early with undefined outputs and counts
+ * the event in a device word of the current device.  This call reads and clears that word:
+ * ATTNRES_ERR_TIMEOUT if any wait gave up since the previous poll, ATTNRES_OK otherwise,
+ * ATTNRES_ERR_CUDA if the word could not be read.  It synchronises with the device (it is a
+ * diagnostic, not part of the hot path).
+ */
+attnres_status attnres_poll_device_errors(void);
 
 /*
  * Query preparation (row a0): u = w ⊙ gamma_key, row by row.

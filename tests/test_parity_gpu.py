@@ -22,6 +22,17 @@ def dev():
     return torch.device("cuda:0")
 
 
+@pytest.fixture(params=["default", "cuda_cores"])
+def p1path(request, monkeypatch):
+    """Phase-1 kernel choice: the default (tensor-core logits where supported: bf16,
+    2 <= S <= 24, n <= 16) or the CUDA-core kernel for every shape."""
+    if request.param == "cuda_cores":
+        monkeypatch.setenv("ATTNRES_PHASE1_PATH", "cuda_cores")
+    else:
+        monkeypatch.delenv("ATTNRES_PHASE1_PATH", raising=False)
+    return request.param
+
+
 def _dt(name):
     return torch.float32 if name == "f32" else torch.bfloat16
 
@@ -73,11 +84,15 @@ P1_CASES = [
     (64, 2, 11, 64, "bf16"),        # n at its maximum with two queries
     (2, 2, 70, 136, "f32"),
     (7, 5, 23, 96, "f32"),
+    (16, 24, 21, 320, "bf16"),      # the tensor-core path's largest tile (16 sources x 8 tokens)
+    (1, 2, 9, 64, "bf16"),          # its smallest (one source, two queries)
+    (3, 7, 8, 136, "bf16"),         # odd S, ragged last column stage
+    (17, 24, 12, 128, "bf16"),      # n beyond the tensor-core tile: CUDA-core kernel
 ]
 
 
 @pytest.mark.parametrize("n,S,T,d,dt", P1_CASES)
-def test_phase1_matches_oracle(dev, n, S, T, d, dt):
+def test_phase1_matches_oracle(dev, p1path, n, S, T, d, dt):
     seed = 1000 + n * 7 + S
     reps = make_reps(n, T, d, _dt(dt), dev, seed)
     W, G, U = make_queries(S, d, dev, seed)
@@ -90,7 +105,7 @@ def test_phase1_matches_oracle(dev, n, S, T, d, dt):
     check_close(alpha, oalpha, tol["weight"], "alpha")
 
 
-def test_phase1_chunk_view(dev):
+def test_phase1_chunk_view(dev, p1path):
     """A token chunk of a larger cache: source stride != T*d and an offset base pointer."""
     n, Ttot, d, S = 9, 300, 512, 24
     reps_all = make_reps(n, Ttot, d, torch.bfloat16, dev, 77)
@@ -113,7 +128,7 @@ def test_phase1_zero_queries_give_mean(dev):
     check_close(lse, np.full((S, T), np.log(n)), 1e-5, "lse = ln n")
 
 
-def test_phase1_extreme_logits(dev):
+def test_phase1_extreme_logits(dev, p1path):
     """Large queries push the softmax towards one-hot; max subtraction keeps it finite."""
     n, T, d, S = 9, 24, 512, 24
     reps = make_reps(n, T, d, torch.bfloat16, dev, 9)
@@ -126,7 +141,7 @@ def test_phase1_extreme_logits(dev):
     check_close(lse, olse, 2e-3 * max(1.0, float(np.abs(olse).max()) / 100), "lse")
 
 
-def test_phase1_deterministic(dev):
+def test_phase1_deterministic(dev, p1path):
     reps = make_reps(9, 50, 1024, torch.bfloat16, dev, 3)
     _, _, U = make_queries(24, 1024, dev, 3)
     a = run_phase1(reps, U)
@@ -258,3 +273,12 @@ def test_scale_invariance_on_gpu(dev):
     ar.attnres_phase1(reps2, U, o, alpha_out=scaled, eps=0.0)
     torch.cuda.synchronize()
     check_close(scaled, base, 2e-6, "weights under source scaling")
+
+
+def test_no_bounded_wait_gave_up(dev, p1path):
+    """Every phase-1 launch above finished its copies: no bounded wait in a kernel timed out."""
+    n, T, d, S = 9, 300, 7168, 24
+    reps = make_reps(n, T, d, torch.bfloat16, dev, 31)
+    W, G, U = make_queries(S, d, dev, 31)
+    run_phase1(reps, U)
+    ar.attnres_poll_device_errors()
