@@ -76,6 +76,7 @@ class LongContextStep:
         self.vbuf = I.make_outputs(wl, 1, S, dev, T=ch)   # stand-ins for f_i, shared by chunks
         self.P = I.block_params(wl, dev)
         self.U = torch.empty_like(self.P.W)
+        self.U_split = torch.empty((2 * S, d), dtype=torch.bfloat16, device=dev)
         self.uf = torch.empty((1, d), device=dev)
         self.out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
         self.timer = timer
@@ -89,7 +90,7 @@ class LongContextStep:
 
     def prep(self):
         from depth_wise_softmax_block_b300.schedule import _call
-        _call(self.timer, "query_prep", self._prep, self.P.W, self.P.G_key, self.U)
+        _call(self.timer, "query_prep", self._prep, self.P.W, self.P.G_key, self.U, self.U_split)
         _call(self.timer, "query_prep", self._prep, self.P.w_final.view(1, -1),
               self.P.g_final.view(1, -1), self.uf)
 
@@ -101,7 +102,7 @@ class LongContextStep:
         from depth_wise_softmax_block_b300.schedule import final_aggregation
         reps_c, close_c, all_c, out_c = self.chunk_views(c)
         self.runner.run_block(reps_c, self.U, self.P.G_in, self.sublayer, close_c, self.wl.eps,
-                              self.wl.eps, on_call=on_call)
+                              self.wl.eps, on_call=on_call, U_split=self.U_split)
         final_aggregation(all_c, self.uf[0], out_c, self.wl.eps, timer=self.timer)
 
     def run(self):

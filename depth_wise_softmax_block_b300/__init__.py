@@ -27,8 +27,8 @@ SIGNATURES = {
     "attnres_status_string": ([_I], ctypes.c_char_p),
     "attnres_last_cuda_error": ([], ctypes.c_char_p),
     "attnres_poll_device_errors": ([], _I),
-    "attnres_query_prep": ([_P, _P, _P, _I, _I, _P], _I),
-    "attnres_phase1": ([_P, _I64, _I, _I64, _I, _I, _P, _I, _F, _P, _P, _P, _P, _P], _I),
+    "attnres_query_prep": ([_P, _P, _P, _P, _I, _I, _P], _I),
+    "attnres_phase1": ([_P, _I64, _I, _I64, _I, _I, _P, _P, _I, _F, _P, _P, _P, _P, _P], _I),
     "attnres_phase2_merge": ([_P, _P, _P, _P, _P, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _P],
                              _I),
     "attnres_partial_update": ([_P, _P, _P, _I64, _I, _I, _P], _I),
@@ -97,26 +97,36 @@ def attnres_poll_device_errors():
     _check(library().attnres_poll_device_errors(), "attnres_poll_device_errors")
 
 
-def attnres_query_prep(w, gamma_key, u_out, stream=None):
-    """u = w ⊙ gamma_key (query with the key-norm gain folded in), [rows, d] fp32."""
+def attnres_query_prep(w, gamma_key, u_out, u_split_out=None, stream=None):
+    """u = w ⊙ gamma_key (query with the key-norm gain folded in), [rows, d] fp32; optionally
+    its bf16 hi/lo split [2 * rows, d] for the tensor-core phase 1."""
     rows, d = w.shape
-    _check(library().attnres_query_prep(_ptr(w), _ptr(gamma_key), _ptr(u_out), rows, d,
-                                        _stream(stream)), "attnres_query_prep")
+    if u_split_out is not None:
+        if (tuple(u_split_out.shape) != (2 * rows, d) or u_split_out.dtype != torch.bfloat16
+                or not u_split_out.is_contiguous()):
+            raise ValueError("u_split_out must be a contiguous bf16 [2 * rows, d] tensor")
+    _check(library().attnres_query_prep(_ptr(w), _ptr(gamma_key), _ptr(u_out),
+                                        _ptr(u_split_out), rows, d, _stream(stream)),
+           "attnres_query_prep")
     return u_out
 
 
 def attnres_phase1(reps, u, o_out, m_out=None, lse_out=None, alpha_out=None, eps=1e-6,
-                   stream=None):
+                   u_split=None, stream=None):
     """Phase 1 over ``reps`` [n, T, d] (any source stride, rows of stride d) for the S queries
-    ``u`` [S, d]; writes o [S, T, d] and the optional statistics."""
+    ``u`` [S, d]; writes o [S, T, d] and the optional statistics.  ``u_split`` ([2S, d] bf16,
+    from attnres_query_prep) puts the logits on the tensor cores where the shape allows."""
     n, T, d = reps.shape
     S = u.shape[0]
+    if u_split is not None and (tuple(u_split.shape) != (2 * S, d) or not u_split.is_contiguous()
+                                or u_split.dtype != torch.bfloat16):
+        raise ValueError("u_split must be a contiguous bf16 [2S, d] tensor")
     _rows(reps[0], T, d, "reps")
     if tuple(o_out.shape) != (S, T, d) or not o_out.is_contiguous():
         raise ValueError("o_out must be a contiguous [S, T, d] tensor")
     src_stride = reps.stride(0) if n > 1 else T * d
-    _check(library().attnres_phase1(_ptr(reps), src_stride, n, T, d, _io(reps), _ptr(u), S,
-                                    eps, _ptr(o_out), _ptr(m_out), _ptr(lse_out),
+    _check(library().attnres_phase1(_ptr(reps), src_stride, n, T, d, _io(reps), _ptr(u),
+                                    _ptr(u_split), S, eps, _ptr(o_out), _ptr(m_out), _ptr(lse_out),
                                     _ptr(alpha_out), _stream(stream)), "attnres_phase1")
     return o_out
 

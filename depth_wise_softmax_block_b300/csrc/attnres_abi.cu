@@ -64,23 +64,24 @@ attnres_status attnres_poll_device_errors(void) {
   return n == 0 ? ATTNRES_OK : ATTNRES_ERR_TIMEOUT;
 }
 
-attnres_status attnres_query_prep(const float* w, const float* gamma_key, float* u_out, int rows,
-                                  int d, void* stream) {
+attnres_status attnres_query_prep(const float* w, const float* gamma_key, float* u_out,
+                                  void* u_split_out, int rows, int d, void* stream) {
   if (rows < 0) return ATTNRES_ERR_INVALID_ARG;
   const attnres_status sh = check_shape(rows, d);
   if (sh != ATTNRES_OK) return sh;
   if (rows == 0) return ATTNRES_OK;
   if (w == nullptr || u_out == nullptr) return ATTNRES_ERR_INVALID_ARG;
-  if (!aligned16(w) || !aligned16(u_out) || !opt_aligned16(gamma_key))
+  if (!aligned16(w) || !aligned16(u_out) || !opt_aligned16(gamma_key) ||
+      !opt_aligned16(u_split_out))
     return ATTNRES_ERR_MISALIGNED;
-  return cuda_status(attnres::launch_query_prep(w, gamma_key, u_out,
-                                                static_cast<int64_t>(rows) * d,
+  return cuda_status(attnres::launch_query_prep(w, gamma_key, u_out, u_split_out, rows, d,
                                                 static_cast<cudaStream_t>(stream)));
 }
 
 attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, int64_t T, int d,
-                              attnres_dtype io, const float* u, int S, float eps, void* o_out,
-                              float* m_out, float* lse_out, float* alpha_out, void* stream) {
+                              attnres_dtype io, const float* u, const void* u_split, int S,
+                              float eps, void* o_out, float* m_out, float* lse_out,
+                              float* alpha_out, void* stream) {
   if (!valid_io(io)) return ATTNRES_ERR_INVALID_ARG;
   const attnres_status sh = check_shape(T, d);
   if (sh != ATTNRES_OK) return sh;
@@ -91,9 +92,11 @@ attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, i
   if (reps == nullptr || u == nullptr || o_out == nullptr) return ATTNRES_ERR_INVALID_ARG;
   if (n_src > 1 && src_stride < T * d) return ATTNRES_ERR_INVALID_ARG;
   if (src_stride < 0) return ATTNRES_ERR_INVALID_ARG;
-  if (!aligned16(reps) || !aligned16(u) || !aligned16(o_out) || src_stride % 8 != 0)
+  if (!aligned16(reps) || !aligned16(u) || !aligned16(o_out) || !opt_aligned16(u_split) ||
+      src_stride % 8 != 0)
     return ATTNRES_ERR_MISALIGNED;
-  attnres::Phase1Args a{reps, src_stride, n_src, T, d, u, S, eps, o_out, m_out, lse_out, alpha_out};
+  attnres::Phase1Args a{reps,  src_stride, n_src, T,      d,       u,        u_split,
+                        S,     eps,        o_out, m_out, lse_out, alpha_out};
   return cuda_status(attnres::launch_phase1(static_cast<IO>(io), a,
                                             static_cast<cudaStream_t>(stream)));
 }

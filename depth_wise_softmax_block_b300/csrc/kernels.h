@@ -17,6 +17,7 @@ struct Phase1Args {
   int64_t T;
   int d;
   const float* u;      // [S, d]
+  const void* u_split; // [2S, d] bf16 (hi, lo row pairs) or null
   int S;
   float eps;
   void* o;             // [S, T, d]
@@ -68,16 +69,22 @@ cudaError_t launch_phase2(IO io, const Phase2Args& a, cudaStream_t s);
 cudaError_t launch_full(IO io, const FullArgs& a, cudaStream_t s);
 cudaError_t launch_partial_update(IO io, const void* a, const void* b, void* out, int64_t n_elems,
                                   cudaStream_t s);
-cudaError_t launch_query_prep(const float* w, const float* g, float* u, int64_t n_elems,
-                              cudaStream_t s);
+// u = w * g (g null: copy); u_split (null: not written) receives rows 2r, 2r + 1 = the bf16
+// hi and lo parts of row r of u.
+cudaError_t launch_query_prep(const float* w, const float* g, float* u, void* u_split, int rows,
+                              int d, cudaStream_t s);
 // Tensor-copy descriptors (tmap.cu).  Sources: dims (column, token, source) of a [n][T][d]
 // tensor whose sources are src_stride elements apart, box (box_k, box_t, n), 128-byte swizzle.
 // Queries: dims (column, query) of an fp32 [S][d] tensor, box (32, S), 128-byte swizzle.
 cudaError_t encode_source_map(CUtensorMap* map, const void* reps, int64_t src_stride, int n,
                               int64_t T, int d, int E, int box_k, int box_t);
 cudaError_t encode_query_map(CUtensorMap* map, const float* u, int S, int d);
+// Split queries: dims (column, row) of a bf16 [2S][d] tensor, box (64, rows_box) with rows past
+// 2S zero-filled, 128-byte swizzle.
+cudaError_t encode_split_query_map(CUtensorMap* map, const void* u_split, int S, int d,
+                                   int rows_box);
 
-// Tensor-core phase 1 (phase1_tc.cu): bf16 I/O, 2 <= S <= 24, n <= 16.
+// Tensor-core phase 1 (phase1_tc.cu): bf16 I/O, 2 <= S <= 24, n <= 9, split queries given.
 bool phase1_tc_supported(int n, int S);
 cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s);
 unsigned int phase1_tc_poll_timeouts();

@@ -20,7 +20,6 @@
 // every wait is bounded (tma.cuh).  Arithmetic is fp32; o is rounded once to the I/O type.
 // A single query (S = 1, the final aggregation) has nothing to share across queries and runs
 // on the row-wise single-pass kernel instead.
-#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -451,11 +450,8 @@ cudaError_t launch_phase1(IO io, const Phase1Args& a, cudaStream_t s) {
     f.lse = a.lse;
     return launch_full(io, f, s);
   }
-  if (io == IO::BF16 && phase1_tc_supported(a.n, a.S)) {
-    // ATTNRES_PHASE1_PATH=cuda_cores keeps the logits on the CUDA cores (comparison runs)
-    const char* path = getenv("ATTNRES_PHASE1_PATH");
-    if (path == nullptr || strcmp(path, "cuda_cores") != 0) return launch_phase1_tc(a, s);
-  }
+  if (io == IO::BF16 && a.u_split != nullptr && phase1_tc_supported(a.n, a.S))
+    return launch_phase1_tc(a, s);
   return io == IO::BF16 ? launch_io<bf16>(a, s) : launch_io<float>(a, s);
 }
 

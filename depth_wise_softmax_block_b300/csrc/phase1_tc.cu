@@ -5,27 +5,28 @@
 //
 // The logit numerators of all tokens form one dense product: U [S x d] (the block's queries,
 // shared by every token) times the source rows b_j[t] [d] of every (source, token) pair.  This
-// kernel computes it with tcgen05 MMAs (bf16 x bf16 -> fp32 in tensor memory).  U is fp32; each
-// query row is split exactly enough into two bf16 rows, u = hi + lo with |u - hi - lo| <=
-// 2^-16 |u|, and both rows enter the product, so the logits keep fp32-level accuracy (the
-// sources are bf16 already).  Everything else runs on the CUDA cores:
+// kernel computes it with tcgen05 MMAs (bf16 x bf16 -> fp32 in tensor memory).  U is fp32; the
+// caller passes it also as split bf16 rows (attnres_query_prep): row 2s = hi(u_s), row 2s + 1 =
+// lo(u_s), with |u - hi - lo| <= 2^-16 |u|, so the logits keep fp32-level accuracy (the sources
+// are bf16 already).  Everything else runs on the CUDA cores:
 //   sweep 1  a copy-issuing warp streams 64-column stages of the tile (n sources x 8 tokens,
-//            128-byte swizzled rows) through a ring of up to 12 slots, and the same columns of
-//            U (fp32) through a ring of 4; the 16 compute warps split U into the hi/lo bf16
-//            operand tile and accumulate each source row's sum of squares; thread 0 issues the
-//            four K=16 MMAs of the stage, D[row, 2s + {hi,lo}] += b_row . u_s, with the tile's
-//            n*8 rows as M (= 128, unused rows ignored);
+//            128-byte swizzled rows) and of the split queries through a ring of up to 12 slots;
+//            thread 0 issues the stage's four K=16 MMAs, D[row, 2s + {hi,lo}] += b_row . u_s,
+//            with the tile's n*8 rows as M (= 128, unused rows ignored), while the 16 compute
+//            warps accumulate each source row's sum of squares;
 //   softmax  warps 0-3 read D from tensor memory (one row per thread), form
 //            z = (hi + lo) / r_j, and one thread per (token, query) computes m, lse, alpha;
 //   sweep 2  the tile streams through the ring again, columns in reverse order so that the
 //            chunks read last in sweep 1 are still in L2, and the 16 warps write
 //            o[s,t,:] = sum_j alpha_j b_j[t,:] (packed fp32 FMAs, 16-byte streaming stores).
-// Stage hand-off uses mbarriers ("full": copy landed; "conv": split queries written; "empty":
-// all warps and the stage's MMAs done); every wait is bounded (tma.cuh).  The tensor-memory
-// allocation is released on every path before the CTA exits.
+// Stage hand-off uses mbarriers ("full": copy landed; "empty": all compute warps and the
+// stage's MMAs done); every wait is bounded (tma.cuh).  The tensor-memory allocation is
+// released on every path before the CTA exits.
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -42,19 +43,17 @@ constexpr int kTT = 8;              // tokens per CTA tile
 constexpr int kKC = 64;             // bf16 columns per stage (one 128-byte row slice)
 constexpr int kM = 128;             // MMA rows (tile rows n * 8 <= 128)
 constexpr int kMaxS = 24;           // sweep 2 covers 8 groups of 3 queries
-constexpr int kMaxN = kM / kTT;     // 16 sources
+constexpr int kMaxN = 9;            // sources: the sweep-2 weights of a thread live in registers
 constexpr int kTmemCols = 64;       // D uses at most 2 * 24 = 48 columns
-constexpr int kMaxB = 12;           // source-ring slots
-constexpr int kQStages = 4;         // query-ring slots (sweep 1 only)
+constexpr int kMaxSlots = 12;       // ring slots
 constexpr int kMaxSmem = 227 * 1024;
 
 struct TcPlan {
   int Npad;           // MMA N: 2S rounded up to 16
   int bBytes;         // source box bytes as copied (n * 8 * 128)
-  int bSlot, SB;      // source-ring slot bytes (1024-aligned), slots
-  int uBox, uSpan;    // one fp32 query box (S rows x 128 bytes) / rounded up to 1024
-  int qSlot;          // query-ring slot: two fp32 boxes + the split operand tile
-  int offQ;           // query ring (after the source ring and its MMA read-over slack)
+  int bSpan;          // rounded up to 1024
+  int qBytes;         // split-query box bytes (Npad rows x 128 bytes, rows >= 2S zero-filled)
+  int slot, SB;       // ring slot bytes ([sources][split queries]), slots
   int offZ, offAlph, offSs, offBar, offTmem;
   int smem;
 };
@@ -65,25 +64,23 @@ bool make_tc_plan(int n, int S, TcPlan& p) {
   if (n < 1 || n > kMaxN || S < 2 || S > kMaxS) return false;
   p.Npad = align_up(2 * S, 16);
   p.bBytes = n * kTT * 128;
-  p.bSlot = align_up(p.bBytes, 1024);
-  p.uBox = S * 128;
-  p.uSpan = align_up(p.uBox, 1024);
-  p.qSlot = 2 * p.uSpan + align_up(p.Npad * 128, 1024);
-  // The MMA reads 128 rows (16 KB) from a source slot's base; rows past the tile's n * 8 are
-  // ignored but must lie inside the allocation, hence the slack after the last slot.
-  const int slack = kM * 128 - p.bSlot;
+  p.bSpan = align_up(p.bBytes, 1024);
+  p.qBytes = p.Npad * 128;
+  p.slot = p.bSpan + align_up(p.qBytes, 1024);
+  // The MMA reads 128 rows (16 KB) from a slot's base; rows past the tile's n * 8 are ignored
+  // but must lie inside the allocation, hence the slack after the last slot.
+  const int slack = std::max(0, kM * 128 - p.slot);
   const int zb = kM * S * 4;
   const int ab = kTT * n * 8 * 8 * 4;
-  const int fixed = slack + kQStages * p.qSlot + align_up(zb, 16) + align_up(ab, 16) + kM * 4 +
-                    (2 * kMaxB + 3 * kQStages + 2) * 8 + 16;
-  p.SB = std::min(kMaxB, (kMaxSmem - 1024 - fixed) / p.bSlot);
+  const int fixed = slack + align_up(zb, 16) + align_up(ab, 16) + kM * 4 +
+                    (2 * kMaxSlots + 2) * 8 + 16;
+  p.SB = std::min(kMaxSlots, (kMaxSmem - 1024 - fixed) / p.slot);
   if (p.SB < 3) return false;
-  p.offQ = p.SB * p.bSlot + slack;
-  p.offZ = p.offQ + kQStages * p.qSlot;
+  p.offZ = p.SB * p.slot + slack;
   p.offAlph = p.offZ + align_up(zb, 16);
   p.offSs = p.offAlph + align_up(ab, 16);
   p.offBar = p.offSs + kM * 4;
-  p.offTmem = p.offBar + (2 * p.SB + 3 * kQStages + 2) * 8;
+  p.offTmem = p.offBar + (2 * p.SB + 2) * 8;
   p.smem = 1024 + p.offTmem + 16;
   return true;
 }
@@ -97,7 +94,7 @@ __device__ __forceinline__ void unpack_pairs(const uint4& v, float2 (&f)[4]) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
-                 const __grid_constant__ CUtensorMap tm_u, const Phase1Args a, const TcPlan pl) {
+                 const __grid_constant__ CUtensorMap tm_q, const Phase1Args a, const TcPlan pl) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -107,12 +104,9 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   const int nch = (d + kKC - 1) / kKC;
   const int total = 2 * nch;  // source-ring iterations: sweep 1, then sweep 2
 
-  uint64_t* full_b = reinterpret_cast<uint64_t*>(smem + pl.offBar);
-  uint64_t* empty_b = full_b + SB;
-  uint64_t* full_q = empty_b + SB;
-  uint64_t* conv = full_q + kQStages;
-  uint64_t* empty_q = conv + kQStages;
-  uint64_t* dready = empty_q + kQStages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.offBar);
+  uint64_t* empty = full + SB;
+  uint64_t* dready = empty + SB;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(dready + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + pl.offTmem);
   float* zbuf = reinterpret_cast<float*>(smem + pl.offZ);     // [128 rows][S]
@@ -121,27 +115,12 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
 
   if (tid == 0) {
     for (int s = 0; s < SB; ++s) {
-      mbar_init(&full_b[s], 1);
-      mbar_init(&empty_b[s], kWarps + 1);  // every compute warp + the stage's MMAs (or thread 0)
-    }
-    for (int s = 0; s < kQStages; ++s) {
-      mbar_init(&full_q[s], 1);
-      mbar_init(&conv[s], kWarps);         // split queries written
-      mbar_init(&empty_q[s], 1);           // the stage's MMAs completed
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps + 1);  // every compute warp + the stage's MMAs (or thread 0)
     }
     mbar_init(dready, 1);
     *abort_flag = 0;
     mbar_fence_init();
-  }
-  // Rows [2S, Npad) of every split-query tile stay zero for the whole kernel.
-  {
-    const int zrows = pl.Npad - 2 * S;
-    for (int i = tid; i < kQStages * zrows * 8; i += kThreads) {
-      const int s = i / (zrows * 8), rr = 2 * S + (i / 8) % zrows, ch = i % 8;
-      *reinterpret_cast<uint4*>(smem + pl.offQ + s * pl.qSlot + 2 * pl.uSpan + sw128(rr, ch)) =
-          make_uint4(0u, 0u, 0u, 0u);
-    }
-    fence_async_smem();
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -155,41 +134,27 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   if (warp == kWarps) {
     if (lane == 0) {
       tma_prefetch_map(&tm_b);
-      tma_prefetch_map(&tm_u);
-      int ib = 0, iq = 0;  // copies issued into each ring
+      tma_prefetch_map(&tm_q);
+      int ib = 0;  // ring iterations issued
       for (; ib < total; ++ib) {
-        if (ib < nch) {  // the stage's query columns first: the MMAs need both
-          const int qs = ib % kQStages;
-          if (ib >= kQStages && !mbar_wait(&empty_q[qs], ((ib / kQStages) - 1) & 1)) {
-            *abort_flag = 1;
-            break;
-          }
-          if (*abort_flag) break;
-          unsigned char* q = smem + pl.offQ + qs * pl.qSlot;
-          mbar_arrive_expect_tx(&full_q[qs], 2 * pl.uBox);
-          tma_load_2d(q, &tm_u, ib * kKC, 0, &full_q[qs]);
-          tma_load_2d(q + pl.uSpan, &tm_u, ib * kKC + 32, 0, &full_q[qs]);
-          iq = ib + 1;
-        }
         const int bs = ib % SB;
-        if (ib >= SB && !mbar_wait(&empty_b[bs], ((ib / SB) - 1) & 1)) {
+        if (ib >= SB && !mbar_wait(&empty[bs], ((ib / SB) - 1) & 1)) {
           *abort_flag = 1;
           break;
         }
         if (*abort_flag) break;
         // sweep 2 walks the columns backwards: the chunks read last come back first, from L2
-        const int c = ib < nch ? ib : total - 1 - ib;
-        mbar_arrive_expect_tx(&full_b[bs], pl.bBytes);
-        tma_load_3d(smem + bs * pl.bSlot, &tm_b, c * kKC, static_cast<int>(t0), 0, &full_b[bs]);
+        const bool first = ib < nch;
+        const int c = first ? ib : total - 1 - ib;
+        unsigned char* st = smem + bs * pl.slot;
+        mbar_arrive_expect_tx(&full[bs], pl.bBytes + (first ? pl.qBytes : 0));
+        tma_load_3d(st, &tm_b, c * kKC, static_cast<int>(t0), 0, &full[bs]);
+        if (first) tma_load_2d(st + pl.bSpan, &tm_q, c * kKC, 0, &full[bs]);
       }
       // Drain: the last copy issued into every slot has landed before the CTA may exit.
       for (int s = 0; s < SB && s < ib; ++s) {
         const int last = ib - 1 - ((ib - 1 - s) % SB);
-        mbar_wait(&full_b[s], (last / SB) & 1);
-      }
-      for (int s = 0; s < kQStages && s < iq; ++s) {
-        const int last = iq - 1 - ((iq - 1 - s) % kQStages);
-        mbar_wait(&full_q[s], (last / kQStages) & 1);
+        mbar_wait(&full[s], (last / SB) & 1);
       }
     }
     return;
@@ -201,44 +166,31 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     if (!*abort_flag && !mbar_wait(bar, parity)) *abort_flag = 1;
   };
-  auto release_b = [&](int bs, bool substitute_mma) {
+  auto release = [&](int bs, bool substitute_mma) {
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty_b[bs]);
-    if (substitute_mma && tid == 0) mbar_arrive(&empty_b[bs]);
+    if (lane == 0) mbar_arrive(&empty[bs]);
+    if (substitute_mma && tid == 0) mbar_arrive(&empty[bs]);
   };
 
   // ------------------------------------ sweep 1 ------------------------------------
   const int nrows = n * kTT;  // tile rows: row j * 8 + t
   float2 ssa[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   for (int c = 0; c < nch; ++c) {
-    const int bs = c % SB, qs = c % kQStages;
-    unsigned char* st = smem + bs * pl.bSlot;
-    unsigned char* qb = smem + pl.offQ + qs * pl.qSlot;
-    // split the stage's queries: operand rows 2s (hi) and 2s + 1 (lo), bf16, swizzled
-    wait(&full_q[qs], (c / kQStages) & 1);
-    if (tid < S * 8) {
-      const int q = tid >> 3, g8 = tid & 7;
-      const unsigned char* ub = qb + (g8 >> 2) * pl.uSpan;
-      const float4 x0 = *reinterpret_cast<const float4*>(ub + sw128(q, 2 * (g8 & 3)));
-      const float4 x1 = *reinterpret_cast<const float4*>(ub + sw128(q, 2 * (g8 & 3) + 1));
-      const float u[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-      uint32_t hi[4], lo[4];
+    const int bs = c % SB;
+    const unsigned char* st = smem + bs * pl.slot;
+    wait(&full[bs], (c / SB) & 1);
+    // the stage's four K = 16 MMAs: D[row, 2s + {hi, lo}] += b_row . u_s
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t a0 = smem_addr(st), b0 = smem_addr(st + pl.bSpan);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        hi[e] = pack_bf16x2(u[2 * e], u[2 * e + 1]);
-        lo[e] = pack_bf16x2(u[2 * e] - __uint_as_float(hi[e] << 16),
-                            u[2 * e + 1] - __uint_as_float(hi[e] & 0xffff0000u));
-      }
-      unsigned char* bt = qb + 2 * pl.uSpan;
-      *reinterpret_cast<uint4*>(bt + sw128(2 * q, g8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(bt + sw128(2 * q + 1, g8)) =
-          make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      fence_async_smem();
+      for (int kk = 0; kk < 4; ++kk)
+        tc_mma_bf16(tmem, desc_kmajor_sw128(a0 + 32 * kk), desc_kmajor_sw128(b0 + 32 * kk), idesc,
+                    (c | kk) != 0 ? 1u : 0u);
+      tc_commit(&empty[bs]);
+      if (c == nch - 1) tc_commit(dready);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&conv[qs]);
     // sums of squares: (row, 16-byte chunk) pairs tid and tid + 512
-    wait(&full_b[bs], (c / SB) & 1);
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const int i = tid + k * kCompute;
@@ -249,22 +201,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
         for (int e = 0; e < 4; ++e) ssa[k] = __ffma2_rn(f[e], f[e], ssa[k]);
       }
     }
-    // the stage's four K = 16 MMAs, issued by thread 0 once the split queries are in place
-    if (warp == 0) {
-      wait(&conv[qs], (c / kQStages) & 1);
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t a0 = smem_addr(st), b0 = smem_addr(qb + 2 * pl.uSpan);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc_mma_bf16(tmem, desc_kmajor_sw128(a0 + 32 * kk), desc_kmajor_sw128(b0 + 32 * kk),
-                      idesc, (c | kk) != 0 ? 1u : 0u);
-        tc_commit(&empty_b[bs]);
-        tc_commit(&empty_q[qs]);
-        if (c == nch - 1) tc_commit(dready);
-      }
-    }
-    release_b(bs, false);
+    release(bs, false);
   }
 
   // row sums of squares: the 8 chunks of a row sit in 8 consecutive lanes
@@ -327,43 +264,54 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   named_barrier(1, kCompute);
 
   // ------------------------------------ sweep 2 ------------------------------------
-  // warp w: token w / 2, queries (w % 2) * 12 + [0, 12); lane: group of 3 queries, chunk
+  // warp w: token w / 2, queries (w % 2) * 12 + [0, 12); lane: group of 3 queries, chunk.
+  // The thread's weights (n sources x 3 queries, as (a, a) pairs) stay in registers.
   const int t2 = warp >> 1;
   const int grp = (warp & 1) * 4 + (lane >> 3);
   const int kg = lane & 7;
   const int64_t tok2 = t0 + t2;
   const bool active2 = grp * 3 < S;
-  const float* at = alph + ((t2 * n) * 8 + grp) * 8;
+  float2 al[kMaxN][3];
+#pragma unroll
+  for (int j = 0; j < kMaxN; ++j) {
+    const float* ap = alph + ((t2 * n + j) * 8 + grp) * 8;
+#pragma unroll
+    for (int qq = 0; qq < 3; ++qq)
+      al[j][qq] = j < n ? *reinterpret_cast<const float2*>(ap + 2 * qq) : make_float2(0.f, 0.f);
+  }
+  // source j's chunk: row j * 8 + t2, swizzled chunk kg ^ t2 (independent of j)
+  const int boff = t2 * 128 + ((kg ^ t2) << 4);
   char* o = static_cast<char*>(a.o);
   for (int ib = nch; ib < total; ++ib) {
     const int bs = ib % SB;
     const int c = total - 1 - ib;  // columns in reverse
-    wait(&full_b[bs], (ib / SB) & 1);
+    wait(&full[bs], (ib / SB) & 1);
     if (active2) {
-      const unsigned char* st = smem + bs * pl.bSlot;
+      const unsigned char* st = smem + bs * pl.slot + boff;
       float2 acc[3][4];
 #pragma unroll
       for (int qq = 0; qq < 3; ++qq)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[qq][e] = make_float2(0.f, 0.f);
-      for (int j = 0; j < n; ++j) {
-        float2 bv[4];
-        unpack_pairs(*reinterpret_cast<const uint4*>(st + sw128(j * kTT + t2, kg)), bv);
-        const float4 a01 = *reinterpret_cast<const float4*>(at + j * 64);
-        const float2 a2 = *reinterpret_cast<const float2*>(at + j * 64 + 4);
-        const float2 al[3] = {make_float2(a01.x, a01.y), make_float2(a01.z, a01.w), a2};
 #pragma unroll
-        for (int qq = 0; qq < 3; ++qq)
+      for (int j = 0; j < kMaxN; ++j) {
+        if (j < n) {
+          float2 bv[4];
+          unpack_pairs(*reinterpret_cast<const uint4*>(st + j * 1024), bv);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc[qq][e] = __ffma2_rn(al[qq], bv[e], acc[qq][e]);
+          for (int qq = 0; qq < 3; ++qq)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[qq][e] = __ffma2_rn(al[j][qq], bv[e], acc[qq][e]);
+        }
       }
       const int k = c * kKC + kg * 8;
       if (tok2 < T && k < d) {
+        char* op = o + ((static_cast<int64_t>(grp * 3) * T + tok2) * d + k) * 2;
+        const int64_t qstride = T * d * 2;
 #pragma unroll
         for (int qq = 0; qq < 3; ++qq) {
-          const int q = grp * 3 + qq;
-          if (q < S)
-            __stcs(reinterpret_cast<uint4*>(o + ((static_cast<int64_t>(q) * T + tok2) * d + k) * 2),
+          if (grp * 3 + qq < S)
+            __stcs(reinterpret_cast<uint4*>(op + qq * qstride),
                    make_uint4(pack_bf16x2(acc[qq][0].x, acc[qq][0].y),
                               pack_bf16x2(acc[qq][1].x, acc[qq][1].y),
                               pack_bf16x2(acc[qq][2].x, acc[qq][2].y),
@@ -371,7 +319,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
         }
       }
     }
-    release_b(bs, true);
+    release(bs, true);
   }
 
   // ------------------------------------ teardown ------------------------------------
@@ -394,15 +342,15 @@ bool phase1_tc_supported(int n, int S) {
 
 cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s) {
   TcPlan pl;
-  if (!make_tc_plan(a.n, a.S, pl)) return cudaErrorInvalidValue;
-  CUtensorMap mb, mu;
+  if (a.u_split == nullptr || !make_tc_plan(a.n, a.S, pl)) return cudaErrorInvalidValue;
+  CUtensorMap mb, mq;
   cudaError_t e = encode_source_map(&mb, a.reps, a.src_stride, a.n, a.T, a.d, 2, kKC, kTT);
-  if (e == cudaSuccess) e = encode_query_map(&mu, a.u, a.S, a.d);
+  if (e == cudaSuccess) e = encode_split_query_map(&mq, a.u_split, a.S, a.d, pl.Npad);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(phase1_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
   if (e != cudaSuccess) return e;
   const int64_t blocks = (a.T + kTT - 1) / kTT;
-  phase1_tc_kernel<<<static_cast<unsigned>(blocks), kThreads, pl.smem, s>>>(mb, mu, a, pl);
+  phase1_tc_kernel<<<static_cast<unsigned>(blocks), kThreads, pl.smem, s>>>(mb, mq, a, pl);
   return cudaGetLastError();
 }
 

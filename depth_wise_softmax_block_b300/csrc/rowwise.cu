@@ -8,7 +8,7 @@
 //   full_kernel    the direct single-pass aggregation over an explicit source list (§7),
 //                  online softmax over the sources, then the input RMSNorm.
 //   add_kernel     partial-sum update / block close: out = partial + v.
-//   prep_kernel    query preparation u = w ⊙ gamma_key.
+//   prep_kernel    query preparation u = w ⊙ gamma_key (and its bf16 hi/lo split).
 //
 // Each thread owns VPT 16-byte vectors of the row (vector v = threadIdx.x + k * blockDim.x).
 #include <math.h>
@@ -286,7 +286,10 @@ __global__ void add_kernel(const T* __restrict__ pa, const T* __restrict__ pb, T
   }
 }
 
-__global__ void prep_kernel(const float* w, const float* g, float* u, int64_t n4) {
+// u = w * g; with `split`, also rows 2r (hi) and 2r + 1 (lo) of the bf16 split of u:
+// hi = bf16(u), lo = bf16(u - hi), both rounded to nearest even.
+__global__ void prep_kernel(const float* w, const float* g, float* u, uint16_t* split, int d,
+                            int64_t n4) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float4 x = reinterpret_cast<const float4*>(w)[i];
@@ -298,6 +301,16 @@ __global__ void prep_kernel(const float* w, const float* g, float* u, int64_t n4
       x.w *= y.w;
     }
     reinterpret_cast<float4*>(u)[i] = x;
+    if (split != nullptr) {
+      const int64_t e = i * 4, r = e / d, c = e - r * d;
+      const uint32_t h0 = pack_bf16x2(x.x, x.y), h1 = pack_bf16x2(x.z, x.w);
+      const uint32_t l0 = pack_bf16x2(x.x - __uint_as_float(h0 << 16),
+                                      x.y - __uint_as_float(h0 & 0xffff0000u));
+      const uint32_t l1 = pack_bf16x2(x.z - __uint_as_float(h1 << 16),
+                                      x.w - __uint_as_float(h1 & 0xffff0000u));
+      *reinterpret_cast<uint2*>(split + (2 * r) * d + c) = make_uint2(h0, h1);
+      *reinterpret_cast<uint2*>(split + (2 * r + 1) * d + c) = make_uint2(l0, l1);
+    }
   }
 }
 
@@ -375,11 +388,13 @@ cudaError_t launch_partial_update(IO io, const void* pa, const void* pb, void* o
   return cudaGetLastError();
 }
 
-cudaError_t launch_query_prep(const float* w, const float* g, float* u, int64_t n_elems,
-                              cudaStream_t s) {
+cudaError_t launch_query_prep(const float* w, const float* g, float* u, void* u_split, int rows,
+                              int d, cudaStream_t s) {
+  const int64_t n_elems = static_cast<int64_t>(rows) * d;
   if (n_elems == 0) return cudaSuccess;
   constexpr int threads = 256;
-  prep_kernel<<<grid_for(n_elems / 4, threads), threads, 0, s>>>(w, g, u, n_elems / 4);
+  prep_kernel<<<grid_for(n_elems / 4, threads), threads, 0, s>>>(
+      w, g, u, static_cast<uint16_t*>(u_split), d, n_elems / 4);
   return cudaGetLastError();
 }
 

@@ -57,4 +57,19 @@ cudaError_t encode_query_map(CUtensorMap* map, const float* u, int S, int d) {
   return cudaSuccess;
 }
 
+cudaError_t encode_split_query_map(CUtensorMap* map, const void* u_split, int S, int d,
+                                   int rows_box) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const cuuint32_t unit[2] = {1, 1};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(2 * S)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(rows_box)};
+  if (enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(u_split), dims, strides, box,
+          unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
 }  // namespace attnres

@@ -71,19 +71,21 @@ class BlockRunner:
     def run_block(self, reps: torch.Tensor, U: torch.Tensor, G_in: Optional[torch.Tensor],
                   sublayer: Callable[[int, torch.Tensor], torch.Tensor], close_out: torch.Tensor,
                   eps_key: float = 1e-6, eps_in: float = 1e-6,
-                  on_call: Optional[Callable] = None) -> None:
+                  on_call: Optional[Callable] = None,
+                  U_split: Optional[torch.Tensor] = None) -> None:
         """Run one block.
 
         reps: [n, T, d] completed sources (any source stride); U: [S, d] folded queries;
         G_in: [S, d] input-norm gains or None; sublayer(i, y_i) -> v_i ([T, d], 1-based i);
         close_out: [T, d] receives b^S.  ``on_call(i, kind, args)`` is invoked before each
-        phase-2 call (tests use it to snapshot the exact inputs).
+        phase-2 call (tests use it to snapshot the exact inputs).  U_split: [2S, d] bf16
+        hi/lo split of U (attnres_query_prep), which puts phase 1's logits on the tensor cores.
         """
         S = U.shape[0]
         assert S <= self.S_max
         o, lse = self.o[:S], self.lse[:S]
         tm = self.timer
-        _call(tm, "phase1", attnres_phase1, reps, U, o, lse_out=lse, eps=eps_key)
+        _call(tm, "phase1", attnres_phase1, reps, U, o, lse_out=lse, eps=eps_key, u_split=U_split)
         v_prev = None       # v_{i-1}
         part = None         # tensor holding b^{i-2} (None while it is zero)
         for i in range(1, S + 1):

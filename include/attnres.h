@@ -57,7 +57,7 @@ typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype;
 #define ATTNRES_MAX_D 16384        /* hidden size (a row stays in registers)               */
 
 /* ABI version of this header; attnres_abi_version() returns the library's. */
-#define ATTNRES_ABI_VERSION 1
+#define ATTNRES_ABI_VERSION 2
 int attnres_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -67,8 +67,8 @@ const char* attnres_status_string(attnres_status status);
 const char* attnres_last_cuda_error(void);
 
 /*
- * Device-side error poll.  The phase-1 kernel stages its tiles with asynchronous tensor copies
- * and waits for them on shared-memory barriers; every such wait is bounded.  A wait that gives
+ * Device-side error poll.  The phase-1 kernels stage their tiles with asynchronous tensor
+ * copies and wait for them on shared-memory barriers; every such wait is bounded.  A wait that gives
  * up (a copy that never lands) makes the kernel finish early with undefined outputs and counts
  * the event in a device word of the current device.  This call reads and clears that word:
  * ATTNRES_ERR_TIMEOUT if any wait gave up since the previous poll, ATTNRES_OK otherwise,
@@ -84,12 +84,16 @@ attnres_status attnres_poll_device_errors(void);
  * w . RMSNorm(v) = (w ⊙ gamma_key) . v / r(v).  The gain belongs to the target sublayer
  * (one query and one set of key-norm gains per sublayer), so the product is a per-sublayer
  * parameter: compute it once and pass u to the calls below.
- *   w          device, fp32 [rows, d]
- *   gamma_key  device, fp32 [rows, d], or NULL for all-ones gains (u = w)
- *   u_out      device, fp32 [rows, d]; may alias w (in place)
+ *   w            device, fp32 [rows, d]
+ *   gamma_key    device, fp32 [rows, d], or NULL for all-ones gains (u = w)
+ *   u_out        device, fp32 [rows, d]; may alias w (in place)
+ *   u_split_out  device, bf16 [2 * rows, d], or NULL: rows 2r and 2r + 1 receive
+ *                hi = bf16(u_r) and lo = bf16(u_r - hi) (round to nearest even), so that
+ *                |u - hi - lo| <= 2^-16 |u|.  Phase 1 computes its logits on the tensor cores
+ *                from this form (see attnres_phase1).  Must not overlap w or u_out.
  */
 attnres_status attnres_query_prep(const float* w, const float* gamma_key, float* u_out,
-                                  int rows, int d, void* stream);
+                                  void* u_split_out, int rows, int d, void* stream);
 
 /*
  * Phase 1 (rows a1-a4): the S queries of one block against the n completed sources,
@@ -104,6 +108,12 @@ attnres_status attnres_query_prep(const float* w, const float* gamma_key, float*
  *               reps + j*src_stride + t*d elements.  src_stride >= T*d, a multiple of 8.
  *   u           device fp32 [S, d]: the block's queries with key gains folded in
  *               (attnres_query_prep)
+ *   u_split     device bf16 [2S, d] or NULL: the same queries split into hi/lo rows
+ *               (attnres_query_prep's u_split_out for these S rows).  When it is given, the I/O
+ *               type is bf16, 2 <= S <= 24 and n_src <= 9, the logit numerators u_s . b_j[t] are
+ *               computed on the tensor cores as (hi + lo) . b_j[t] with fp32 accumulation;
+ *               otherwise the CUDA cores compute them from u in fp32.  Both agree to fp32
+ *               rounding plus the split's 2^-16 relative error in u.
  *   o_out       device [S][T][d] (io dtype), required
  *   m_out, lse_out  device fp32 [S][T], each optional (NULL = not written)
  *   alpha_out   device fp32 [S][T][n_src], optional
@@ -113,9 +123,9 @@ attnres_status attnres_query_prep(const float* w, const float* gamma_key, float*
  * b_0 .. b_N (row a10).
  */
 attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, int64_t T,
-                              int d, attnres_dtype io, const float* u, int S, float eps,
-                              void* o_out, float* m_out, float* lse_out, float* alpha_out,
-                              void* stream);
+                              int d, attnres_dtype io, const float* u, const void* u_split,
+                              int S, float eps, void* o_out, float* m_out, float* lse_out,
+                              float* alpha_out, void* stream);
 
 /*
  * Phase 2 merge (rows a5-a8): one sublayer l of the block ("Attention Residuals" §10,

@@ -45,14 +45,14 @@ def test_header_symbols_exported(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.attnres_abi_version() == 1
+    assert lib.attnres_abi_version() == 2
     for code, name in ar.STATUS.items():
         assert lib.attnres_status_string(code).decode() == name
     assert lib.attnres_status_string(99).decode() == "ATTNRES_ERR_UNKNOWN"
 
 
-def p1(lib, reps=P, stride=1024 * 64, n=2, T=0, d=64, io=1, u=P, S=4, eps=1e-6, o=P):
-    return lib.attnres_phase1(reps, stride, n, T, d, io, u, S, eps, o, None, None, None, None)
+def p1(lib, reps=P, stride=1024 * 64, n=2, T=0, d=64, io=1, u=P, S=4, eps=1e-6, o=P, us=None):
+    return lib.attnres_phase1(reps, stride, n, T, d, io, u, us, S, eps, o, None, None, None, None)
 
 
 def test_phase1_validation(lib):
@@ -81,6 +81,8 @@ def test_phase1_validation(lib):
     assert err(p1(lib, T=4, u=PM)) == MISALIGNED
     assert err(p1(lib, T=4, o=PM)) == MISALIGNED
     assert err(p1(lib, T=4, stride=1024 * 64 + 4)) == MISALIGNED  # source 1 misaligned
+    assert err(p1(lib, T=4, us=PM)) == MISALIGNED         # split queries misaligned
+    assert p1(lib, us=P) == OK
 
 
 def p2(lib, o=P, lse=P, part=None, v=None, pout=None, T=0, d=64, io=1, u=P, g=None, y=P, h=None):
@@ -124,9 +126,11 @@ def test_full_and_update_validation(lib):
     assert err(up(P, P, PM, 4, 64, 1, None)) == MISALIGNED
     assert up(P, P, P, 0, 63, 1, None) == INVALID
     qp = lib.attnres_query_prep
-    assert qp(P, None, P, 0, 64, None) == OK
-    assert err(qp(None, None, P, 4, 64, None)) == INVALID
-    assert err(qp(P, PM, P, 4, 64, None)) == MISALIGNED
+    assert qp(P, None, P, None, 0, 64, None) == OK
+    assert qp(P, None, P, P, 0, 64, None) == OK
+    assert err(qp(None, None, P, None, 4, 64, None)) == INVALID
+    assert err(qp(P, PM, P, None, 4, 64, None)) == MISALIGNED
+    assert err(qp(P, None, P, PM, 4, 64, None)) == MISALIGNED
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

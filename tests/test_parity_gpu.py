@@ -22,14 +22,10 @@ def dev():
     return torch.device("cuda:0")
 
 
-@pytest.fixture(params=["default", "cuda_cores"])
-def p1path(request, monkeypatch):
-    """Phase-1 kernel choice: the default (tensor-core logits where supported: bf16,
-    2 <= S <= 24, n <= 16) or the CUDA-core kernel for every shape."""
-    if request.param == "cuda_cores":
-        monkeypatch.setenv("ATTNRES_PHASE1_PATH", "cuda_cores")
-    else:
-        monkeypatch.delenv("ATTNRES_PHASE1_PATH", raising=False)
+@pytest.fixture(params=["tensor_cores", "cuda_cores"])
+def p1path(request):
+    """Phase-1 kernel choice: with the split queries (tensor-core logits where the shape
+    allows: bf16, 2 <= S <= 24, n <= 9) or without them (CUDA-core kernel for every shape)."""
     return request.param
 
 
@@ -54,14 +50,22 @@ def make_queries(S, d, dev, seed, jitter=0.02, scale=1.0, zero=False):
     return W, G, U
 
 
-def run_phase1(reps, U):
+def split_of(U):
+    """The bf16 hi/lo split of the queries U, as attnres_query_prep writes it."""
+    us = torch.empty((2 * U.shape[0], U.shape[1]), dtype=torch.bfloat16, device=U.device)
+    ar.attnres_query_prep(U, None, torch.empty_like(U), us)
+    return us
+
+
+def run_phase1(reps, U, path="cuda_cores"):
     n, T, d = reps.shape
     S = U.shape[0]
     o = torch.empty((S, T, d), dtype=reps.dtype, device=reps.device)
     m = torch.empty((S, T), dtype=torch.float32, device=reps.device)
     lse = torch.empty_like(m)
     alpha = torch.empty((S, T, n), dtype=torch.float32, device=reps.device)
-    ar.attnres_phase1(reps, U, o, m, lse, alpha, eps=EPS)
+    us = split_of(U) if path == "tensor_cores" else None
+    ar.attnres_phase1(reps, U, o, m, lse, alpha, eps=EPS, u_split=us)
     torch.cuda.synchronize()
     return o, m, lse, alpha
 
@@ -84,7 +88,8 @@ P1_CASES = [
     (64, 2, 11, 64, "bf16"),        # n at its maximum with two queries
     (2, 2, 70, 136, "f32"),
     (7, 5, 23, 96, "f32"),
-    (16, 24, 21, 320, "bf16"),      # the tensor-core path's largest tile (16 sources x 8 tokens)
+    (9, 24, 21, 320, "bf16"),       # the tensor-core path's largest tile (9 sources x 8 tokens)
+    (16, 24, 21, 320, "bf16"),      # beyond it: CUDA-core kernel
     (1, 2, 9, 64, "bf16"),          # its smallest (one source, two queries)
     (3, 7, 8, 136, "bf16"),         # odd S, ragged last column stage
     (17, 24, 12, 128, "bf16"),      # n beyond the tensor-core tile: CUDA-core kernel
@@ -96,7 +101,7 @@ def test_phase1_matches_oracle(dev, p1path, n, S, T, d, dt):
     seed = 1000 + n * 7 + S
     reps = make_reps(n, T, d, _dt(dt), dev, seed)
     W, G, U = make_queries(S, d, dev, seed)
-    o, m, lse, alpha = run_phase1(reps, U)
+    o, m, lse, alpha = run_phase1(reps, U, p1path)
     oo, om, olse, oalpha = O.phase1(to64(reps), to64(W), to64(G), EPS)
     tol = TOL[dt]
     check_outputs(o, oo, dt, "o")
@@ -105,13 +110,29 @@ def test_phase1_matches_oracle(dev, p1path, n, S, T, d, dt):
     check_close(alpha, oalpha, tol["weight"], "alpha")
 
 
+def test_query_split(dev):
+    """attnres_query_prep's split: hi = bf16(u), lo = bf16(u - hi), |u - hi - lo| <= 2^-16 |u|."""
+    S, d = 24, 7168
+    W = I.queries(S, d, 5, "w", dev)
+    G = I.gains(S, d, 0.02, 5, "g", dev)
+    U = torch.empty_like(W)
+    us = torch.empty((2 * S, d), dtype=torch.bfloat16, device=dev)
+    ar.attnres_query_prep(W, G, U, us)
+    torch.cuda.synchronize()
+    u = to64(U)
+    hi, lo = to64(us[0::2]), to64(us[1::2])
+    assert torch.equal(us[0::2], U.to(torch.bfloat16))                   # round to nearest even
+    assert torch.equal(us[1::2], (U - us[0::2].float()).to(torch.bfloat16))
+    assert np.all(np.abs(u - hi - lo) <= 2.0 ** -16 * np.abs(u))
+
+
 def test_phase1_chunk_view(dev, p1path):
     """A token chunk of a larger cache: source stride != T*d and an offset base pointer."""
     n, Ttot, d, S = 9, 300, 512, 24
     reps_all = make_reps(n, Ttot, d, torch.bfloat16, dev, 77)
     W, G, U = make_queries(S, d, dev, 77)
     view = reps_all[:, 128:245]
-    o, m, lse, alpha = run_phase1(view, U)
+    o, m, lse, alpha = run_phase1(view, U, p1path)
     oo, om, olse, oalpha = O.phase1(to64(view), to64(W), to64(G), EPS)
     check_outputs(o, oo, "bf16", "o (chunk view)")
     check_close(lse, olse, 1e-3, "lse (chunk view)")
@@ -133,7 +154,7 @@ def test_phase1_extreme_logits(dev, p1path):
     n, T, d, S = 9, 24, 512, 24
     reps = make_reps(n, T, d, torch.bfloat16, dev, 9)
     W, G, U = make_queries(S, d, dev, 9, scale=60.0)
-    o, m, lse, alpha = run_phase1(reps, U)
+    o, m, lse, alpha = run_phase1(reps, U, p1path)
     oo, om, olse, oalpha = O.phase1(to64(reps), to64(W), to64(G), EPS)
     assert float(to64(alpha).max()) > 0.999
     check_outputs(o, oo, "bf16", "o (near one-hot)")
@@ -144,8 +165,8 @@ def test_phase1_extreme_logits(dev, p1path):
 def test_phase1_deterministic(dev, p1path):
     reps = make_reps(9, 50, 1024, torch.bfloat16, dev, 3)
     _, _, U = make_queries(24, 1024, dev, 3)
-    a = run_phase1(reps, U)
-    b = run_phase1(reps, U)
+    a = run_phase1(reps, U, p1path)
+    b = run_phase1(reps, U, p1path)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
 
@@ -280,5 +301,5 @@ def test_no_bounded_wait_gave_up(dev, p1path):
     n, T, d, S = 9, 300, 7168, 24
     reps = make_reps(n, T, d, torch.bfloat16, dev, 31)
     W, G, U = make_queries(S, d, dev, 31)
-    run_phase1(reps, U)
+    run_phase1(reps, U, p1path)
     ar.attnres_poll_device_errors()

@@ -33,14 +33,17 @@ def dev():
 
 
 def folded(P, dev):
+    """Folded queries U [L, d], the final query, and U's bf16 hi/lo split [2L, d] (which the
+    bf16 walks pass to phase 1, as the bench does)."""
     U = torch.empty_like(P.W)
-    ar.attnres_query_prep(P.W, P.G_key, U)
+    U_split = torch.empty((2 * U.shape[0], U.shape[1]), dtype=torch.bfloat16, device=dev)
+    ar.attnres_query_prep(P.W, P.G_key, U, U_split)
     uf = torch.empty_like(P.w_final)
     ar.attnres_query_prep(P.w_final.view(1, -1), P.g_final.view(1, -1), uf.view(1, -1))
-    return U, uf
+    return U, uf, U_split
 
 
-def gpu_block_walk(wl, reps, v, P, U, uf, dev, consistent=False):
+def gpu_block_walk(wl, reps, v, P, U, uf, dev, consistent=False, U_split=None):
     """The whole depth on the GPU.  reps: [N+1, T, d] (slot 0 = b_0, given blocks after);
     v: [L, T, d].  Returns (ys [L, T, d], final [T, d], closed blocks)."""
     T, d, L, S = wl.T, wl.d, wl.L, wl.S
@@ -57,7 +60,9 @@ def gpu_block_walk(wl, reps, v, P, U, uf, dev, consistent=False):
             ys[l0 + i - 1].copy_(y)
             return v[l0 + i - 1]
 
-        runner.run_block(src[:n], U[l0:l0 + Sn], P.G_in[l0:l0 + Sn], sublayer, closed[n - 1])
+        us = None if U_split is None else U_split[2 * l0:2 * (l0 + Sn)]
+        runner.run_block(src[:n], U[l0:l0 + Sn], P.G_in[l0:l0 + Sn], sublayer, closed[n - 1],
+                         U_split=us)
         if consistent:
             src[n].copy_(closed[n - 1])
     fin = torch.empty((T, d), dtype=wl.torch_dtype, device=dev)
@@ -74,7 +79,7 @@ def test_tiny_block_f32_every_element(dev, zero, consistent):
     reps = I.make_reps(wl, N + 1, dev)
     v = I.make_outputs(wl, 1, wl.L, dev)
     P = I.block_params(wl, dev, zero_queries=zero)
-    U, uf = folded(P, dev)
+    U, uf, _ = folded(P, dev)
     ys, fin, closed = gpu_block_walk(wl, reps, v, P, U, uf, dev, consistent)
     ow = O.block_attnres_walk(to64(reps[0]), to64(reps[1:]), to64(v), wl.S, to64(P.W),
                               to64(P.G_key), to64(P.G_in), to64(P.w_final), to64(P.g_final),
@@ -92,7 +97,7 @@ def _block_walk_checked(wl, dev, rows_k, report):
     rows = sample_rows(T, rows_k, seed=wl.seed)
     reps = I.make_reps(wl, N + 1, dev)
     P = I.block_params(wl, dev)
-    U, uf = folded(P, dev)
+    U, uf, U_split = folded(P, dev)
     runner = BlockRunner(T, d, S, wl.torch_dtype, dev)
     vbuf = torch.empty((S, T, d), dtype=wl.torch_dtype, device=dev)
     close = torch.empty((T, d), dtype=wl.torch_dtype, device=dev)
@@ -103,7 +108,7 @@ def _block_walk_checked(wl, dev, rows_k, report):
             I.fill_sublayer_output(vbuf[i], l0 + i + 1, wl.seed)
         run_checked_block(runner, reps[:n], U[l0:l0 + Sn], P.W[l0:l0 + Sn],
                           P.G_key[l0:l0 + Sn], P.G_in[l0:l0 + Sn], vbuf[:Sn], close, "bf16",
-                          rows, report=report)
+                          rows, report=report, U_split=U_split[2 * l0:2 * (l0 + Sn)])
     fin = torch.empty((T, d), dtype=wl.torch_dtype, device=dev)
     final_aggregation(reps[:N + 1], uf, fin)
     torch.cuda.synchronize()
@@ -133,7 +138,7 @@ def test_full_attnres_bf16(dev):
     for l in range(1, L + 1):
         I.fill_sublayer_output(hist[l], l, wl.seed, wl.v_growth)    # v_l ~ N(0,1)(1 + 0.05 l)
     P = I.block_params(wl, dev)
-    U, uf = folded(P, dev)
+    U, uf, _ = folded(P, dev)
     y_full = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
     h_full = torch.empty_like(y_full)
     o = torch.empty((1, T, d), dtype=torch.bfloat16, device=dev)
@@ -174,7 +179,7 @@ def test_longctx_prefill_bench_step_sampled(dev):
         reps_c, close_c, all_c, out_c = st.chunk_views(c)
         rep = {}
         run_checked_block(st.runner, reps_c, st.U, st.P.W, st.P.G_key, st.P.G_in, st.vbuf,
-                          close_c, "bf16", rows, wl.eps, rep)
+                          close_c, "bf16", rows, wl.eps, rep, U_split=st.U_split)
         final_aggregation(all_c, st.uf[0], out_c, wl.eps)
         torch.cuda.synchronize()
         want, _, _ = O.aggregate(to64(all_c[:, rows]), to64(st.P.w_final), to64(st.P.g_final),

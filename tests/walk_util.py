@@ -70,8 +70,9 @@ class BlockChecker:
 
 
 def run_checked_block(runner, reps, U, W, Gk, Gin, vbuf, close_out, dtype, rows, eps=1e-6,
-                      report=None):
-    """Run one block with per-call checks.  vbuf: [S, T, d] stand-in sublayer outputs."""
+                      report=None, U_split=None):
+    """Run one block with per-call checks.  vbuf: [S, T, d] stand-in sublayer outputs;
+    U_split: the queries' bf16 split (tensor-core phase 1) or None."""
     chk = BlockChecker(reps, W, Gk, Gin, dtype, rows, eps, report)
     S = U.shape[0]
 
@@ -84,7 +85,8 @@ def run_checked_block(runner, reps, U, W, Gk, Gin, vbuf, close_out, dtype, rows,
             chk.phase1_done(runner.o[:S], runner.lse[:S])
         chk.before(i, args)
 
-    runner.run_block(reps, U, Gin, sublayer, close_out, eps, eps, on_call=on_call)
+    runner.run_block(reps, U, Gin, sublayer, close_out, eps, eps, on_call=on_call,
+                     U_split=U_split)
     torch.cuda.synchronize()
     # the close is exactly round(b^{S-1} + v_S) of the stored tensors
     if S >= 2:
