@@ -17,6 +17,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libattnres.so")
 
 F32, BF16 = 0, 1
+SIGMOID_WEIGHTS, NO_KEY_NORM = 0x1, 0x2   # variant flags (include/attnres.h)
+_U = ctypes.c_uint
 STATUS = {0: "ATTNRES_OK", 1: "ATTNRES_ERR_INVALID_ARG", 2: "ATTNRES_ERR_UNSUPPORTED",
           3: "ATTNRES_ERR_MISALIGNED", 4: "ATTNRES_ERR_CUDA", 5: "ATTNRES_ERR_TIMEOUT"}
 
@@ -28,11 +30,13 @@ SIGNATURES = {
     "attnres_last_cuda_error": ([], ctypes.c_char_p),
     "attnres_poll_device_errors": ([], _I),
     "attnres_query_prep": ([_P, _P, _P, _P, _I, _I, _P], _I),
-    "attnres_phase1": ([_P, _I64, _I, _I64, _I, _I, _P, _P, _I, _F, _P, _P, _P, _P, _P], _I),
-    "attnres_phase2_merge": ([_P, _P, _P, _P, _P, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _P],
-                             _I),
+    "attnres_phase1": ([_P, _I64, _I, _I64, _I, _I, _P, _P, _I, _F, _P, _P, _P, _P, _U, _P],
+                       _I),
+    "attnres_phase2_merge": ([_P, _P, _P, _P, _P, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _U,
+                              _P], _I),
     "attnres_partial_update": ([_P, _P, _P, _I64, _I, _I, _P], _I),
-    "attnres_full_reference_path": ([_P, _I, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _P], _I),
+    "attnres_full_reference_path": ([_P, _I, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _U, _P],
+                                    _I),
 }
 
 
@@ -112,7 +116,7 @@ def attnres_query_prep(w, gamma_key, u_out, u_split_out=None, stream=None):
 
 
 def attnres_phase1(reps, u, o_out, m_out=None, lse_out=None, alpha_out=None, eps=1e-6,
-                   u_split=None, stream=None):
+                   u_split=None, flags=0, stream=None):
     """Phase 1 over ``reps`` [n, T, d] (any source stride, rows of stride d) for the S queries
     ``u`` [S, d]; writes o [S, T, d] and the optional statistics.  ``u_split`` ([2S, d] bf16,
     from attnres_query_prep) puts the logits on the tensor cores where the shape allows."""
@@ -127,12 +131,13 @@ def attnres_phase1(reps, u, o_out, m_out=None, lse_out=None, alpha_out=None, eps
     src_stride = reps.stride(0) if n > 1 else T * d
     _check(library().attnres_phase1(_ptr(reps), src_stride, n, T, d, _io(reps), _ptr(u),
                                     _ptr(u_split), S, eps, _ptr(o_out), _ptr(m_out), _ptr(lse_out),
-                                    _ptr(alpha_out), _stream(stream)), "attnres_phase1")
+                                    _ptr(alpha_out), flags, _stream(stream)), "attnres_phase1")
     return o_out
 
 
 def attnres_phase2_merge(o_l, lse_l, partial, v_prev, partial_out, u_l, gamma_in, y_out,
-                         h_out=None, alpha_p_out=None, eps_key=1e-6, eps_in=1e-6, stream=None):
+                         h_out=None, alpha_p_out=None, eps_key=1e-6, eps_in=1e-6, flags=0,
+                         stream=None):
     """Phase 2 for one sublayer: merge the partial-sum source (partial + v_prev) into the
     phase-1 result and apply the input RMSNorm.  Tensors are [T, d]."""
     T, d = o_l.shape
@@ -142,7 +147,7 @@ def attnres_phase2_merge(o_l, lse_l, partial, v_prev, partial_out, u_l, gamma_in
     _check(library().attnres_phase2_merge(
         _ptr(o_l), _ptr(lse_l), _ptr(partial), _ptr(v_prev), _ptr(partial_out), T, d, _io(o_l),
         _ptr(u_l), eps_key, _ptr(gamma_in), eps_in, _ptr(h_out), _ptr(y_out), _ptr(alpha_p_out),
-        _stream(stream)), "attnres_phase2_merge")
+        flags, _stream(stream)), "attnres_phase2_merge")
     return y_out
 
 
@@ -158,7 +163,7 @@ def attnres_partial_update(partial, v, out, stream=None):
 
 
 def attnres_full_reference_path(srcs, u_l, gamma_in, h_out=None, y_out=None, alpha_out=None,
-                                eps_key=1e-6, eps_in=1e-6, stream=None):
+                                eps_key=1e-6, eps_in=1e-6, flags=0, stream=None):
     """Direct single-pass aggregation over the list of [T, d] source tensors ``srcs``."""
     T, d = srcs[0].shape
     for t in srcs:
@@ -166,6 +171,6 @@ def attnres_full_reference_path(srcs, u_l, gamma_in, h_out=None, y_out=None, alp
     arr = (ctypes.c_void_p * len(srcs))(*[t.data_ptr() for t in srcs])
     _check(library().attnres_full_reference_path(
         arr, len(srcs), T, d, _io(srcs[0]), _ptr(u_l), eps_key, _ptr(gamma_in), eps_in,
-        _ptr(h_out), _ptr(y_out), _ptr(alpha_out), _stream(stream)),
+        _ptr(h_out), _ptr(y_out), _ptr(alpha_out), flags, _stream(stream)),
         "attnres_full_reference_path")
     return h_out if y_out is None else y_out

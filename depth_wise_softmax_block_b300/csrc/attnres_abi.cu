@@ -17,6 +17,9 @@ using attnres::IO;
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool opt_aligned16(const void* p) { return p == nullptr || aligned16(p); }
 bool valid_io(attnres_dtype io) { return io == ATTNRES_F32 || io == ATTNRES_BF16; }
+bool valid_flags(unsigned flags) {
+  return (flags & ~(ATTNRES_SIGMOID_WEIGHTS | ATTNRES_NO_KEY_NORM)) == 0;
+}
 
 attnres_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return ATTNRES_OK;
@@ -81,8 +84,8 @@ attnres_status attnres_query_prep(const float* w, const float* gamma_key, float*
 attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, int64_t T, int d,
                               attnres_dtype io, const float* u, const void* u_split, int S,
                               float eps, void* o_out, float* m_out, float* lse_out,
-                              float* alpha_out, void* stream) {
-  if (!valid_io(io)) return ATTNRES_ERR_INVALID_ARG;
+                              float* alpha_out, unsigned int flags, void* stream) {
+  if (!valid_io(io) || !valid_flags(flags)) return ATTNRES_ERR_INVALID_ARG;
   const attnres_status sh = check_shape(T, d);
   if (sh != ATTNRES_OK) return sh;
   if (n_src < 1 || S < 1 || !(eps >= 0.f)) return ATTNRES_ERR_INVALID_ARG;
@@ -96,7 +99,7 @@ attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, i
       src_stride % 8 != 0)
     return ATTNRES_ERR_MISALIGNED;
   attnres::Phase1Args a{reps,  src_stride, n_src, T,      d,       u,        u_split,
-                        S,     eps,        o_out, m_out, lse_out, alpha_out};
+                        S,     eps,        o_out, m_out, lse_out, alpha_out, flags};
   return cuda_status(attnres::launch_phase1(static_cast<IO>(io), a,
                                             static_cast<cudaStream_t>(stream)));
 }
@@ -105,15 +108,17 @@ attnres_status attnres_phase2_merge(const void* o_l, const float* lse_l, const v
                                     const void* v_prev, void* partial_out, int64_t T, int d,
                                     attnres_dtype io, const float* u_l, float eps_key,
                                     const float* gamma_in, float eps_in, void* h_out, void* y_out,
-                                    float* alpha_p_out, void* stream) {
-  if (!valid_io(io)) return ATTNRES_ERR_INVALID_ARG;
+                                    float* alpha_p_out, unsigned int flags, void* stream) {
+  if (!valid_io(io) || !valid_flags(flags)) return ATTNRES_ERR_INVALID_ARG;
   const attnres_status sh = check_shape(T, d);
   if (sh != ATTNRES_OK) return sh;
   if (!(eps_key >= 0.f) || !(eps_in >= 0.f)) return ATTNRES_ERR_INVALID_ARG;
   if (T == 0) return ATTNRES_OK;
   if (o_l == nullptr || y_out == nullptr) return ATTNRES_ERR_INVALID_ARG;
   const bool has_p = partial != nullptr || v_prev != nullptr;
-  if (has_p && (lse_l == nullptr || u_l == nullptr)) return ATTNRES_ERR_INVALID_ARG;
+  if (has_p && u_l == nullptr) return ATTNRES_ERR_INVALID_ARG;
+  if (has_p && lse_l == nullptr && !(flags & ATTNRES_SIGMOID_WEIGHTS))
+    return ATTNRES_ERR_INVALID_ARG;
   if (partial_out != nullptr && !has_p) return ATTNRES_ERR_INVALID_ARG;
   if (!(eps_key >= 0.f) || !(eps_in >= 0.f)) return ATTNRES_ERR_INVALID_ARG;
   if (!aligned16(o_l) || !aligned16(y_out) || !opt_aligned16(partial) || !opt_aligned16(v_prev) ||
@@ -121,7 +126,7 @@ attnres_status attnres_phase2_merge(const void* o_l, const float* lse_l, const v
       !opt_aligned16(h_out))
     return ATTNRES_ERR_MISALIGNED;
   attnres::Phase2Args a{o_l, lse_l, partial, v_prev, partial_out, T, d, u_l, eps_key, gamma_in,
-                        eps_in, h_out, y_out, alpha_p_out};
+                        eps_in, h_out, y_out, alpha_p_out, flags};
   return cuda_status(attnres::launch_phase2(static_cast<IO>(io), a,
                                             static_cast<cudaStream_t>(stream)));
 }
@@ -141,8 +146,9 @@ attnres_status attnres_partial_update(const void* partial, const void* v, void* 
 attnres_status attnres_full_reference_path(const void* const* srcs, int n_src, int64_t T, int d,
                                            attnres_dtype io, const float* u_l, float eps_key,
                                            const float* gamma_in, float eps_in, void* h_out,
-                                           void* y_out, float* alpha_out, void* stream) {
-  if (!valid_io(io)) return ATTNRES_ERR_INVALID_ARG;
+                                           void* y_out, float* alpha_out, unsigned int flags,
+                                           void* stream) {
+  if (!valid_io(io) || !valid_flags(flags)) return ATTNRES_ERR_INVALID_ARG;
   const attnres_status sh = check_shape(T, d);
   if (sh != ATTNRES_OK) return sh;
   if (n_src < 1) return ATTNRES_ERR_INVALID_ARG;
@@ -171,6 +177,7 @@ attnres_status attnres_full_reference_path(const void* const* srcs, int n_src, i
   a.h = h_out;
   a.y = y_out;
   a.alpha = alpha_out;
+  a.flags = flags;
   return cuda_status(attnres::launch_full(static_cast<IO>(io), a,
                                           static_cast<cudaStream_t>(stream)));
 }

@@ -10,6 +10,10 @@ namespace attnres {
 
 enum class IO { F32 = 0, BF16 = 1 };
 
+// Variant flags (values of ATTNRES_SIGMOID_WEIGHTS / ATTNRES_NO_KEY_NORM in attnres.h).
+constexpr unsigned kSigmoid = 1u;    // alpha_i = sigmoid(z_i), no normalisation over sources
+constexpr unsigned kNoKeyNorm = 2u;  // z_i = u . v_i, no RMS division
+
 struct Phase1Args {
   const void* reps;
   int64_t src_stride;  // elements between sources
@@ -24,6 +28,7 @@ struct Phase1Args {
   float* m;            // [S, T] or null
   float* lse;          // [S, T] or null
   float* alpha;        // [S, T, n] or null
+  unsigned flags;      // kSigmoid | kNoKeyNorm
 };
 
 struct Phase2Args {
@@ -41,6 +46,7 @@ struct Phase2Args {
   void* h;
   void* y;
   float* alpha_p;
+  unsigned flags;
 };
 
 constexpr int kMaxSources = 64;
@@ -59,6 +65,7 @@ struct FullArgs {
   float* alpha;     // [T][n] or null
   float* m;         // [T] or null: max logit
   float* lse;       // [T] or null: log-sum-exp of the logits
+  unsigned flags;
 };
 
 // Each launcher returns cudaSuccess or the launch error.

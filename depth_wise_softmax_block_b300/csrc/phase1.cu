@@ -293,11 +293,13 @@ phase1_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ 
     dots[i] = sum;
   }
   __syncthreads();
-  // 1 / r_j in place of the sum of squares
+  // 1 / r_j (1 without the key RMSNorm) in place of the sum of squares
   const float fd = static_cast<float>(d);
+  const bool key_norm = (a.flags & kNoKeyNorm) == 0;
+  const bool sigmoid = (a.flags & kSigmoid) != 0;
   for (int i = tid; i < TT * n; i += kThreads) {
     float* p = dots + i * S1 + S;
-    *p = 1.f / sqrtf(*p / fd + a.eps);
+    *p = key_norm ? 1.f / sqrtf(*p / fd + a.eps) : 1.f;
   }
   __syncthreads();
 
@@ -312,11 +314,13 @@ phase1_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ 
     float m = -INFINITY;
     for (int j = 0; j < n; ++j) m = fmaxf(m, dt[j * S1 + s] * dt[j * S1 + S]);
     float l = 0.f;
-    for (int j = 0; j < n; ++j) l += expf(dt[j * S1 + s] * dt[j * S1 + S] - m);
+    if (!sigmoid)
+      for (int j = 0; j < n; ++j) l += expf(dt[j * S1 + s] * dt[j * S1 + S] - m);
     const float lse = m + logf(l);
     const float rl = 1.f / l;
     for (int j = 0; j < n; ++j) {
-      const float al = expf(dt[j * S1 + s] * dt[j * S1 + S] - m) * rl;
+      const float zj = dt[j * S1 + s] * dt[j * S1 + S];
+      const float al = sigmoid ? 1.f / (1.f + expf(-zj)) : expf(zj - m) * rl;
       float* ap = alph + (((t * n + j) * QG + s / NQ) * NQ + s % NQ) * 2;
       ap[0] = al;
       ap[1] = al;
@@ -324,7 +328,7 @@ phase1_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ 
     }
     if (tok < T) {
       if (a.m != nullptr) a.m[static_cast<int64_t>(s) * T + tok] = m;
-      if (a.lse != nullptr) a.lse[static_cast<int64_t>(s) * T + tok] = lse;
+      if (a.lse != nullptr && !sigmoid) a.lse[static_cast<int64_t>(s) * T + tok] = lse;
     }
   }
   __syncthreads();
@@ -448,6 +452,7 @@ cudaError_t launch_phase1(IO io, const Phase1Args& a, cudaStream_t s) {
     f.alpha = a.alpha;
     f.m = a.m;
     f.lse = a.lse;
+    f.flags = a.flags;
     return launch_full(io, f, s);
   }
   if (io == IO::BF16 && a.u_split != nullptr && phase1_tc_supported(a.n, a.S))

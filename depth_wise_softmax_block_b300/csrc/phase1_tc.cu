@@ -174,6 +174,8 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
 
   // ------------------------------------ sweep 1 ------------------------------------
   const int nrows = n * kTT;  // tile rows: row j * 8 + t
+  const bool key_norm = (a.flags & kNoKeyNorm) == 0;
+  const bool sigmoid = (a.flags & kSigmoid) != 0;
   float2 ssa[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   for (int c = 0; c < nch; ++c) {
     const int bs = c % SB;
@@ -194,7 +196,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const int i = tid + k * kCompute;
-      if (i < nrows * 8) {
+      if (key_norm && i < nrows * 8) {
         float2 f[4];
         unpack_pairs(*reinterpret_cast<const uint4*>(st + sw128(i >> 3, i & 7)), f);
 #pragma unroll
@@ -222,7 +224,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
     wait(dready, 0);
     tc_fence_after();
     const int r = warp * 32 + lane;
-    const float rinv = r < nrows ? 1.f / sqrtf(ssbuf[r] / fd + a.eps) : 0.f;
+    const float rinv = r >= nrows ? 0.f : key_norm ? 1.f / sqrtf(ssbuf[r] / fd + a.eps) : 1.f;
     for (int cc = 0; cc < pl.Npad / 16; ++cc) {
       uint32_t v[16];
       tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + cc * 16, v);
@@ -245,12 +247,14 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
     float m = -INFINITY;
     for (int j = 0; j < n; ++j) m = fmaxf(m, zbuf[(j * kTT + t) * S + s]);
     float l = 0.f;
-    for (int j = 0; j < n; ++j) l += expf(zbuf[(j * kTT + t) * S + s] - m);
+    if (!sigmoid)
+      for (int j = 0; j < n; ++j) l += expf(zbuf[(j * kTT + t) * S + s] - m);
     const float lse = m + logf(l);
     const float rl = 1.f / l;
     const int g = s / 3, pp = s % 3;
     for (int j = 0; j < n; ++j) {
-      const float al = expf(zbuf[(j * kTT + t) * S + s] - m) * rl;
+      const float zj = zbuf[(j * kTT + t) * S + s];
+      const float al = sigmoid ? 1.f / (1.f + expf(-zj)) : expf(zj - m) * rl;
       float* ap = alph + (((t * n + j) * 8 + g) * 4 + pp) * 2;
       ap[0] = al;
       ap[1] = al;
@@ -258,7 +262,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
     }
     if (tok < T) {
       if (a.m != nullptr) a.m[static_cast<int64_t>(s) * T + tok] = m;
-      if (a.lse != nullptr) a.lse[static_cast<int64_t>(s) * T + tok] = lse;
+      if (a.lse != nullptr && !sigmoid) a.lse[static_cast<int64_t>(s) * T + tok] = lse;
     }
   }
   named_barrier(1, kCompute);

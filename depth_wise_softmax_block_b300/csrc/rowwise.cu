@@ -7,6 +7,8 @@
 //                  merge of two partitions) and applies the sublayer's input RMSNorm.
 //   full_kernel    the direct single-pass aggregation over an explicit source list (§7),
 //                  online softmax over the sources, then the input RMSNorm.
+// Both take the Table 4 variant flags (sigmoid weights, no key RMSNorm; "Attention
+// Residuals" note, result 4).
 //   add_kernel     partial-sum update / block close: out = partial + v.
 //   prep_kernel    query preparation u = w ⊙ gamma_key (and its bf16 hi/lo split).
 //
@@ -87,15 +89,22 @@ __global__ void __launch_bounds__(kMergeThreads) phase2_kernel(const Phase2Args 
     block_sum2(ssp, dot, scratch);
   }
 
-  // Online-softmax merge of the phase-1 partition (lse) with the partial source (z_p).
+  // Online-softmax merge of the phase-1 partition (lse) with the partial source (z_p); with
+  // sigmoid weights the two partitions simply add, h = o + sigmoid(z_p) p.
   float wa = 1.f, wc = 0.f;
   if (has_p) {
-    const float z = dot / sqrtf(ssp / static_cast<float>(a.d) + a.eps_key);
-    const float L = a.lse[row];
-    const float M = fmaxf(L, z);
-    const float ea = expf(L - M), ec = expf(z - M);
-    wa = ea / (ea + ec);
-    wc = ec / (ea + ec);
+    const float z = (a.flags & kNoKeyNorm)
+                        ? dot
+                        : dot / sqrtf(ssp / static_cast<float>(a.d) + a.eps_key);
+    if (a.flags & kSigmoid) {
+      wc = 1.f / (1.f + expf(-z));
+    } else {
+      const float L = a.lse[row];
+      const float M = fmaxf(L, z);
+      const float ea = expf(L - M), ec = expf(z - M);
+      wa = ea / (ea + ec);
+      wc = ec / (ea + ec);
+    }
     if (a.alpha_p != nullptr && threadIdx.x == 0) a.alpha_p[row] = wc;
   }
 
@@ -189,13 +198,20 @@ __global__ void __launch_bounds__(kRowThreads) full_kernel(const FullArgs a) {
       }
     }
     block_sum2(ss, dot, scratch);
-    const float z = dot / sqrtf(ss / fd + a.eps_key);
+    const float z = (a.flags & kNoKeyNorm) ? dot : dot / sqrtf(ss / fd + a.eps_key);
     if (threadIdx.x == 0) zs[j] = z;
-    const float mnew = fmaxf(mrun, z);
-    const float sc = expf(mrun - mnew);  // 0 for the first source (mrun = -inf)
-    const float ez = expf(z - mnew);
-    lrun = lrun * sc + ez;
-    mrun = mnew;
+    float sc, ez;
+    if (a.flags & kSigmoid) {  // independent weights: no running max, no rescaling
+      sc = 1.f;
+      ez = 1.f / (1.f + expf(-z));
+      mrun = fmaxf(mrun, z);
+    } else {
+      const float mnew = fmaxf(mrun, z);
+      sc = expf(mrun - mnew);  // 0 for the first source (mrun = -inf)
+      ez = expf(z - mnew);
+      lrun = lrun * sc + ez;
+      mrun = mnew;
+    }
 #pragma unroll
     for (int k = 0; k < VPT; ++k)
 #pragma unroll
@@ -219,7 +235,8 @@ __global__ void __launch_bounds__(kRowThreads) full_kernel(const FullArgs a) {
     }
   }
 
-  const float rl = 1.f / lrun;
+  const bool sigmoid = (a.flags & kSigmoid) != 0;
+  const float rl = sigmoid ? 1.f : 1.f / lrun;
   float ssh = 0.f, unused = 0.f;
 #pragma unroll
   for (int k = 0; k < VPT; ++k)
@@ -239,11 +256,11 @@ __global__ void __launch_bounds__(kRowThreads) full_kernel(const FullArgs a) {
   const float lse = mrun + logf(lrun);
   if (threadIdx.x == 0) {
     if (a.m != nullptr) a.m[row] = mrun;
-    if (a.lse != nullptr) a.lse[row] = lse;
+    if (a.lse != nullptr && !sigmoid) a.lse[row] = lse;
   }
   if (a.alpha != nullptr) {
     for (int j = threadIdx.x; j < a.n; j += blockDim.x)
-      a.alpha[row * a.n + j] = expf(zs[j] - lse);
+      a.alpha[row * a.n + j] = sigmoid ? 1.f / (1.f + expf(-zs[j])) : expf(zs[j] - lse);
   }
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {

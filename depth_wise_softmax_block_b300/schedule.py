@@ -72,7 +72,7 @@ class BlockRunner:
                   sublayer: Callable[[int, torch.Tensor], torch.Tensor], close_out: torch.Tensor,
                   eps_key: float = 1e-6, eps_in: float = 1e-6,
                   on_call: Optional[Callable] = None,
-                  U_split: Optional[torch.Tensor] = None) -> None:
+                  U_split: Optional[torch.Tensor] = None, flags: int = 0) -> None:
         """Run one block.
 
         reps: [n, T, d] completed sources (any source stride); U: [S, d] folded queries;
@@ -80,12 +80,14 @@ class BlockRunner:
         close_out: [T, d] receives b^S.  ``on_call(i, kind, args)`` is invoked before each
         phase-2 call (tests use it to snapshot the exact inputs).  U_split: [2S, d] bf16
         hi/lo split of U (attnres_query_prep), which puts phase 1's logits on the tensor cores.
+        flags: variant flags (sigmoid weights, no key RMSNorm) for every call of the block.
         """
         S = U.shape[0]
         assert S <= self.S_max
         o, lse = self.o[:S], self.lse[:S]
         tm = self.timer
-        _call(tm, "phase1", attnres_phase1, reps, U, o, lse_out=lse, eps=eps_key, u_split=U_split)
+        _call(tm, "phase1", attnres_phase1, reps, U, o, lse_out=lse, eps=eps_key, u_split=U_split,
+              flags=flags)
         v_prev = None       # v_{i-1}
         part = None         # tensor holding b^{i-2} (None while it is zero)
         for i in range(1, S + 1):
@@ -102,7 +104,7 @@ class BlockRunner:
             kind = "phase2_first" if i == 1 else ("phase2" if i == 2 else "phase2_fused")
             _call(tm, kind, attnres_phase2_merge, o[i - 1], lse[i - 1], args["partial"],
                   args["v_prev"], args["partial_out"], U[i - 1], g, y, eps_key=eps_key,
-                  eps_in=eps_in)
+                  eps_in=eps_in, flags=flags)
             # b^{i-1} now lives in args["partial"] (i == 2) or self.partial (i >= 3)
             if i == 2:
                 part = v_prev
@@ -117,10 +119,11 @@ class BlockRunner:
 
 
 def final_aggregation(reps: torch.Tensor, u_final: torch.Tensor, out: torch.Tensor,
-                      eps: float = 1e-6, timer: Optional[KernelTimer] = None) -> torch.Tensor:
+                      eps: float = 1e-6, timer: Optional[KernelTimer] = None,
+                      flags: int = 0) -> torch.Tensor:
     """Final output over b_0 .. b_N: phase 1 with the single extra pseudo-query."""
     _call(timer, "final", attnres_phase1, reps, u_final.view(1, -1), out.view(1, *out.shape),
-          eps=eps)
+          eps=eps, flags=flags)
     return out
 
 

@@ -51,13 +51,29 @@ typedef enum {
 
 typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype;
 
+/*
+ * Variant flags (bitwise or; 0 = the method as defined), the ablation variants of the report's
+ * Table 4 ("Attention Residuals" note, result 4):
+ *   ATTNRES_SIGMOID_WEIGHTS  alpha_i = sigmoid(z_i) = 1 / (1 + exp(-z_i)) for every source on
+ *                            its own: no softmax competition, no sum-to-1.  h = sum_i alpha_i v_i.
+ *                            Two-phase: phase 1 returns o = sum over its sources of
+ *                            alpha_i b_i (unnormalised) and phase 2 adds the partial's term,
+ *                            h = o + sigmoid(z_p) p; no log-sum-exp is involved.
+ *   ATTNRES_NO_KEY_NORM      z_i = u . v_i: the key is the raw source (no RMS division, eps
+ *                            unused); the key-norm gain goes with the norm, so u should carry
+ *                            no gain (attnres_query_prep with gamma_key = NULL).
+ * Any other bit returns ATTNRES_ERR_INVALID_ARG.
+ */
+#define ATTNRES_SIGMOID_WEIGHTS 0x1u
+#define ATTNRES_NO_KEY_NORM 0x2u
+
 /* Limits (checked; larger values return ATTNRES_ERR_UNSUPPORTED). */
 #define ATTNRES_MAX_SOURCES 64     /* sources per call (phase 1 and the full path)          */
 #define ATTNRES_MAX_QUERIES 64     /* queries S per phase-1 call                             */
 #define ATTNRES_MAX_D 16384        /* hidden size (a row stays in registers)               */
 
 /* ABI version of this header; attnres_abi_version() returns the library's. */
-#define ATTNRES_ABI_VERSION 2
+#define ATTNRES_ABI_VERSION 3
 int attnres_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -115,8 +131,10 @@ attnres_status attnres_query_prep(const float* w, const float* gamma_key, float*
  *               otherwise the CUDA cores compute them from u in fp32.  Both agree to fp32
  *               rounding plus the split's 2^-16 relative error in u.
  *   o_out       device [S][T][d] (io dtype), required
- *   m_out, lse_out  device fp32 [S][T], each optional (NULL = not written)
+ *   m_out, lse_out  device fp32 [S][T], each optional (NULL = not written); with
+ *               ATTNRES_SIGMOID_WEIGHTS, o is the unnormalised sum and lse_out is not written
  *   alpha_out   device fp32 [S][T][n_src], optional
+ *   flags       ATTNRES_SIGMOID_WEIGHTS | ATTNRES_NO_KEY_NORM (see above), 0 by default
  * Limits: 1 <= n_src <= 64, 1 <= S <= 64, and n_src <= 16 when S > 24 (the per-token tile
  * must fit one CTA); otherwise ATTNRES_ERR_UNSUPPORTED.
  * With S = 1 and the final pseudo-query this is also the final aggregation over
@@ -125,7 +143,7 @@ attnres_status attnres_query_prep(const float* w, const float* gamma_key, float*
 attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, int64_t T,
                               int d, attnres_dtype io, const float* u, const void* u_split,
                               int S, float eps, void* o_out, float* m_out, float* lse_out,
-                              float* alpha_out, void* stream);
+                              float* alpha_out, unsigned int flags, void* stream);
 
 /*
  * Phase 2 merge (rows a5-a8): one sublayer l of the block ("Attention Residuals" §10,
@@ -146,12 +164,15 @@ attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, i
  *   gamma_in     device fp32 [d] or NULL (all ones): input-norm gain of sublayer l
  *   h_out        device [T, d] or NULL;  y_out device [T, d], required
  *   alpha_p_out  device fp32 [T] or NULL: weight of the partial source, c / (a + c)
+ *   flags        variant flags; with ATTNRES_SIGMOID_WEIGHTS h = o_l + sigmoid(z_p) p, lse_l is
+ *                not read (may be NULL) and alpha_p_out receives sigmoid(z_p)
  */
 attnres_status attnres_phase2_merge(const void* o_l, const float* lse_l, const void* partial,
                                     const void* v_prev, void* partial_out, int64_t T, int d,
                                     attnres_dtype io, const float* u_l, float eps_key,
                                     const float* gamma_in, float eps_in, void* h_out,
-                                    void* y_out, float* alpha_p_out, void* stream);
+                                    void* y_out, float* alpha_p_out, unsigned int flags,
+                                    void* stream);
 
 /*
  * Partial-sum update / block close (rows a8-a9): out = partial + v, elementwise, rounded to
@@ -170,13 +191,14 @@ attnres_status attnres_partial_update(const void* partial, const void* v, void* 
  *   u_l         device fp32 [d]; gamma_in device fp32 [d] or NULL
  *   h_out       device [T, d] or NULL; y_out device [T, d] or NULL (at least one required)
  *   alpha_out   device fp32 [T][n_src] or NULL
+ *   flags       variant flags (sigmoid weights: h = sum_i sigmoid(z_i) v_i)
  * Limits: 1 <= n_src <= 64.
  */
 attnres_status attnres_full_reference_path(const void* const* srcs, int n_src, int64_t T,
                                            int d, attnres_dtype io, const float* u_l,
                                            float eps_key, const float* gamma_in,
                                            float eps_in, void* h_out, void* y_out,
-                                           float* alpha_out, void* stream);
+                                           float* alpha_out, unsigned int flags, void* stream);
 
 #ifdef __cplusplus
 }

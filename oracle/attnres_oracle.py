@@ -275,6 +275,120 @@ def full_attnres_walk(v0, v, W, G_key, G_in, w_final, g_final, eps_key: float, e
 
 
 # ---------------------------------------------------------------------------------------------
+# Ablation variants of the report's Table 4 (page 2 "Attention Residuals" note, result 4):
+# "sigmoid weights" (no softmax competition between sources, no sum-to-1 constraint) and
+# "no key RMSNorm" (the source magnitude enters the score directly).  The pages give one line
+# per variant; the readings taken here:
+#   * sigmoid weights: alpha_i = sigmoid(z_i) = 1 / (1 + exp(-z_i)) for every source on its
+#     own, h = sum_i alpha_i v_i with no normalisation;
+#   * no key RMSNorm: z_i = w^T v_i.  The key-norm gain is part of that RMSNorm, so it goes
+#     with it (a caller folds no gain into the query).
+# ---------------------------------------------------------------------------------------------
+def depth_logits_raw(sources, w):
+    """No key RMSNorm: z_i = w^T v_i for every source i.  sources [n,T,d], w [d] -> z [n,T]."""
+    return np.sum(_f64(sources) * _f64(w), axis=-1)
+
+
+def depth_sigmoid(z):
+    """alpha_i = 1 / (1 + exp(-z_i)), each source on its own (no sum over sources)."""
+    return 1.0 / (1.0 + np.exp(-_f64(z)))
+
+
+def variant_logits(sources, w, gamma_key, eps: float, key_norm: bool):
+    """z with the key RMSNorm (page 2 §7) or without it (Table 4 variant)."""
+    if key_norm:
+        return depth_logits(sources, w, gamma_key, eps)
+    return depth_logits_raw(sources, w)
+
+
+def variant_weights(z, weights: str):
+    """softmax over the sources (page 2 §7) or the per-source sigmoid (Table 4 variant)."""
+    if weights == "softmax":
+        return depth_softmax(z)
+    if weights == "sigmoid":
+        return depth_sigmoid(z)
+    raise ValueError(weights)
+
+
+def aggregate_variant(sources, w, gamma_key, eps: float, weights: str = "softmax",
+                      key_norm: bool = True):
+    """h = sum_i alpha_i v_i with the variant's logits and weights.  Returns (h, alpha, z)."""
+    src = _f64(sources)
+    z = variant_logits(src, w, gamma_key, eps, key_norm)
+    alpha = variant_weights(z, weights)
+    return np.sum(alpha[..., None] * src, axis=0), alpha, z
+
+
+def phase1_variant(reps, W, G_key, eps: float, weights: str = "softmax", key_norm: bool = True):
+    """Phase 1 of one block under a variant, per query s over the partition A = reps:
+    softmax weights -> (o normalised, m, lse, alpha) exactly as phase1(); sigmoid weights ->
+    o = sum_{i in A} sigmoid(z_i) v_i (the partition's contribution; no statistics are needed
+    to merge sums), m = max_i z_i, lse = None, alpha = sigmoid(z).
+    reps: [n,T,d]; W: [S,d]; G_key: [S,d] or None.  o [S,T,d], m [S,T], alpha [S,T,n]."""
+    reps = _f64(reps)
+    S = np.shape(W)[0]
+    o, m, lse, alpha = [], [], [], []
+    for s in range(S):
+        g = None if G_key is None else _f64(G_key)[s]
+        z = variant_logits(reps, _f64(W)[s], g, eps, key_norm)
+        mz = np.max(z, axis=0)
+        if weights == "softmax":
+            e = np.exp(z - mz)
+            ell = np.sum(e, axis=0)
+            a = e / ell
+            lse.append(mz + np.log(ell))
+        else:
+            a = depth_sigmoid(z)
+        o.append(np.sum(a[..., None] * reps, axis=0))
+        m.append(mz)
+        alpha.append(np.moveaxis(a, 0, -1))
+    return (np.stack(o), np.stack(m), np.stack(lse) if lse else None, np.stack(alpha))
+
+
+def merge_reference_variant(o_A, lse_A, p, w, gamma_key, eps_key: float, gamma_in,
+                            eps_in: float, weights: str = "softmax", key_norm: bool = True):
+    """Phase 2 of one sublayer under a variant, on the inputs it receives.  Softmax weights:
+    the partition merge of merge_reference() with the variant's logit for p.  Sigmoid
+    weights: the weights do not depend on each other, so the two partitions simply add,
+    h = o_A + sigmoid(z_p) p (o_A as phase1_variant returns it).
+    Returns (h, y = RMSNorm_in(h), weight of p)."""
+    o_A = _f64(o_A)
+    if p is None:
+        return o_A, rmsnorm(o_A, gamma_in, eps_in), np.zeros(o_A.shape[:-1])
+    p = _f64(p)
+    z = variant_logits(p[None], w, gamma_key, eps_key, key_norm)[0]
+    if weights == "sigmoid":
+        a_p = depth_sigmoid(z)
+        h = o_A + a_p[..., None] * p
+    else:
+        lse_A = _f64(lse_A)
+        M = np.maximum(lse_A, z)
+        ca, cb = np.exp(lse_A - M), np.exp(z - M)
+        h = (ca[..., None] * o_A + cb[..., None] * p) / (ca + cb)[..., None]
+        a_p = cb / (ca + cb)
+    return h, rmsnorm(h, gamma_in, eps_in), a_p
+
+
+def single_block_variant(completed, v, W, G_key, G_in, eps_key: float, eps_in: float,
+                         weights: str = "softmax", key_norm: bool = True):
+    """single_block() under a variant (direct definition for every sublayer of one block):
+    returns (y per sublayer [S][T,d], h per sublayer, closed block b^S)."""
+    completed = [_f64(b) for b in completed]
+    v = _f64(v)
+    ys, hs = [], []
+    partial = None
+    for i in range(1, v.shape[0] + 1):
+        srcs = block_sources(completed, partial)
+        gk = None if G_key is None else _f64(G_key)[i - 1]
+        gi = None if G_in is None else _f64(G_in)[i - 1]
+        h, _, _ = aggregate_variant(srcs, _f64(W)[i - 1], gk, eps_key, weights, key_norm)
+        hs.append(h)
+        ys.append(rmsnorm(h, gi, eps_in))
+        partial = v[i - 1].copy() if partial is None else partial + v[i - 1]
+    return ys, hs, partial
+
+
+# ---------------------------------------------------------------------------------------------
 # Reference values for one phase-2 call and one partial update, on given inputs
 # ---------------------------------------------------------------------------------------------
 def phase2_reference(reps, partial_prev, v_prev, w, gamma_key, eps_key, gamma_in, eps_in):

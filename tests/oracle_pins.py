@@ -428,4 +428,144 @@ def pin_merge_reference(O):
     assert np.all(a0 == 0.0)
 
 
+# --- Table 4 ablation variants (page 2 "Attention Residuals" note, result 4) -------------------
+def pin_sigmoid_zero_query_half(O):
+    """Sigmoid weights with zero queries: every weight is sigmoid(0) = 1/2 (no sum-to-1), so
+    h = (1/2) sum_i v_i."""
+    r = _rng(30)
+    v = _sources(r, 5, 7, 20)
+    for kn in (True, False):
+        h, alpha, _ = O.aggregate_variant(v, np.zeros(20), None, 1e-6, "sigmoid", kn)
+        _close(alpha, np.full((5, 7), 0.5), 0.0, "alpha = 1/2")
+        _close(h, 0.5 * v.sum(axis=0), 1e-12, "h = half the sum")
+
+
+def pin_sigmoid_rational(O):
+    """Sources on distinct scaled basis vectors and queries with z_j = ln(p_j / (1 - p_j)):
+    then alpha_j = p_j exactly and h[k_j] = c_j p_j (sigmoid weights, key RMSNorm at eps = 0,
+    where RMSNorm(c e_k) = sign(c) sqrt(d) gamma_k e_k)."""
+    d = 8
+    ks, cs, ps = [2, 5, 7], [3.0, -0.5, 12.0], [0.2, 0.5, 0.9]
+    v = np.zeros((3, 1, d))
+    for j, (k, c) in enumerate(zip(ks, cs)):
+        v[j, 0, k] = c
+    g = np.linspace(0.5, 1.5, d)
+    w = np.zeros(d)
+    for k, c, p in zip(ks, cs, ps):
+        w[k] = math.log(p / (1 - p)) / (math.copysign(1.0, c) * math.sqrt(d) * g[k])
+    h, alpha, _ = O.aggregate_variant(v, w, g, 0.0, "sigmoid", True)
+    _close(alpha[:, 0], np.array(ps), 1e-14, "alpha = p")
+    want = np.zeros(d)
+    for k, c, p in zip(ks, cs, ps):
+        want[k] = c * p
+    _close(h[0], want, 1e-13, "h[k_j] = c_j p_j")
+
+
+def pin_sigmoid_reflection(O):
+    """sigmoid(z) + sigmoid(-z) = 1, so h(w) + h(-w) = sum_i v_i for any sources."""
+    r = _rng(31)
+    v = _sources(r, 6, 5, 16)
+    w = r.normal(0.0, 1.0, size=16)
+    for kn in (True, False):
+        h1, _, _ = O.aggregate_variant(v, w, None, 1e-6, "sigmoid", kn)
+        h2, _, _ = O.aggregate_variant(v, -w, None, 1e-6, "sigmoid", kn)
+        _close(h1 + h2, v.sum(axis=0), 1e-12, "h(w) + h(-w)")
+
+
+def pin_sigmoid_partitions_add(O):
+    """With sigmoid weights the partitions of any split simply add (brute force over every
+    split of 5 sources), and the phase-2 merge of phase 1's partition plus a partial source
+    equals the direct aggregation over both."""
+    r = _rng(32)
+    n, T, d = 5, 3, 12
+    v = _sources(r, n, T, d)
+    W = r.normal(0.0, 1.0, size=(2, d))
+    G = r.normal(1.0, 0.1, size=(2, d))
+    for kn in (True, False):
+        o_all, _, lse, _ = O.phase1_variant(v, W, G, 1e-6, "sigmoid", kn)
+        assert lse is None
+        for s in range(2):
+            h, _, _ = O.aggregate_variant(v, W[s], G[s], 1e-6, "sigmoid", kn)
+            _close(o_all[s], h, 1e-12, "phase 1 over all = direct")
+        for k in range(1, n):
+            for A in itertools.combinations(range(n), k):
+                B = [i for i in range(n) if i not in A]
+                oA = O.phase1_variant(v[list(A)], W, G, 1e-6, "sigmoid", kn)[0]
+                oB = O.phase1_variant(v[B], W, G, 1e-6, "sigmoid", kn)[0]
+                _close(oA + oB, o_all, 1e-12, f"split {A}")
+        gi = r.normal(1.0, 0.1, size=d)
+        p = r.normal(0.0, 2.0, size=(T, d))
+        oA = O.phase1_variant(v[:3], W[:1], G[:1], 1e-6, "sigmoid", kn)[0][0]
+        h, y, ap = O.merge_reference_variant(oA, None, p, W[0], G[0], 1e-6, gi, 1e-6, "sigmoid",
+                                             kn)
+        h2, a2, _ = O.aggregate_variant(np.concatenate([v[:3], p[None]]), W[0], G[0], 1e-6,
+                                        "sigmoid", kn)
+        _close(h, h2, 1e-12, "merge = direct")
+        _close(ap, a2[-1], 1e-15, "weight of the partial")
+        _close(y, O.rmsnorm(h2, gi, 1e-6), 1e-12, "y")
+
+
+def pin_raw_logits(O):
+    """No key RMSNorm: the logit of c e_k is w_k c exactly, and scaling one source by a scales
+    its logit by a (the magnitude enters the score, unlike the normalised key)."""
+    d = 10
+    w = np.arange(1.0, d + 1.0) / 7.0
+    for k, c in ((0, 2.0), (4, -3.5), (9, 0.25)):
+        v = np.zeros((1, 1, d))
+        v[0, 0, k] = c
+        _close(O.depth_logits_raw(v, w), [[w[k] * c]], 1e-15, "z = w_k c")
+    r = _rng(33)
+    v = _sources(r, 4, 6, d)
+    z0 = O.variant_logits(v, w, None, 1e-6, False)
+    v2 = v.copy()
+    v2[1] *= -2.5
+    z1 = O.variant_logits(v2, w, None, 1e-6, False)
+    _close(z1[1], -2.5 * z0[1], 1e-12, "z scales with the source")
+    _close(np.delete(z1, 1, 0), np.delete(z0, 1, 0), 0.0, "other logits unchanged")
+
+
+def pin_raw_equals_scaled_query(O):
+    """When every source row has the same RMS r (eps = 0, no gain), w^T v = r w^T RMSNorm(v),
+    so dropping the key norm equals keeping it with the query scaled by r."""
+    r = _rng(34)
+    v = _sources(r, 5, 4, 32)
+    rr = 1.7
+    v = v / O.rms(v, 0.0)[..., None] * rr
+    w = r.normal(0.0, 0.3, size=32)
+    for weights in ("softmax", "sigmoid"):
+        h1, a1, z1 = O.aggregate_variant(v, w, None, 0.0, weights, False)
+        h2, a2, z2 = O.aggregate_variant(v, rr * w, None, 0.0, weights, True)
+        _close(z1, z2, 1e-12, "logits")
+        _close(h1, h2, 1e-12, f"h ({weights})")
+
+
+def pin_variant_defaults(O):
+    """The variant functions with softmax weights and the key RMSNorm are the default ones."""
+    r = _rng(35)
+    v = _sources(r, 4, 5, 24)
+    W = r.normal(0.0, 0.5, size=(3, 24))
+    G = r.normal(1.0, 0.1, size=(3, 24))
+    gi = r.normal(1.0, 0.1, size=24)
+    h, a, z = O.aggregate(v, W[0], G[0], 1e-6)
+    h2, a2, z2 = O.aggregate_variant(v, W[0], G[0], 1e-6)
+    _close(h2, h, 0.0, "h")
+    _close(a2, a, 0.0, "alpha")
+    base = O.phase1(v, W, G, 1e-6)
+    var = O.phase1_variant(v, W, G, 1e-6)
+    for x, y, nm in zip(var, base, ("o", "m", "lse", "alpha")):
+        _close(x, y, 1e-14, f"phase1 {nm}")
+    p = r.normal(0.0, 1.0, size=(5, 24))
+    m1 = O.merge_reference(base[0][0], base[2][0], p, W[0], G[0], 1e-6, gi, 1e-6)
+    m2 = O.merge_reference_variant(base[0][0], base[2][0], p, W[0], G[0], 1e-6, gi, 1e-6)
+    for x, y in zip(m2, m1):
+        _close(x, y, 0.0, "merge")
+    vv = r.normal(0.0, 1.0, size=(3, 5, 24))
+    ys, hs, closed = O.single_block_variant(v[:2], vv, W, G, np.stack([gi] * 3), 1e-6, 1e-6)
+    for i in range(3):
+        srcs = O.block_sources(list(v[:2]), None if i == 0 else vv[:i].sum(axis=0))
+        _, y, _ = O.sublayer_input(srcs, W[i], G[i], 1e-6, gi, 1e-6)
+        _close(ys[i], y, 1e-13, f"single_block_variant y_{i + 1}")
+    _close(closed, vv.sum(axis=0), 1e-12, "closed block")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -45,14 +45,16 @@ def test_header_symbols_exported(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.attnres_abi_version() == 2
+    assert lib.attnres_abi_version() == 3
     for code, name in ar.STATUS.items():
         assert lib.attnres_status_string(code).decode() == name
     assert lib.attnres_status_string(99).decode() == "ATTNRES_ERR_UNKNOWN"
 
 
-def p1(lib, reps=P, stride=1024 * 64, n=2, T=0, d=64, io=1, u=P, S=4, eps=1e-6, o=P, us=None):
-    return lib.attnres_phase1(reps, stride, n, T, d, io, u, us, S, eps, o, None, None, None, None)
+def p1(lib, reps=P, stride=1024 * 64, n=2, T=0, d=64, io=1, u=P, S=4, eps=1e-6, o=P, us=None,
+       flags=0):
+    return lib.attnres_phase1(reps, stride, n, T, d, io, u, us, S, eps, o, None, None, None, flags,
+                              None)
 
 
 def test_phase1_validation(lib):
@@ -83,11 +85,14 @@ def test_phase1_validation(lib):
     assert err(p1(lib, T=4, stride=1024 * 64 + 4)) == MISALIGNED  # source 1 misaligned
     assert err(p1(lib, T=4, us=PM)) == MISALIGNED         # split queries misaligned
     assert p1(lib, us=P) == OK
+    assert p1(lib, flags=3) == OK                         # both variant flags
+    assert p1(lib, flags=4) == INVALID                    # unknown flag
 
 
-def p2(lib, o=P, lse=P, part=None, v=None, pout=None, T=0, d=64, io=1, u=P, g=None, y=P, h=None):
+def p2(lib, o=P, lse=P, part=None, v=None, pout=None, T=0, d=64, io=1, u=P, g=None, y=P, h=None,
+       flags=0):
     return lib.attnres_phase2_merge(o, lse, part, v, pout, T, d, io, u, 1e-6, g, 1e-6, h, y, None,
-                                    None)
+                                    flags, None)
 
 
 def test_phase2_validation(lib):
@@ -96,7 +101,9 @@ def test_phase2_validation(lib):
     assert p2(lib, part=P, v=P, pout=P) == OK
     assert err(p2(lib, T=4, o=None)) == INVALID
     assert err(p2(lib, T=4, y=None)) == INVALID
-    assert err(p2(lib, T=4, part=P, lse=None)) == INVALID  # a partial source needs lse
+    assert err(p2(lib, T=4, part=P, lse=None)) == INVALID  # a partial source needs lse ...
+    assert p2(lib, part=P, lse=None, flags=1) == OK       # ... except with sigmoid weights
+    assert p2(lib, flags=8) == INVALID
     assert err(p2(lib, T=4, v=P, u=None)) == INVALID       # ... and the query
     assert err(p2(lib, T=4, pout=P)) == INVALID            # nothing to write without a partial
     assert p2(lib, d=12) == INVALID
@@ -110,7 +117,8 @@ def test_phase2_validation(lib):
 def test_full_and_update_validation(lib):
     import ctypes
     arr = (ctypes.c_void_p * 3)(P, P + 4096, P + 8192)
-    f = lib.attnres_full_reference_path
+    def f(*args):
+        return lib.attnres_full_reference_path(*args[:-1], 0, args[-1])
     assert f(arr, 3, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None) == OK
     assert err(f(None, 3, 4, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None)) == INVALID
     assert f(arr, 0, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None) == INVALID
@@ -120,6 +128,8 @@ def test_full_and_update_validation(lib):
     assert err(f(bad, 2, 4, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None)) == MISALIGNED
     nul = (ctypes.c_void_p * 2)(P, None)
     assert err(f(nul, 2, 4, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None)) == INVALID
+    assert lib.attnres_full_reference_path(arr, 3, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None,
+                                           16, None) == INVALID
     up = lib.attnres_partial_update
     assert up(P, P, P, 0, 64, 1, None) == OK
     assert err(up(None, P, P, 4, 64, 1, None)) == INVALID

@@ -87,7 +87,30 @@ def _merge_ignores_lse(o_A, lse_A, p, w, gamma_key, eps_key, gamma_in, eps_in): 
     return h, y, a
 
 
+def _sigmoid_normalised(z):                 # sigmoid weights divided by their sum
+    a = 1.0 / (1.0 + np.exp(-np.asarray(z, np.float64)))
+    return a / a.sum(axis=0, keepdims=True)
+
+
+def _sigmoid_sign(z):                       # sigmoid of -z
+    return 1.0 / (1.0 + np.exp(np.asarray(z, np.float64)))
+
+
+def _raw_logits_still_normalised(sources, w):  # "no key norm" that still divides by r
+    src = np.asarray(sources, np.float64)
+    return np.sum(src / O.rms(src, 0.0)[..., None] * np.asarray(w, np.float64), axis=-1)
+
+
+def _merge_variant_softmax_for_sigmoid(o_A, lse_A, p, w, gamma_key, eps_key, gamma_in, eps_in,
+                                       weights="softmax", key_norm=True):
+    # merges sigmoid partitions as if they were softmax partitions (lse taken as 0)
+    lse = np.zeros(np.shape(o_A)[:-1]) if lse_A is None else lse_A
+    return _ORIG_MERGE_V(o_A, lse, p, w, gamma_key, eps_key, gamma_in, eps_in, "softmax",
+                         key_norm)
+
+
 _ORIG_PARTITION = O.partition_stats
+_ORIG_MERGE_V = O.merge_reference_variant
 _ORIG_MERGE = O.merge_reference
 
 MUTATIONS = {
@@ -105,6 +128,10 @@ MUTATIONS = {
     "zero_partial_source": ("block_sources", _block_sources_zero_partial),
     "block_index_off_by_one": ("block_of", _block_of_off_by_one),
     "merge_ignores_lse": ("merge_reference", _merge_ignores_lse),
+    "sigmoid_normalised": ("depth_sigmoid", _sigmoid_normalised),
+    "sigmoid_sign": ("depth_sigmoid", _sigmoid_sign),
+    "raw_logits_normalised": ("depth_logits_raw", _raw_logits_still_normalised),
+    "sigmoid_merged_as_softmax": ("merge_reference_variant", _merge_variant_softmax_for_sigmoid),
 }
 
 
