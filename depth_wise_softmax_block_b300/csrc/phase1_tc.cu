@@ -11,14 +11,16 @@
 // are bf16 already).  Everything else runs on the CUDA cores:
 //   sweep 1  a copy-issuing warp streams 64-column stages of the tile (n sources x 8 tokens,
 //            128-byte swizzled rows) and of the split queries through a ring of up to 12 slots;
-//            thread 0 issues the stage's four K=16 MMAs, D[row, 2s + {hi,lo}] += b_row . u_s,
-//            with the tile's n*8 rows as M (= 128, unused rows ignored), while the 16 compute
-//            warps accumulate each source row's sum of squares;
+//            an MMA-issuing warp issues the stage's four K=16 MMAs, D[row, 2s + {hi,lo}] +=
+//            b_row . u_s, with the tile's n*8 rows as M (= 128, unused rows ignored), while the
+//            16 compute warps accumulate each source row's sum of squares;
 //   softmax  warps 0-3 read D from tensor memory (one row per thread), form
 //            z = (hi + lo) / r_j, and one thread per (token, query) computes m, lse, alpha;
 //   sweep 2  the tile streams through the ring again, columns in reverse order so that the
-//            chunks read last in sweep 1 are still in L2, and the 16 warps write
+//            chunks read last in sweep 1 are still in L2, and the compute warps write
 //            o[s,t,:] = sum_j alpha_j b_j[t,:] (packed fp32 FMAs, 16-byte streaming stores).
+// The compute warps work in two halves of 8 that take alternate stages of the ring, so one
+// half's loads and stores overlap the other half's arithmetic.
 // Stage hand-off uses mbarriers ("full": copy landed; "empty": all compute warps and the
 // stage's MMAs done); every wait is bounded (tma.cuh).  The tensor-memory allocation is
 // released on every path before the CTA exits.
@@ -38,7 +40,7 @@ namespace {
 
 constexpr int kCompute = 512;              // 16 compute warps
 constexpr int kWarps = kCompute / 32;
-constexpr int kThreads = kCompute + 32;    // + 1 copy-issuing warp
+constexpr int kThreads = kCompute + 64;    // + a copy-issuing warp and an MMA-issuing warp
 constexpr int kTT = 8;              // tokens per CTA tile
 constexpr int kKC = 64;             // bf16 columns per stage (one 128-byte row slice)
 constexpr int kM = 128;             // MMA rows (tile rows n * 8 <= 128)
@@ -71,7 +73,7 @@ bool make_tc_plan(int n, int S, TcPlan& p) {
   // but must lie inside the allocation, hence the slack after the last slot.
   const int slack = std::max(0, kM * 128 - p.slot);
   const int zb = kM * S * 4;
-  const int ab = kTT * n * 8 * 8 * 4;
+  const int ab = kTT * n * 4 * 12 * 4;   // [token][source][4 groups][6 pairs][2]
   const int fixed = slack + align_up(zb, 16) + align_up(ab, 16) + kM * 4 +
                     (2 * kMaxSlots + 2) * 8 + 16;
   p.SB = std::min(kMaxSlots, (kMaxSmem - 1024 - fixed) / p.slot);
@@ -110,13 +112,13 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   volatile int* abort_flag = reinterpret_cast<volatile int*>(dready + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + pl.offTmem);
   float* zbuf = reinterpret_cast<float*>(smem + pl.offZ);     // [128 rows][S]
-  float* alph = reinterpret_cast<float*>(smem + pl.offAlph);  // [8][n][8 groups][4 pairs][2]
+  float* alph = reinterpret_cast<float*>(smem + pl.offAlph);  // [8][n][4 groups][6 pairs][2]
   float* ssbuf = reinterpret_cast<float*>(smem + pl.offSs);   // [128 rows]
 
   if (tid == 0) {
     for (int s = 0; s < SB; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kWarps + 1);  // every compute warp + the stage's MMAs (or thread 0)
+      mbar_init(&empty[s], kWarps / 2 + 1);  // the consuming half + the stage's MMAs (or a stand-in)
     }
     mbar_init(dready, 1);
     *abort_flag = 0;
@@ -160,42 +162,60 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
     return;
   }
 
+  // ------------------------------- MMA-issuing warp -------------------------------
+  // The stage's four K = 16 MMAs, D[row, 2s + {hi, lo}] += b_row . u_s, as soon as its copies
+  // land; completion arrives on the stage's "empty" barrier (and, after the last stage, on
+  // "dready").  An MMA costs about the same for every N up to 128, so issuing from a warp of
+  // its own keeps the tensor core off the compute warps' critical path.
+  if (warp == kWarps + 1) {
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t idesc = idesc_bf16_f32(kM, pl.Npad);
+    for (int c = 0; c < nch; ++c) {
+      const int bs = c % SB;
+      if (!*abort_flag && !mbar_wait(&full[bs], (c / SB) & 1)) *abort_flag = 1;
+      tc_fence_after();
+      if (lane == 0) {
+        const unsigned char* st = smem + bs * pl.slot;
+        const uint32_t a0 = smem_addr(st), b0 = smem_addr(st + pl.bSpan);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_bf16(tmem, desc_kmajor_sw128(a0 + 32 * kk), desc_kmajor_sw128(b0 + 32 * kk),
+                      idesc, (c | kk) != 0 ? 1u : 0u);
+        tc_commit(&empty[bs]);
+        if (c == nch - 1) tc_commit(dready);
+      }
+      __syncwarp();
+    }
+    return;
+  }
+
   // -------------------------------- compute warps --------------------------------
   const uint32_t tmem = *tmem_slot;
-  const uint32_t idesc = idesc_bf16_f32(kM, pl.Npad);
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     if (!*abort_flag && !mbar_wait(bar, parity)) *abort_flag = 1;
   };
+  // Stage `it` of the ring is consumed by half (it & 1) of the compute warps: warps 0-7 take the
+  // even stages, warps 8-15 the odd ones, so the two halves work on different stages at once.
+  const int half = warp >> 3, hw = warp & 7, ht = tid & 255;
   auto release = [&](int bs, bool substitute_mma) {
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[bs]);
-    if (substitute_mma && tid == 0) mbar_arrive(&empty[bs]);
+    if (substitute_mma && ht == 0) mbar_arrive(&empty[bs]);
   };
 
   // ------------------------------------ sweep 1 ------------------------------------
   const int nrows = n * kTT;  // tile rows: row j * 8 + t
   const bool key_norm = (a.flags & kNoKeyNorm) == 0;
   const bool sigmoid = (a.flags & kSigmoid) != 0;
-  float2 ssa[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-  for (int c = 0; c < nch; ++c) {
+  // sums of squares: the half's thread ht takes the (row, 16-byte chunk) pairs ht + 256 k
+  float2 ssa[3] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  for (int c = half; c < nch; c += 2) {
     const int bs = c % SB;
     const unsigned char* st = smem + bs * pl.slot;
     wait(&full[bs], (c / SB) & 1);
-    // the stage's four K = 16 MMAs: D[row, 2s + {hi, lo}] += b_row . u_s
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t a0 = smem_addr(st), b0 = smem_addr(st + pl.bSpan);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        tc_mma_bf16(tmem, desc_kmajor_sw128(a0 + 32 * kk), desc_kmajor_sw128(b0 + 32 * kk), idesc,
-                    (c | kk) != 0 ? 1u : 0u);
-      tc_commit(&empty[bs]);
-      if (c == nch - 1) tc_commit(dready);
-    }
-    // sums of squares: (row, 16-byte chunk) pairs tid and tid + 512
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i = tid + k * kCompute;
+    for (int k = 0; k < 3; ++k) {
+      const int i = ht + k * 256;
       if (key_norm && i < nrows * 8) {
         float2 f[4];
         unpack_pairs(*reinterpret_cast<const uint4*>(st + sw128(i >> 3, i & 7)), f);
@@ -206,17 +226,27 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
     release(bs, false);
   }
 
-  // row sums of squares: the 8 chunks of a row sit in 8 consecutive lanes
+  // row sums of squares: the 8 chunks of a row sit in 8 consecutive lanes; half 0 writes its
+  // sums, then half 1 adds its own (fixed order: deterministic)
+  float rowsum[3];
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int i = tid + k * kCompute;
+  for (int k = 0; k < 3; ++k) {
     float x = ssa[k].x + ssa[k].y;
     x += __shfl_xor_sync(0xffffffffu, x, 1);
     x += __shfl_xor_sync(0xffffffffu, x, 2);
     x += __shfl_xor_sync(0xffffffffu, x, 4);
-    if (i < nrows * 8 && (i & 7) == 0) ssbuf[i >> 3] = x;
+    rowsum[k] = x;
   }
-  named_barrier(1, kCompute);
+  for (int h = 0; h < 2; ++h) {
+    if (half == h) {
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        const int i = ht + k * 256;
+        if (i < nrows * 8 && (i & 7) == 0) ssbuf[i >> 3] = h == 0 ? rowsum[k] : ssbuf[i >> 3] + rowsum[k];
+      }
+    }
+    named_barrier(1, kCompute);
+  }
 
   // ------------------------- logits from tensor memory -------------------------------
   const float fd = static_cast<float>(d);
@@ -251,11 +281,11 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
       for (int j = 0; j < n; ++j) l += expf(zbuf[(j * kTT + t) * S + s] - m);
     const float lse = m + logf(l);
     const float rl = 1.f / l;
-    const int g = s / 3, pp = s % 3;
+    const int g = s / 6, pp = s % 6;
     for (int j = 0; j < n; ++j) {
       const float zj = zbuf[(j * kTT + t) * S + s];
       const float al = sigmoid ? 1.f / (1.f + expf(-zj)) : expf(zj - m) * rl;
-      float* ap = alph + (((t * n + j) * 8 + g) * 4 + pp) * 2;
+      float* ap = alph + (((t * n + j) * 4 + g) * 6 + pp) * 2;
       ap[0] = al;
       ap[1] = al;
       if (a.alpha != nullptr && tok < T) a.alpha[(static_cast<int64_t>(s) * T + tok) * n + j] = al;
@@ -268,33 +298,28 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   named_barrier(1, kCompute);
 
   // ------------------------------------ sweep 2 ------------------------------------
-  // warp w: token w / 2, queries (w % 2) * 12 + [0, 12); lane: group of 3 queries, chunk.
-  // The thread's weights (n sources x 3 queries, as (a, a) pairs) stay in registers.
-  const int t2 = warp >> 1;
-  const int grp = (warp & 1) * 4 + (lane >> 3);
+  // Half h takes the ring's stages of parity h.  Within a half, warp hw is token hw; lane:
+  // group of 6 queries (lane / 8) and 16-byte chunk (lane % 8).  The weights come from shared
+  // memory as ready-made (a, a) pairs, 3 x 16 bytes per source.
+  const int t2 = hw;
+  const int grp = lane >> 3;
   const int kg = lane & 7;
   const int64_t tok2 = t0 + t2;
-  const bool active2 = grp * 3 < S;
-  float2 al[kMaxN][3];
-#pragma unroll
-  for (int j = 0; j < kMaxN; ++j) {
-    const float* ap = alph + ((t2 * n + j) * 8 + grp) * 8;
-#pragma unroll
-    for (int qq = 0; qq < 3; ++qq)
-      al[j][qq] = j < n ? *reinterpret_cast<const float2*>(ap + 2 * qq) : make_float2(0.f, 0.f);
-  }
+  const bool active2 = grp * 6 < S;
+  const float* at = alph + (t2 * n * 4 + grp) * 12;
   // source j's chunk: row j * 8 + t2, swizzled chunk kg ^ t2 (independent of j)
   const int boff = t2 * 128 + ((kg ^ t2) << 4);
   char* o = static_cast<char*>(a.o);
-  for (int ib = nch; ib < total; ++ib) {
+  const int first2 = nch + (((nch & 1) != half) ? 1 : 0);
+  for (int ib = first2; ib < total; ib += 2) {
     const int bs = ib % SB;
     const int c = total - 1 - ib;  // columns in reverse
     wait(&full[bs], (ib / SB) & 1);
     if (active2) {
       const unsigned char* st = smem + bs * pl.slot + boff;
-      float2 acc[3][4];
+      float2 acc[6][4];
 #pragma unroll
-      for (int qq = 0; qq < 3; ++qq)
+      for (int qq = 0; qq < 6; ++qq)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[qq][e] = make_float2(0.f, 0.f);
 #pragma unroll
@@ -302,19 +327,24 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
         if (j < n) {
           float2 bv[4];
           unpack_pairs(*reinterpret_cast<const uint4*>(st + j * 1024), bv);
+          const float4* ap = reinterpret_cast<const float4*>(at + j * 48);
+          const float4 a0 = ap[0], a1 = ap[1], a2 = ap[2];
+          const float2 al[6] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w),
+                                make_float2(a1.x, a1.y), make_float2(a1.z, a1.w),
+                                make_float2(a2.x, a2.y), make_float2(a2.z, a2.w)};
 #pragma unroll
-          for (int qq = 0; qq < 3; ++qq)
+          for (int qq = 0; qq < 6; ++qq)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[qq][e] = __ffma2_rn(al[j][qq], bv[e], acc[qq][e]);
+            for (int e = 0; e < 4; ++e) acc[qq][e] = __ffma2_rn(al[qq], bv[e], acc[qq][e]);
         }
       }
       const int k = c * kKC + kg * 8;
       if (tok2 < T && k < d) {
-        char* op = o + ((static_cast<int64_t>(grp * 3) * T + tok2) * d + k) * 2;
+        char* op = o + ((static_cast<int64_t>(grp * 6) * T + tok2) * d + k) * 2;
         const int64_t qstride = T * d * 2;
 #pragma unroll
-        for (int qq = 0; qq < 3; ++qq) {
-          if (grp * 3 + qq < S)
+        for (int qq = 0; qq < 6; ++qq) {
+          if (grp * 6 + qq < S)
             __stcs(reinterpret_cast<uint4*>(op + qq * qstride),
                    make_uint4(pack_bf16x2(acc[qq][0].x, acc[qq][0].y),
                               pack_bf16x2(acc[qq][1].x, acc[qq][1].y),

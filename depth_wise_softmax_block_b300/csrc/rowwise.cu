@@ -15,6 +15,8 @@
 // Each thread owns VPT 16-byte vectors of the row (vector v = threadIdx.x + k * blockDim.x).
 #include <math.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -26,30 +28,21 @@ constexpr int kRowThreads = 256;    // full path: at most 256 threads per row
 // 448 x 2: 0.219 ms against 0.239 ms for a 16384-row fused call)
 constexpr int kMergeThreads = 256;
 
+// Phase 2 of one row from the vectors this thread holds (vector v = threadIdx.x + k *
+// blockDim.x of the row): o_l in ro, the stored partial in rp, v_prev in rv (each used only if
+// the corresponding input is present).  Ends with the row's stores; `scratch` is the CTA's
+// reduction buffer (the block reductions synchronise the CTA).
 template <typename T, int VPT>
-__global__ void __launch_bounds__(kMergeThreads) phase2_kernel(const Phase2Args a) {
+__device__ __forceinline__ void merge_row(const Phase2Args& a, int64_t row, const uint4 (&ro)[VPT],
+                                          const uint4 (&rp)[VPT], const uint4 (&rv)[VPT],
+                                          float* scratch) {
   constexpr int VE = Vec<T>::N;
-  __shared__ float scratch[66];
-  const int64_t row = blockIdx.x;
   const int nv = a.d / VE;
   const int64_t base = row * a.d;
-  const T* o = static_cast<const T*>(a.o) + base;
   const bool has_p = a.partial != nullptr || a.v_prev != nullptr;
 
   float h[VPT][VE];
   float p[VPT][VE];
-  // Issue every load of the row before any arithmetic.
-  uint4 ro[VPT], rp[VPT], rv[VPT];
-#pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int v = threadIdx.x + k * blockDim.x;
-    if (v < nv) {
-      ro[k] = ld_stream(o + v * VE);
-      if (a.partial) rp[k] = ld_stream(static_cast<const T*>(a.partial) + base + v * VE);
-      if (a.v_prev) rv[k] = ld_stream(static_cast<const T*>(a.v_prev) + base + v * VE);
-    }
-  }
-
   float ssp = 0.f, dot = 0.f;
   if (has_p) {
 #pragma unroll
@@ -148,6 +141,27 @@ __global__ void __launch_bounds__(kMergeThreads) phase2_kernel(const Phase2Args 
       st_global(static_cast<T*>(a.y) + base + v * VE, pack(y));
     }
   }
+}
+
+// One CTA per row; every load of the row is issued before any arithmetic.
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kMergeThreads) phase2_kernel(const Phase2Args a) {
+  constexpr int VE = Vec<T>::N;
+  __shared__ float scratch[66];
+  const int64_t row = blockIdx.x;
+  const int nv = a.d / VE;
+  const int64_t base = row * a.d;
+  uint4 ro[VPT], rp[VPT], rv[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = threadIdx.x + k * blockDim.x;
+    if (v < nv) {
+      ro[k] = ld_stream(static_cast<const T*>(a.o) + base + v * VE);
+      if (a.partial) rp[k] = ld_stream(static_cast<const T*>(a.partial) + base + v * VE);
+      if (a.v_prev) rv[k] = ld_stream(static_cast<const T*>(a.v_prev) + base + v * VE);
+    }
+  }
+  merge_row<T, VPT>(a, row, ro, rp, rv, scratch);
 }
 
 // Online softmax over the sources, one source per step, with the rows of the next two sources
@@ -382,6 +396,7 @@ cudaError_t launch_phase2(IO io, const Phase2Args& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
   return io == IO::BF16 ? phase2_io<bf16>(a, s) : phase2_io<float>(a, s);
 }
+
 
 cudaError_t launch_full(IO io, const FullArgs& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
