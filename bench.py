@@ -337,6 +337,97 @@ def run_e2e(step: LongContextStep, iters: int):
             "d2h_bytes_per_step": d2h, "ms_per_step": el * 1e3}
 
 
+def full_grouped_bytes(L: int, S: int, d: int, E: int) -> int:
+    """Algorithmic bytes per token of a whole Full AttnRes depth by the grouped two-phase
+    schedule: per group starting at layer l0 + 1 with Sg layers, phase 1 reads the l0 + 1
+    history rows and writes Sg outputs o (+ 4 B of lse each); layer l0 + i reads o, its i - 1
+    in-group rows, the lse, and writes y."""
+    total = 0
+    for l0 in range(0, L, S):
+        Sg = min(S, L - l0)
+        total += (l0 + 1 + Sg) * d * E + 4 * Sg
+        for i in range(1, Sg + 1):
+            total += (1 + (i - 1) + 1) * d * E + 4
+    return total
+
+
+def full_direct_bytes(L: int, d: int, E: int) -> int:
+    """The same depth one layer at a time (the naive path): layer l reads l rows, writes y."""
+    return sum((l + 1) * d * E for l in range(1, L + 1))
+
+
+def run_full_grouped(args):
+    """Full AttnRes interpolation workload (54 sublayers, 8192 tokens, d = 2048, bf16, every
+    sublayer output its own source): one whole depth by the grouped two-phase schedule (groups
+    of --group sublayers), timed against the direct path (one single-pass aggregation per
+    layer over all its sources).  Prints one JSON line."""
+    from depth_wise_softmax_block_b300 import build as B
+    B.build()
+    import depth_wise_softmax_block_b300 as ar
+    from depth_wise_softmax_block_b300.schedule import FullGroupedRunner, KernelTimer
+    dev = torch.device("cuda", 0)
+    wl = I.FULL_INTERP_BF16
+    T, d, L, S = wl.T, wl.d, wl.L, args.group
+    hist = torch.empty((L + 1, T, d), dtype=torch.bfloat16, device=dev)
+    hist[0].copy_(I.normal((T, d), 1.0, wl.seed, "v0", dev, torch.bfloat16))
+    v = torch.stack([I.normal((T, d), 1.0 + wl.v_growth * l, wl.seed, f"v{l}", dev,
+                              torch.bfloat16) for l in range(1, L + 1)])
+    W = I.queries(L, d, wl.seed, "w", dev)
+    U = torch.empty_like(W)
+    Us = torch.empty((2 * L, d), dtype=torch.bfloat16, device=dev)
+    ar.attnres_query_prep(W, None, U, Us)
+    G_in = I.gains(L, d, 0.0, wl.seed, "gin", dev)
+    ys = torch.empty((L, T, d), dtype=torch.bfloat16, device=dev)
+    timer = KernelTimer()
+    runner = FullGroupedRunner(T, d, S, torch.bfloat16, dev, timer=timer)
+
+    def grouped():
+        runner.run(hist, U, G_in, ys, lambda l, y: v[l - 1], wl.eps, wl.eps, U_split=Us)
+
+    def direct():
+        for l in range(1, L + 1):
+            ar.attnres_full_reference_path([hist[j] for j in range(l)], U[l - 1], G_in[l - 1],
+                                           y_out=ys[l - 1], eps_key=wl.eps, eps_in=wl.eps)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        timer.clear()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    ms_g = timed(grouped)
+    kern = {k: {"launches_per_step": c // args.steps, "avg_ms": t / c}
+            for k, (t, c) in timer.totals_ms().items()}
+    runner.timer = None
+    ms_d = timed(direct)
+    bg, bd = full_grouped_bytes(L, S, d, 2) * T, full_direct_bytes(L, d, 2) * T
+    peak, kind = peaks()
+    line = {
+        "metric": "Full AttnRes whole-depth tokens/s and achieved HBM GB/s, grouped two-phase "
+                  "vs direct, 1 GPU",
+        "value": T / (ms_g / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_g, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name + f"_grouped_S{S}", "tokens": T, "d": d, "layers": L,
+                   "group": S},
+        "grouped": {"ms": ms_g, "bytes": bg, "achieved_gbs": bg / (ms_g / 1e3) / 1e9,
+                    "frac_of_peak": bg / (ms_g / 1e3) / 1e9 / peak,
+                    "d_elements_per_layer": bg / T / L / d / 2, "kernels": kern},
+        "direct": {"ms": ms_d, "bytes": bd, "achieved_gbs": bd / (ms_d / 1e3) / 1e9,
+                   "d_elements_per_layer": bd / T / L / d / 2},
+        "speedup_grouped_over_direct": ms_d / ms_g, "peak_gbs": peak, "peak_source": kind,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -352,9 +443,14 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the token count (profiling a smaller case)")
     ap.add_argument("--chunk", type=int, default=0, help="override the chunk size")
+    ap.add_argument("--workload", default="longctx", choices=["longctx", "full_grouped"],
+                    help="full_grouped: the Full AttnRes depth, grouped two-phase vs direct")
+    ap.add_argument("--group", type=int, default=8, help="group size of --workload full_grouped")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
 
+    if args.workload == "full_grouped" and args.impl == "ours":
+        return run_full_grouped(args)
     if args.impl == "reference":
         line = reference_arm(args, world, rank)
         if line is not None:

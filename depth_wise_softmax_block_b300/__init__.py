@@ -37,6 +37,8 @@ SIGNATURES = {
     "attnres_partial_update": ([_P, _P, _P, _I64, _I, _I, _P], _I),
     "attnres_full_reference_path": ([_P, _I, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _U, _P],
                                     _I),
+    "attnres_phase2_merge_sources": ([_P, _P, _P, _I, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _U,
+                                      _P], _I),
 }
 
 
@@ -173,4 +175,20 @@ def attnres_full_reference_path(srcs, u_l, gamma_in, h_out=None, y_out=None, alp
         arr, len(srcs), T, d, _io(srcs[0]), _ptr(u_l), eps_key, _ptr(gamma_in), eps_in,
         _ptr(h_out), _ptr(y_out), _ptr(alpha_out), flags, _stream(stream)),
         "attnres_full_reference_path")
+    return h_out if y_out is None else y_out
+
+
+def attnres_phase2_merge_sources(o_l, lse_l, srcs, u_l, gamma_in, h_out=None, y_out=None,
+                                 alpha_out=None, eps_key=1e-6, eps_in=1e-6, flags=0, stream=None):
+    """Grouped Full AttnRes phase 2 for one layer: merge phase 1's (o_l, lse_l) with the
+    group's in-group sources ``srcs`` (a list of [T, d] tensors, possibly empty)."""
+    T, d = o_l.shape
+    for name, t in [("o_l", o_l), ("h_out", h_out), ("y_out", y_out)] + \
+            [("srcs[j]", t) for t in srcs]:
+        _rows(t, T, d, name)
+    arr = (ctypes.c_void_p * max(1, len(srcs)))(*[t.data_ptr() for t in srcs])
+    _check(library().attnres_phase2_merge_sources(
+        _ptr(o_l), _ptr(lse_l), arr if srcs else None, len(srcs), T, d, _io(o_l), _ptr(u_l),
+        eps_key, _ptr(gamma_in), eps_in, _ptr(h_out), _ptr(y_out), _ptr(alpha_out), flags,
+        _stream(stream)), "attnres_phase2_merge_sources")
     return h_out if y_out is None else y_out

@@ -182,4 +182,47 @@ attnres_status attnres_full_reference_path(const void* const* srcs, int n_src, i
                                           static_cast<cudaStream_t>(stream)));
 }
 
+attnres_status attnres_phase2_merge_sources(const void* o_l, const float* lse_l,
+                                            const void* const* srcs, int k, int64_t T, int d,
+                                            attnres_dtype io, const float* u_l, float eps_key,
+                                            const float* gamma_in, float eps_in, void* h_out,
+                                            void* y_out, float* alpha_out, unsigned int flags,
+                                            void* stream) {
+  if (!valid_io(io) || !valid_flags(flags)) return ATTNRES_ERR_INVALID_ARG;
+  const attnres_status sh = check_shape(T, d);
+  if (sh != ATTNRES_OK) return sh;
+  if (k < 0) return ATTNRES_ERR_INVALID_ARG;
+  if (k > ATTNRES_MAX_SOURCES) return ATTNRES_ERR_UNSUPPORTED;
+  if (!(eps_key >= 0.f) || !(eps_in >= 0.f)) return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (o_l == nullptr || (h_out == nullptr && y_out == nullptr)) return ATTNRES_ERR_INVALID_ARG;
+  if (lse_l == nullptr && !(flags & ATTNRES_SIGMOID_WEIGHTS)) return ATTNRES_ERR_INVALID_ARG;
+  if (k > 0 && (srcs == nullptr || u_l == nullptr)) return ATTNRES_ERR_INVALID_ARG;
+  attnres::FullArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int j = 0; j < k; ++j) {
+    if (srcs[j] == nullptr) return ATTNRES_ERR_INVALID_ARG;
+    if (!aligned16(srcs[j])) return ATTNRES_ERR_MISALIGNED;
+    a.srcs[j] = srcs[j];
+  }
+  if (!aligned16(o_l) || !opt_aligned16(u_l) || !opt_aligned16(gamma_in) ||
+      !opt_aligned16(h_out) || !opt_aligned16(y_out))
+    return ATTNRES_ERR_MISALIGNED;
+  a.n = k;
+  a.T = T;
+  a.d = d;
+  a.u = u_l;
+  a.eps_key = eps_key;
+  a.gamma_in = gamma_in;
+  a.eps_in = eps_in;
+  a.h = h_out;
+  a.y = y_out;
+  a.alpha = alpha_out;
+  a.flags = flags;
+  a.o0 = o_l;
+  a.lse0 = lse_l;
+  return cuda_status(attnres::launch_full(static_cast<IO>(io), a,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -66,6 +66,8 @@ struct FullArgs {
   float* m;         // [T] or null: max logit
   float* lse;       // [T] or null: log-sum-exp of the logits
   unsigned flags;
+  const void* o0;   // [T, d] or null: normalised output of an earlier source partition
+  const float* lse0;  // [T]: its log-sum-exp (required with o0 unless sigmoid weights)
 };
 
 // Each launcher returns cudaSuccess or the launch error.

@@ -6,7 +6,10 @@
 //                  with the phase-1 result by online softmax ("Attention Residuals 阅读补充",
 //                  merge of two partitions) and applies the sublayer's input RMSNorm.
 //   full_kernel    the direct single-pass aggregation over an explicit source list (§7),
-//                  online softmax over the sources, then the input RMSNorm.
+//                  online softmax over the sources, then the input RMSNorm; optionally seeded
+//                  with an earlier partition (o, lse), which makes it the phase 2 of the
+//                  grouped Full AttnRes schedule ("Attention Residuals 阅读补充", section
+//                  "静态 Query 与两阶段计算").
 // Both take the Table 4 variant flags (sigmoid weights, no key RMSNorm; "Attention
 // Residuals" note, result 4).
 //   add_kernel     partial-sum update / block close: out = partial + v.
@@ -182,6 +185,19 @@ __global__ void __launch_bounds__(kRowThreads) full_kernel(const FullArgs a) {
 #pragma unroll
     for (int e = 0; e < VE; ++e) acc[k][e] = 0.f;
   float mrun = -INFINITY, lrun = 0.f;
+  // An earlier partition of the sources (phase 1 of a group: normalised o0 and its lse) starts
+  // the online softmax: with the running max at lse0 it contributes o0 with exp-sum 1.
+  if (a.o0 != nullptr) {
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = threadIdx.x + k * blockDim.x;
+      if (v < nv) unpack(ld_stream(static_cast<const T*>(a.o0) + base + v * VE), acc[k]);
+    }
+    if ((a.flags & kSigmoid) == 0) {
+      mrun = a.lse0[row];
+      lrun = 1.f;
+    }
+  }
 
   auto load = [&](uint4 (&r)[VPT], int j) {
 #pragma unroll
@@ -233,7 +249,7 @@ __global__ void __launch_bounds__(kRowThreads) full_kernel(const FullArgs a) {
   };
 
   uint4 bufA[VPT], bufB[VPT];
-  load(bufA, 0);
+  if (a.n > 0) load(bufA, 0);
   if (a.n > 1) load(bufB, 1);
   for (int j = 0; j < a.n; j += 2) {
     float x[VPT][VE];

@@ -21,7 +21,7 @@ from typing import Callable, Optional
 import torch
 
 from . import (attnres_full_reference_path, attnres_partial_update, attnres_phase1,
-               attnres_phase2_merge)
+               attnres_phase2_merge, attnres_phase2_merge_sources)
 
 
 class KernelTimer:
@@ -132,3 +132,45 @@ def full_attnres_sublayer(history, u_l, g_in, y_out, h_out=None, alpha_out=None,
     """Full AttnRes input of one sublayer over the explicit history v_0 .. v_{l-1}."""
     return attnres_full_reference_path(list(history), u_l, g_in, h_out=h_out, y_out=y_out,
                                        alpha_out=alpha_out, eps_key=eps_key, eps_in=eps_in)
+
+
+class FullGroupedRunner:
+    """Full AttnRes (layer l reads v_0 .. v_{l-1}) by the grouped two-phase schedule ("Attention
+    Residuals 阅读补充", section "静态 Query 与两阶段计算"): groups of S layers; phase 1
+    scores a group's queries against the history [v_0 .. v_{l0}] in one pass; layer l0 + i then
+    merges the group's own outputs v_{l0+1} .. v_{l0+i-1} into phase 1's result.
+
+    ``hist`` [L + 1, T, d] holds v_0 in slot 0; slot l receives v_l = sublayer(l, y_l) (the
+    model's attention or MLP; a stand-in for the synthetic workloads)."""
+
+    def __init__(self, T: int, d: int, S: int, dtype, device, timer: Optional[KernelTimer] = None):
+        self.S, self.timer = S, timer
+        self.o = torch.empty((S, T, d), dtype=dtype, device=device)
+        self.lse = torch.empty((S, T), dtype=torch.float32, device=device)
+
+    def run(self, hist: torch.Tensor, U: torch.Tensor, G_in: Optional[torch.Tensor],
+            y_out: torch.Tensor, sublayer: Callable[[int, torch.Tensor], torch.Tensor],
+            eps_key: float = 1e-6, eps_in: float = 1e-6, U_split: Optional[torch.Tensor] = None,
+            flags: int = 0) -> None:
+        """U [L, d] folded queries; y_out [L, T, d] receives every layer's input y_l;
+        U_split [2L, d] (optional) puts phase 1's logits on the tensor cores where the shape
+        allows."""
+        L = U.shape[0]
+        tm = self.timer
+        for l0 in range(0, L, self.S):
+            Sg = min(self.S, L - l0)
+            o, lse = self.o[:Sg], self.lse[:Sg]
+            us = None if U_split is None else U_split[2 * l0:2 * (l0 + Sg)]
+            _call(tm, "phase1", attnres_phase1, hist[:l0 + 1], U[l0:l0 + Sg], o, lse_out=lse,
+                  eps=eps_key, u_split=us, flags=flags)
+            for i in range(1, Sg + 1):
+                l = l0 + i
+                g = None if G_in is None else G_in[l - 1]
+                srcs = [hist[j] for j in range(l0 + 1, l)]
+                _call(tm, "phase2_sources", attnres_phase2_merge_sources, o[i - 1], lse[i - 1],
+                      srcs, U[l - 1], g, y_out=y_out[l - 1], eps_key=eps_key, eps_in=eps_in,
+                      flags=flags)
+                v = sublayer(l, y_out[l - 1])
+                if v.data_ptr() != hist[l].data_ptr():
+                    hist[l].copy_(v)
+

@@ -73,7 +73,7 @@ typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype;
 #define ATTNRES_MAX_D 16384        /* hidden size (a row stays in registers)               */
 
 /* ABI version of this header; attnres_abi_version() returns the library's. */
-#define ATTNRES_ABI_VERSION 3
+#define ATTNRES_ABI_VERSION 4
 int attnres_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -199,6 +199,32 @@ attnres_status attnres_full_reference_path(const void* const* srcs, int n_src, i
                                            float eps_key, const float* gamma_in,
                                            float eps_in, void* h_out, void* y_out,
                                            float* alpha_out, unsigned int flags, void* stream);
+
+/*
+ * Phase 2 of Full AttnRes run by the grouped two-phase schedule ("Attention Residuals 阅读补充",
+ * section "静态 Query 与两阶段计算": the layers fall into groups of S; phase 1
+ * (attnres_phase1) scores a group's S queries against the history in one pass; phase 2 takes
+ * the group's layers one by one and merges, by online softmax, the k representations the
+ * group has produced so far).  For layer l with phase-1 result (o_l, lse_l) over the history A
+ * and in-group sources B = srcs[0 .. k-1]:
+ *     M = max(lse_l, max_{i in B} z_i)
+ *     h = (e^{lse_l - M} o_l + sum_{i in B} e^{z_i - M} v_i) / (e^{lse_l - M} + sum_{i in B} e^{z_i - M})
+ *     y = gamma_in ⊙ h / sqrt(mean h^2 + eps_in)
+ * (k = 0 gives h = o_l.)  With ATTNRES_SIGMOID_WEIGHTS, h = o_l + sum_{i in B} sigmoid(z_i) v_i
+ * and lse_l is not read.
+ *   o_l, lse_l  device [T, d] (io dtype) and fp32 [T]: phase 1's output row block of layer l
+ *   srcs        HOST array of k device pointers, each [T, d] (io dtype); may be NULL when k = 0
+ *   u_l, gamma_in, eps_key, eps_in: as for attnres_phase2_merge
+ *   h_out, y_out  device [T, d] or NULL (at least one required)
+ *   alpha_out   device fp32 [T][k] or NULL: weights of the in-group sources
+ * Limits: 0 <= k <= 64.
+ */
+attnres_status attnres_phase2_merge_sources(const void* o_l, const float* lse_l,
+                                            const void* const* srcs, int k, int64_t T, int d,
+                                            attnres_dtype io, const float* u_l, float eps_key,
+                                            const float* gamma_in, float eps_in, void* h_out,
+                                            void* y_out, float* alpha_out, unsigned int flags,
+                                            void* stream);
 
 #ifdef __cplusplus
 }

@@ -275,6 +275,61 @@ def full_attnres_walk(v0, v, W, G_key, G_in, w_final, g_final, eps_key: float, e
 
 
 # ---------------------------------------------------------------------------------------------
+# Full AttnRes with the grouped two-phase schedule (page 1, "静态 Query 与两阶段计算": the L
+# layers fall into G scheduling groups of S = L / G; phase 1 scores the S queries of a group
+# against the history in one pass and keeps the softmax statistics; phase 2 takes the layers
+# of the group one by one and merges the representations the group has produced so far by
+# online softmax)
+# ---------------------------------------------------------------------------------------------
+def merge_sources_reference(o_A, lse_A, sources_B, w, gamma_key, eps_key: float, gamma_in,
+                            eps_in: float):
+    """Phase 2 of one layer of a group: partition A as phase 1 hands it over (normalised o_A
+    [T,d], lse_A [T]) merged with the in-group sources B ([k,T,d], k >= 0) by the partition
+    merge of page 1: with m = max(lse_A, max_{i in B} z_i),
+        h = (e^{lse_A - m} o_A + sum_{i in B} e^{z_i - m} v_i)
+            / (e^{lse_A - m} + sum_{i in B} e^{z_i - m}).
+    Returns (h, y = RMSNorm_in(h), alpha_B [k,T], weight of A [T])."""
+    o_A, lse_A = _f64(o_A), _f64(lse_A)
+    B = _f64(sources_B).reshape((-1,) + o_A.shape)
+    if B.shape[0] == 0:
+        return o_A, rmsnorm(o_A, gamma_in, eps_in), np.zeros((0,) + lse_A.shape), \
+            np.ones_like(lse_A)
+    z = depth_logits(B, w, gamma_key, eps_key)              # [k, T]
+    m = np.maximum(lse_A, np.max(z, axis=0))
+    ca = np.exp(lse_A - m)
+    cb = np.exp(z - m)
+    den = ca + np.sum(cb, axis=0)
+    h = (ca[..., None] * o_A + np.sum(cb[..., None] * B, axis=0)) / den[..., None]
+    return h, rmsnorm(h, gamma_in, eps_in), cb / den, ca / den
+
+
+def grouped_full_walk(v0, v, W, G_key, G_in, S: int, eps_key: float, eps_in: float):
+    """Full AttnRes (page 2 §7: layer l reads v_0 .. v_{l-1}) run by the grouped two-phase
+    schedule with groups of S layers (the last group may be shorter): for group g starting at
+    layer l0 + 1, phase 1 = partition_stats over A = [v_0 .. v_{l0}] for each of its queries;
+    layer l0 + i then merges B = [v_{l0+1} .. v_{l0+i-1}].
+    v: [L, T, d] (v[i-1] = v_i).  Returns a BlockWalk (h, y, and alpha over A followed by B)."""
+    v = _f64(v)
+    L = v.shape[0]
+    hist = [_f64(v0)] + [v[i] for i in range(L)]
+    out = BlockWalk()
+    for l0 in range(0, L, S):
+        A = np.stack(hist[:l0 + 1])
+        for l in range(l0 + 1, min(l0 + S, L) + 1):
+            gk = None if G_key is None else _f64(G_key)[l - 1]
+            gi = None if G_in is None else _f64(G_in)[l - 1]
+            o, m, lse, aA = partition_stats(A, _f64(W)[l - 1], gk, eps_key)
+            B = np.stack(hist[l0 + 1:l]) if l > l0 + 1 else np.zeros((0,) + A.shape[1:])
+            h, y, aB, wA = merge_sources_reference(o, lse, B, _f64(W)[l - 1], gk, eps_key, gi,
+                                                   eps_in)
+            out.h.append(h)
+            out.y.append(y)
+            out.alpha.append(np.concatenate([aA * wA, aB]))
+            out.n_sources.append(l)
+    return out
+
+
+# ---------------------------------------------------------------------------------------------
 # Ablation variants of the report's Table 4 (page 2 "Attention Residuals" note, result 4):
 # "sigmoid weights" (no softmax competition between sources, no sum-to-1 constraint) and
 # "no key RMSNorm" (the source magnitude enters the score directly).  The pages give one line

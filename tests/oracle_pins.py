@@ -428,6 +428,55 @@ def pin_merge_reference(O):
     assert np.all(a0 == 0.0)
 
 
+# --- grouped two-phase Full AttnRes (page 1, "静态 Query 与两阶段计算") ------------------------
+def pin_grouped_full_equals_direct(O):
+    """The grouped two-phase schedule reproduces the direct Full AttnRes walk for every group
+    size, including S = 1 (phase 1 alone) and S = L (one group, phase 2 merges up to L - 1
+    in-group sources)."""
+    r = _rng(40)
+    L, T, d = 7, 3, 16
+    v0 = r.normal(0.0, 1.0, size=(T, d))
+    v = r.normal(0.0, 1.0, size=(L, T, d)) * (1.0 + 0.1 * np.arange(1, L + 1))[:, None, None]
+    W = r.normal(0.0, 0.5, size=(L, d))
+    Gk = r.normal(1.0, 0.1, size=(L, d))
+    Gi = r.normal(1.0, 0.1, size=(L, d))
+    full = O.full_attnres_walk(v0, v, W, Gk, Gi, None, None, 1e-6, 1e-6)
+    for S in (1, 2, 3, L):
+        g = O.grouped_full_walk(v0, v, W, Gk, Gi, S, 1e-6, 1e-6)
+        for l in range(L):
+            _close(g.y[l], full.y[l], 1e-12, f"S={S} y_{l + 1}")
+            _close(g.h[l], full.h[l], 1e-12, f"S={S} h_{l + 1}")
+            _close(g.alpha[l], full.alpha[l], 1e-14, f"S={S} alpha_{l + 1}")
+
+
+def pin_merge_sources(O):
+    """Merging partition A with a list B of in-group sources equals the direct softmax over
+    A u B for every split of 5 sources; with one source it is merge_reference; with none it
+    returns o_A."""
+    r = _rng(41)
+    n, T, d = 5, 4, 12
+    v = _sources(r, n, T, d)
+    w = r.normal(0.0, 1.0, size=d)
+    g = r.normal(1.0, 0.1, size=d)
+    gi = r.normal(1.0, 0.1, size=d)
+    h_d, a_d, _ = O.aggregate(v, w, g, 1e-6)
+    for k in range(1, n):
+        o, m, lse, aA = O.partition_stats(v[:k], w, g, 1e-6)
+        h, y, aB, wA = O.merge_sources_reference(o, lse, v[k:], w, g, 1e-6, gi, 1e-6)
+        _close(h, h_d, 1e-12, f"A = first {k}")
+        _close(aB, a_d[k:], 1e-14, "in-group weights")
+        _close(aA * wA, a_d[:k], 1e-14, "history weights")
+        _close(y, O.rmsnorm(h_d, gi, 1e-6), 1e-12, "y")
+    o, m, lse, _ = O.partition_stats(v[:4], w, g, 1e-6)
+    h1, y1, aB, _ = O.merge_sources_reference(o, lse, v[4:], w, g, 1e-6, gi, 1e-6)
+    h2, y2, ap = O.merge_reference(o, lse, v[4], w, g, 1e-6, gi, 1e-6)
+    _close(h1, h2, 1e-13, "one source = merge_reference")
+    _close(aB[0], ap, 1e-15, "its weight")
+    h0, _, aB0, wA0 = O.merge_sources_reference(o, lse, v[:0], w, g, 1e-6, gi, 1e-6)
+    _close(h0, o, 0.0, "no source: o_A")
+    assert aB0.shape[0] == 0 and np.all(wA0 == 1.0)
+
+
 # --- Table 4 ablation variants (page 2 "Attention Residuals" note, result 4) -------------------
 def pin_sigmoid_zero_query_half(O):
     """Sigmoid weights with zero queries: every weight is sigmoid(0) = 1/2 (no sum-to-1), so

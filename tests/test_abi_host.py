@@ -45,7 +45,7 @@ def test_header_symbols_exported(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.attnres_abi_version() == 3
+    assert lib.attnres_abi_version() == 4
     for code, name in ar.STATUS.items():
         assert lib.attnres_status_string(code).decode() == name
     assert lib.attnres_status_string(99).decode() == "ATTNRES_ERR_UNKNOWN"
@@ -141,6 +141,28 @@ def test_full_and_update_validation(lib):
     assert err(qp(None, None, P, None, 4, 64, None)) == INVALID
     assert err(qp(P, PM, P, None, 4, 64, None)) == MISALIGNED
     assert err(qp(P, None, P, PM, 4, 64, None)) == MISALIGNED
+
+
+def test_merge_sources_validation(lib):
+    import ctypes
+    arr = (ctypes.c_void_p * 2)(P, P + 4096)
+    ms = lib.attnres_phase2_merge_sources
+
+    def call(o=P, lse=P, srcs=arr, k=2, T=0, d=64, u=P, h=None, y=P, flags=0):
+        return ms(o, lse, srcs, k, T, d, 1, u, 1e-6, None, 1e-6, h, y, None, flags, None)
+    assert call() == OK
+    assert call(k=0, srcs=None) == OK
+    assert call(k=-1) == INVALID
+    assert call(k=65) == UNSUPPORTED
+    assert err(call(T=4, o=None)) == INVALID
+    assert err(call(T=4, lse=None)) == INVALID           # the history's lse is needed ...
+    assert call(lse=None, flags=1) == OK                  # ... except with sigmoid weights
+    assert err(call(T=4, y=None)) == INVALID              # nothing to write
+    assert err(call(T=4, srcs=None)) == INVALID
+    assert err(call(T=4, o=PM)) == MISALIGNED
+    bad = (ctypes.c_void_p * 2)(P, PM)
+    assert err(call(T=4, srcs=bad)) == MISALIGNED
+    assert call(flags=4) == INVALID
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -109,7 +109,15 @@ def _merge_variant_softmax_for_sigmoid(o_A, lse_A, p, w, gamma_key, eps_key, gam
                          key_norm)
 
 
+def _merge_sources_drops_history(o_A, lse_A, sources_B, w, gamma_key, eps_key, gamma_in,
+                                 eps_in):               # forgets partition A's exp-sum weight
+    h, y, aB, wA = _ORIG_MERGE_S(o_A, np.full_like(np.asarray(lse_A, np.float64), -50.0),
+                                 sources_B, w, gamma_key, eps_key, gamma_in, eps_in)
+    return h, y, aB, wA
+
+
 _ORIG_PARTITION = O.partition_stats
+_ORIG_MERGE_S = O.merge_sources_reference
 _ORIG_MERGE_V = O.merge_reference_variant
 _ORIG_MERGE = O.merge_reference
 
@@ -132,6 +140,7 @@ MUTATIONS = {
     "sigmoid_sign": ("depth_sigmoid", _sigmoid_sign),
     "raw_logits_normalised": ("depth_logits_raw", _raw_logits_still_normalised),
     "sigmoid_merged_as_softmax": ("merge_reference_variant", _merge_variant_softmax_for_sigmoid),
+    "merge_sources_drops_history": ("merge_sources_reference", _merge_sources_drops_history),
 }
 
 
