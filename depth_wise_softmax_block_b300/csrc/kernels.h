@@ -93,7 +93,7 @@ cudaError_t encode_query_map(CUtensorMap* map, const float* u, int S, int d);
 cudaError_t encode_split_query_map(CUtensorMap* map, const void* u_split, int S, int d,
                                    int rows_box);
 
-// Tensor-core phase 1 (phase1_tc.cu): bf16 I/O, 2 <= S <= 24, n <= 9, split queries given.
+// Tensor-core phase 1 (phase1_tc.cu): bf16 I/O, 2 <= S <= 24, n <= 64, split queries given.
 bool phase1_tc_supported(int n, int S);
 cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s);
 unsigned int phase1_tc_poll_timeouts();

@@ -43,16 +43,18 @@ constexpr int kWarps = kCompute / 32;
 constexpr int kThreads = kCompute + 64;    // + a copy-issuing warp and an MMA-issuing warp
 constexpr int kTT = 8;              // tokens per CTA tile
 constexpr int kKC = 64;             // bf16 columns per stage (one 128-byte row slice)
-constexpr int kM = 128;             // MMA rows (tile rows n * 8 <= 128)
-constexpr int kMaxS = 24;           // sweep 2 covers 8 groups of 3 queries
-constexpr int kMaxN = 9;            // sources: the sweep-2 weights of a thread live in registers
-constexpr int kTmemCols = 64;       // D uses at most 2 * 24 = 48 columns
+constexpr int kM = 128;             // rows per MMA (M-tile); a tile has n * 8 rows
+constexpr int kMaxS = 24;           // sweep 2 covers 4 groups of 6 queries
+constexpr int kMaxN = 64;           // sources (up to 4 M-tiles)
+constexpr int kSmallN = 9;          // up to here the sweep-2 weights are stored as ready pairs
+constexpr int kTmemCols = 256;      // D: up to 4 M-tiles x 2S <= 48 columns (one: 64)
 constexpr int kMaxSlots = 12;       // ring slots
 constexpr int kMaxSmem = 227 * 1024;
 
 struct TcPlan {
   int Npad;           // MMA N: 2S rounded up to 16
-  int bBytes;         // source box bytes as copied (n * 8 * 128)
+  int rows, nMT;      // tile rows (n * 8) and M-tiles (ceil(rows / 128))
+  int bBytes;         // source box bytes as copied (rows * 128)
   int bSpan;          // rounded up to 1024
   int qBytes;         // split-query box bytes (Npad rows x 128 bytes, rows >= 2S zero-filled)
   int slot, SB;       // ring slot bytes ([sources][split queries]), slots
@@ -65,23 +67,28 @@ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 bool make_tc_plan(int n, int S, TcPlan& p) {
   if (n < 1 || n > kMaxN || S < 2 || S > kMaxS) return false;
   p.Npad = align_up(2 * S, 16);
-  p.bBytes = n * kTT * 128;
+  p.rows = n * kTT;
+  p.nMT = (p.rows + kM - 1) / kM;
+  p.bBytes = p.rows * 128;
   p.bSpan = align_up(p.bBytes, 1024);
   p.qBytes = p.Npad * 128;
   p.slot = p.bSpan + align_up(p.qBytes, 1024);
-  // The MMA reads 128 rows (16 KB) from a slot's base; rows past the tile's n * 8 are ignored
-  // but must lie inside the allocation, hence the slack after the last slot.
-  const int slack = std::max(0, kM * 128 - p.slot);
-  const int zb = kM * S * 4;
-  const int ab = kTT * n * 4 * 12 * 4;   // [token][source][4 groups][6 pairs][2]
-  const int fixed = slack + align_up(zb, 16) + align_up(ab, 16) + kM * 4 +
+  // The MMAs read nMT * 128 rows from a slot's base; rows past the tile's n * 8 are ignored but
+  // must lie inside the allocation, hence the slack after the last slot.
+  const int slack = std::max(0, p.nMT * kM * 128 - p.slot);
+  // logits [rows][SZ] (SZ = S rounded up to even, for 8-byte loads), then (n > 9) the
+  // weights in their place; 8 floats of padding for the last query group's 6-wide read
+  const int zb = (p.nMT * kM * ((S + 1) & ~1) + 8) * 4;
+  const int ab = n <= kSmallN ? kTT * n * 4 * 12 * 4 : 0;  // [token][source][4][6 pairs][2]
+  const int sb = 2 * p.nMT * kM * 4;                       // per-half row sums of squares
+  const int fixed = slack + align_up(zb, 16) + align_up(ab, 16) + sb +
                     (2 * kMaxSlots + 2) * 8 + 16;
   p.SB = std::min(kMaxSlots, (kMaxSmem - 1024 - fixed) / p.slot);
-  if (p.SB < 3) return false;
+  if (p.SB < 2) return false;
   p.offZ = p.SB * p.slot + slack;
   p.offAlph = p.offZ + align_up(zb, 16);
   p.offSs = p.offAlph + align_up(ab, 16);
-  p.offBar = p.offSs + kM * 4;
+  p.offBar = p.offSs + sb;
   p.offTmem = p.offBar + (2 * p.SB + 2) * 8;
   p.smem = 1024 + p.offTmem + 16;
   return true;
@@ -94,6 +101,9 @@ __device__ __forceinline__ void unpack_pairs(const uint4& v, float2 (&f)[4]) {
     f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
 }
 
+// kSmall: n <= 9 (one M-tile, sweep-2 weights as ready-made pairs, sums of squares in
+// registers), compiled without the paths for larger n.
+template <bool kSmall>
 __global__ void __launch_bounds__(kThreads, 1)
 phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
                  const __grid_constant__ CUtensorMap tm_q, const Phase1Args a, const TcPlan pl) {
@@ -111,9 +121,10 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   uint64_t* dready = empty + SB;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(dready + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + pl.offTmem);
-  float* zbuf = reinterpret_cast<float*>(smem + pl.offZ);     // [128 rows][S]
-  float* alph = reinterpret_cast<float*>(smem + pl.offAlph);  // [8][n][4 groups][6 pairs][2]
-  float* ssbuf = reinterpret_cast<float*>(smem + pl.offSs);   // [128 rows]
+  float* zbuf = reinterpret_cast<float*>(smem + pl.offZ);     // [nMT * 128 rows][SZ]
+  const int SZ = (S + 1) & ~1;
+  float* alph = reinterpret_cast<float*>(smem + pl.offAlph);  // n <= 9: [8][n][4][6 pairs][2]
+  float* ssbuf = reinterpret_cast<float*>(smem + pl.offSs);   // [2 halves][nMT * 128 rows]
 
   if (tid == 0) {
     for (int s = 0; s < SB; ++s) {
@@ -125,7 +136,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
     mbar_fence_init();
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_alloc(tmem_slot, kSmall ? 64 : kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -163,8 +174,8 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   }
 
   // ------------------------------- MMA-issuing warp -------------------------------
-  // The stage's four K = 16 MMAs, D[row, 2s + {hi, lo}] += b_row . u_s, as soon as its copies
-  // land; completion arrives on the stage's "empty" barrier (and, after the last stage, on
+  // The stage's K = 16 MMAs (four per M-tile), D[row, 2s + {hi, lo}] += b_row . u_s, as soon
+  // as its copies land; completion arrives on the stage's "empty" barrier (and, after the last stage, on
   // "dready").  An MMA costs about the same for every N up to 128, so issuing from a warp of
   // its own keeps the tensor core off the compute warps' critical path.
   if (warp == kWarps + 1) {
@@ -176,11 +187,14 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
       tc_fence_after();
       if (lane == 0) {
         const unsigned char* st = smem + bs * pl.slot;
-        const uint32_t a0 = smem_addr(st), b0 = smem_addr(st + pl.bSpan);
+        const uint32_t b0 = smem_addr(st + pl.bSpan);
+        for (int mt = 0; mt < (kSmall ? 1 : pl.nMT); ++mt) {  // M-tile mt: rows mt * 128 ..
+          const uint32_t a0 = smem_addr(st + mt * kM * 128);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc_mma_bf16(tmem, desc_kmajor_sw128(a0 + 32 * kk), desc_kmajor_sw128(b0 + 32 * kk),
-                      idesc, (c | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16(tmem + mt * pl.Npad, desc_kmajor_sw128(a0 + 32 * kk),
+                        desc_kmajor_sw128(b0 + 32 * kk), idesc, (c | kk) != 0 ? 1u : 0u);
+        }
         tc_commit(&empty[bs]);
         if (c == nch - 1) tc_commit(dready);
       }
@@ -207,63 +221,84 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   const int nrows = n * kTT;  // tile rows: row j * 8 + t
   const bool key_norm = (a.flags & kNoKeyNorm) == 0;
   const bool sigmoid = (a.flags & kSigmoid) != 0;
-  // sums of squares: the half's thread ht takes the (row, 16-byte chunk) pairs ht + 256 k
-  float2 ssa[3] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  // sums of squares: the half's thread ht takes the (row, 16-byte chunk) pairs ht + 256 k, and
+  // each half sums its stages into its own row buffer.  Up to 4 pairs per thread (n <= 16) the
+  // sums stay in registers until the end of the sweep; beyond that the 8 chunks of a row (8
+  // consecutive lanes) are summed with shuffles every stage and added to the buffer (one owner
+  // per row within a half: no race).
+  const int ntask = (nrows * 8 + 255) / 256;
+  const bool reg_ss = kSmall || ntask <= 4;
+  float* ssh = ssbuf + half * (pl.nMT * kM);
+  for (int i = tid; i < 2 * pl.nMT * kM; i += kCompute) ssbuf[i] = 0.f;
+  named_barrier(1, kCompute);
+  float2 ssa[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                   make_float2(0.f, 0.f)};
   for (int c = half; c < nch; c += 2) {
     const int bs = c % SB;
     const unsigned char* st = smem + bs * pl.slot;
     wait(&full[bs], (c / SB) & 1);
+    if (key_norm && reg_ss) {
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
-      const int i = ht + k * 256;
-      if (key_norm && i < nrows * 8) {
-        float2 f[4];
-        unpack_pairs(*reinterpret_cast<const uint4*>(st + sw128(i >> 3, i & 7)), f);
+      for (int k = 0; k < 4; ++k) {
+        const int i = ht + k * 256;
+        if (i < nrows * 8) {
+          float2 f[4];
+          unpack_pairs(*reinterpret_cast<const uint4*>(st + sw128(i >> 3, i & 7)), f);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) ssa[k] = __ffma2_rn(f[e], f[e], ssa[k]);
+          for (int e = 0; e < 4; ++e) ssa[k] = __ffma2_rn(f[e], f[e], ssa[k]);
+        }
+      }
+    } else if (!kSmall && key_norm) {
+      for (int k = 0; k < ntask; ++k) {
+        const int i = ht + k * 256;
+        float x = 0.f;
+        if (i < nrows * 8) {
+          float2 f[4];
+          unpack_pairs(*reinterpret_cast<const uint4*>(st + sw128(i >> 3, i & 7)), f);
+          float2 sq = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sq = __ffma2_rn(f[e], f[e], sq);
+          x = sq.x + sq.y;
+        }
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        if (i < nrows * 8 && (i & 7) == 0) ssh[i >> 3] += x;
       }
     }
     release(bs, false);
   }
-
-  // row sums of squares: the 8 chunks of a row sit in 8 consecutive lanes; half 0 writes its
-  // sums, then half 1 adds its own (fixed order: deterministic)
-  float rowsum[3];
+  if (reg_ss) {
 #pragma unroll
-  for (int k = 0; k < 3; ++k) {
-    float x = ssa[k].x + ssa[k].y;
-    x += __shfl_xor_sync(0xffffffffu, x, 1);
-    x += __shfl_xor_sync(0xffffffffu, x, 2);
-    x += __shfl_xor_sync(0xffffffffu, x, 4);
-    rowsum[k] = x;
-  }
-  for (int h = 0; h < 2; ++h) {
-    if (half == h) {
-#pragma unroll
-      for (int k = 0; k < 3; ++k) {
-        const int i = ht + k * 256;
-        if (i < nrows * 8 && (i & 7) == 0) ssbuf[i >> 3] = h == 0 ? rowsum[k] : ssbuf[i >> 3] + rowsum[k];
-      }
+    for (int k = 0; k < 4; ++k) {
+      const int i = ht + k * 256;
+      float x = ssa[k].x + ssa[k].y;
+      x += __shfl_xor_sync(0xffffffffu, x, 1);
+      x += __shfl_xor_sync(0xffffffffu, x, 2);
+      x += __shfl_xor_sync(0xffffffffu, x, 4);
+      if (i < nrows * 8 && (i & 7) == 0) ssh[i >> 3] = x;
     }
-    named_barrier(1, kCompute);
   }
+  named_barrier(1, kCompute);
 
   // ------------------------- logits from tensor memory -------------------------------
   const float fd = static_cast<float>(d);
-  if (warp < 4) {
+  if (warp < 4 * pl.nMT) {  // warp w reads TMEM lanes 32 (w % 4) .. of M-tile w / 4
     wait(dready, 0);
     tc_fence_after();
-    const int r = warp * 32 + lane;
-    const float rinv = r >= nrows ? 0.f : key_norm ? 1.f / sqrtf(ssbuf[r] / fd + a.eps) : 1.f;
+    const int mt = warp >> 2, sub = warp & 3;
+    const int r = mt * kM + sub * 32 + lane;
+    const float ss = r < nrows ? ssbuf[r] + ssbuf[pl.nMT * kM + r] : 0.f;
+    const float rinv = r >= nrows ? 0.f : key_norm ? 1.f / sqrtf(ss / fd + a.eps) : 1.f;
     for (int cc = 0; cc < pl.Npad / 16; ++cc) {
       uint32_t v[16];
-      tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + cc * 16, v);
+      tmem_ld16(tmem + (static_cast<uint32_t>(sub * 32) << 16) + mt * pl.Npad + cc * 16, v);
       tmem_ld_wait();
       if (r < nrows) {
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
           const int s = cc * 8 + e / 2;
-          if (s < S) zbuf[r * S + s] = (__uint_as_float(v[e]) + __uint_as_float(v[e + 1])) * rinv;
+          if (s < S) zbuf[r * SZ + s] = (__uint_as_float(v[e]) + __uint_as_float(v[e + 1])) * rinv;
         }
       }
     }
@@ -275,19 +310,24 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
     const int t = i / S, s = i % S;
     const int64_t tok = t0 + t;
     float m = -INFINITY;
-    for (int j = 0; j < n; ++j) m = fmaxf(m, zbuf[(j * kTT + t) * S + s]);
+    for (int j = 0; j < n; ++j) m = fmaxf(m, zbuf[(j * kTT + t) * SZ + s]);
     float l = 0.f;
     if (!sigmoid)
-      for (int j = 0; j < n; ++j) l += expf(zbuf[(j * kTT + t) * S + s] - m);
+      for (int j = 0; j < n; ++j) l += expf(zbuf[(j * kTT + t) * SZ + s] - m);
     const float lse = m + logf(l);
     const float rl = 1.f / l;
     const int g = s / 6, pp = s % 6;
     for (int j = 0; j < n; ++j) {
-      const float zj = zbuf[(j * kTT + t) * S + s];
+      float* zp = zbuf + (j * kTT + t) * SZ + s;
+      const float zj = *zp;
       const float al = sigmoid ? 1.f / (1.f + expf(-zj)) : expf(zj - m) * rl;
-      float* ap = alph + (((t * n + j) * 4 + g) * 6 + pp) * 2;
-      ap[0] = al;
-      ap[1] = al;
+      if (kSmall) {  // ready-made (a, a) pairs
+        float* ap = alph + (((t * n + j) * 4 + g) * 6 + pp) * 2;
+        ap[0] = al;
+        ap[1] = al;
+      } else {             // in place of the logit, which this thread alone reads
+        *zp = al;
+      }
       if (a.alpha != nullptr && tok < T) a.alpha[(static_cast<int64_t>(s) * T + tok) * n + j] = al;
     }
     if (tok < T) {
@@ -306,7 +346,8 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   const int kg = lane & 7;
   const int64_t tok2 = t0 + t2;
   const bool active2 = grp * 6 < S;
-  const float* at = alph + (t2 * n * 4 + grp) * 12;
+  const float* at = alph + (t2 * n * 4 + grp) * 12;     // n <= 9
+  const float* zt = zbuf + t2 * SZ + grp * 6;            // n > 9: weights of (j, t2, 6 queries)
   // source j's chunk: row j * 8 + t2, swizzled chunk kg ^ t2 (independent of j)
   const int boff = t2 * 128 + ((kg ^ t2) << 4);
   char* o = static_cast<char*>(a.o);
@@ -322,16 +363,32 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
       for (int qq = 0; qq < 6; ++qq)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[qq][e] = make_float2(0.f, 0.f);
+      if (kSmall) {
 #pragma unroll
-      for (int j = 0; j < kMaxN; ++j) {
-        if (j < n) {
+        for (int j = 0; j < kSmallN; ++j) {
+          if (j < n) {
+            float2 bv[4];
+            unpack_pairs(*reinterpret_cast<const uint4*>(st + j * 1024), bv);
+            const float4* ap = reinterpret_cast<const float4*>(at + j * 48);
+            const float4 a0 = ap[0], a1 = ap[1], a2 = ap[2];
+            const float2 al[6] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w),
+                                  make_float2(a1.x, a1.y), make_float2(a1.z, a1.w),
+                                  make_float2(a2.x, a2.y), make_float2(a2.z, a2.w)};
+#pragma unroll
+            for (int qq = 0; qq < 6; ++qq)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc[qq][e] = __ffma2_rn(al[qq], bv[e], acc[qq][e]);
+          }
+        }
+      } else {
+        for (int j = 0; j < n; ++j) {
           float2 bv[4];
           unpack_pairs(*reinterpret_cast<const uint4*>(st + j * 1024), bv);
-          const float4* ap = reinterpret_cast<const float4*>(at + j * 48);
-          const float4 a0 = ap[0], a1 = ap[1], a2 = ap[2];
-          const float2 al[6] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w),
-                                make_float2(a1.x, a1.y), make_float2(a1.z, a1.w),
-                                make_float2(a2.x, a2.y), make_float2(a2.z, a2.w)};
+          const float2* zp = reinterpret_cast<const float2*>(zt + j * kTT * SZ);
+          const float2 w01 = zp[0], w23 = zp[1], w45 = zp[2];
+          const float2 al[6] = {make_float2(w01.x, w01.x), make_float2(w01.y, w01.y),
+                                make_float2(w23.x, w23.x), make_float2(w23.y, w23.y),
+                                make_float2(w45.x, w45.x), make_float2(w45.y, w45.y)};
 #pragma unroll
           for (int qq = 0; qq < 6; ++qq)
 #pragma unroll
@@ -363,7 +420,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   if (warp == 0) {
     if (lane == 0 && *abort_flag) mbar_wait(dready, 0);  // MMAs of an aborted run may still run
     __syncwarp();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, kSmall ? 64 : kTmemCols);
   }
 }
 
@@ -381,10 +438,11 @@ cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s) {
   cudaError_t e = encode_source_map(&mb, a.reps, a.src_stride, a.n, a.T, a.d, 2, kKC, kTT);
   if (e == cudaSuccess) e = encode_split_query_map(&mq, a.u_split, a.S, a.d, pl.Npad);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(phase1_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
+  auto kern = a.n <= kSmallN ? phase1_tc_kernel<true> : phase1_tc_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
   if (e != cudaSuccess) return e;
   const int64_t blocks = (a.T + kTT - 1) / kTT;
-  phase1_tc_kernel<<<static_cast<unsigned>(blocks), kThreads, pl.smem, s>>>(mb, mq, a, pl);
+  kern<<<static_cast<unsigned>(blocks), kThreads, pl.smem, s>>>(mb, mq, a, pl);
   return cudaGetLastError();
 }
 

@@ -126,7 +126,7 @@ attnres_status attnres_query_prep(const float* w, const float* gamma_key, float*
  *               (attnres_query_prep)
  *   u_split     device bf16 [2S, d] or NULL: the same queries split into hi/lo rows
  *               (attnres_query_prep's u_split_out for these S rows).  When it is given, the I/O
- *               type is bf16, 2 <= S <= 24 and n_src <= 9, the logit numerators u_s . b_j[t] are
+ *               type is bf16, 2 <= S <= 24 and n_src <= 64, the logit numerators u_s . b_j[t] are
  *               computed on the tensor cores as (hi + lo) . b_j[t] with fp32 accumulation;
  *               otherwise the CUDA cores compute them from u in fp32.  Both agree to fp32
  *               rounding plus the split's 2^-16 relative error in u.

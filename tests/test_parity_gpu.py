@@ -25,7 +25,7 @@ def dev():
 @pytest.fixture(params=["tensor_cores", "cuda_cores"])
 def p1path(request):
     """Phase-1 kernel choice: with the split queries (tensor-core logits where the shape
-    allows: bf16, 2 <= S <= 24, n <= 9) or without them (CUDA-core kernel for every shape)."""
+    allows: bf16, 2 <= S <= 24, n <= 64) or without them (CUDA-core kernel for every shape)."""
     return request.param
 
 
@@ -88,11 +88,13 @@ P1_CASES = [
     (64, 2, 11, 64, "bf16"),        # n at its maximum with two queries
     (2, 2, 70, 136, "f32"),
     (7, 5, 23, 96, "f32"),
-    (9, 24, 21, 320, "bf16"),       # the tensor-core path's largest tile (9 sources x 8 tokens)
-    (16, 24, 21, 320, "bf16"),      # beyond it: CUDA-core kernel
+    (9, 24, 21, 320, "bf16"),       # the largest tensor-core tile with weights kept as pairs
+    (16, 24, 21, 320, "bf16"),      # one full M-tile (16 sources x 8 tokens)
     (1, 2, 9, 64, "bf16"),          # its smallest (one source, two queries)
     (3, 7, 8, 136, "bf16"),         # odd S, ragged last column stage
-    (17, 24, 12, 128, "bf16"),      # n beyond the tensor-core tile: CUDA-core kernel
+    (17, 24, 12, 128, "bf16"),      # two M-tiles
+    (33, 8, 19, 1024, "bf16"),      # three M-tiles
+    (49, 16, 9, 2048, "bf16"),      # four M-tiles (the largest Full AttnRes history)
 ]
 
 
