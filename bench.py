@@ -428,6 +428,51 @@ def run_full_grouped(args):
     return 0
 
 
+def run_backward(args):
+    """Backward of one sublayer's aggregation at the long-context shape: 16384 tokens,
+    d = 7168, bf16, 10 sources (the embedding, 8 completed blocks and a partial sum).  Prints
+    one JSON line: tokens/s and algorithmic GB/s ((2 n + 1) rows of d per token: the sources and
+    g_y read, the source gradients written)."""
+    from depth_wise_softmax_block_b300 import build as B
+    B.build()
+    import depth_wise_softmax_block_b300 as ar
+    dev = torch.device("cuda", 0)
+    T, d, n = 16384, 7168, 10
+    srcs = [I.normal((T, d), 1.0 + 0.1 * j, 9, f"v{j}", dev, torch.bfloat16) for j in range(n)]
+    U = (I.queries(1, d, 9, "w", dev)[0] * 3.0).contiguous()
+    Gi = I.gains(1, d, 0.02, 9, "gi", dev)[0]
+    gy = I.normal((T, d), 1.0, 9, "gy", dev, torch.bfloat16)
+    dsrcs = [torch.empty_like(s) for s in srcs]
+    du = torch.zeros((d,), device=dev)
+    dgi = torch.zeros((d,), device=dev)
+
+    def step():
+        ar.attnres_backward(srcs, U, Gi, gy, dsrcs, du, dgi)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    byt = (2 * n + 1) * d * 2 * T
+    peak, kind = peaks()
+    line = {"metric": "AttnRes aggregation backward tokens/s and achieved HBM GB/s, 1 GPU",
+            "value": T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"backward_bf16_T{T}_d{d}_n{n}", "tokens": T, "d": d,
+                       "sources": n},
+            "achieved_gbs": byt / (ms / 1e3) / 1e9, "frac_of_peak": byt / (ms / 1e3) / 1e9 / peak,
+            "peak_gbs": peak, "peak_source": kind}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -443,14 +488,18 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the token count (profiling a smaller case)")
     ap.add_argument("--chunk", type=int, default=0, help="override the chunk size")
-    ap.add_argument("--workload", default="longctx", choices=["longctx", "full_grouped"],
-                    help="full_grouped: the Full AttnRes depth, grouped two-phase vs direct")
+    ap.add_argument("--workload", default="longctx",
+                    choices=["longctx", "full_grouped", "backward"],
+                    help="full_grouped: the Full AttnRes depth, grouped two-phase vs direct; "
+                         "backward: one sublayer's aggregation backward")
     ap.add_argument("--group", type=int, default=8, help="group size of --workload full_grouped")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
 
     if args.workload == "full_grouped" and args.impl == "ours":
         return run_full_grouped(args)
+    if args.workload == "backward" and args.impl == "ours":
+        return run_backward(args)
     if args.impl == "reference":
         line = reference_arm(args, world, rank)
         if line is not None:

@@ -39,6 +39,7 @@ SIGNATURES = {
                                     _I),
     "attnres_phase2_merge_sources": ([_P, _P, _P, _I, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _U,
                                       _P], _I),
+    "attnres_backward": ([_P, _I, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _P, _P], _I),
 }
 
 
@@ -192,3 +193,22 @@ def attnres_phase2_merge_sources(o_l, lse_l, srcs, u_l, gamma_in, h_out=None, y_
         eps_key, _ptr(gamma_in), eps_in, _ptr(h_out), _ptr(y_out), _ptr(alpha_out), flags,
         _stream(stream)), "attnres_phase2_merge_sources")
     return h_out if y_out is None else y_out
+
+
+def attnres_backward(srcs, u, gamma_in, g_y, dsrcs, du, dgamma_in=None, eps_key=1e-6,
+                     eps_in=1e-6, stream=None):
+    """Backward of one sublayer's aggregation over ``srcs`` ([T, d] tensors): writes dL/dv_i
+    into ``dsrcs`` and ADDS dL/du (and dL/dgamma_in) into the fp32 [d] accumulators."""
+    T, d = srcs[0].shape
+    for name, t in [("g_y", g_y)] + [("srcs[j]", t) for t in srcs] + \
+            [("dsrcs[j]", t) for t in dsrcs]:
+        _rows(t, T, d, name)
+    if len(dsrcs) != len(srcs):
+        raise ValueError("one gradient tensor per source")
+    a_src = (ctypes.c_void_p * len(srcs))(*[t.data_ptr() for t in srcs])
+    a_dst = (ctypes.c_void_p * len(dsrcs))(*[t.data_ptr() for t in dsrcs])
+    _check(library().attnres_backward(a_src, len(srcs), T, d, _io(srcs[0]), _ptr(u), eps_key,
+                                      _ptr(gamma_in), eps_in, _ptr(g_y), a_dst, _ptr(du),
+                                      _ptr(dgamma_in), _stream(stream)), "attnres_backward")
+    return dsrcs
+

@@ -225,4 +225,43 @@ attnres_status attnres_phase2_merge_sources(const void* o_l, const float* lse_l,
                                           static_cast<cudaStream_t>(stream)));
 }
 
+attnres_status attnres_backward(const void* const* srcs, int n_src, int64_t T, int d,
+                                attnres_dtype io, const float* u, float eps_key,
+                                const float* gamma_in, float eps_in, const void* g_y,
+                                void* const* dsrcs, float* du, float* dgamma_in, void* stream) {
+  if (!valid_io(io)) return ATTNRES_ERR_INVALID_ARG;
+  const attnres_status sh = check_shape(T, d);
+  if (sh != ATTNRES_OK) return sh;
+  if (n_src < 1) return ATTNRES_ERR_INVALID_ARG;
+  if (n_src > attnres::kBwdMaxSources) return ATTNRES_ERR_UNSUPPORTED;
+  if (d / (io == ATTNRES_BF16 ? 8 : 4) > attnres::kBwdMaxVectors) return ATTNRES_ERR_UNSUPPORTED;
+  if (!(eps_key >= 0.f) || !(eps_in >= 0.f)) return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (srcs == nullptr || dsrcs == nullptr || u == nullptr || g_y == nullptr || du == nullptr)
+    return ATTNRES_ERR_INVALID_ARG;
+  attnres::BwdArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int j = 0; j < n_src; ++j) {
+    if (srcs[j] == nullptr || dsrcs[j] == nullptr) return ATTNRES_ERR_INVALID_ARG;
+    if (!aligned16(srcs[j]) || !aligned16(dsrcs[j])) return ATTNRES_ERR_MISALIGNED;
+    a.srcs[j] = srcs[j];
+    a.dsrcs[j] = dsrcs[j];
+  }
+  if (!aligned16(u) || !aligned16(g_y) || !opt_aligned16(gamma_in) || !aligned16(du) ||
+      !opt_aligned16(dgamma_in))
+    return ATTNRES_ERR_MISALIGNED;
+  a.n = n_src;
+  a.T = T;
+  a.d = d;
+  a.u = u;
+  a.eps_key = eps_key;
+  a.gamma_in = gamma_in;
+  a.eps_in = eps_in;
+  a.g_y = g_y;
+  a.du = du;
+  a.dgamma_in = dgamma_in;
+  return cuda_status(attnres::launch_backward(static_cast<IO>(io), a,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -70,6 +70,26 @@ struct FullArgs {
   const float* lse0;  // [T]: its log-sum-exp (required with o0 unless sigmoid weights)
 };
 
+// Backward of one sublayer's aggregation (backward.cu).
+constexpr int kBwdMaxSources = 16;
+struct BwdArgs {
+  const void* srcs[kBwdMaxSources];   // [T, d] each
+  void* dsrcs[kBwdMaxSources];        // [T, d] each: dL/dv_i
+  int n;
+  int64_t T;
+  int d;
+  const float* u;         // [d] folded query
+  float eps_key;
+  const float* gamma_in;  // [d] or null
+  float eps_in;
+  const void* g_y;        // [T, d] dL/dy
+  float* du;              // [d] accumulated
+  float* dgamma_in;       // [d] accumulated, or null
+};
+// Row-vector limit of the backward kernel: d / (elements per 16 bytes) <= 4 * 256.
+constexpr int kBwdMaxVectors = 1024;
+cudaError_t launch_backward(IO io, const BwdArgs& a, cudaStream_t s);
+
 // Each launcher returns cudaSuccess or the launch error.
 cudaError_t launch_phase1(IO io, const Phase1Args& a, cudaStream_t s);
 // Returns false when the (n, S) combination does not fit the phase-1 kernel.

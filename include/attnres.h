@@ -73,7 +73,7 @@ typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype;
 #define ATTNRES_MAX_D 16384        /* hidden size (a row stays in registers)               */
 
 /* ABI version of this header; attnres_abi_version() returns the library's. */
-#define ATTNRES_ABI_VERSION 4
+#define ATTNRES_ABI_VERSION 5
 int attnres_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -225,6 +225,34 @@ attnres_status attnres_phase2_merge_sources(const void* o_l, const float* lse_l,
                                             const float* gamma_in, float eps_in, void* h_out,
                                             void* y_out, float* alpha_out, unsigned int flags,
                                             void* stream);
+
+/*
+ * Backward of one sublayer's aggregation over an explicit source list (the direct form of
+ * attnres_full_reference_path with its output y; softmax weights, key RMSNorm): the logit
+ * gradient dL/dz_i = alpha_i g_h^T (v_i - h) ("Attention Residuals" note §7) and the RMSNorm
+ * input gradient (1/r)(g' - yhat (yhat^T g') / d) with g' = gamma ⊙ g ("Attention Residuals
+ * 阅读补充", section "梯度沿切向传播").  Given g_y = dL/dy:
+ *     g_h  = gamma_in ⊙ g_y / r_h - h (sum_k gamma_in,k g_y,k h_k) / (d r_h^3)
+ *     dz_i = alpha_i (g_h . v_i - g_h . h)
+ *     dL/dv_i = alpha_i g_h + (dz_i / r_i) u - (dz_i z_i / (d r_i^2)) v_i
+ *     du        += sum over tokens and sources of (dz_i / r_i) v_i
+ *     dgamma_in += sum over tokens of g_y ⊙ h / r_h
+ * u = w ⊙ gamma_key is the folded query; the parameter gradients follow elementwise:
+ * dL/dw = gamma_key ⊙ du and dL/dgamma_key = w ⊙ du.  The forward quantities (r_i, z, alpha,
+ * h, r_h) are recomputed from the sources.
+ *   srcs        HOST array of n_src device pointers, each [T, d] (io dtype)
+ *   u           device fp32 [d]; gamma_in device fp32 [d] or NULL (ones)
+ *   g_y         device [T, d] (io dtype): dL/dy
+ *   dsrcs       HOST array of n_src device pointers, each [T, d] (io dtype): receive dL/dv_i
+ *   du          device fp32 [d]: the gradient is ADDED (zero it first for a fresh sum)
+ *   dgamma_in   device fp32 [d] or NULL: added, like du
+ * The sums over tokens are accumulated with atomic additions, so their last bits may vary
+ * from run to run.  Limits: 1 <= n_src <= 16; d <= 8192 (bf16) or 4096 (fp32).
+ */
+attnres_status attnres_backward(const void* const* srcs, int n_src, int64_t T, int d,
+                                attnres_dtype io, const float* u, float eps_key,
+                                const float* gamma_in, float eps_in, const void* g_y,
+                                void* const* dsrcs, float* du, float* dgamma_in, void* stream);
 
 #ifdef __cplusplus
 }

@@ -275,6 +275,66 @@ def full_attnres_walk(v0, v, W, G_key, G_in, w_final, g_final, eps_key: float, e
 
 
 # ---------------------------------------------------------------------------------------------
+# Backward of one aggregation (page 2 §7, the logit gradient; page 1, "梯度沿切向传播", the
+# RMSNorm input gradient).  The chain rule written out; pinned against finite differences.
+# ---------------------------------------------------------------------------------------------
+def rmsnorm_backward(x, gamma, eps: float, g):
+    """dL/dx for y = gamma ⊙ x / r_eps(x) and upstream g = dL/dy, over the last axis.  Page 1
+    ("梯度沿切向传播"): the upstream gradient is first multiplied by gamma, then with
+    yhat = x / r,  dL/dx = (1/r) (g' - yhat (yhat^T g') / d).  Also returns dL/dgamma = g ⊙ yhat
+    (per token, not summed)."""
+    x, g = _f64(x), _f64(g)
+    d = x.shape[-1]
+    r = rms(x, eps)[..., None]
+    yhat = x / r
+    gp = g if gamma is None else g * _f64(gamma)
+    dx = (gp - yhat * np.sum(yhat * gp, axis=-1, keepdims=True) / d) / r
+    return dx, g * yhat
+
+
+@dataclass
+class AggregateGrads:
+    dsources: np.ndarray      # [n, T, d]  dL/dv_i (value path + key path)
+    dw: np.ndarray            # [d]  dL/dw, summed over tokens
+    dgamma_key: np.ndarray    # [d]  or None when gamma_key is None
+    dgamma_in: np.ndarray     # [d]  or None when gamma_in is None
+    du: np.ndarray            # [d]  dL/du for the folded query u = w ⊙ gamma_key
+    dz: np.ndarray            # [n, T] dL/dz_i
+    g_h: np.ndarray           # [T, d] dL/dh
+
+
+def aggregate_backward(sources, w, gamma_key, eps_key: float, gamma_in, eps_in: float, g_y):
+    """Gradients of y = RMSNorm_in(h), h = sum_i alpha_i v_i, alpha = softmax(z),
+    z_i = w^T RMSNorm_key(v_i), for the upstream gradient g_y = dL/dy [T, d]:
+      g_h   = RMSNorm backward of the input norm (page 1);
+      dz_i  = alpha_i g_h^T (v_i - h)                     (page 2 §7);
+      dv_i  = alpha_i g_h  (value path)  +  RMSNorm backward of the key norm with upstream
+              dz_i w  (key path);
+      dw    = sum_{t,i} dz_i RMSNorm_key(v_i);  dgamma_key = sum_{t,i} dz_i w ⊙ v_i / r_i;
+      dgamma_in = sum_t g_y ⊙ h / r_h;  du = sum_{t,i} dz_i v_i / r_i."""
+    v = _f64(sources)
+    w = _f64(w)
+    keys = rmsnorm(v, gamma_key, eps_key)
+    z = np.sum(keys * w, axis=-1)
+    alpha = depth_softmax(z)
+    h = np.sum(alpha[..., None] * v, axis=0)
+    g_h, dgi = rmsnorm_backward(h, gamma_in, eps_in, g_y)
+    dz = alpha * np.sum(g_h[None] * (v - h[None]), axis=-1)
+    dv = alpha[..., None] * g_h[None]
+    dkey = dz[..., None] * w
+    dv_key, dgk = rmsnorm_backward(v, gamma_key, eps_key, dkey)
+    dv = dv + dv_key
+    dw = np.sum(dz[..., None] * keys, axis=(0, 1))
+    r = rms(v, eps_key)[..., None]
+    du = np.sum(dz[..., None] * v / r, axis=(0, 1))
+    return AggregateGrads(
+        dsources=dv, dw=dw,
+        dgamma_key=None if gamma_key is None else np.sum(dgk, axis=(0, 1)),
+        dgamma_in=None if gamma_in is None else np.sum(dgi, axis=0),
+        du=du, dz=dz, g_h=g_h)
+
+
+# ---------------------------------------------------------------------------------------------
 # Full AttnRes with the grouped two-phase schedule (page 1, "静态 Query 与两阶段计算": the L
 # layers fall into G scheduling groups of S = L / G; phase 1 scores the S queries of a group
 # against the history in one pass and keeps the softmax statistics; phase 2 takes the layers

@@ -428,6 +428,88 @@ def pin_merge_reference(O):
     assert np.all(a0 == 0.0)
 
 
+# --- backward (page 2 §7 logit gradient; page 1 "梯度沿切向传播") ------------------------------
+def _fd_grad(f, x, h=1e-6):
+    """Central finite differences of the scalar f at x (any shape), in fp64."""
+    x = np.array(x, dtype=np.float64)
+    g = np.zeros_like(x)
+    it = np.nditer(x, flags=["multi_index"])
+    for _ in it:
+        i = it.multi_index
+        xp, xm = x.copy(), x.copy()
+        xp[i] += h
+        xm[i] -= h
+        g[i] = (f(xp) - f(xm)) / (2 * h)
+    return g
+
+
+def pin_rmsnorm_backward(O):
+    """The RMSNorm input gradient against finite differences (with gain and eps), and the
+    pages' radial property: at eps = 0 the Jacobian maps x to 0, so x^T dL/dx = 0; with eps the
+    radial eigenvalue is eps / r^3 (page 1, "梯度沿切向传播")."""
+    r = _rng(50)
+    d = 6
+    x = r.normal(0.3, 1.2, size=d)
+    g = r.normal(0.0, 1.0, size=d)
+    gam = r.normal(1.0, 0.2, size=d)
+    for eps in (0.0, 0.3):
+        dx, dg = O.rmsnorm_backward(x, gam, eps, g)
+        fd = _fd_grad(lambda xx: float(np.sum(g * O.rmsnorm(xx, gam, eps))), x)
+        _close(dx, fd, 1e-8, f"dL/dx eps={eps}")
+        fdg = _fd_grad(lambda gg: float(np.sum(g * O.rmsnorm(x, gg, eps))), gam)
+        _close(dg, fdg, 1e-8, "dL/dgamma")
+    dx, _ = O.rmsnorm_backward(x, None, 0.0, g)
+    assert abs(float(np.dot(x, dx))) < 1e-12, "radial component at eps = 0"
+    eps = 0.3
+    rr = float(O.rms(x, eps))
+    dx, _ = O.rmsnorm_backward(x, None, eps, g)
+    _close(np.dot(x, dx), eps / rr ** 3 * np.dot(x, g), 1e-12, "radial eigenvalue eps / r^3")
+
+
+def pin_aggregate_backward_fd(O):
+    """Every gradient of the aggregation (sources, query, both gains) against central finite
+    differences of L = sum g_y ⊙ y computed by the forward oracle."""
+    r = _rng(51)
+    n, T, d = 3, 2, 5
+    v = _sources(r, n, T, d)
+    w = r.normal(0.0, 0.7, size=d)
+    gk = r.normal(1.0, 0.2, size=d)
+    gi = r.normal(1.0, 0.2, size=d)
+    gy = r.normal(0.0, 1.0, size=(T, d))
+    ek, ei = 1e-3, 2e-3
+    G = O.aggregate_backward(v, w, gk, ek, gi, ei, gy)
+
+    def loss(vv=v, ww=w, kk=gk, ii=gi):
+        _, y, _ = O.sublayer_input(vv, ww, kk, ek, ii, ei)
+        return float(np.sum(gy * y))
+    _close(G.dsources, _fd_grad(lambda x: loss(vv=x), v), 1e-7, "dL/dv")
+    _close(G.dw, _fd_grad(lambda x: loss(ww=x), w), 1e-7, "dL/dw")
+    _close(G.dgamma_key, _fd_grad(lambda x: loss(kk=x), gk), 1e-7, "dL/dgamma_key")
+    _close(G.dgamma_in, _fd_grad(lambda x: loss(ii=x), gi), 1e-7, "dL/dgamma_in")
+    # the folded query: z_i = u . v_i / r_i with u = w ⊙ gamma_key
+    _close(G.dw, gk * G.du, 1e-13, "dw = gamma_key ⊙ du")
+    _close(G.dgamma_key, w * G.du, 1e-13, "dgamma_key = w ⊙ du")
+
+
+def pin_backward_scale_invariance(O):
+    """At eps = 0 both norms are scale invariant, so the key-path gradient of each source is
+    orthogonal to it (v_i^T (dv_i - alpha_i g_h) = 0) and the norm's input gradient is
+    orthogonal to h (h^T g_h = 0); and the logit gradients sum to 0 over the sources
+    (softmax: sum_i alpha_i (v_i - h) = 0)."""
+    r = _rng(52)
+    n, T, d = 4, 3, 16
+    v = _sources(r, n, T, d)
+    w = r.normal(0.0, 0.5, size=d)
+    gy = r.normal(0.0, 1.0, size=(T, d))
+    G = O.aggregate_backward(v, w, None, 0.0, None, 0.0, gy)
+    _, alpha, _ = O.aggregate(v, w, None, 0.0)
+    h, _, _ = O.aggregate(v, w, None, 0.0)
+    key_path = G.dsources - alpha[..., None] * G.g_h[None]
+    _close(np.sum(key_path * v, axis=-1), np.zeros((n, T)), 1e-12, "v_i . key-path gradient")
+    _close(np.sum(G.g_h * h, axis=-1), np.zeros(T), 1e-12, "h . g_h")
+    _close(G.dz.sum(axis=0), np.zeros(T), 1e-12, "sum_i dz_i")
+
+
 # --- grouped two-phase Full AttnRes (page 1, "静态 Query 与两阶段计算") ------------------------
 def pin_grouped_full_equals_direct(O):
     """The grouped two-phase schedule reproduces the direct Full AttnRes walk for every group

@@ -45,7 +45,7 @@ def test_header_symbols_exported(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.attnres_abi_version() == 4
+    assert lib.attnres_abi_version() == 5
     for code, name in ar.STATUS.items():
         assert lib.attnres_status_string(code).decode() == name
     assert lib.attnres_status_string(99).decode() == "ATTNRES_ERR_UNKNOWN"
@@ -163,6 +163,27 @@ def test_merge_sources_validation(lib):
     bad = (ctypes.c_void_p * 2)(P, PM)
     assert err(call(T=4, srcs=bad)) == MISALIGNED
     assert call(flags=4) == INVALID
+
+
+def test_backward_validation(lib):
+    import ctypes
+    src = (ctypes.c_void_p * 2)(P, P + 4096)
+    dst = (ctypes.c_void_p * 2)(P + 8192, P + 12288)
+    bw = lib.attnres_backward
+
+    def call(srcs=src, n=2, T=0, d=64, io=1, u=P, gy=P, dsrcs=dst, du=P, dgi=None):
+        return bw(srcs, n, T, d, io, u, 1e-6, None, 1e-6, gy, dsrcs, du, dgi, None)
+    assert call() == OK
+    assert call(n=0) == INVALID
+    assert call(n=17) == UNSUPPORTED
+    assert call(d=8192 + 8) == UNSUPPORTED                 # bf16 rows beyond 1024 vectors
+    assert call(d=4096 + 8, io=0) == UNSUPPORTED           # fp32 rows beyond 1024 vectors
+    assert err(call(T=4, du=None)) == INVALID
+    assert err(call(T=4, gy=None)) == INVALID
+    assert err(call(T=4, dsrcs=None)) == INVALID
+    assert err(call(T=4, du=PM)) == MISALIGNED
+    bad = (ctypes.c_void_p * 2)(P, PM)
+    assert err(call(T=4, dsrcs=bad)) == MISALIGNED
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -116,7 +116,27 @@ def _merge_sources_drops_history(o_A, lse_A, sources_B, w, gamma_key, eps_key, g
     return h, y, aB, wA
 
 
+def _rmsnorm_backward_no_radial(x, gamma, eps, g):   # drops the radial correction term
+    x, g = np.asarray(x, np.float64), np.asarray(g, np.float64)
+    r = O.rms(x, eps)[..., None]
+    gp = g if gamma is None else g * np.asarray(gamma, np.float64)
+    return gp / r, g * x / r
+
+
+def _aggregate_backward_no_minus_h(sources, w, gamma_key, eps_key, gamma_in, eps_in, g_y):
+    # logit gradient alpha_i g^T v_i, without the - h of page 2 §7
+    G = _ORIG_BACKWARD(sources, w, gamma_key, eps_key, gamma_in, eps_in, g_y)
+    v = np.asarray(sources, np.float64)
+    _, alpha, _ = O.aggregate(v, w, gamma_key, eps_key)
+    dz_bad = alpha * np.sum(G.g_h[None] * v, axis=-1)
+    keys = O.rmsnorm(v, gamma_key, eps_key)
+    G.dw = np.sum(dz_bad[..., None] * keys, axis=(0, 1))
+    G.dz = dz_bad
+    return G
+
+
 _ORIG_PARTITION = O.partition_stats
+_ORIG_BACKWARD = O.aggregate_backward
 _ORIG_MERGE_S = O.merge_sources_reference
 _ORIG_MERGE_V = O.merge_reference_variant
 _ORIG_MERGE = O.merge_reference
@@ -141,6 +161,8 @@ MUTATIONS = {
     "raw_logits_normalised": ("depth_logits_raw", _raw_logits_still_normalised),
     "sigmoid_merged_as_softmax": ("merge_reference_variant", _merge_variant_softmax_for_sigmoid),
     "merge_sources_drops_history": ("merge_sources_reference", _merge_sources_drops_history),
+    "rmsnorm_backward_no_radial": ("rmsnorm_backward", _rmsnorm_backward_no_radial),
+    "logit_gradient_without_h": ("aggregate_backward", _aggregate_backward_no_minus_h),
 }
 
 
