@@ -275,6 +275,75 @@ def full_attnres_walk(v0, v, W, G_key, G_in, w_final, g_final, eps_key: float, e
 
 
 # ---------------------------------------------------------------------------------------------
+# Multi-head depth attention (page 2 "Attention Residuals" note, result 4, Table 4: "Block,
+# multi-head H = 16 adds depth attention heads"; no formula on the pages).  Reading: the d
+# features split into H contiguous slices of d / H; each head is a complete AttnRes
+# aggregation on its slice (the key is the RMSNorm of the source's slice with the slice of the
+# gain, the logit uses the slice of the query, the softmax runs per head) and the heads'
+# outputs are concatenated; the sublayer's input RMSNorm then normalises the whole vector.
+# ---------------------------------------------------------------------------------------------
+def head_slices(d: int, H: int):
+    """The H contiguous feature slices of a d-vector."""
+    assert d % H == 0
+    dh = d // H
+    return [slice(k * dh, (k + 1) * dh) for k in range(H)]
+
+
+def multihead_aggregate(sources, w, gamma_key, eps: float, H: int, weights: str = "softmax",
+                        key_norm: bool = True):
+    """h = concat_k aggregate_k, each head k on its feature slice.  Returns (h [T,d],
+    alpha [H,n,T], z [H,n,T])."""
+    src = _f64(sources)
+    d = src.shape[-1]
+    h = np.zeros(src.shape[1:])
+    al, zz = [], []
+    for sl in head_slices(d, H):
+        g = None if gamma_key is None else _f64(gamma_key)[sl]
+        hk, ak, zk = aggregate_variant(src[..., sl], _f64(w)[sl], g, eps, weights, key_norm)
+        h[..., sl] = hk
+        al.append(ak)
+        zz.append(zk)
+    return h, np.stack(al), np.stack(zz)
+
+
+def multihead_phase1(reps, W, G_key, eps: float, H: int):
+    """Phase 1 per head: for each query s and head k, the partition statistics of the head's
+    slice.  Returns o [S,T,d] (heads concatenated), m and lse [S,H,T], alpha [S,H,T,n]."""
+    reps = _f64(reps)
+    S, d = np.shape(W)
+    o = np.zeros((S,) + reps.shape[1:])
+    m = np.zeros((S, H, reps.shape[1]))
+    lse = np.zeros_like(m)
+    alpha = np.zeros((S, H, reps.shape[1], reps.shape[0]))
+    for k, sl in enumerate(head_slices(d, H)):
+        gk = None if G_key is None else _f64(G_key)[:, sl]
+        ok, mk, lk, ak = phase1(reps[..., sl], _f64(W)[:, sl], gk, eps)
+        o[..., sl] = ok
+        m[:, k], lse[:, k], alpha[:, k] = mk, lk, ak
+    return o, m, lse, alpha
+
+
+def multihead_merge_reference(o_A, lse_A, p, w, gamma_key, eps_key: float, gamma_in,
+                              eps_in: float, H: int):
+    """Phase 2 per head: each head merges its slice of phase 1's result (o_A, lse_A [H,T])
+    with its slice of the partial source p (merge_reference on the slice); the heads are
+    concatenated and the input RMSNorm normalises the whole h.  Returns (h, y, weights of p
+    [H,T])."""
+    o_A = _f64(o_A)
+    d = o_A.shape[-1]
+    h = np.zeros_like(o_A)
+    ap = np.zeros((H,) + o_A.shape[:-1])
+    for k, sl in enumerate(head_slices(d, H)):
+        g = None if gamma_key is None else _f64(gamma_key)[sl]
+        hk, _, ak = merge_reference(o_A[..., sl], _f64(lse_A)[k],
+                                    None if p is None else _f64(p)[..., sl], _f64(w)[sl], g,
+                                    eps_key, None, eps_in)
+        h[..., sl] = hk
+        ap[k] = ak
+    return h, rmsnorm(h, gamma_in, eps_in), ap
+
+
+# ---------------------------------------------------------------------------------------------
 # Backward of one aggregation (page 2 §7, the logit gradient; page 1, "梯度沿切向传播", the
 # RMSNorm input gradient).  The chain rule written out; pinned against finite differences.
 # ---------------------------------------------------------------------------------------------

@@ -428,6 +428,78 @@ def pin_merge_reference(O):
     assert np.all(a0 == 0.0)
 
 
+# --- multi-head depth attention (Table 4 variant; reading in the oracle) ---------------------
+def pin_multihead_one_head(O):
+    """H = 1 is the single-head aggregation, phase 1 and merge."""
+    r = _rng(60)
+    v = _sources(r, 4, 5, 24)
+    W = r.normal(0.0, 0.5, size=(3, 24))
+    G = r.normal(1.0, 0.1, size=(3, 24))
+    h1, a1, _ = O.multihead_aggregate(v, W[0], G[0], 1e-6, 1)
+    h0, a0, _ = O.aggregate(v, W[0], G[0], 1e-6)
+    _close(h1, h0, 0.0, "h")
+    _close(a1[0], a0, 0.0, "alpha")
+    o, m, lse, al = O.multihead_phase1(v, W, G, 1e-6, 1)
+    o0, m0, l0, al0 = O.phase1(v, W, G, 1e-6)
+    _close(o, o0, 0.0, "o")
+    _close(lse[:, 0], l0, 0.0, "lse")
+
+
+def pin_multihead_scalar_heads(O):
+    """H = d: every head is one feature, whose RMSNorm at eps = 0 is sign(v_k) gamma_k, so the
+    logit of source i in head k is w_k gamma_k sign(v_ik) and head k's output is the softmax of
+    those logits over the sources applied to v_ik (closed form, element by element)."""
+    r = _rng(61)
+    n, T, d = 3, 2, 6
+    v = _sources(r, n, T, d)
+    w = r.normal(0.0, 1.0, size=d)
+    g = r.normal(1.0, 0.3, size=d)
+    h, alpha, z = O.multihead_aggregate(v, w, g, 0.0, d)
+    zw = (w * g)[None, None, :] * np.sign(v)                 # [n, T, d]
+    e = np.exp(zw - zw.max(axis=0, keepdims=True))
+    a = e / e.sum(axis=0, keepdims=True)
+    _close(np.moveaxis(z, 0, -1), zw, 1e-12, "scalar-head logits")
+    _close(h, np.sum(a * v, axis=0), 1e-12, "scalar-head outputs")
+
+
+def pin_multihead_heads_independent(O):
+    """Changing one head's slice of the query or of a source changes only that head's output
+    slice (heads do not mix), and zero queries give the mean in every head."""
+    r = _rng(62)
+    n, T, d, H = 4, 3, 24, 3
+    v = _sources(r, n, T, d)
+    w = r.normal(0.0, 0.8, size=d)
+    h0, _, _ = O.multihead_aggregate(v, w, None, 1e-6, H)
+    w2 = w.copy()
+    w2[8:16] *= -3.0                    # head 1
+    v2 = v.copy()
+    v2[2, :, 16:24] += 5.0              # head 2
+    h1, _, _ = O.multihead_aggregate(v2, w2, None, 1e-6, H)
+    _close(h1[..., 0:8], h0[..., 0:8], 0.0, "head 0 unchanged")
+    assert np.max(np.abs(h1[..., 8:16] - h0[..., 8:16])) > 1e-3
+    assert np.max(np.abs(h1[..., 16:24] - h0[..., 16:24])) > 1e-3
+    hz, _, _ = O.multihead_aggregate(v, np.zeros(d), None, 1e-6, H)
+    _close(hz, v.mean(axis=0), 1e-12, "zero queries: mean")
+
+
+def pin_multihead_merge(O):
+    """Per-head phase 1 over A plus the per-head merge of a partial source equals the direct
+    per-head aggregation over A plus the partial, then the whole-vector input RMSNorm."""
+    r = _rng(63)
+    n, T, d, H = 4, 3, 32, 4
+    A = _sources(r, n, T, d)
+    p = r.normal(0.0, 2.0, size=(T, d))
+    W = r.normal(0.0, 0.5, size=(1, d))
+    G = r.normal(1.0, 0.1, size=(1, d))
+    gi = r.normal(1.0, 0.1, size=d)
+    o, m, lse, _ = O.multihead_phase1(A, W, G, 1e-6, H)
+    h, y, ap = O.multihead_merge_reference(o[0], lse[0], p, W[0], G[0], 1e-6, gi, 1e-6, H)
+    hd, ad, _ = O.multihead_aggregate(np.concatenate([A, p[None]]), W[0], G[0], 1e-6, H)
+    _close(h, hd, 1e-12, "merge = direct")
+    _close(y, O.rmsnorm(hd, gi, 1e-6), 1e-12, "y")
+    _close(ap, ad[:, -1], 1e-14, "weights of the partial")
+
+
 # --- backward (page 2 §7 logit gradient; page 1 "梯度沿切向传播") ------------------------------
 def _fd_grad(f, x, h=1e-6):
     """Central finite differences of the scalar f at x (any shape), in fp64."""
