@@ -61,10 +61,10 @@ def peaks():
 class LongContextStep:
     """The bench step.  Allocates everything once; ``run()`` allocates nothing."""
 
-    def __init__(self, wl: I.Workload, dev, timer=None):
+    def __init__(self, wl: I.Workload, dev, timer=None, heads: int = 1):
         from depth_wise_softmax_block_b300 import attnres_query_prep
         from depth_wise_softmax_block_b300.schedule import BlockRunner
-        self.wl, self.dev = wl, dev
+        self.wl, self.dev, self.heads = wl, dev, heads
         self.n = 9                                   # embedding + 8 completed blocks
         T, d, S, ch = wl.T, wl.d, wl.S, wl.chunk
         self.nchunks = T // ch
@@ -80,7 +80,7 @@ class LongContextStep:
         self.uf = torch.empty((1, d), device=dev)
         self.out = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
         self.timer = timer
-        self.runner = BlockRunner(ch, d, S, torch.bfloat16, dev, timer=timer)
+        self.runner = BlockRunner(ch, d, S, torch.bfloat16, dev, timer=timer, heads=heads)
         self._prep = attnres_query_prep
 
     def chunk_views(self, c):
@@ -103,7 +103,8 @@ class LongContextStep:
         reps_c, close_c, all_c, out_c = self.chunk_views(c)
         self.runner.run_block(reps_c, self.U, self.P.G_in, self.sublayer, close_c, self.wl.eps,
                               self.wl.eps, on_call=on_call, U_split=self.U_split)
-        final_aggregation(all_c, self.uf[0], out_c, self.wl.eps, timer=self.timer)
+        final_aggregation(all_c, self.uf[0], out_c, self.wl.eps, timer=self.timer,
+                          heads=self.heads)
 
     def run(self):
         self.prep()
@@ -112,12 +113,12 @@ class LongContextStep:
 
     # algorithmic bytes, per step, per kernel kind
     def bytes_per_launch(self):
-        d, E, ch, S, n = self.wl.d, 2, self.wl.chunk, self.wl.S, self.n
+        d, E, ch, S, n, H = self.wl.d, 2, self.wl.chunk, self.wl.S, self.n, self.heads
         return {
-            "phase1": C.phase1_bytes(n, S, d, E) * ch,
+            "phase1": C.phase1_bytes(n, S, d, E, heads=H) * ch,
             "phase2_first": C.phase2_bytes(d, E, False, False) * ch,
-            "phase2": C.phase2_bytes(d, E, True, False) * ch,
-            "phase2_fused": C.phase2_bytes(d, E, True, True) * ch,
+            "phase2": C.phase2_bytes(d, E, True, False, heads=H) * ch,
+            "phase2_fused": C.phase2_bytes(d, E, True, True, heads=H) * ch,
             "close": C.partial_update_bytes(d, E) * ch,
             "final": C.phase1_bytes(n + 1, 1, d, E, with_lse=False) * ch,
         }
@@ -126,7 +127,8 @@ class LongContextStep:
         return 2 + self.nchunks * (1 + self.wl.S + 1 + 1)
 
     def step_bytes(self):
-        per_tok = C.block_step_bytes(self.n, self.wl.S, self.wl.d, 2, self.n + 1).total
+        per_tok = C.block_step_bytes(self.n, self.wl.S, self.wl.d, 2, self.n + 1,
+                                     heads=self.heads).total
         return per_tok * self.wl.T
 
 
@@ -493,6 +495,8 @@ def main(argv=None):
                     help="full_grouped: the Full AttnRes depth, grouped two-phase vs direct; "
                          "backward: one sublayer's aggregation backward")
     ap.add_argument("--group", type=int, default=8, help="group size of --workload full_grouped")
+    ap.add_argument("--heads", type=int, default=1,
+                    help="depth-attention heads of the longctx step (Table 4 multi-head: 16)")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
 
@@ -521,7 +525,10 @@ def main(argv=None):
         wl = dataclasses.replace(wl, T=T, chunk=ch,
                                  name=f"longctx_prefill_bf16_T{T}_chunk{ch}_d7168_S24_n9")
     timer = KernelTimer()
-    step = LongContextStep(wl, dev, timer=timer)
+    if args.heads != 1:
+        import dataclasses
+        wl = dataclasses.replace(wl, name=f"{wl.name}_heads{args.heads}")
+    step = LongContextStep(wl, dev, timer=timer, heads=args.heads)
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
@@ -567,7 +574,7 @@ def main(argv=None):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": wl.name, "tokens": wl.T, "chunk": wl.chunk, "d": wl.d,
-                   "sources": step.n, "S": wl.S, "accumulate": "f32",
+                   "sources": step.n, "S": wl.S, "heads": args.heads, "accumulate": "f32",
                    "l2": "no flush: every launch streams >= 235 MB (> 126 MB L2)",
                    "parallelism": f"replicas x{world} (tokens independent)"},
         "achieved_gbs_step": step_gbs, "frac_of_peak_step": step_gbs / peak,

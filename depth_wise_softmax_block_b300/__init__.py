@@ -30,15 +30,15 @@ SIGNATURES = {
     "attnres_last_cuda_error": ([], ctypes.c_char_p),
     "attnres_poll_device_errors": ([], _I),
     "attnres_query_prep": ([_P, _P, _P, _P, _I, _I, _P], _I),
-    "attnres_phase1": ([_P, _I64, _I, _I64, _I, _I, _P, _P, _I, _F, _P, _P, _P, _P, _U, _P],
-                       _I),
+    "attnres_phase1": ([_P, _I64, _I, _I64, _I, _I, _P, _P, _I, _F, _P, _P, _P, _P, _U, _I,
+                        _P], _I),
     "attnres_phase2_merge": ([_P, _P, _P, _P, _P, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _U,
-                              _P], _I),
+                              _I, _P], _I),
     "attnres_partial_update": ([_P, _P, _P, _I64, _I, _I, _P], _I),
-    "attnres_full_reference_path": ([_P, _I, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _U, _P],
-                                    _I),
+    "attnres_full_reference_path": ([_P, _I, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _U, _I,
+                                     _P], _I),
     "attnres_phase2_merge_sources": ([_P, _P, _P, _I, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _U,
-                                      _P], _I),
+                                      _I, _P], _I),
     "attnres_backward": ([_P, _I, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _P, _P], _I),
 }
 
@@ -99,6 +99,14 @@ def _rows(t: torch.Tensor, T: int, d: int, name: str):
         raise ValueError(f"{name}: expected rows of shape [{T}, {d}] with row stride {d}")
 
 
+def _stats(t: torch.Tensor, numel: int, name: str):
+    """A statistics output must be a contiguous fp32 tensor of the expected size."""
+    if t is None:
+        return
+    if t.dtype != torch.float32 or not t.is_contiguous() or t.numel() != numel:
+        raise ValueError(f"{name}: expected a contiguous fp32 tensor of {numel} elements")
+
+
 def attnres_poll_device_errors():
     """Raise if a kernel's bounded wait gave up since the previous poll (synchronises)."""
     _check(library().attnres_poll_device_errors(), "attnres_poll_device_errors")
@@ -119,10 +127,12 @@ def attnres_query_prep(w, gamma_key, u_out, u_split_out=None, stream=None):
 
 
 def attnres_phase1(reps, u, o_out, m_out=None, lse_out=None, alpha_out=None, eps=1e-6,
-                   u_split=None, flags=0, stream=None):
+                   u_split=None, flags=0, heads=1, stream=None):
     """Phase 1 over ``reps`` [n, T, d] (any source stride, rows of stride d) for the S queries
-    ``u`` [S, d]; writes o [S, T, d] and the optional statistics.  ``u_split`` ([2S, d] bf16,
-    from attnres_query_prep) puts the logits on the tensor cores where the shape allows."""
+    ``u`` [S, d]; writes o [S, T, d] and the optional statistics (m, lse [S, heads, T], alpha
+    [S, heads, T, n]; with one head the head axis may be left out).  ``u_split`` ([2S, d]
+    bf16, from attnres_query_prep) puts the logits on the tensor cores where the shape
+    allows."""
     n, T, d = reps.shape
     S = u.shape[0]
     if u_split is not None and (tuple(u_split.shape) != (2 * S, d) or not u_split.is_contiguous()
@@ -132,25 +142,31 @@ def attnres_phase1(reps, u, o_out, m_out=None, lse_out=None, alpha_out=None, eps
     if tuple(o_out.shape) != (S, T, d) or not o_out.is_contiguous():
         raise ValueError("o_out must be a contiguous [S, T, d] tensor")
     src_stride = reps.stride(0) if n > 1 else T * d
+    for name, t, per in (("m_out", m_out, 1), ("lse_out", lse_out, 1), ("alpha_out", alpha_out, n)):
+        _stats(t, S * heads * T * per, name)
     _check(library().attnres_phase1(_ptr(reps), src_stride, n, T, d, _io(reps), _ptr(u),
                                     _ptr(u_split), S, eps, _ptr(o_out), _ptr(m_out), _ptr(lse_out),
-                                    _ptr(alpha_out), flags, _stream(stream)), "attnres_phase1")
+                                    _ptr(alpha_out), flags, heads, _stream(stream)),
+           "attnres_phase1")
     return o_out
 
 
 def attnres_phase2_merge(o_l, lse_l, partial, v_prev, partial_out, u_l, gamma_in, y_out,
                          h_out=None, alpha_p_out=None, eps_key=1e-6, eps_in=1e-6, flags=0,
-                         stream=None):
+                         heads=1, stream=None):
     """Phase 2 for one sublayer: merge the partial-sum source (partial + v_prev) into the
-    phase-1 result and apply the input RMSNorm.  Tensors are [T, d]."""
+    phase-1 result and apply the input RMSNorm.  Tensors are [T, d]; lse_l and alpha_p_out
+    are [heads, T] (or [T] with one head)."""
     T, d = o_l.shape
     for name, t in (("o_l", o_l), ("partial", partial), ("v_prev", v_prev),
                     ("partial_out", partial_out), ("y_out", y_out), ("h_out", h_out)):
         _rows(t, T, d, name)
+    _stats(lse_l, heads * T, "lse_l")
+    _stats(alpha_p_out, heads * T, "alpha_p_out")
     _check(library().attnres_phase2_merge(
         _ptr(o_l), _ptr(lse_l), _ptr(partial), _ptr(v_prev), _ptr(partial_out), T, d, _io(o_l),
         _ptr(u_l), eps_key, _ptr(gamma_in), eps_in, _ptr(h_out), _ptr(y_out), _ptr(alpha_p_out),
-        flags, _stream(stream)), "attnres_phase2_merge")
+        flags, heads, _stream(stream)), "attnres_phase2_merge")
     return y_out
 
 
@@ -166,31 +182,37 @@ def attnres_partial_update(partial, v, out, stream=None):
 
 
 def attnres_full_reference_path(srcs, u_l, gamma_in, h_out=None, y_out=None, alpha_out=None,
-                                eps_key=1e-6, eps_in=1e-6, flags=0, stream=None):
-    """Direct single-pass aggregation over the list of [T, d] source tensors ``srcs``."""
+                                eps_key=1e-6, eps_in=1e-6, flags=0, heads=1, stream=None):
+    """Direct single-pass aggregation over the list of [T, d] source tensors ``srcs``;
+    alpha_out is [heads, T, n] (or [T, n] with one head)."""
     T, d = srcs[0].shape
     for t in srcs:
         _rows(t, T, d, "srcs[j]")
+    _stats(alpha_out, heads * T * len(srcs), "alpha_out")
     arr = (ctypes.c_void_p * len(srcs))(*[t.data_ptr() for t in srcs])
     _check(library().attnres_full_reference_path(
         arr, len(srcs), T, d, _io(srcs[0]), _ptr(u_l), eps_key, _ptr(gamma_in), eps_in,
-        _ptr(h_out), _ptr(y_out), _ptr(alpha_out), flags, _stream(stream)),
+        _ptr(h_out), _ptr(y_out), _ptr(alpha_out), flags, heads, _stream(stream)),
         "attnres_full_reference_path")
     return h_out if y_out is None else y_out
 
 
 def attnres_phase2_merge_sources(o_l, lse_l, srcs, u_l, gamma_in, h_out=None, y_out=None,
-                                 alpha_out=None, eps_key=1e-6, eps_in=1e-6, flags=0, stream=None):
+                                 alpha_out=None, eps_key=1e-6, eps_in=1e-6, flags=0, heads=1,
+                                 stream=None):
     """Grouped Full AttnRes phase 2 for one layer: merge phase 1's (o_l, lse_l) with the
-    group's in-group sources ``srcs`` (a list of [T, d] tensors, possibly empty)."""
+    group's in-group sources ``srcs`` (a list of [T, d] tensors, possibly empty); lse_l is
+    [heads, T] and alpha_out [heads, T, k] (head axis optional with one head)."""
     T, d = o_l.shape
     for name, t in [("o_l", o_l), ("h_out", h_out), ("y_out", y_out)] + \
             [("srcs[j]", t) for t in srcs]:
         _rows(t, T, d, name)
+    _stats(lse_l, heads * T, "lse_l")
+    _stats(alpha_out, heads * T * len(srcs), "alpha_out")
     arr = (ctypes.c_void_p * max(1, len(srcs)))(*[t.data_ptr() for t in srcs])
     _check(library().attnres_phase2_merge_sources(
         _ptr(o_l), _ptr(lse_l), arr if srcs else None, len(srcs), T, d, _io(o_l), _ptr(u_l),
-        eps_key, _ptr(gamma_in), eps_in, _ptr(h_out), _ptr(y_out), _ptr(alpha_out), flags,
+        eps_key, _ptr(gamma_in), eps_in, _ptr(h_out), _ptr(y_out), _ptr(alpha_out), flags, heads,
         _stream(stream)), "attnres_phase2_merge_sources")
     return h_out if y_out is None else y_out
 

@@ -12,6 +12,8 @@ for fp32; statistics are fp32):
   phase 2, fused partial update:            5 d E + 4                  (+ read v, write p)
   partial update / block close:             3 d E
   full reference path, n sources:           (n + 1) d E (+ d E with h)
+With H depth-attention heads every statistic (lse, m, alpha) is kept per head: H times the
+4-byte terms above.
 """
 from __future__ import annotations
 
@@ -19,20 +21,20 @@ from dataclasses import dataclass
 
 
 def phase1_bytes(n: int, S: int, d: int, E: int, with_m: bool = False, with_lse: bool = True,
-                 with_alpha: bool = False) -> int:
+                 with_alpha: bool = False, heads: int = 1) -> int:
     b = (n + S) * d * E
-    b += 4 * S * (int(with_m) + int(with_lse))
+    b += 4 * S * heads * (int(with_m) + int(with_lse))
     if with_alpha:
-        b += 4 * S * n
+        b += 4 * S * heads * n
     return b
 
 
 def phase2_bytes(d: int, E: int, has_partial: bool, fused_update: bool,
-                 write_h: bool = False) -> int:
+                 write_h: bool = False, heads: int = 1) -> int:
     if not has_partial:
         b = 2 * d * E
     else:
-        b = 3 * d * E + 4
+        b = 3 * d * E + 4 * heads
         if fused_update:
             b += 2 * d * E
     if write_h:
@@ -66,16 +68,17 @@ class BlockStepBytes:
         return self.phase1 + self.phase2 + self.close + self.final
 
 
-def block_step_bytes(n: int, S: int, d: int, E: int, final_sources: int) -> BlockStepBytes:
+def block_step_bytes(n: int, S: int, d: int, E: int, final_sources: int,
+                     heads: int = 1) -> BlockStepBytes:
     """Per-token bytes of one block of the chunked-prefill step: phase 1 over n sources with
     S queries; phase 2 for i = 1 (no partial), i = 2 (partial = v_1, nothing to write) and
     i = 3 .. S (fused partial update); the block close b^S = b^{S-1} + v_S; the final
     aggregation (phase 1 with one query over ``final_sources`` sources, no statistics)."""
-    p1 = phase1_bytes(n, S, d, E)
+    p1 = phase1_bytes(n, S, d, E, heads=heads)
     p2 = phase2_bytes(d, E, False, False)
     if S >= 2:
-        p2 += phase2_bytes(d, E, True, False)
-    p2 += max(0, S - 2) * phase2_bytes(d, E, True, True)
+        p2 += phase2_bytes(d, E, True, False, heads=heads)
+    p2 += max(0, S - 2) * phase2_bytes(d, E, True, True, heads=heads)
     close = partial_update_bytes(d, E)
     final = phase1_bytes(final_sources, 1, d, E, with_lse=False) if final_sources else 0
     return BlockStepBytes(p1, p2, close, final)

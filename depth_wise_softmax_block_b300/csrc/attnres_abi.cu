@@ -36,6 +36,14 @@ attnres_status check_shape(int64_t T, int d) {
   return ATTNRES_OK;
 }
 
+// Depth-attention heads: d splits into `heads` slices whose width is a multiple of 8.
+attnres_status check_heads(int d, int heads) {
+  if (heads < 1) return ATTNRES_ERR_INVALID_ARG;
+  if (heads > ATTNRES_MAX_HEADS) return ATTNRES_ERR_UNSUPPORTED;
+  if (d % heads != 0 || (d / heads) % 8 != 0) return ATTNRES_ERR_INVALID_ARG;
+  return ATTNRES_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -84,9 +92,10 @@ attnres_status attnres_query_prep(const float* w, const float* gamma_key, float*
 attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, int64_t T, int d,
                               attnres_dtype io, const float* u, const void* u_split, int S,
                               float eps, void* o_out, float* m_out, float* lse_out,
-                              float* alpha_out, unsigned int flags, void* stream) {
+                              float* alpha_out, unsigned int flags, int heads, void* stream) {
   if (!valid_io(io) || !valid_flags(flags)) return ATTNRES_ERR_INVALID_ARG;
-  const attnres_status sh = check_shape(T, d);
+  attnres_status sh = check_shape(T, d);
+  if (sh == ATTNRES_OK) sh = check_heads(d, heads);
   if (sh != ATTNRES_OK) return sh;
   if (n_src < 1 || S < 1 || !(eps >= 0.f)) return ATTNRES_ERR_INVALID_ARG;
   if (n_src > ATTNRES_MAX_SOURCES || S > ATTNRES_MAX_QUERIES) return ATTNRES_ERR_UNSUPPORTED;
@@ -99,7 +108,7 @@ attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, i
       src_stride % 8 != 0)
     return ATTNRES_ERR_MISALIGNED;
   attnres::Phase1Args a{reps,  src_stride, n_src, T,      d,       u,        u_split,
-                        S,     eps,        o_out, m_out, lse_out, alpha_out, flags};
+                        S,     eps,        o_out, m_out, lse_out, alpha_out, flags, heads};
   return cuda_status(attnres::launch_phase1(static_cast<IO>(io), a,
                                             static_cast<cudaStream_t>(stream)));
 }
@@ -108,9 +117,11 @@ attnres_status attnres_phase2_merge(const void* o_l, const float* lse_l, const v
                                     const void* v_prev, void* partial_out, int64_t T, int d,
                                     attnres_dtype io, const float* u_l, float eps_key,
                                     const float* gamma_in, float eps_in, void* h_out, void* y_out,
-                                    float* alpha_p_out, unsigned int flags, void* stream) {
+                                    float* alpha_p_out, unsigned int flags, int heads,
+                                    void* stream) {
   if (!valid_io(io) || !valid_flags(flags)) return ATTNRES_ERR_INVALID_ARG;
-  const attnres_status sh = check_shape(T, d);
+  attnres_status sh = check_shape(T, d);
+  if (sh == ATTNRES_OK) sh = check_heads(d, heads);
   if (sh != ATTNRES_OK) return sh;
   if (!(eps_key >= 0.f) || !(eps_in >= 0.f)) return ATTNRES_ERR_INVALID_ARG;
   if (T == 0) return ATTNRES_OK;
@@ -126,7 +137,7 @@ attnres_status attnres_phase2_merge(const void* o_l, const float* lse_l, const v
       !opt_aligned16(h_out))
     return ATTNRES_ERR_MISALIGNED;
   attnres::Phase2Args a{o_l, lse_l, partial, v_prev, partial_out, T, d, u_l, eps_key, gamma_in,
-                        eps_in, h_out, y_out, alpha_p_out, flags};
+                        eps_in, h_out, y_out, alpha_p_out, flags, heads};
   return cuda_status(attnres::launch_phase2(static_cast<IO>(io), a,
                                             static_cast<cudaStream_t>(stream)));
 }
@@ -147,9 +158,10 @@ attnres_status attnres_full_reference_path(const void* const* srcs, int n_src, i
                                            attnres_dtype io, const float* u_l, float eps_key,
                                            const float* gamma_in, float eps_in, void* h_out,
                                            void* y_out, float* alpha_out, unsigned int flags,
-                                           void* stream) {
+                                           int heads, void* stream) {
   if (!valid_io(io) || !valid_flags(flags)) return ATTNRES_ERR_INVALID_ARG;
-  const attnres_status sh = check_shape(T, d);
+  attnres_status sh = check_shape(T, d);
+  if (sh == ATTNRES_OK) sh = check_heads(d, heads);
   if (sh != ATTNRES_OK) return sh;
   if (n_src < 1) return ATTNRES_ERR_INVALID_ARG;
   if (n_src > ATTNRES_MAX_SOURCES) return ATTNRES_ERR_UNSUPPORTED;
@@ -178,6 +190,7 @@ attnres_status attnres_full_reference_path(const void* const* srcs, int n_src, i
   a.y = y_out;
   a.alpha = alpha_out;
   a.flags = flags;
+  a.heads = heads;
   return cuda_status(attnres::launch_full(static_cast<IO>(io), a,
                                           static_cast<cudaStream_t>(stream)));
 }
@@ -187,9 +200,10 @@ attnres_status attnres_phase2_merge_sources(const void* o_l, const float* lse_l,
                                             attnres_dtype io, const float* u_l, float eps_key,
                                             const float* gamma_in, float eps_in, void* h_out,
                                             void* y_out, float* alpha_out, unsigned int flags,
-                                            void* stream) {
+                                            int heads, void* stream) {
   if (!valid_io(io) || !valid_flags(flags)) return ATTNRES_ERR_INVALID_ARG;
-  const attnres_status sh = check_shape(T, d);
+  attnres_status sh = check_shape(T, d);
+  if (sh == ATTNRES_OK) sh = check_heads(d, heads);
   if (sh != ATTNRES_OK) return sh;
   if (k < 0) return ATTNRES_ERR_INVALID_ARG;
   if (k > ATTNRES_MAX_SOURCES) return ATTNRES_ERR_UNSUPPORTED;
@@ -219,6 +233,7 @@ attnres_status attnres_phase2_merge_sources(const void* o_l, const float* lse_l,
   a.y = y_out;
   a.alpha = alpha_out;
   a.flags = flags;
+  a.heads = heads;
   a.o0 = o_l;
   a.lse0 = lse_l;
   return cuda_status(attnres::launch_full(static_cast<IO>(io), a,

@@ -25,10 +25,11 @@ struct Phase1Args {
   int S;
   float eps;
   void* o;             // [S, T, d]
-  float* m;            // [S, T] or null
-  float* lse;          // [S, T] or null
-  float* alpha;        // [S, T, n] or null
+  float* m;            // [S, H, T] or null
+  float* lse;          // [S, H, T] or null
+  float* alpha;        // [S, H, T, n] or null
   unsigned flags;      // kSigmoid | kNoKeyNorm
+  int heads;           // depth-attention heads H: m, lse [S][H][T], alpha [S][H][T][n]
 };
 
 struct Phase2Args {
@@ -45,8 +46,9 @@ struct Phase2Args {
   float eps_in;
   void* h;
   void* y;
-  float* alpha_p;
+  float* alpha_p;      // [H][T] or null
   unsigned flags;
+  int heads;           // lse [H][T]
 };
 
 constexpr int kMaxSources = 64;
@@ -62,12 +64,13 @@ struct FullArgs {
   float eps_in;
   void* h;
   void* y;
-  float* alpha;     // [T][n] or null
-  float* m;         // [T] or null: max logit
-  float* lse;       // [T] or null: log-sum-exp of the logits
+  float* alpha;     // [H][T][n] or null
+  float* m;         // [H][T] or null: max logit
+  float* lse;       // [H][T] or null: log-sum-exp of the logits
   unsigned flags;
   const void* o0;   // [T, d] or null: normalised output of an earlier source partition
-  const float* lse0;  // [T]: its log-sum-exp (required with o0 unless sigmoid weights)
+  const float* lse0;  // [H][T]: its log-sum-exp (required with o0 unless sigmoid weights)
+  int heads;          // alpha [H][T][n], m and lse [H][T]
 };
 
 // Backward of one sublayer's aggregation (backward.cu).
@@ -113,8 +116,9 @@ cudaError_t encode_query_map(CUtensorMap* map, const float* u, int S, int d);
 cudaError_t encode_split_query_map(CUtensorMap* map, const void* u_split, int S, int d,
                                    int rows_box);
 
-// Tensor-core phase 1 (phase1_tc.cu): bf16 I/O, 2 <= S <= 24, n <= 64, split queries given.
-bool phase1_tc_supported(int n, int S);
+// Tensor-core phase 1 (phase1_tc.cu): bf16 I/O, 2 <= S <= 24, n <= 64, split queries given;
+// with H > 1 heads, d / H a multiple of 64.
+bool phase1_tc_supported(int n, int S, int d, int heads);
 cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s);
 unsigned int phase1_tc_poll_timeouts();
 

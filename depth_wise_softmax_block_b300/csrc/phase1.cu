@@ -20,6 +20,10 @@
 // every wait is bounded (tma.cuh).  Arithmetic is fp32; o is rounded once to the I/O type.
 // A single query (S = 1, the final aggregation) has nothing to share across queries and runs
 // on the row-wise single-pass kernel instead.
+// Depth-attention heads (multi-head variant of Table 4, "Attention Residuals" note, result 4):
+// grid.y walks the H heads and a CTA covers its head's columns k*dh .. k*dh + dh - 1 only
+// (dh = d / H); a stage's column chunks past the head's end hold the next head's columns and
+// are skipped.  Statistics are per (query, head).
 #include <string.h>
 
 #include <algorithm>
@@ -139,11 +143,14 @@ phase1_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ 
   constexpr int PR = Chunk<IOT>::PR;         // column pairs per chunk
   constexpr int NUC = VE / 4;                // 16-byte query chunks per column chunk
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n = a.n, S = a.S, d = a.d;
+  const int n = a.n, S = a.S, d = a.d, H = a.heads;
   const int TT = pl.TT, QG = pl.QG, SG = pl.SG, ST = pl.ST, KC = pl.KC;
   const int64_t T = a.T;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * TT;
-  const int nch = (d + KC - 1) / KC;
+  const int head = static_cast<int>(blockIdx.y);
+  const int dh = d / H;          // this CTA's columns: cw .. cw + dh - 1
+  const int cw = head * dh;
+  const int nch = (dh + KC - 1) / KC;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.offBar);
   uint64_t* empty = full + ST;
@@ -169,10 +176,10 @@ phase1_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ 
     const int c = first ? i : i - nch;
     unsigned char* st = smem + slot * pl.stageBytes;
     mbar_arrive_expect_tx(&full[slot], pl.bBytes + (first ? pl.nUBox * pl.uBox : 0));
-    tma_load_3d(st, &tm_b, c * KC, static_cast<int>(t0), 0, &full[slot]);
+    tma_load_3d(st, &tm_b, cw + c * KC, static_cast<int>(t0), 0, &full[slot]);
     if (first) {
       for (int h = 0; h < pl.nUBox; ++h)
-        tma_load_2d(st + pl.bSpan + h * pl.uSpan, &tm_u, c * KC + 32 * h, 0, &full[slot]);
+        tma_load_2d(st + pl.bSpan + h * pl.uSpan, &tm_u, cw + c * KC + 32 * h, 0, &full[slot]);
     }
   };
   int issued = 0;  // meaningful in thread 0 only
@@ -234,7 +241,7 @@ phase1_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ 
   for (int c = 0; c < nch; ++c, ++it) {
     const int slot = it % ST;
     acquire(slot);
-    if (active1) {
+    if (active1 && c * KC + warp * VE < dh) {  // the warp's chunk lies in the head
       const unsigned char* st = smem + slot * pl.stageBytes;
       float2 uv[NQ][PR];
 #pragma unroll
@@ -294,7 +301,7 @@ phase1_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ 
   }
   __syncthreads();
   // 1 / r_j (1 without the key RMSNorm) in place of the sum of squares
-  const float fd = static_cast<float>(d);
+  const float fd = static_cast<float>(dh);
   const bool key_norm = (a.flags & kNoKeyNorm) == 0;
   const bool sigmoid = (a.flags & kSigmoid) != 0;
   for (int i = tid; i < TT * n; i += kThreads) {
@@ -310,6 +317,7 @@ phase1_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ 
   for (int i = tid; i < TT * S; i += kThreads) {
     const int t = i / S, s = i % S;
     const int64_t tok = t0 + t;
+    const int64_t sh = static_cast<int64_t>(s) * H + head;  // row of the [S][H] statistics
     const float* dt = dots + t * n * S1;
     float m = -INFINITY;
     for (int j = 0; j < n; ++j) m = fmaxf(m, dt[j * S1 + s] * dt[j * S1 + S]);
@@ -324,11 +332,11 @@ phase1_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ 
       float* ap = alph + (((t * n + j) * QG + s / NQ) * NQ + s % NQ) * 2;
       ap[0] = al;
       ap[1] = al;
-      if (a.alpha != nullptr && tok < T) a.alpha[(static_cast<int64_t>(s) * T + tok) * n + j] = al;
+      if (a.alpha != nullptr && tok < T) a.alpha[(sh * T + tok) * n + j] = al;
     }
     if (tok < T) {
-      if (a.m != nullptr) a.m[static_cast<int64_t>(s) * T + tok] = m;
-      if (a.lse != nullptr && !sigmoid) a.lse[static_cast<int64_t>(s) * T + tok] = lse;
+      if (a.m != nullptr) a.m[sh * T + tok] = m;
+      if (a.lse != nullptr && !sigmoid) a.lse[sh * T + tok] = lse;
     }
   }
   __syncthreads();
@@ -378,13 +386,14 @@ phase1_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ 
 #pragma unroll
           for (int i = 0; i < PR; ++i) acc2[qq][i] = __ffma2_rn(al[qq], bv[i], acc2[qq][i]);
       }
-      const int k = c * KC + kg * VE;
-      if (tok2 < T && k < d) {
+      const int k = c * KC + kg * VE;  // column in the head
+      if (tok2 < T && k < dh) {
 #pragma unroll
         for (int qq = 0; qq < NQ; ++qq) {
           const int q = g2 * NQ + qq;
           if (q < S)
-            Chunk<IOT>::store(o + ((static_cast<int64_t>(q) * T + tok2) * d + k) * E, acc2[qq]);
+            Chunk<IOT>::store(o + ((static_cast<int64_t>(q) * T + tok2) * d + cw + k) * E,
+                              acc2[qq]);
         }
       }
     }
@@ -412,7 +421,8 @@ cudaError_t launch_t(const Phase1Args& a, const P1Plan& pl, cudaStream_t s) {
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
   if (e != cudaSuccess) return e;
   const int64_t blocks = (a.T + pl.TT - 1) / pl.TT;
-  kern<<<static_cast<unsigned>(blocks), kThreads, pl.smem, s>>>(mb, mu, a, pl);
+  const dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(a.heads));
+  kern<<<grid, kThreads, pl.smem, s>>>(mb, mu, a, pl);
   return cudaGetLastError();
 }
 
@@ -453,9 +463,10 @@ cudaError_t launch_phase1(IO io, const Phase1Args& a, cudaStream_t s) {
     f.m = a.m;
     f.lse = a.lse;
     f.flags = a.flags;
+    f.heads = a.heads;
     return launch_full(io, f, s);
   }
-  if (io == IO::BF16 && a.u_split != nullptr && phase1_tc_supported(a.n, a.S))
+  if (io == IO::BF16 && a.u_split != nullptr && phase1_tc_supported(a.n, a.S, a.d, a.heads))
     return launch_phase1_tc(a, s);
   return io == IO::BF16 ? launch_io<bf16>(a, s) : launch_io<float>(a, s);
 }

@@ -21,6 +21,13 @@
 //            o[s,t,:] = sum_j alpha_j b_j[t,:] (packed fp32 FMAs, 16-byte streaming stores).
 // The compute warps work in two halves of 8 that take alternate stages of the ring, so one
 // half's loads and stores overlap the other half's arithmetic.
+// Depth-attention heads (the multi-head variant of Table 4, "Attention Residuals" note,
+// result 4): head k owns the contiguous columns k*dh .. k*dh + dh - 1 (dh = d / H, a multiple of
+// 64 so that every stage lies in one head).  A CTA covers a window of Hs whole heads (grid.y
+// walks the windows): the MMAs of a head accumulate into its own block of tensor-memory columns,
+// the sums of squares, logits and softmax statistics are kept per head, and sweep 2 weights a
+// stage with its head's alpha.  Hs is the largest divisor of H whose columns fit the 512
+// tensor-memory columns (H = 1: one window, the whole row).
 // Stage hand-off uses mbarriers ("full": copy landed; "empty": all compute warps and the
 // stage's MMAs done); every wait is bounded (tma.cuh).  The tensor-memory allocation is
 // released on every path before the CTA exits.
@@ -47,11 +54,14 @@ constexpr int kM = 128;             // rows per MMA (M-tile); a tile has n * 8 r
 constexpr int kMaxS = 24;           // sweep 2 covers 4 groups of 6 queries
 constexpr int kMaxN = 64;           // sources (up to 4 M-tiles)
 constexpr int kSmallN = 9;          // up to here the sweep-2 weights are stored as ready pairs
-constexpr int kTmemCols = 256;      // D: up to 4 M-tiles x 2S <= 48 columns (one: 64)
+constexpr int kTmemMax = 512;       // tensor-memory columns of an SM
 constexpr int kMaxSlots = 12;       // ring slots
 constexpr int kMaxSmem = 227 * 1024;
 
 struct TcPlan {
+  int Hs, windows;    // heads per CTA window, windows (= H / Hs)
+  int tcols;          // tensor-memory columns allocated: nMT * Hs * Npad rounded up to 2^k >= 32
+  int R;              // rows of a per-head sum-of-squares buffer (nMT * 128)
   int Npad;           // MMA N: 2S rounded up to 16
   int rows, nMT;      // tile rows (n * 8) and M-tiles (ceil(rows / 128))
   int bBytes;         // source box bytes as copied (rows * 128)
@@ -64,11 +74,18 @@ struct TcPlan {
 
 inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-bool make_tc_plan(int n, int S, TcPlan& p) {
-  if (n < 1 || n > kMaxN || S < 2 || S > kMaxS) return false;
+// Layout for n sources, S queries and a window of Hs heads; false if it does not fit.
+bool make_tc_window(int n, int S, int H, int Hs, TcPlan& p) {
+  p.Hs = Hs;
+  p.windows = H / Hs;
   p.Npad = align_up(2 * S, 16);
   p.rows = n * kTT;
   p.nMT = (p.rows + kM - 1) / kM;
+  p.R = p.nMT * kM;
+  const int cols = p.nMT * Hs * p.Npad;
+  if (cols > kTmemMax) return false;
+  for (p.tcols = 32; p.tcols < cols; p.tcols *= 2) {
+  }
   p.bBytes = p.rows * 128;
   p.bSpan = align_up(p.bBytes, 1024);
   p.qBytes = p.Npad * 128;
@@ -76,11 +93,13 @@ bool make_tc_plan(int n, int S, TcPlan& p) {
   // The MMAs read nMT * 128 rows from a slot's base; rows past the tile's n * 8 are ignored but
   // must lie inside the allocation, hence the slack after the last slot.
   const int slack = std::max(0, p.nMT * kM * 128 - p.slot);
-  // logits [rows][SZ] (SZ = S rounded up to even, for 8-byte loads), then (n > 9) the
-  // weights in their place; 8 floats of padding for the last query group's 6-wide read
-  const int zb = (p.nMT * kM * ((S + 1) & ~1) + 8) * 4;
-  const int ab = n <= kSmallN ? kTT * n * 4 * 12 * 4 : 0;  // [token][source][4][6 pairs][2]
-  const int sb = 2 * p.nMT * kM * 4;                       // per-half row sums of squares
+  // logits [rows][Hs][SZ] (SZ = S rounded up to even, for 8-byte loads), then (unless the
+  // small layout) the weights in their place; 8 floats of padding for the last query group's
+  // 6-wide read
+  const int zb = (p.rows * Hs * ((S + 1) & ~1) + 8) * 4;
+  const bool small = H == 1 && n <= kSmallN;
+  const int ab = small ? kTT * n * 4 * 12 * 4 : 0;  // [token][source][4][6 pairs][2]
+  const int sb = 2 * Hs * p.R * 4;                  // per-half, per-head row sums of squares
   const int fixed = slack + align_up(zb, 16) + align_up(ab, 16) + sb +
                     (2 * kMaxSlots + 2) * 8 + 16;
   p.SB = std::min(kMaxSlots, (kMaxSmem - 1024 - fixed) / p.slot);
@@ -94,6 +113,15 @@ bool make_tc_plan(int n, int S, TcPlan& p) {
   return true;
 }
 
+// The widest window (most heads per CTA) that fits; false if none does.
+bool make_tc_plan(int n, int S, int d, int H, TcPlan& p) {
+  if (n < 1 || n > kMaxN || S < 2 || S > kMaxS || H < 1 || d % H != 0) return false;
+  if (H > 1 && (d / H) % kKC != 0) return false;
+  for (int Hs = H; Hs >= 1; --Hs)
+    if (H % Hs == 0 && make_tc_window(n, S, H, Hs, p)) return true;
+  return false;
+}
+
 __device__ __forceinline__ void unpack_pairs(const uint4& v, float2 (&f)[4]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -101,8 +129,22 @@ __device__ __forceinline__ void unpack_pairs(const uint4& v, float2 (&f)[4]) {
     f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
 }
 
-// kSmall: n <= 9 (one M-tile, sweep-2 weights as ready-made pairs, sums of squares in
-// registers), compiled without the paths for larger n.
+// Slot and phase parity of ring position `it` (it % SB, (it / SB) & 1), advanced without
+// divisions (a step of at most SB positions).
+struct RingPos {
+  int bs, ph;
+  __device__ __forceinline__ RingPos(int it, int SB) : bs(it % SB), ph((it / SB) & 1) {}
+  __device__ __forceinline__ void advance(int step, int SB) {
+    bs += step;
+    if (bs >= SB) {
+      bs -= SB;
+      ph ^= 1;
+    }
+  }
+};
+
+// kSmall: n <= 9 and one head (one M-tile, sweep-2 weights as ready-made pairs, sums of
+// squares in registers), compiled without the paths for larger n.
 template <bool kSmall>
 __global__ void __launch_bounds__(kThreads, 1)
 phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
@@ -111,9 +153,15 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = a.n, S = a.S, d = a.d, SB = pl.SB;
+  const int H = a.heads, Hs = pl.Hs, R = pl.R;
   const int64_t T = a.T;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTT;
-  const int nch = (d + kKC - 1) / kKC;
+  const int dh = d / H;                       // columns per head
+  const int wcols = Hs * dh;                  // columns of this CTA's window of heads
+  const int cw = static_cast<int>(blockIdx.y) * wcols;  // its first column
+  const int h0 = static_cast<int>(blockIdx.y) * Hs;     // its first head
+  const int cph = (dh + kKC - 1) / kKC;       // stages per head (all of them when H = 1)
+  const int nch = (wcols + kKC - 1) / kKC;
   const int total = 2 * nch;  // source-ring iterations: sweep 1, then sweep 2
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.offBar);
@@ -121,10 +169,11 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   uint64_t* dready = empty + SB;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(dready + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + pl.offTmem);
-  float* zbuf = reinterpret_cast<float*>(smem + pl.offZ);     // [nMT * 128 rows][SZ]
+  float* zbuf = reinterpret_cast<float*>(smem + pl.offZ);     // [n * 8 rows][Hs][SZ]
   const int SZ = (S + 1) & ~1;
-  float* alph = reinterpret_cast<float*>(smem + pl.offAlph);  // n <= 9: [8][n][4][6 pairs][2]
-  float* ssbuf = reinterpret_cast<float*>(smem + pl.offSs);   // [2 halves][nMT * 128 rows]
+  const int ZR = Hs * SZ;                                      // zbuf row stride
+  float* alph = reinterpret_cast<float*>(smem + pl.offAlph);  // small: [8][n][4][6 pairs][2]
+  float* ssbuf = reinterpret_cast<float*>(smem + pl.offSs);   // [2 halves][Hs][R rows]
 
   if (tid == 0) {
     for (int s = 0; s < SB; ++s) {
@@ -136,7 +185,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
     mbar_fence_init();
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, kSmall ? 64 : kTmemCols);
+    tmem_alloc(tmem_slot, pl.tcols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -149,9 +198,9 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
       tma_prefetch_map(&tm_b);
       tma_prefetch_map(&tm_q);
       int ib = 0;  // ring iterations issued
-      for (; ib < total; ++ib) {
-        const int bs = ib % SB;
-        if (ib >= SB && !mbar_wait(&empty[bs], ((ib / SB) - 1) & 1)) {
+      for (RingPos rp(0, SB); ib < total; ++ib, rp.advance(1, SB)) {
+        const int bs = rp.bs;
+        if (ib >= SB && !mbar_wait(&empty[bs], rp.ph ^ 1)) {
           *abort_flag = 1;
           break;
         }
@@ -161,8 +210,8 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
         const int c = first ? ib : total - 1 - ib;
         unsigned char* st = smem + bs * pl.slot;
         mbar_arrive_expect_tx(&full[bs], pl.bBytes + (first ? pl.qBytes : 0));
-        tma_load_3d(st, &tm_b, c * kKC, static_cast<int>(t0), 0, &full[bs]);
-        if (first) tma_load_2d(st + pl.bSpan, &tm_q, c * kKC, 0, &full[bs]);
+        tma_load_3d(st, &tm_b, cw + c * kKC, static_cast<int>(t0), 0, &full[bs]);
+        if (first) tma_load_2d(st + pl.bSpan, &tm_q, cw + c * kKC, 0, &full[bs]);
       }
       // Drain: the last copy issued into every slot has landed before the CTA may exit.
       for (int s = 0; s < SB && s < ib; ++s) {
@@ -174,16 +223,18 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   }
 
   // ------------------------------- MMA-issuing warp -------------------------------
-  // The stage's K = 16 MMAs (four per M-tile), D[row, 2s + {hi, lo}] += b_row . u_s, as soon
-  // as its copies land; completion arrives on the stage's "empty" barrier (and, after the last stage, on
+  // The stage's K = 16 MMAs (four per M-tile), D[row, 2s + {hi, lo}] += b_row . u_s into the
+  // columns of the stage's head, as soon as its copies land; completion arrives on the stage's "empty" barrier (and, after the last stage, on
   // "dready").  An MMA costs about the same for every N up to 128, so issuing from a warp of
   // its own keeps the tensor core off the compute warps' critical path.
   if (warp == kWarps + 1) {
     const uint32_t tmem = *tmem_slot;
     const uint32_t idesc = idesc_bf16_f32(kM, pl.Npad);
-    for (int c = 0; c < nch; ++c) {
-      const int bs = c % SB;
-      if (!*abort_flag && !mbar_wait(&full[bs], (c / SB) & 1)) *abort_flag = 1;
+    int hs = 0, ch = 0;  // head in the window and stage in the head of stage c
+    RingPos rp(0, SB);
+    for (int c = 0; c < nch; ++c, rp.advance(1, SB)) {
+      const int bs = rp.bs;
+      if (!*abort_flag && !mbar_wait(&full[bs], rp.ph)) *abort_flag = 1;
       tc_fence_after();
       if (lane == 0) {
         const unsigned char* st = smem + bs * pl.slot;
@@ -192,13 +243,17 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
           const uint32_t a0 = smem_addr(st + mt * kM * 128);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma_bf16(tmem + mt * pl.Npad, desc_kmajor_sw128(a0 + 32 * kk),
-                        desc_kmajor_sw128(b0 + 32 * kk), idesc, (c | kk) != 0 ? 1u : 0u);
+            tc_mma_bf16(tmem + (mt * Hs + hs) * pl.Npad, desc_kmajor_sw128(a0 + 32 * kk),
+                        desc_kmajor_sw128(b0 + 32 * kk), idesc, (ch | kk) != 0 ? 1u : 0u);
         }
         tc_commit(&empty[bs]);
         if (c == nch - 1) tc_commit(dready);
       }
       __syncwarp();
+      if (++ch == cph) {
+        ch = 0;
+        ++hs;
+      }
     }
     return;
   }
@@ -222,22 +277,45 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   const bool key_norm = (a.flags & kNoKeyNorm) == 0;
   const bool sigmoid = (a.flags & kSigmoid) != 0;
   // sums of squares: the half's thread ht takes the (row, 16-byte chunk) pairs ht + 256 k, and
-  // each half sums its stages into its own row buffer.  Up to 4 pairs per thread (n <= 16) the
-  // sums stay in registers until the end of the sweep; beyond that the 8 chunks of a row (8
-  // consecutive lanes) are summed with shuffles every stage and added to the buffer (one owner
-  // per row within a half: no race).
+  // each half sums its stages into its own per-head row buffer.  Up to 4 pairs per thread
+  // (n <= 16) the sums stay in registers until the half's last stage of the head; beyond that
+  // the 8 chunks of a row (8 consecutive lanes) are summed with shuffles every stage and added
+  // to the buffer (one owner per row within a half: no race).
   const int ntask = (nrows * 8 + 255) / 256;
   const bool reg_ss = kSmall || ntask <= 4;
-  float* ssh = ssbuf + half * (pl.nMT * kM);
-  for (int i = tid; i < 2 * pl.nMT * kM; i += kCompute) ssbuf[i] = 0.f;
+  float* ssh = ssbuf + half * (Hs * R);
+  for (int i = tid; i < 2 * Hs * R; i += kCompute) ssbuf[i] = 0.f;
   named_barrier(1, kCompute);
   float2 ssa[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                    make_float2(0.f, 0.f)};
-  for (int c = half; c < nch; c += 2) {
-    const int bs = c % SB;
+  auto flush = [&](int hs) {  // register sums of head hs into the half's buffer
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = ht + k * 256;
+      float x = ssa[k].x + ssa[k].y;
+      x += __shfl_xor_sync(0xffffffffu, x, 1);
+      x += __shfl_xor_sync(0xffffffffu, x, 2);
+      x += __shfl_xor_sync(0xffffffffu, x, 4);
+      if (i < nrows * 8 && (i & 7) == 0) ssh[hs * R + (i >> 3)] += x;
+      ssa[k] = make_float2(0.f, 0.f);
+    }
+  };
+  int cur = -1;          // head whose sums the registers hold
+  int hs = 0, hend = cph;  // head of stage c and the first stage past it
+  RingPos rp1(half, SB);
+  for (int c = half; c < nch; c += 2, rp1.advance(2, SB)) {
+    const int bs = rp1.bs;
     const unsigned char* st = smem + bs * pl.slot;
-    wait(&full[bs], (c / SB) & 1);
+    while (c >= hend) {
+      ++hs;
+      hend += cph;
+    }
+    wait(&full[bs], rp1.ph);
     if (key_norm && reg_ss) {
+      if (hs != cur) {
+        if (cur >= 0) flush(cur);
+        cur = hs;
+      }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int i = ht + k * 256;
@@ -263,62 +341,60 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
         x += __shfl_xor_sync(0xffffffffu, x, 1);
         x += __shfl_xor_sync(0xffffffffu, x, 2);
         x += __shfl_xor_sync(0xffffffffu, x, 4);
-        if (i < nrows * 8 && (i & 7) == 0) ssh[i >> 3] += x;
+        if (i < nrows * 8 && (i & 7) == 0) ssh[hs * R + (i >> 3)] += x;
       }
     }
     release(bs, false);
   }
-  if (reg_ss) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = ht + k * 256;
-      float x = ssa[k].x + ssa[k].y;
-      x += __shfl_xor_sync(0xffffffffu, x, 1);
-      x += __shfl_xor_sync(0xffffffffu, x, 2);
-      x += __shfl_xor_sync(0xffffffffu, x, 4);
-      if (i < nrows * 8 && (i & 7) == 0) ssh[i >> 3] = x;
-    }
-  }
+  if (key_norm && reg_ss && cur >= 0) flush(cur);
   named_barrier(1, kCompute);
 
   // ------------------------- logits from tensor memory -------------------------------
-  const float fd = static_cast<float>(d);
+  const float fd = static_cast<float>(dh);
   if (warp < 4 * pl.nMT) {  // warp w reads TMEM lanes 32 (w % 4) .. of M-tile w / 4
     wait(dready, 0);
     tc_fence_after();
     const int mt = warp >> 2, sub = warp & 3;
     const int r = mt * kM + sub * 32 + lane;
-    const float ss = r < nrows ? ssbuf[r] + ssbuf[pl.nMT * kM + r] : 0.f;
-    const float rinv = r >= nrows ? 0.f : key_norm ? 1.f / sqrtf(ss / fd + a.eps) : 1.f;
-    for (int cc = 0; cc < pl.Npad / 16; ++cc) {
-      uint32_t v[16];
-      tmem_ld16(tmem + (static_cast<uint32_t>(sub * 32) << 16) + mt * pl.Npad + cc * 16, v);
-      tmem_ld_wait();
-      if (r < nrows) {
+    for (int hs = 0; hs < Hs; ++hs) {
+      const float ss = r < nrows ? ssbuf[hs * R + r] + ssbuf[(Hs + hs) * R + r] : 0.f;
+      const float rinv = r >= nrows ? 0.f : key_norm ? 1.f / sqrtf(ss / fd + a.eps) : 1.f;
+      for (int cc = 0; cc < pl.Npad / 16; ++cc) {
+        uint32_t v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(sub * 32) << 16) + (mt * Hs + hs) * pl.Npad +
+                      cc * 16,
+                  v);
+        tmem_ld_wait();
+        if (r < nrows) {
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          const int s = cc * 8 + e / 2;
-          if (s < S) zbuf[r * SZ + s] = (__uint_as_float(v[e]) + __uint_as_float(v[e + 1])) * rinv;
+          for (int e = 0; e < 16; e += 2) {
+            const int s = cc * 8 + e / 2;
+            if (s < S)
+              zbuf[r * ZR + hs * SZ + s] =
+                  (__uint_as_float(v[e]) + __uint_as_float(v[e + 1])) * rinv;
+          }
         }
       }
     }
   }
   named_barrier(1, kCompute);
 
-  // ---------------- softmax statistics, one thread per (token, query) ----------------
-  for (int i = tid; i < kTT * S; i += kCompute) {
-    const int t = i / S, s = i % S;
+  // ------------- softmax statistics, one thread per (token, head, query) -------------
+  for (int i = tid; i < kTT * Hs * S; i += kCompute) {
+    const int t = i / (Hs * S), hs = (i / S) % Hs, s = i % S;
     const int64_t tok = t0 + t;
+    const int64_t sh = static_cast<int64_t>(s) * H + h0 + hs;  // row of the [S][H] statistics
+    const float* zc = zbuf + t * ZR + hs * SZ + s;             // source j at zc + j * 8 * ZR
     float m = -INFINITY;
-    for (int j = 0; j < n; ++j) m = fmaxf(m, zbuf[(j * kTT + t) * SZ + s]);
+    for (int j = 0; j < n; ++j) m = fmaxf(m, zc[j * kTT * ZR]);
     float l = 0.f;
     if (!sigmoid)
-      for (int j = 0; j < n; ++j) l += expf(zbuf[(j * kTT + t) * SZ + s] - m);
+      for (int j = 0; j < n; ++j) l += expf(zc[j * kTT * ZR] - m);
     const float lse = m + logf(l);
     const float rl = 1.f / l;
     const int g = s / 6, pp = s % 6;
     for (int j = 0; j < n; ++j) {
-      float* zp = zbuf + (j * kTT + t) * SZ + s;
+      float* zp = zbuf + (j * kTT + t) * ZR + hs * SZ + s;
       const float zj = *zp;
       const float al = sigmoid ? 1.f / (1.f + expf(-zj)) : expf(zj - m) * rl;
       if (kSmall) {  // ready-made (a, a) pairs
@@ -328,11 +404,11 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
       } else {             // in place of the logit, which this thread alone reads
         *zp = al;
       }
-      if (a.alpha != nullptr && tok < T) a.alpha[(static_cast<int64_t>(s) * T + tok) * n + j] = al;
+      if (a.alpha != nullptr && tok < T) a.alpha[(sh * T + tok) * n + j] = al;
     }
     if (tok < T) {
-      if (a.m != nullptr) a.m[static_cast<int64_t>(s) * T + tok] = m;
-      if (a.lse != nullptr && !sigmoid) a.lse[static_cast<int64_t>(s) * T + tok] = lse;
+      if (a.m != nullptr) a.m[sh * T + tok] = m;
+      if (a.lse != nullptr && !sigmoid) a.lse[sh * T + tok] = lse;
     }
   }
   named_barrier(1, kCompute);
@@ -347,15 +423,16 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   const int64_t tok2 = t0 + t2;
   const bool active2 = grp * 6 < S;
   const float* at = alph + (t2 * n * 4 + grp) * 12;     // n <= 9
-  const float* zt = zbuf + t2 * SZ + grp * 6;            // n > 9: weights of (j, t2, 6 queries)
+  const float* zt = zbuf + t2 * ZR + grp * 6;  // weights of (j, t2, head, 6 queries)
   // source j's chunk: row j * 8 + t2, swizzled chunk kg ^ t2 (independent of j)
   const int boff = t2 * 128 + ((kg ^ t2) << 4);
   char* o = static_cast<char*>(a.o);
   const int first2 = nch + (((nch & 1) != half) ? 1 : 0);
-  for (int ib = first2; ib < total; ib += 2) {
-    const int bs = ib % SB;
+  RingPos rp2(first2, SB);
+  for (int ib = first2; ib < total; ib += 2, rp2.advance(2, SB)) {
+    const int bs = rp2.bs;
     const int c = total - 1 - ib;  // columns in reverse
-    wait(&full[bs], (ib / SB) & 1);
+    wait(&full[bs], rp2.ph);
     if (active2) {
       const unsigned char* st = smem + bs * pl.slot + boff;
       float2 acc[6][4];
@@ -381,10 +458,11 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
           }
         }
       } else {
+        const float* zh = zt + (c / cph) * SZ;  // the stage's head
         for (int j = 0; j < n; ++j) {
           float2 bv[4];
           unpack_pairs(*reinterpret_cast<const uint4*>(st + j * 1024), bv);
-          const float2* zp = reinterpret_cast<const float2*>(zt + j * kTT * SZ);
+          const float2* zp = reinterpret_cast<const float2*>(zh + j * kTT * ZR);
           const float2 w01 = zp[0], w23 = zp[1], w45 = zp[2];
           const float2 al[6] = {make_float2(w01.x, w01.x), make_float2(w01.y, w01.y),
                                 make_float2(w23.x, w23.x), make_float2(w23.y, w23.y),
@@ -395,9 +473,9 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
             for (int e = 0; e < 4; ++e) acc[qq][e] = __ffma2_rn(al[qq], bv[e], acc[qq][e]);
         }
       }
-      const int k = c * kKC + kg * 8;
-      if (tok2 < T && k < d) {
-        char* op = o + ((static_cast<int64_t>(grp * 6) * T + tok2) * d + k) * 2;
+      const int k = c * kKC + kg * 8;  // column in the window
+      if (tok2 < T && k < wcols) {
+        char* op = o + ((static_cast<int64_t>(grp * 6) * T + tok2) * d + cw + k) * 2;
         const int64_t qstride = T * d * 2;
 #pragma unroll
         for (int qq = 0; qq < 6; ++qq) {
@@ -420,29 +498,31 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   if (warp == 0) {
     if (lane == 0 && *abort_flag) mbar_wait(dready, 0);  // MMAs of an aborted run may still run
     __syncwarp();
-    tmem_dealloc(tmem, kSmall ? 64 : kTmemCols);
+    tmem_dealloc(tmem, pl.tcols);
   }
 }
 
 }  // namespace
 
-bool phase1_tc_supported(int n, int S) {
+bool phase1_tc_supported(int n, int S, int d, int heads) {
   TcPlan p;
-  return make_tc_plan(n, S, p);
+  return make_tc_plan(n, S, d, heads, p);
 }
 
 cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s) {
   TcPlan pl;
-  if (a.u_split == nullptr || !make_tc_plan(a.n, a.S, pl)) return cudaErrorInvalidValue;
+  if (a.u_split == nullptr || !make_tc_plan(a.n, a.S, a.d, a.heads, pl))
+    return cudaErrorInvalidValue;
   CUtensorMap mb, mq;
   cudaError_t e = encode_source_map(&mb, a.reps, a.src_stride, a.n, a.T, a.d, 2, kKC, kTT);
   if (e == cudaSuccess) e = encode_split_query_map(&mq, a.u_split, a.S, a.d, pl.Npad);
   if (e != cudaSuccess) return e;
-  auto kern = a.n <= kSmallN ? phase1_tc_kernel<true> : phase1_tc_kernel<false>;
+  auto kern = a.heads == 1 && a.n <= kSmallN ? phase1_tc_kernel<true> : phase1_tc_kernel<false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
   if (e != cudaSuccess) return e;
   const int64_t blocks = (a.T + kTT - 1) / kTT;
-  kern<<<static_cast<unsigned>(blocks), kThreads, pl.smem, s>>>(mb, mq, a, pl);
+  const dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(pl.windows));
+  kern<<<grid, kThreads, pl.smem, s>>>(mb, mq, a, pl);
   return cudaGetLastError();
 }
 

@@ -52,14 +52,15 @@ def _call(timer, kind, fn, *args, **kw):
 
 
 class BlockRunner:
-    """Work buffers for blocks of up to ``S_max`` sublayers over ``T`` tokens."""
+    """Work buffers for blocks of up to ``S_max`` sublayers over ``T`` tokens, with ``heads``
+    depth-attention heads (per-head log-sum-exps)."""
 
     def __init__(self, T: int, d: int, S_max: int, dtype, device, keep_y: bool = False,
-                 timer: Optional[KernelTimer] = None):
+                 timer: Optional[KernelTimer] = None, heads: int = 1):
         self.timer = timer
-        self.T, self.d, self.S_max = T, d, S_max
+        self.T, self.d, self.S_max, self.heads = T, d, S_max, heads
         self.o = torch.empty((S_max, T, d), dtype=dtype, device=device)
-        self.lse = torch.empty((S_max, T), dtype=torch.float32, device=device)
+        self.lse = torch.empty((S_max, heads, T), dtype=torch.float32, device=device)
         self.partial = torch.empty((T, d), dtype=dtype, device=device)
         self.keep_y = keep_y
         n_y = S_max if keep_y else 1
@@ -87,7 +88,7 @@ class BlockRunner:
         o, lse = self.o[:S], self.lse[:S]
         tm = self.timer
         _call(tm, "phase1", attnres_phase1, reps, U, o, lse_out=lse, eps=eps_key, u_split=U_split,
-              flags=flags)
+              flags=flags, heads=self.heads)
         v_prev = None       # v_{i-1}
         part = None         # tensor holding b^{i-2} (None while it is zero)
         for i in range(1, S + 1):
@@ -104,7 +105,7 @@ class BlockRunner:
             kind = "phase2_first" if i == 1 else ("phase2" if i == 2 else "phase2_fused")
             _call(tm, kind, attnres_phase2_merge, o[i - 1], lse[i - 1], args["partial"],
                   args["v_prev"], args["partial_out"], U[i - 1], g, y, eps_key=eps_key,
-                  eps_in=eps_in, flags=flags)
+                  eps_in=eps_in, flags=flags, heads=self.heads)
             # b^{i-1} now lives in args["partial"] (i == 2) or self.partial (i >= 3)
             if i == 2:
                 part = v_prev
@@ -120,10 +121,10 @@ class BlockRunner:
 
 def final_aggregation(reps: torch.Tensor, u_final: torch.Tensor, out: torch.Tensor,
                       eps: float = 1e-6, timer: Optional[KernelTimer] = None,
-                      flags: int = 0) -> torch.Tensor:
+                      flags: int = 0, heads: int = 1) -> torch.Tensor:
     """Final output over b_0 .. b_N: phase 1 with the single extra pseudo-query."""
     _call(timer, "final", attnres_phase1, reps, u_final.view(1, -1), out.view(1, *out.shape),
-          eps=eps, flags=flags)
+          eps=eps, flags=flags, heads=heads)
     return out
 
 
@@ -143,10 +144,11 @@ class FullGroupedRunner:
     ``hist`` [L + 1, T, d] holds v_0 in slot 0; slot l receives v_l = sublayer(l, y_l) (the
     model's attention or MLP; a stand-in for the synthetic workloads)."""
 
-    def __init__(self, T: int, d: int, S: int, dtype, device, timer: Optional[KernelTimer] = None):
-        self.S, self.timer = S, timer
+    def __init__(self, T: int, d: int, S: int, dtype, device, timer: Optional[KernelTimer] = None,
+                 heads: int = 1):
+        self.S, self.timer, self.heads = S, timer, heads
         self.o = torch.empty((S, T, d), dtype=dtype, device=device)
-        self.lse = torch.empty((S, T), dtype=torch.float32, device=device)
+        self.lse = torch.empty((S, heads, T), dtype=torch.float32, device=device)
 
     def run(self, hist: torch.Tensor, U: torch.Tensor, G_in: Optional[torch.Tensor],
             y_out: torch.Tensor, sublayer: Callable[[int, torch.Tensor], torch.Tensor],
@@ -162,14 +164,14 @@ class FullGroupedRunner:
             o, lse = self.o[:Sg], self.lse[:Sg]
             us = None if U_split is None else U_split[2 * l0:2 * (l0 + Sg)]
             _call(tm, "phase1", attnres_phase1, hist[:l0 + 1], U[l0:l0 + Sg], o, lse_out=lse,
-                  eps=eps_key, u_split=us, flags=flags)
+                  eps=eps_key, u_split=us, flags=flags, heads=self.heads)
             for i in range(1, Sg + 1):
                 l = l0 + i
                 g = None if G_in is None else G_in[l - 1]
                 srcs = [hist[j] for j in range(l0 + 1, l)]
                 _call(tm, "phase2_sources", attnres_phase2_merge_sources, o[i - 1], lse[i - 1],
                       srcs, U[l - 1], g, y_out=y_out[l - 1], eps_key=eps_key, eps_in=eps_in,
-                      flags=flags)
+                      flags=flags, heads=self.heads)
                 v = sublayer(l, y_out[l - 1])
                 if v.data_ptr() != hist[l].data_ptr():
                     hist[l].copy_(v)

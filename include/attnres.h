@@ -67,13 +67,26 @@ typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype;
 #define ATTNRES_SIGMOID_WEIGHTS 0x1u
 #define ATTNRES_NO_KEY_NORM 0x2u
 
+/*
+ * Depth-attention heads (`heads` argument; 1 = the method as defined), the multi-head variant
+ * of Table 4 ("Attention Residuals" note, result 4: "Block, multi-head H = 16").  The pages
+ * give no formula; the reading implemented here: the d features split into H contiguous slices
+ * of dh = d / H, and head k is a complete aggregation on its slice (columns k*dh .. k*dh+dh-1):
+ * the key RMS r_j,k is taken over the slice, the logit is u[slice] . b_j[slice] / r_j,k, and
+ * the softmax (or sigmoid) over the sources runs per head.  The heads' outputs are
+ * concatenated, and the sublayer's input RMSNorm normalises the whole d-vector.  Per-head
+ * statistics gain a head index after the query (phase 1) or first (phase 2):
+ * m, lse [S][H][T]; alpha [S][H][T][n].  Requires d % H == 0 and dh a multiple of 8.
+ */
+#define ATTNRES_MAX_HEADS 64
+
 /* Limits (checked; larger values return ATTNRES_ERR_UNSUPPORTED). */
 #define ATTNRES_MAX_SOURCES 64     /* sources per call (phase 1 and the full path)          */
 #define ATTNRES_MAX_QUERIES 64     /* queries S per phase-1 call                             */
 #define ATTNRES_MAX_D 16384        /* hidden size (a row stays in registers)               */
 
 /* ABI version of this header; attnres_abi_version() returns the library's. */
-#define ATTNRES_ABI_VERSION 5
+#define ATTNRES_ABI_VERSION 6
 int attnres_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -135,15 +148,18 @@ attnres_status attnres_query_prep(const float* w, const float* gamma_key, float*
  *               ATTNRES_SIGMOID_WEIGHTS, o is the unnormalised sum and lse_out is not written
  *   alpha_out   device fp32 [S][T][n_src], optional
  *   flags       ATTNRES_SIGMOID_WEIGHTS | ATTNRES_NO_KEY_NORM (see above), 0 by default
+ *   heads       depth-attention heads H (see above), 1 by default: m_out and lse_out are then
+ *               [S][H][T] and alpha_out [S][H][T][n_src]; the tensor cores take H > 1 when
+ *               d / H is a multiple of 64
  * Limits: 1 <= n_src <= 64, 1 <= S <= 64, and n_src <= 16 when S > 24 (the per-token tile
- * must fit one CTA); otherwise ATTNRES_ERR_UNSUPPORTED.
+ * must fit one CTA); 1 <= heads <= 64; otherwise ATTNRES_ERR_UNSUPPORTED.
  * With S = 1 and the final pseudo-query this is also the final aggregation over
  * b_0 .. b_N (row a10).
  */
 attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, int64_t T,
                               int d, attnres_dtype io, const float* u, const void* u_split,
                               int S, float eps, void* o_out, float* m_out, float* lse_out,
-                              float* alpha_out, unsigned int flags, void* stream);
+                              float* alpha_out, unsigned int flags, int heads, void* stream);
 
 /*
  * Phase 2 merge (rows a5-a8): one sublayer l of the block ("Attention Residuals" §10,
@@ -166,13 +182,15 @@ attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, i
  *   alpha_p_out  device fp32 [T] or NULL: weight of the partial source, c / (a + c)
  *   flags        variant flags; with ATTNRES_SIGMOID_WEIGHTS h = o_l + sigmoid(z_p) p, lse_l is
  *                not read (may be NULL) and alpha_p_out receives sigmoid(z_p)
+ *   heads        depth-attention heads H: each head merges its slice with its own r, z_p and
+ *                lse (lse_l and alpha_p_out are then [H][T]); y normalises the whole row
  */
 attnres_status attnres_phase2_merge(const void* o_l, const float* lse_l, const void* partial,
                                     const void* v_prev, void* partial_out, int64_t T, int d,
                                     attnres_dtype io, const float* u_l, float eps_key,
                                     const float* gamma_in, float eps_in, void* h_out,
                                     void* y_out, float* alpha_p_out, unsigned int flags,
-                                    void* stream);
+                                    int heads, void* stream);
 
 /*
  * Partial-sum update / block close (rows a8-a9): out = partial + v, elementwise, rounded to
@@ -192,13 +210,15 @@ attnres_status attnres_partial_update(const void* partial, const void* v, void* 
  *   h_out       device [T, d] or NULL; y_out device [T, d] or NULL (at least one required)
  *   alpha_out   device fp32 [T][n_src] or NULL
  *   flags       variant flags (sigmoid weights: h = sum_i sigmoid(z_i) v_i)
+ *   heads       depth-attention heads H (alpha_out is then [H][T][n_src])
  * Limits: 1 <= n_src <= 64.
  */
 attnres_status attnres_full_reference_path(const void* const* srcs, int n_src, int64_t T,
                                            int d, attnres_dtype io, const float* u_l,
                                            float eps_key, const float* gamma_in,
                                            float eps_in, void* h_out, void* y_out,
-                                           float* alpha_out, unsigned int flags, void* stream);
+                                           float* alpha_out, unsigned int flags, int heads,
+                                           void* stream);
 
 /*
  * Phase 2 of Full AttnRes run by the grouped two-phase schedule ("Attention Residuals 阅读补充",
@@ -217,6 +237,7 @@ attnres_status attnres_full_reference_path(const void* const* srcs, int n_src, i
  *   u_l, gamma_in, eps_key, eps_in: as for attnres_phase2_merge
  *   h_out, y_out  device [T, d] or NULL (at least one required)
  *   alpha_out   device fp32 [T][k] or NULL: weights of the in-group sources
+ *   heads       depth-attention heads H: lse_l is [H][T] and alpha_out [H][T][k]
  * Limits: 0 <= k <= 64.
  */
 attnres_status attnres_phase2_merge_sources(const void* o_l, const float* lse_l,
@@ -224,7 +245,7 @@ attnres_status attnres_phase2_merge_sources(const void* o_l, const float* lse_l,
                                             attnres_dtype io, const float* u_l, float eps_key,
                                             const float* gamma_in, float eps_in, void* h_out,
                                             void* y_out, float* alpha_out, unsigned int flags,
-                                            void* stream);
+                                            int heads, void* stream);
 
 /*
  * Backward of one sublayer's aggregation over an explicit source list (the direct form of
@@ -247,7 +268,8 @@ attnres_status attnres_phase2_merge_sources(const void* o_l, const float* lse_l,
  *   du          device fp32 [d]: the gradient is ADDED (zero it first for a fresh sum)
  *   dgamma_in   device fp32 [d] or NULL: added, like du
  * The sums over tokens are accumulated with atomic additions, so their last bits may vary
- * from run to run.  Limits: 1 <= n_src <= 16; d <= 8192 (bf16) or 4096 (fp32).
+ * from run to run.  Single-head (softmax, key RMSNorm) only.  Limits: 1 <= n_src <= 16;
+ * d <= 8192 (bf16) or 4096 (fp32).
  */
 attnres_status attnres_backward(const void* const* srcs, int n_src, int64_t T, int d,
                                 attnres_dtype io, const float* u, float eps_key,

@@ -306,38 +306,54 @@ def multihead_aggregate(sources, w, gamma_key, eps: float, H: int, weights: str 
     return h, np.stack(al), np.stack(zz)
 
 
-def multihead_phase1(reps, W, G_key, eps: float, H: int):
+def multihead_phase1(reps, W, G_key, eps: float, H: int, weights: str = "softmax",
+                     key_norm: bool = True):
     """Phase 1 per head: for each query s and head k, the partition statistics of the head's
-    slice.  Returns o [S,T,d] (heads concatenated), m and lse [S,H,T], alpha [S,H,T,n]."""
+    slice (phase1, or phase1_variant under a Table 4 variant).  Returns o [S,T,d] (heads
+    concatenated), m and lse [S,H,T] (lse None with sigmoid weights), alpha [S,H,T,n]."""
     reps = _f64(reps)
     S, d = np.shape(W)
     o = np.zeros((S,) + reps.shape[1:])
     m = np.zeros((S, H, reps.shape[1]))
     lse = np.zeros_like(m)
     alpha = np.zeros((S, H, reps.shape[1], reps.shape[0]))
+    plain = weights == "softmax" and key_norm
     for k, sl in enumerate(head_slices(d, H)):
         gk = None if G_key is None else _f64(G_key)[:, sl]
-        ok, mk, lk, ak = phase1(reps[..., sl], _f64(W)[:, sl], gk, eps)
+        if plain:
+            ok, mk, lk, ak = phase1(reps[..., sl], _f64(W)[:, sl], gk, eps)
+        else:
+            ok, mk, lk, ak = phase1_variant(reps[..., sl], _f64(W)[:, sl], gk, eps, weights,
+                                            key_norm)
         o[..., sl] = ok
-        m[:, k], lse[:, k], alpha[:, k] = mk, lk, ak
-    return o, m, lse, alpha
+        m[:, k], alpha[:, k] = mk, ak
+        if lk is not None:
+            lse[:, k] = lk
+    return o, m, (lse if weights == "softmax" else None), alpha
 
 
 def multihead_merge_reference(o_A, lse_A, p, w, gamma_key, eps_key: float, gamma_in,
-                              eps_in: float, H: int):
+                              eps_in: float, H: int, weights: str = "softmax",
+                              key_norm: bool = True):
     """Phase 2 per head: each head merges its slice of phase 1's result (o_A, lse_A [H,T])
-    with its slice of the partial source p (merge_reference on the slice); the heads are
-    concatenated and the input RMSNorm normalises the whole h.  Returns (h, y, weights of p
-    [H,T])."""
+    with its slice of the partial source p (merge_reference on the slice, or
+    merge_reference_variant under a Table 4 variant); the heads are concatenated and the input
+    RMSNorm normalises the whole h.  Returns (h, y, weights of p [H,T])."""
     o_A = _f64(o_A)
     d = o_A.shape[-1]
     h = np.zeros_like(o_A)
     ap = np.zeros((H,) + o_A.shape[:-1])
+    plain = weights == "softmax" and key_norm
     for k, sl in enumerate(head_slices(d, H)):
         g = None if gamma_key is None else _f64(gamma_key)[sl]
-        hk, _, ak = merge_reference(o_A[..., sl], _f64(lse_A)[k],
-                                    None if p is None else _f64(p)[..., sl], _f64(w)[sl], g,
-                                    eps_key, None, eps_in)
+        pk = None if p is None else _f64(p)[..., sl]
+        lk = None if lse_A is None else _f64(lse_A)[k]
+        if plain:
+            hk, _, ak = merge_reference(o_A[..., sl], lk, pk, _f64(w)[sl], g, eps_key, None,
+                                        eps_in)
+        else:
+            hk, _, ak = merge_reference_variant(o_A[..., sl], lk, pk, _f64(w)[sl], g, eps_key,
+                                                None, eps_in, weights, key_norm)
         h[..., sl] = hk
         ap[k] = ak
     return h, rmsnorm(h, gamma_in, eps_in), ap

@@ -45,16 +45,16 @@ def test_header_symbols_exported(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.attnres_abi_version() == 5
+    assert lib.attnres_abi_version() == 6
     for code, name in ar.STATUS.items():
         assert lib.attnres_status_string(code).decode() == name
     assert lib.attnres_status_string(99).decode() == "ATTNRES_ERR_UNKNOWN"
 
 
 def p1(lib, reps=P, stride=1024 * 64, n=2, T=0, d=64, io=1, u=P, S=4, eps=1e-6, o=P, us=None,
-       flags=0):
+       flags=0, heads=1):
     return lib.attnres_phase1(reps, stride, n, T, d, io, u, us, S, eps, o, None, None, None, flags,
-                              None)
+                              heads, None)
 
 
 def test_phase1_validation(lib):
@@ -87,12 +87,20 @@ def test_phase1_validation(lib):
     assert p1(lib, us=P) == OK
     assert p1(lib, flags=3) == OK                         # both variant flags
     assert p1(lib, flags=4) == INVALID                    # unknown flag
+    assert p1(lib, d=128, heads=16) == OK                 # depth-attention heads of 8 columns
+    assert p1(lib, d=128, heads=0) == INVALID
+    assert p1(lib, d=128, heads=3) == INVALID             # d % heads
+    assert p1(lib, d=96, heads=3) == OK
+    assert p1(lib, d=120, heads=5) == OK                  # heads of 24 columns
+    assert p1(lib, d=120, heads=10) == INVALID            # heads of 12 columns (not 8k)
+    assert p1(lib, d=64, heads=16) == INVALID             # heads of 4 columns (not 8)
+    assert p1(lib, d=1024, heads=65) == UNSUPPORTED
 
 
 def p2(lib, o=P, lse=P, part=None, v=None, pout=None, T=0, d=64, io=1, u=P, g=None, y=P, h=None,
-       flags=0):
+       flags=0, heads=1):
     return lib.attnres_phase2_merge(o, lse, part, v, pout, T, d, io, u, 1e-6, g, 1e-6, h, y, None,
-                                    flags, None)
+                                    flags, heads, None)
 
 
 def test_phase2_validation(lib):
@@ -112,13 +120,16 @@ def test_phase2_validation(lib):
     assert err(p2(lib, T=4, part=PM)) == MISALIGNED
     assert err(p2(lib, T=4, v=P, g=PM)) == MISALIGNED
     assert err(p2(lib, T=4, h=PM)) == MISALIGNED
+    assert p2(lib, heads=8) == OK
+    assert p2(lib, heads=16) == INVALID                   # heads of 4 columns
+    assert p2(lib, heads=-1) == INVALID
 
 
 def test_full_and_update_validation(lib):
     import ctypes
     arr = (ctypes.c_void_p * 3)(P, P + 4096, P + 8192)
-    def f(*args):
-        return lib.attnres_full_reference_path(*args[:-1], 0, args[-1])
+    def f(*args, heads=1):
+        return lib.attnres_full_reference_path(*args[:-1], 0, heads, args[-1])
     assert f(arr, 3, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None) == OK
     assert err(f(None, 3, 4, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None)) == INVALID
     assert f(arr, 0, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None) == INVALID
@@ -129,7 +140,9 @@ def test_full_and_update_validation(lib):
     nul = (ctypes.c_void_p * 2)(P, None)
     assert err(f(nul, 2, 4, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None)) == INVALID
     assert lib.attnres_full_reference_path(arr, 3, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None,
-                                           16, None) == INVALID
+                                           16, 1, None) == INVALID
+    assert f(arr, 3, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None, heads=8) == OK
+    assert f(arr, 3, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None, heads=7) == INVALID
     up = lib.attnres_partial_update
     assert up(P, P, P, 0, 64, 1, None) == OK
     assert err(up(None, P, P, 4, 64, 1, None)) == INVALID
@@ -148,8 +161,8 @@ def test_merge_sources_validation(lib):
     arr = (ctypes.c_void_p * 2)(P, P + 4096)
     ms = lib.attnres_phase2_merge_sources
 
-    def call(o=P, lse=P, srcs=arr, k=2, T=0, d=64, u=P, h=None, y=P, flags=0):
-        return ms(o, lse, srcs, k, T, d, 1, u, 1e-6, None, 1e-6, h, y, None, flags, None)
+    def call(o=P, lse=P, srcs=arr, k=2, T=0, d=64, u=P, h=None, y=P, flags=0, heads=1):
+        return ms(o, lse, srcs, k, T, d, 1, u, 1e-6, None, 1e-6, h, y, None, flags, heads, None)
     assert call() == OK
     assert call(k=0, srcs=None) == OK
     assert call(k=-1) == INVALID
@@ -163,6 +176,8 @@ def test_merge_sources_validation(lib):
     bad = (ctypes.c_void_p * 2)(P, PM)
     assert err(call(T=4, srcs=bad)) == MISALIGNED
     assert call(flags=4) == INVALID
+    assert call(heads=2) == OK
+    assert call(heads=128) == UNSUPPORTED
 
 
 def test_backward_validation(lib):

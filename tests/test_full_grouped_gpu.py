@@ -48,7 +48,7 @@ def _run(hist, v, U, Gi, S, dtype, split, snap=None):
     def sub(l, y):
         if snap is not None:   # the stored phase-1 result this layer merged from
             i = (l - 1) % S
-            snap[l] = (runner.o[i].clone(), runner.lse[i].clone())
+            snap[l] = (runner.o[i].clone(), runner.lse[i, 0].clone())   # one head
         return v[l - 1]
 
     runner.run(hist, U, Gi, ys, sub, EPS, EPS, U_split=split)

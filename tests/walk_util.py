@@ -38,7 +38,7 @@ class BlockChecker:
     def phase1_done(self, o, lse):
         """Snapshot the phase-1 outputs (rows) and check them against the oracle."""
         self.o_gpu = to64(o[:, self.rows])
-        self.lse_gpu = to64(lse[:, self.rows])
+        self.lse_gpu = to64(lse[:, 0, self.rows])    # one head
         oo, _, olse, _ = O.phase1(self.reps64, self.W, self.Gk, self.eps)
         self.oA = oo
         check_outputs(self.o_gpu, oo, self.dt, "phase-1 o")
