@@ -106,12 +106,13 @@ class BlockRunner:
             _call(tm, kind, attnres_phase2_merge, o[i - 1], lse[i - 1], args["partial"],
                   args["v_prev"], args["partial_out"], U[i - 1], g, y, eps_key=eps_key,
                   eps_in=eps_in, flags=flags, heads=self.heads)
-            # b^{i-1} now lives in args["partial"] (i == 2) or self.partial (i >= 3)
+            # b^{i-1} now lives in args["partial"] (i == 2) or args["partial_out"] (i >= 3)
             if i == 2:
                 part = v_prev
             elif i >= 3:
-                part = self.partial
+                part = args["partial_out"]
             v_prev = sublayer(i, y)
+        self.last_partial = part  # b^{S-1} (None when S == 1)
         # close: b^S = b^{S-1} + v_S  (b^{S-1} = v_1 when S == 2; b^1 = v_1 when S == 1)
         if S == 1:
             close_out.copy_(v_prev)

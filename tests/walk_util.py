@@ -90,7 +90,7 @@ def run_checked_block(runner, reps, U, W, Gk, Gin, vbuf, close_out, dtype, rows,
     torch.cuda.synchronize()
     # the close is exactly round(b^{S-1} + v_S) of the stored tensors
     if S >= 2:
-        prev = vbuf[0] if S == 2 else runner.partial
+        prev = runner.last_partial      # b^{S-1}: v_1 when S == 2
         want = (prev[rows].float() + vbuf[S - 1][rows].float()).to(close_out.dtype)
         assert torch.equal(close_out[rows], want), "block close"
     assert chk.calls == S
