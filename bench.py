@@ -269,9 +269,10 @@ def reference_arm(args, world, rank):
     return line
 
 
-def traffic_for(kernel: str):
+def traffic_for(kernel: str, heads: int = 1):
     """dram bytes per launch from a committed ncu summary, if it matches the current source."""
-    p = os.path.join(ROOT, "profiles", "dram_traffic_longctx_T4096.json")
+    tag = "" if heads == 1 else f"_heads{heads}"
+    p = os.path.join(ROOT, "profiles", f"dram_traffic_longctx{tag}_T4096.json")
     if not os.path.exists(p):
         return None
     j = json.load(open(p))
@@ -580,7 +581,7 @@ def main(argv=None):
         "achieved_gbs_step": step_gbs, "frac_of_peak_step": step_gbs / peak,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak,
                      "peak_source": peak_kind, "unit": "GB/s", "frac": ach / peak,
-                     "traffic": traffic_for(dom)},
+                     "traffic": traffic_for(dom, args.heads)},
         "kernels": per_kernel,
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clk.summary(),
