@@ -135,6 +135,28 @@ def _aggregate_backward_no_minus_h(sources, w, gamma_key, eps_key, gamma_in, eps
     return G
 
 
+def _head_slices_interleaved(d, H):        # head k takes every H-th feature instead of a block
+    assert d % H == 0
+    return [slice(k, d, H) for k in range(H)]
+
+
+def _multihead_row_norm(sources, w, gamma_key, eps, H, weights="softmax", key_norm=True):
+    # the key RMS over the whole row instead of the head's slice
+    src = np.asarray(sources, np.float64)
+    d = src.shape[-1]
+    r = O.rms(src, eps)[..., None]
+    h = np.zeros(src.shape[1:])
+    al, zz = [], []
+    for sl in O.head_slices(d, H):
+        g = 1.0 if gamma_key is None else np.asarray(gamma_key, np.float64)[sl]
+        z = np.sum(np.asarray(w, np.float64)[sl] * g * src[..., sl] / r, axis=-1)
+        a = O.depth_softmax(z)
+        h[..., sl] = np.sum(a[..., None] * src[..., sl], axis=0)
+        al.append(a)
+        zz.append(z)
+    return h, np.stack(al), np.stack(zz)
+
+
 _ORIG_PARTITION = O.partition_stats
 _ORIG_BACKWARD = O.aggregate_backward
 _ORIG_MERGE_S = O.merge_sources_reference
@@ -163,6 +185,8 @@ MUTATIONS = {
     "merge_sources_drops_history": ("merge_sources_reference", _merge_sources_drops_history),
     "rmsnorm_backward_no_radial": ("rmsnorm_backward", _rmsnorm_backward_no_radial),
     "logit_gradient_without_h": ("aggregate_backward", _aggregate_backward_no_minus_h),
+    "heads_interleaved": ("head_slices", _head_slices_interleaved),
+    "head_key_norm_over_row": ("multihead_aggregate", _multihead_row_norm),
 }
 
 
