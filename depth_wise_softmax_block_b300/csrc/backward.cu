@@ -7,15 +7,20 @@
 // alpha = softmax(z), h = sum_i alpha_i v_i, y = gamma_in ⊙ h / r_h.
 // Backward, given g_y = dL/dy:
 //   g_h   = (gamma_in ⊙ g_y) / r_h - h (sum gamma_in g_y h) / (d r_h^3)
-//   dz_i  = alpha_i (g_h . v_i - g_h . h)
+//   dz_i  = alpha_i (g_h . v_i - g_h . h),   with g_h . h = sum_j alpha_j (g_h . v_j)
 //   dv_i  = alpha_i g_h + (dz_i / r_i) u - (dz_i z_i / (d r_i^2)) v_i
 //   du   += sum_i (dz_i / r_i) v_i          dgamma_in += g_y ⊙ h / r_h       (over tokens)
 //
-// A persistent CTA walks token rows; each thread owns the same columns of every row, so the
-// CTA's partial sums of du and dgamma_in accumulate in shared memory without conflicts and are
-// added to the outputs with one atomic per element at the end.  Per row, four passes over the
-// n source rows (the first from HBM, the others from L1, where a row's sources fit): logits,
-// h and the norm, the logit gradients, the outputs.
+// Persistent CTAs (two per SM) walk token rows.  Per row, four passes over the row's sources
+// (the first from HBM, the others mostly from L1/L2):
+//   A  one warp per source: its sum of squares and u . v_i (warp reductions), so r_i and z_i;
+//   B  one thread per column (the same columns for every row): h, the input norm (one CTA
+//      reduction of two values) and g_h, which goes to shared memory;
+//   C  one warp per source: g_h . v_i;
+//   D  one thread per column: dv_i for every source and the row's du contribution, summed over
+//      the sources in registers and added to the CTA's du partial sums.
+// The partial sums of du and dgamma_in live in shared memory with column (v, e) at e * nv + v,
+// so the threads of a warp touch consecutive words; one atomic per element at the end.
 #include <math.h>
 
 #include <algorithm>
@@ -27,90 +32,136 @@ namespace attnres {
 namespace {
 
 constexpr int kBwdThreads = 256;
+constexpr int kBwdWarps = kBwdThreads / 32;
+constexpr int kBatch = 4;  // 16-byte vectors per lane in flight in the per-source passes
+
+// Warp-wide sums over one source row: sum of squares and dot product with a second vector,
+// `other(v, f)` filling the 8 (bf16) or 4 (fp32) floats of the second vector at vector v.
+template <typename T, typename Other>
+__device__ __forceinline__ void row_dots(const T* p, int nv, int lane, Other other, float& ss,
+                                         float& dot) {
+  constexpr int VE = Vec<T>::N;
+  ss = 0.f;
+  dot = 0.f;
+  for (int v0 = lane; v0 < nv; v0 += 32 * kBatch) {
+    uint4 raw[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int v = v0 + 32 * b;
+      raw[b] = v < nv ? __ldg(reinterpret_cast<const uint4*>(p + v * VE)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int v = v0 + 32 * b;
+      if (v < nv) {
+        float x[VE], o[VE];
+        unpack(raw[b], x);
+        other(v, o);
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          ss = fmaf(x[e], x[e], ss);
+          dot = fmaf(o[e], x[e], dot);
+        }
+      }
+    }
+  }
+  ss = warp_sum(ss);
+  dot = warp_sum(dot);
+}
 
 template <typename T, int VPT>
-__global__ void __launch_bounds__(kBwdThreads, 1) backward_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kBwdThreads, 2) backward_kernel(const BwdArgs a) {
   constexpr int VE = Vec<T>::N;
   constexpr int NM = kBwdMaxSources;
-  extern __shared__ float acc_s[];  // [2][d]: this CTA's du and dgamma_in partial sums
-  __shared__ float scratch[2 * NM * 33];
-  const int nv = a.d / VE, n = a.n, d = a.d;
+  extern __shared__ float sm[];
+  const int d = a.d, nv = d / VE, n = a.n;
+  float* acc_du = sm;         // [VE][nv]: this CTA's du partial sums
+  float* acc_dg = sm + d;     // [VE][nv]: its dgamma_in partial sums
+  float* ghs = sm + 2 * d;    // [nv][VE]: g_h of the current row
+  __shared__ float st_r[NM], st_z[NM], st_pq[NM];  // per source: r_i, z_i, g_h . v_i
+  __shared__ float cf_u[NM], cf_v[NM];             // per source: dz_i / r_i, dz_i z_i / (d r_i^2)
+  __shared__ float scratch[66];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float fd = static_cast<float>(d);
-  for (int i = threadIdx.x; i < 2 * d; i += blockDim.x) acc_s[i] = 0.f;
+  for (int i = tid; i < 2 * d; i += blockDim.x) sm[i] = 0.f;
   __syncthreads();
 
-  // Cached loads: the four passes over a row's sources re-read them from L1.
-  auto load = [&](const void* p, int64_t base, int v, float (&x)[VE]) {
-    unpack(__ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p) + base + v * VE)), x);
+  const float4* u4 = reinterpret_cast<const float4*>(a.u);
+  const float4* g4 = reinterpret_cast<const float4*>(a.gamma_in);  // may be null
+  auto load = [&](const void* p, int64_t off, float (&x)[VE]) {
+    unpack(__ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p) + off)), x);
+  };
+  auto load4s = [&](const float4* p, int v, float (&f)[VE]) {  // VE floats of a float4 array
+#pragma unroll
+    for (int e = 0; e < VE; e += 4) {
+      const float4 q = __ldg(p + (v * VE + e) / 4);
+      f[e] = q.x;
+      f[e + 1] = q.y;
+      f[e + 2] = q.z;
+      f[e + 3] = q.w;
+    }
   };
 
   for (int64_t row = blockIdx.x; row < a.T; row += gridDim.x) {
     const int64_t base = row * d;
-    // ---- pass A: sums of squares and logit numerators of every source ----
-    float part[2 * NM];
-#pragma unroll
-    for (int j = 0; j < 2 * NM; ++j) part[j] = 0.f;
-#pragma unroll
-    for (int j = 0; j < NM; ++j) {
-      if (j < n) {
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-          const int v = threadIdx.x + k * blockDim.x;
-          if (v < nv) {
-            float x[VE];
-            load(a.srcs[j], base, v, x);
-            const float* up = a.u + v * VE;
-#pragma unroll
-            for (int e = 0; e < VE; ++e) {
-              part[2 * j] = fmaf(x[e], x[e], part[2 * j]);
-              part[2 * j + 1] = fmaf(__ldg(up + e), x[e], part[2 * j + 1]);
-            }
-          }
-        }
+    // ---- pass A: r_i and z_i, one warp per source ----
+    for (int j = warp; j < n; j += kBwdWarps) {
+      float ss, dot;
+      row_dots<T>(static_cast<const T*>(a.srcs[j]) + base, nv, lane,
+                  [&](int v, float (&f)[VE]) { load4s(u4, v, f); }, ss, dot);
+      if (lane == 0) {
+        const float r = sqrtf(ss / fd + a.eps_key);
+        st_r[j] = r;
+        st_z[j] = dot / r;
       }
     }
-    block_sum_n<2 * NM>(part, scratch);
-    float r[NM], z[NM], al[NM];
-    float m = -INFINITY;
+    __syncthreads();
+    float al[NM];
+    {
+      float m = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < NM; ++j) {
-      r[j] = sqrtf(part[2 * j] / fd + a.eps_key);
-      z[j] = j < n ? part[2 * j + 1] / r[j] : -INFINITY;
-      m = fmaxf(m, z[j]);
+      for (int j = 0; j < NM; ++j)
+        if (j < n) m = fmaxf(m, st_z[j]);
+      float l = 0.f;
+#pragma unroll
+      for (int j = 0; j < NM; ++j) {
+        al[j] = j < n ? expf(st_z[j] - m) : 0.f;
+        l += al[j];
+      }
+      const float rl = 1.f / l;
+#pragma unroll
+      for (int j = 0; j < NM; ++j) al[j] *= rl;
     }
-    float l = 0.f;
-#pragma unroll
-    for (int j = 0; j < NM; ++j) {
-      al[j] = j < n ? expf(z[j] - m) : 0.f;
-      l += al[j];
-    }
-#pragma unroll
-    for (int j = 0; j < NM; ++j) al[j] /= l;
 
-    // ---- pass B: h, the input norm and its input gradient g_h ----
+    // ---- pass B: h, the input norm and g_h, one thread per column ----
     float h[VPT][VE], gh[VPT][VE];
     float ssh = 0.f, s1 = 0.f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
-      const int v = threadIdx.x + k * blockDim.x;
+      const int v = tid + k * blockDim.x;
 #pragma unroll
-      for (int e = 0; e < VE; ++e) h[k][e] = 0.f;
+      for (int e = 0; e < VE; ++e) h[k][e] = gh[k][e] = 0.f;
       if (v < nv) {
 #pragma unroll
         for (int j = 0; j < NM; ++j) {
           if (j < n) {
             float x[VE];
-            load(a.srcs[j], base, v, x);
+            load(a.srcs[j], base + v * VE, x);
 #pragma unroll
             for (int e = 0; e < VE; ++e) h[k][e] = fmaf(al[j], x[e], h[k][e]);
           }
         }
-        float g[VE];
-        load(a.g_y, base, v, g);
+        float g[VE], gi[VE];
+        load(a.g_y, base + v * VE, g);
+        if (g4) {
+          load4s(g4, v, gi);
+        } else {
+#pragma unroll
+          for (int e = 0; e < VE; ++e) gi[e] = 1.f;
+        }
 #pragma unroll
         for (int e = 0; e < VE; ++e) {
-          const float gi = a.gamma_in ? __ldg(a.gamma_in + v * VE + e) : 1.f;
-          gh[k][e] = gi * g[e];  // gamma_in ⊙ g_y for now
+          gh[k][e] = gi[e] * g[e];  // gamma_in ⊙ g_y for now
           ssh = fmaf(h[k][e], h[k][e], ssh);
           s1 = fmaf(gh[k][e], h[k][e], s1);
         }
@@ -119,95 +170,117 @@ __global__ void __launch_bounds__(kBwdThreads, 1) backward_kernel(const BwdArgs 
     block_sum2(ssh, s1, scratch);
     const float rh = sqrtf(ssh / fd + a.eps_in);
     const float c1 = 1.f / rh, c2 = s1 / (fd * rh * rh * rh);
-    float pq[NM + 1];
-#pragma unroll
-    for (int j = 0; j <= NM; ++j) pq[j] = 0.f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
-      const int v = threadIdx.x + k * blockDim.x;
+      const int v = tid + k * blockDim.x;
       if (v < nv) {
         float g[VE];
-        load(a.g_y, base, v, g);
+        load(a.g_y, base + v * VE, g);
 #pragma unroll
         for (int e = 0; e < VE; ++e) {
-          acc_s[d + v * VE + e] += g[e] * h[k][e] * c1;  // dgamma_in
+          acc_dg[e * nv + v] = fmaf(g[e] * h[k][e], c1, acc_dg[e * nv + v]);
           gh[k][e] = gh[k][e] * c1 - h[k][e] * c2;
-          pq[NM] = fmaf(gh[k][e], h[k][e], pq[NM]);
         }
+        float4* gs = reinterpret_cast<float4*>(ghs + v * VE);
+#pragma unroll
+        for (int e = 0; e < VE; e += 4)
+          gs[e / 4] = make_float4(gh[k][e], gh[k][e + 1], gh[k][e + 2], gh[k][e + 3]);
       }
     }
+    __syncthreads();
 
-    // ---- pass C: g_h . v_i for the logit gradients ----
+    // ---- pass C: g_h . v_i, one warp per source ----
+    for (int j = warp; j < n; j += kBwdWarps) {
+      float ss, dot;
+      row_dots<T>(static_cast<const T*>(a.srcs[j]) + base, nv, lane,
+                  [&](int v, float (&f)[VE]) {
+                    const float4* gs = reinterpret_cast<const float4*>(ghs + v * VE);
 #pragma unroll
-    for (int j = 0; j < NM; ++j) {
-      if (j < n) {
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-          const int v = threadIdx.x + k * blockDim.x;
-          if (v < nv) {
-            float x[VE];
-            load(a.srcs[j], base, v, x);
-#pragma unroll
-            for (int e = 0; e < VE; ++e) pq[j] = fmaf(gh[k][e], x[e], pq[j]);
-          }
-        }
-      }
+                    for (int e = 0; e < VE; e += 4) {
+                      const float4 q = gs[e / 4];
+                      f[e] = q.x;
+                      f[e + 1] = q.y;
+                      f[e + 2] = q.z;
+                      f[e + 3] = q.w;
+                    }
+                  },
+                  ss, dot);
+      if (lane == 0) st_pq[j] = dot;
     }
-    block_sum_n<NM + 1>(pq, scratch);
+    __syncthreads();
+    if (tid < n) {  // coefficients of dv_i; g_h . h = sum_j alpha_j (g_h . v_j)
+      float ghh = 0.f;
+#pragma unroll
+      for (int j = 0; j < NM; ++j)
+        if (j < n) ghh = fmaf(al[j], st_pq[j], ghh);
+      const int j = tid;
+      const float r = st_r[j], z = st_z[j];
+      float aj = 0.f;
+#pragma unroll
+      for (int i = 0; i < NM; ++i)
+        if (i == j) aj = al[i];
+      const float dz = aj * (st_pq[j] - ghh);
+      cf_u[j] = dz / r;
+      cf_v[j] = dz * z / (fd * r * r);
+    }
+    __syncthreads();
 
-    // ---- pass D: source gradients and the du partial sums ----
+    // ---- pass D: dv_i and du, one thread per column ----
 #pragma unroll
-    for (int j = 0; j < NM; ++j) {
-      if (j < n) {
-        const float dz = al[j] * (pq[j] - pq[NM]);
-        const float cu = dz / r[j];
-        const float cv = dz * z[j] / (fd * r[j] * r[j]);
+    for (int k = 0; k < VPT; ++k) {
+      const int v = tid + k * blockDim.x;
+      if (v < nv) {
+        float uu[VE], dacc[VE];
+        load4s(u4, v, uu);
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-          const int v = threadIdx.x + k * blockDim.x;
-          if (v < nv) {
+        for (int e = 0; e < VE; ++e) dacc[e] = 0.f;
+#pragma unroll
+        for (int j = 0; j < NM; ++j) {
+          if (j < n) {
             float x[VE], o[VE];
-            load(a.srcs[j], base, v, x);
+            load(a.srcs[j], base + v * VE, x);
+            const float cu = cf_u[j], cv = cf_v[j];
 #pragma unroll
             for (int e = 0; e < VE; ++e) {
-              const float uu = __ldg(a.u + v * VE + e);
-              o[e] = fmaf(al[j], gh[k][e], fmaf(cu, uu, -cv * x[e]));
-              acc_s[v * VE + e] = fmaf(cu, x[e], acc_s[v * VE + e]);
+              o[e] = fmaf(al[j], gh[k][e], fmaf(cu, uu[e], -cv * x[e]));
+              dacc[e] = fmaf(cu, x[e], dacc[e]);
             }
             st_global(static_cast<T*>(a.dsrcs[j]) + base + v * VE, pack(o));
           }
         }
+#pragma unroll
+        for (int e = 0; e < VE; ++e) acc_du[e * nv + v] += dacc[e];
       }
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    atomicAdd(a.du + i, acc_s[i]);
-    if (a.dgamma_in != nullptr) atomicAdd(a.dgamma_in + i, acc_s[d + i]);
+  for (int c = tid; c < d; c += blockDim.x) {
+    const int v = c / VE, e = c - v * VE;
+    atomicAdd(a.du + c, acc_du[e * nv + v]);
+    if (a.dgamma_in != nullptr) atomicAdd(a.dgamma_in + c, acc_dg[e * nv + v]);
   }
 }
 
 template <typename T>
 cudaError_t backward_io(const BwdArgs& a, cudaStream_t s) {
   const int nv = a.d / Vec<T>::N;
-  int vpt = 1;
-  while ((nv + vpt - 1) / vpt > kBwdThreads) vpt *= 2;
-  const int threads = ((nv + vpt - 1) / vpt + 31) / 32 * 32;
+  const int vpt = (nv + kBwdThreads - 1) / kBwdThreads;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(a.T, sms));
-  const int smem = 2 * a.d * static_cast<int>(sizeof(float));
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(a.T, 2 * sms));
+  const int smem = 3 * a.d * static_cast<int>(sizeof(float));
   auto launch = [&](auto kern) -> cudaError_t {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (r != cudaSuccess) return r;
-    kern<<<grid, threads, smem, s>>>(a);
+    kern<<<grid, kBwdThreads, smem, s>>>(a);
     return cudaGetLastError();
   };
   switch (vpt) {
     case 1: return launch(backward_kernel<T, 1>);
     case 2: return launch(backward_kernel<T, 2>);
+    case 3: return launch(backward_kernel<T, 3>);
     case 4: return launch(backward_kernel<T, 4>);
     default: return cudaErrorInvalidValue;
   }
