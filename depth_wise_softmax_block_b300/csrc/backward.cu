@@ -13,10 +13,11 @@
 //
 // Persistent CTAs (two per SM) walk token rows.  Per row, four passes over the row's sources
 // (the first from HBM, the others mostly from L1/L2):
-//   A  one warp per source: its sum of squares and u . v_i (warp reductions), so r_i and z_i;
+//   A  one warp per quarter of a source row: its sum of squares and u . v_i (warp reductions),
+//      the quarters added in shared memory, so r_i and z_i;
 //   B  one thread per column (the same columns for every row): h, the input norm (one CTA
 //      reduction of two values) and g_h, which goes to shared memory;
-//   C  one warp per source: g_h . v_i;
+//   C  one warp per quarter of a source row: g_h . v_i;
 //   D  one thread per column: dv_i for every source and the row's du contribution, summed over
 //      the sources in registers and added to the CTA's du partial sums.
 // The partial sums of du and dgamma_in live in shared memory with column (v, e) at e * nv + v,
@@ -33,7 +34,8 @@ namespace {
 
 constexpr int kBwdThreads = 256;
 constexpr int kBwdWarps = kBwdThreads / 32;
-constexpr int kBatch = 4;  // 16-byte vectors per lane in flight in the per-source passes
+constexpr int kBatch = 8;  // 16-byte vectors per lane in flight in the per-source passes
+constexpr int kParts = 4;  // a source row is split into this many column ranges, one warp each
 
 // Warp-wide sums over one source row: sum of squares and dot product with a second vector,
 // `other(v, f)` filling the 8 (bf16) or 4 (fp32) floats of the second vector at vector v.
@@ -80,6 +82,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2) backward_kernel(const BwdArgs 
   float* ghs = sm + 2 * d;    // [nv][VE]: g_h of the current row
   __shared__ float st_r[NM], st_z[NM], st_pq[NM];  // per source: r_i, z_i, g_h . v_i
   __shared__ float cf_u[NM], cf_v[NM];             // per source: dz_i / r_i, dz_i z_i / (d r_i^2)
+  __shared__ float st_hs[kParts * NM], st_hd[kParts * NM];  // per row part: sum of squares, dot
   __shared__ float scratch[66];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float fd = static_cast<float>(d);
@@ -104,16 +107,29 @@ __global__ void __launch_bounds__(kBwdThreads, 2) backward_kernel(const BwdArgs 
 
   for (int64_t row = blockIdx.x; row < a.T; row += gridDim.x) {
     const int64_t base = row * d;
-    // ---- pass A: r_i and z_i, one warp per source ----
-    for (int j = warp; j < n; j += kBwdWarps) {
+    // ---- pass A: r_i and z_i, one warp per quarter of a source row ----
+    for (int t = warp; t < kParts * n; t += kBwdWarps) {
+      const int j = t / kParts, q = t - j * kParts;
+      const int vb = q * nv / kParts, vc = (q + 1) * nv / kParts - vb;
       float ss, dot;
-      row_dots<T>(static_cast<const T*>(a.srcs[j]) + base, nv, lane,
-                  [&](int v, float (&f)[VE]) { load4s(u4, v, f); }, ss, dot);
+      row_dots<T>(static_cast<const T*>(a.srcs[j]) + base + vb * VE, vc, lane,
+                  [&](int v, float (&f)[VE]) { load4s(u4, v + vb, f); }, ss, dot);
       if (lane == 0) {
-        const float r = sqrtf(ss / fd + a.eps_key);
-        st_r[j] = r;
-        st_z[j] = dot / r;
+        st_hs[t] = ss;
+        st_hd[t] = dot;
       }
+    }
+    __syncthreads();
+    if (tid < n) {
+      float ss = 0.f, dot = 0.f;
+#pragma unroll
+      for (int q = 0; q < kParts; ++q) {
+        ss += st_hs[kParts * tid + q];
+        dot += st_hd[kParts * tid + q];
+      }
+      const float r = sqrtf(ss / fd + a.eps_key);
+      st_r[tid] = r;
+      st_z[tid] = dot / r;
     }
     __syncthreads();
     float al[NM];
@@ -189,12 +205,14 @@ __global__ void __launch_bounds__(kBwdThreads, 2) backward_kernel(const BwdArgs 
     }
     __syncthreads();
 
-    // ---- pass C: g_h . v_i, one warp per source ----
-    for (int j = warp; j < n; j += kBwdWarps) {
+    // ---- pass C: g_h . v_i, one warp per quarter of a source row ----
+    for (int t = warp; t < kParts * n; t += kBwdWarps) {
+      const int j = t / kParts, q = t - j * kParts;
+      const int vb = q * nv / kParts, vc = (q + 1) * nv / kParts - vb;
       float ss, dot;
-      row_dots<T>(static_cast<const T*>(a.srcs[j]) + base, nv, lane,
+      row_dots<T>(static_cast<const T*>(a.srcs[j]) + base + vb * VE, vc, lane,
                   [&](int v, float (&f)[VE]) {
-                    const float4* gs = reinterpret_cast<const float4*>(ghs + v * VE);
+                    const float4* gs = reinterpret_cast<const float4*>(ghs + (v + vb) * VE);
 #pragma unroll
                     for (int e = 0; e < VE; e += 4) {
                       const float4 q = gs[e / 4];
@@ -205,7 +223,14 @@ __global__ void __launch_bounds__(kBwdThreads, 2) backward_kernel(const BwdArgs 
                     }
                   },
                   ss, dot);
-      if (lane == 0) st_pq[j] = dot;
+      if (lane == 0) st_hd[t] = dot;
+    }
+    __syncthreads();
+    if (tid < n) {
+      float dot = 0.f;
+#pragma unroll
+      for (int q = 0; q < kParts; ++q) dot += st_hd[kParts * tid + q];
+      st_pq[tid] = dot;
     }
     __syncthreads();
     if (tid < n) {  // coefficients of dv_i; g_h . h = sum_j alpha_j (g_h . v_j)
