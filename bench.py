@@ -476,6 +476,118 @@ def run_backward(args):
     return 0
 
 
+def decode_walk_bytes(wl: I.Workload) -> int:
+    """Algorithmic bytes of one decode-shaped depth walk: every block's phase 1 over the
+    sources before it, its phase-2 calls and close, then the final aggregation."""
+    d, E, T, S, L = wl.d, 2, wl.T, wl.S, wl.L
+    total = 0
+    for n in range(1, wl.n_blocks + 1):
+        Sn = min(S, L - (n - 1) * S)
+        b = C.block_step_bytes(n, Sn, d, E, 0)
+        total += b.phase1 + b.phase2 + b.close
+    total += C.phase1_bytes(wl.n_blocks + 1, 1, d, E, with_lse=False)
+    return total * T
+
+
+def run_decode(args):
+    """Decode-shaped Block AttnRes: 256 tokens (one per sequence), d = 7168, the 186-sublayer
+    depth walk in blocks of 24 (phase 1, the phase-2 calls and the close per block, then the
+    final aggregation): 203 launches of a few MB each.  Timed eager (each call launched from
+    Python through the C ABI) and as one CUDA graph of the same calls, captured once and
+    replayed.  Prints one JSON line; ``value`` is tokens/s of the graph replay."""
+    from depth_wise_softmax_block_b300 import attnres_query_prep, build as B
+    from depth_wise_softmax_block_b300.schedule import BlockRunner, KernelTimer, final_aggregation
+    B.build()
+    dev = torch.device("cuda", 0)
+    wl = I.DECODE_BF16
+    T, d, S, L, N = wl.T, wl.d, wl.S, wl.L, wl.n_blocks
+    reps = I.make_reps(wl, N + 1, dev)           # slot 0 = b_0; slot n receives block n
+    P = I.block_params(wl, dev)
+    U = torch.empty_like(P.W)
+    Us = torch.empty((2 * L, d), dtype=torch.bfloat16, device=dev)
+    uf = torch.empty((1, d), device=dev)
+    attnres_query_prep(P.W, P.G_key, U, Us)
+    attnres_query_prep(P.w_final.view(1, -1), P.g_final.view(1, -1), uf)
+    vbuf = I.make_outputs(wl, 1, S, dev)        # stand-ins for f_i, shared by the blocks
+    runner = BlockRunner(T, d, S, torch.bfloat16, dev)
+    fin = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+
+    timer = None
+
+    def walk():
+        for n in range(1, N + 1):
+            l0 = (n - 1) * S
+            Sn = min(S, L - l0)
+            runner.run_block(reps[:n], U[l0:l0 + Sn], P.G_in[l0:l0 + Sn],
+                             lambda i, y: vbuf[i - 1], reps[n], wl.eps, wl.eps,
+                             U_split=Us[2 * l0:2 * (l0 + Sn)])
+        final_aggregation(reps[:N + 1], uf[0], fin, wl.eps, timer=timer)
+
+    def timed(fn, k):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(k):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / k
+
+    for _ in range(args.warmup):
+        walk()
+    torch.cuda.synchronize()
+    eager_ms = timed(walk, args.steps)
+    # per-kernel device times: one more eager walk with CUDA events around every launch
+    timer = KernelTimer()
+    runner.timer = timer
+    walk()
+    torch.cuda.synchronize()
+    per_kernel = {k: {"launches": c, "total_us": t * 1e3, "avg_us": t * 1e3 / c}
+                  for k, (t, c) in timer.totals_ms().items()}
+    runner.timer = None
+    timer = None
+    graph_ms, graph_err = None, None
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            walk()                                # warm the side stream before capture
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            walk()
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        graph_ms = timed(g.replay, args.steps)
+    except Exception as e:  # noqa: BLE001 - reported in the JSON line
+        graph_err = f"{type(e).__name__}: {e}"
+    from depth_wise_softmax_block_b300 import attnres_poll_device_errors
+    attnres_poll_device_errors()
+    byt = decode_walk_bytes(wl)
+    launches = 2 * N + L + 1
+    peak, kind = peaks()
+    best = graph_ms if graph_ms is not None else eager_ms
+    line = {"metric": "Decode-shaped Block AttnRes: tokens/s of the whole 186-sublayer depth walk "
+                      "(256 tokens), 1 GPU",
+            "value": T / (best / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": best, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "tokens": T, "d": d, "sublayers": L, "S": S,
+                       "blocks": N, "launch": "cuda_graph" if graph_ms is not None else "eager"},
+            "eager_ms": eager_ms, "graph_ms": graph_ms,
+            "us_per_sublayer": {"eager": eager_ms * 1e3 / L,
+                                "graph": None if graph_ms is None else graph_ms * 1e3 / L},
+            "bytes_per_step": byt, "achieved_gbs": byt / (best / 1e3) / 1e9,
+            "frac_of_peak": byt / (best / 1e3) / 1e9 / peak, "peak_gbs": peak,
+            "peak_source": kind, "gpu_launches": launches * args.steps,
+            "kernels_eager_one_walk": per_kernel}
+    if graph_err:
+        line["graph_error"] = graph_err
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -492,9 +604,10 @@ def main(argv=None):
                     help="override the token count (profiling a smaller case)")
     ap.add_argument("--chunk", type=int, default=0, help="override the chunk size")
     ap.add_argument("--workload", default="longctx",
-                    choices=["longctx", "full_grouped", "backward"],
+                    choices=["longctx", "full_grouped", "backward", "decode"],
                     help="full_grouped: the Full AttnRes depth, grouped two-phase vs direct; "
-                         "backward: one sublayer's aggregation backward")
+                         "backward: one sublayer's aggregation backward; decode: the "
+                         "256-token depth walk, eager and as a CUDA graph")
     ap.add_argument("--group", type=int, default=8, help="group size of --workload full_grouped")
     ap.add_argument("--heads", type=int, default=1,
                     help="depth-attention heads of the longctx step (Table 4 multi-head: 16)")
@@ -505,6 +618,8 @@ def main(argv=None):
         return run_full_grouped(args)
     if args.workload == "backward" and args.impl == "ours":
         return run_backward(args)
+    if args.workload == "decode" and args.impl == "ours":
+        return run_decode(args)
     if args.impl == "reference":
         line = reference_arm(args, world, rank)
         if line is not None:

@@ -193,3 +193,54 @@ def test_longctx_prefill_bench_step_sampled(dev):
     torch.cuda.synchronize()
     assert torch.equal(st.out, ref)
     print("max |err|/RMS over calls:", max(report.values()))
+
+
+def test_depth_walk_cuda_graph_replay_matches_eager(dev):
+    """The block schedule captured as one CUDA graph (the library launches on the caller's
+    stream and allocates nothing) replays bit for bit what the eager walk computes: 256 tokens,
+    two blocks of 24 sublayers, bf16, tensor-core phase 1."""
+    T, d, S, L = 256, 1024, 24, 48
+    N = L // S
+    reps = torch.empty((N + 1, T, d), dtype=torch.bfloat16, device=dev)
+    for j in range(N + 1):
+        I.fill_block_rep(reps[j], j, 77)
+    W = I.queries(L, d, 77, "w", dev)
+    G = I.gains(L, d, 0.02, 77, "g", dev)
+    Gi = I.gains(L, d, 0.02, 77, "gi", dev)
+    U = torch.empty_like(W)
+    Us = torch.empty((2 * L, d), dtype=torch.bfloat16, device=dev)
+    ar.attnres_query_prep(W, G, U, Us)
+    vbuf = torch.stack([I.normal((T, d), 1.0, 77, f"v{i}", dev, torch.bfloat16) for i in range(S)])
+    runner = BlockRunner(T, d, S, torch.bfloat16, dev, keep_y=True)
+    fin = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+
+    def walk():
+        for n in range(1, N + 1):
+            l0 = (n - 1) * S
+            runner.run_block(reps[:n], U[l0:l0 + S], Gi[l0:l0 + S], lambda i, y: vbuf[i - 1],
+                             reps[n], U_split=Us[2 * l0:2 * (l0 + S)])
+        final_aggregation(reps[:N + 1], U[0], fin)
+
+    walk()
+    torch.cuda.synchronize()
+    eager = (fin.clone(), runner.y.clone(), reps.clone())
+    fin.zero_()
+    runner.y.zero_()
+    reps[1:].zero_()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        walk()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        walk()
+    fin.zero_()
+    runner.y.zero_()
+    reps[1:].zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(fin, eager[0]), "final aggregation differs under graph replay"
+    assert torch.equal(runner.y, eager[1]), "sublayer inputs differ under graph replay"
+    assert torch.equal(reps, eager[2]), "block closes differ under graph replay"
