@@ -41,12 +41,25 @@ METRIC = "AttnRes tokens/s per block and achieved HBM GB/s (% of B300 peak), 1 G
 CSRC = os.path.join(ROOT, "depth_wise_softmax_block_b300", "csrc")
 
 
-def csrc_hash() -> str:
+def csrc_hash(files=None) -> str:
+    """Hash of the kernel sources (all of them, or the named files of csrc/)."""
     h = hashlib.sha256()
-    for f in sorted(os.listdir(CSRC)):
+    for f in sorted(files if files is not None else os.listdir(CSRC)):
         h.update(f.encode())
         h.update(open(os.path.join(CSRC, f), "rb").read())
     return h.hexdigest()[:16]
+
+
+# The source files that make up each kernel kind of the step (for matching a committed ncu
+# capture to the code it measured).
+KERNEL_SOURCES = {
+    "phase1": ["phase1_tc.cu", "tc.cuh", "tma.cuh", "tmap.cu", "common.cuh", "kernels.h"],
+    "rowwise": ["rowwise.cu", "common.cuh", "kernels.h"],
+}
+
+
+def kernel_hash(kind: str) -> str:
+    return csrc_hash(KERNEL_SOURCES["phase1" if kind == "phase1" else "rowwise"])
 
 
 def peaks():
@@ -277,7 +290,7 @@ def traffic_for(kernel: str, heads: int = 1):
         return None
     j = json.load(open(p))
     e = j.get(kernel)
-    if not e or e.get("csrc_hash") != csrc_hash():
+    if not e or e.get("src_hash") != kernel_hash(kernel):
         return None
     return e.get("bytes_per_launch")
 
