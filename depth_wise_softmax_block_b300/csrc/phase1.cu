@@ -165,6 +165,7 @@ phase1_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ 
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_enter();  // the prologue above touches no global memory
 
   // The ring runs 2 * nch iterations: sweep 1 (sources + queries), then sweep 2 (sources).
   // Thread 0 issues the copies: the first ST iterations up front, then, at every iteration,
@@ -422,8 +423,7 @@ cudaError_t launch_t(const Phase1Args& a, const P1Plan& pl, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int64_t blocks = (a.T + pl.TT - 1) / pl.TT;
   const dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(a.heads));
-  kern<<<grid, kThreads, pl.smem, s>>>(mb, mu, a, pl);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, kThreads, pl.smem, s, mb, mu, a, pl);
 }
 
 template <typename T>

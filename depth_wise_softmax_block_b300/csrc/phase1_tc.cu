@@ -191,6 +191,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_enter();  // the prologue above touches no global memory
 
   // ------------------------------ copy-issuing warp ------------------------------
   if (warp == kWarps) {
@@ -522,8 +523,7 @@ cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int64_t blocks = (a.T + kTT - 1) / kTT;
   const dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(pl.windows));
-  kern<<<grid, kThreads, pl.smem, s>>>(mb, mq, a, pl);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, kThreads, pl.smem, s, mb, mq, a, pl);
 }
 
 unsigned int phase1_tc_poll_timeouts() {

@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(kMergeThreads) phase2_kernel(const Phase2Args 
   constexpr int VE = Vec<T>::N;
   __shared__ float scratch[66];
   extern __shared__ float red[];  // kHeads: [2 * nv + 2 * H]
+  pdl_enter();
   const int64_t row = blockIdx.x;
   const int nv = a.d / VE;
   const int64_t base = row * a.d;
@@ -251,6 +252,7 @@ __global__ void __launch_bounds__(kRowThreads) full_kernel(const FullArgs a) {
   __shared__ float scratch[66];
   __shared__ float zs[kHeads ? 1 : kMaxSources];
   extern __shared__ float dyn[];
+  pdl_enter();
   const int64_t row = blockIdx.x;
   const int nv = a.d / VE;
   const int H = kHeads ? a.heads : 1;
@@ -477,6 +479,7 @@ __global__ void __launch_bounds__(kHeadWarpsMax * 32, heads_min_blocks<VH>())
     phase2_heads_kernel(const Phase2Args a) {
   constexpr int VE = Vec<T>::N;
   __shared__ float scratch[66];
+  pdl_enter();
   const int64_t row = blockIdx.x;
   const int hd = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvh = a.d / VE / a.heads;
@@ -592,6 +595,7 @@ __global__ void __launch_bounds__(kHeadWarpsMax * 32, VH <= 2 ? 2 : 1)
   __shared__ float scratch[66];
   __shared__ float zsh[kMaxSources * kHeadWarpsMax];  // [source][head] logits
   __shared__ float hl[kHeadWarpsMax];                 // per-head log-sum-exp
+  pdl_enter();
   const int64_t row = blockIdx.x;
   const int H = a.heads;
   const int hd = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -756,6 +760,7 @@ template <typename T>
 __global__ void add_kernel(const T* __restrict__ pa, const T* __restrict__ pb, T* out,
                            int64_t nvec) {
   constexpr int VE = Vec<T>::N;
+  pdl_enter();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nvec;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float x[VE], y[VE];
@@ -771,6 +776,7 @@ __global__ void add_kernel(const T* __restrict__ pa, const T* __restrict__ pb, T
 // hi = bf16(u), lo = bf16(u - hi), both rounded to nearest even.
 __global__ void prep_kernel(const float* w, const float* g, float* u, uint16_t* split, int d,
                             int64_t n4) {
+  pdl_enter();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float4 x = reinterpret_cast<const float4*>(w)[i];
@@ -807,12 +813,11 @@ cudaError_t phase2_heads(const Phase2Args& a, int vh, cudaStream_t s) {
   const unsigned grid = static_cast<unsigned>(a.T);
   const int threads = 32 * a.heads;
   switch (vh) {
-    case 1: phase2_heads_kernel<T, 1><<<grid, threads, 0, s>>>(a); break;
-    case 2: phase2_heads_kernel<T, 2><<<grid, threads, 0, s>>>(a); break;
-    case 4: phase2_heads_kernel<T, 4><<<grid, threads, 0, s>>>(a); break;
+    case 1: return launch_pdl(phase2_heads_kernel<T, 1>, grid, threads, 0, s, a);
+    case 2: return launch_pdl(phase2_heads_kernel<T, 2>, grid, threads, 0, s, a);
+    case 4: return launch_pdl(phase2_heads_kernel<T, 4>, grid, threads, 0, s, a);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 template <typename T>
@@ -820,23 +825,18 @@ cudaError_t full_heads(const FullArgs& a, int vh, cudaStream_t s) {
   const unsigned grid = static_cast<unsigned>(a.T);
   const int threads = 32 * a.heads;
   switch (vh) {
-    case 1: full_heads_kernel<T, 1><<<grid, threads, 0, s>>>(a); break;
-    case 2: full_heads_kernel<T, 2><<<grid, threads, 0, s>>>(a); break;
-    case 4: full_heads_kernel<T, 4><<<grid, threads, 0, s>>>(a); break;
+    case 1: return launch_pdl(full_heads_kernel<T, 1>, grid, threads, 0, s, a);
+    case 2: return launch_pdl(full_heads_kernel<T, 2>, grid, threads, 0, s, a);
+    case 4: return launch_pdl(full_heads_kernel<T, 4>, grid, threads, 0, s, a);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 template <typename T, int VPT>
 cudaError_t phase2_vpt(const Phase2Args& a, unsigned grid, int threads, cudaStream_t s) {
-  if (a.heads == 1) {
-    phase2_kernel<T, VPT, false><<<grid, threads, 0, s>>>(a);
-  } else {
-    const int smem = (2 * (a.d / Vec<T>::N) + 2 * a.heads) * static_cast<int>(sizeof(float));
-    phase2_kernel<T, VPT, true><<<grid, threads, smem, s>>>(a);
-  }
-  return cudaGetLastError();
+  if (a.heads == 1) return launch_pdl(phase2_kernel<T, VPT, false>, grid, threads, 0, s, a);
+  const int smem = (2 * (a.d / Vec<T>::N) + 2 * a.heads) * static_cast<int>(sizeof(float));
+  return launch_pdl(phase2_kernel<T, VPT, true>, grid, threads, smem, s, a);
 }
 
 template <typename T>
@@ -858,15 +858,11 @@ cudaError_t phase2_io(const Phase2Args& a, cudaStream_t s) {
 
 template <typename T, int VPT>
 cudaError_t full_vpt(const FullArgs& a, unsigned grid, int threads, cudaStream_t s) {
-  if (a.heads == 1) {
-    full_kernel<T, VPT, false><<<grid, threads, 0, s>>>(a);
-  } else {
-    const int H = a.heads;
-    const int smem =
-        (2 * (a.d / Vec<T>::N) + 2 * H + a.n * H + H) * static_cast<int>(sizeof(float));
-    full_kernel<T, VPT, true><<<grid, threads, smem, s>>>(a);
-  }
-  return cudaGetLastError();
+  if (a.heads == 1) return launch_pdl(full_kernel<T, VPT, false>, grid, threads, 0, s, a);
+  const int H = a.heads;
+  const int smem =
+      (2 * (a.d / Vec<T>::N) + 2 * H + a.n * H + H) * static_cast<int>(sizeof(float));
+  return launch_pdl(full_kernel<T, VPT, true>, grid, threads, smem, s, a);
 }
 
 template <typename T>
@@ -911,15 +907,14 @@ cudaError_t launch_partial_update(IO io, const void* pa, const void* pb, void* o
   constexpr int threads = 256;
   if (io == IO::BF16) {
     const int64_t nvec = n_elems / 8;
-    add_kernel<bf16><<<grid_for(nvec, threads), threads, 0, s>>>(
-        static_cast<const bf16*>(pa), static_cast<const bf16*>(pb), static_cast<bf16*>(out), nvec);
-  } else {
-    const int64_t nvec = n_elems / 4;
-    add_kernel<float><<<grid_for(nvec, threads), threads, 0, s>>>(
-        static_cast<const float*>(pa), static_cast<const float*>(pb), static_cast<float*>(out),
-        nvec);
+    return launch_pdl(add_kernel<bf16>, grid_for(nvec, threads), threads, 0, s,
+                      static_cast<const bf16*>(pa), static_cast<const bf16*>(pb),
+                      static_cast<bf16*>(out), nvec);
   }
-  return cudaGetLastError();
+  const int64_t nvec = n_elems / 4;
+  return launch_pdl(add_kernel<float>, grid_for(nvec, threads), threads, 0, s,
+                    static_cast<const float*>(pa), static_cast<const float*>(pb),
+                    static_cast<float*>(out), nvec);
 }
 
 cudaError_t launch_query_prep(const float* w, const float* g, float* u, void* u_split, int rows,
@@ -927,9 +922,8 @@ cudaError_t launch_query_prep(const float* w, const float* g, float* u, void* u_
   const int64_t n_elems = static_cast<int64_t>(rows) * d;
   if (n_elems == 0) return cudaSuccess;
   constexpr int threads = 256;
-  prep_kernel<<<grid_for(n_elems / 4, threads), threads, 0, s>>>(
-      w, g, u, static_cast<uint16_t*>(u_split), d, n_elems / 4);
-  return cudaGetLastError();
+  return launch_pdl(prep_kernel, grid_for(n_elems / 4, threads), threads, 0, s, w, g, u,
+                    static_cast<uint16_t*>(u_split), d, n_elems / 4);
 }
 
 }  // namespace attnres
