@@ -59,7 +59,8 @@ constexpr int kMaxSlots = 12;       // ring slots
 constexpr int kMaxSmem = 227 * 1024;
 
 struct TcPlan {
-  int Hs, windows;    // heads per CTA window, windows (= H / Hs)
+  int Hs, windows;    // heads per CTA window, windows (= H / Hs, or csplit)
+  int csplit;         // > 1: a cluster of csplit CTAs splits one head's columns (few tiles)
   int tcols;          // tensor-memory columns allocated: nMT * Hs * Npad rounded up to 2^k >= 32
   int R;              // rows of a per-head sum-of-squares buffer (nMT * 128)
   int Npad;           // MMA N: 2S rounded up to 16
@@ -78,6 +79,7 @@ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 bool make_tc_window(int n, int S, int H, int Hs, TcPlan& p) {
   p.Hs = Hs;
   p.windows = H / Hs;
+  p.csplit = 1;
   p.Npad = align_up(2 * S, 16);
   p.rows = n * kTT;
   p.nMT = (p.rows + kM - 1) / kM;
@@ -101,14 +103,14 @@ bool make_tc_window(int n, int S, int H, int Hs, TcPlan& p) {
   const int ab = small ? kTT * n * 4 * 12 * 4 : 0;  // [token][source][4][6 pairs][2]
   const int sb = 2 * Hs * p.R * 4;                  // per-half, per-head row sums of squares
   const int fixed = slack + align_up(zb, 16) + align_up(ab, 16) + sb +
-                    (2 * kMaxSlots + 2) * 8 + 16;
+                    (2 * kMaxSlots + 4) * 8 + 16;
   p.SB = std::min(kMaxSlots, (kMaxSmem - 1024 - fixed) / p.slot);
   if (p.SB < 2) return false;
   p.offZ = p.SB * p.slot + slack;
   p.offAlph = p.offZ + align_up(zb, 16);
   p.offSs = p.offAlph + align_up(ab, 16);
   p.offBar = p.offSs + sb;
-  p.offTmem = p.offBar + (2 * p.SB + 2) * 8;
+  p.offTmem = p.offBar + (2 * p.SB + 4) * 8;  // full, empty, dready, abort, xready, xdone
   p.smem = 1024 + p.offTmem + 16;
   return true;
 }
@@ -157,10 +159,12 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   const int64_t T = a.T;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTT;
   const int dh = d / H;                       // columns per head
-  const int wcols = Hs * dh;                  // columns of this CTA's window of heads
+  const int W = pl.csplit;                    // > 1: the cluster's CTAs split the columns
+  const int wcols = W > 1 ? dh / W : Hs * dh;  // columns of this CTA's window
   const int cw = static_cast<int>(blockIdx.y) * wcols;  // its first column
-  const int h0 = static_cast<int>(blockIdx.y) * Hs;     // its first head
-  const int cph = (dh + kKC - 1) / kKC;       // stages per head (all of them when H = 1)
+  const int h0 = W > 1 ? 0 : static_cast<int>(blockIdx.y) * Hs;  // its first head
+  const int cph = (W > 1 ? wcols : dh) / kKC + ((W > 1 ? wcols : dh) % kKC != 0);  // stages per head
+  const bool writer = W == 1 || blockIdx.y == 0;  // writes the statistics of the tile
   const int nch = (wcols + kKC - 1) / kKC;
   const int total = 2 * nch;  // source-ring iterations: sweep 1, then sweep 2
 
@@ -168,6 +172,8 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   uint64_t* empty = full + SB;
   uint64_t* dready = empty + SB;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(dready + 1);
+  uint64_t* xready = dready + 2;  // split: the peers' partial sums are ready to be read
+  uint64_t* xdone = dready + 3;   // split: the peers have read this CTA's partial sums
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + pl.offTmem);
   float* zbuf = reinterpret_cast<float*>(smem + pl.offZ);     // [n * 8 rows][Hs][SZ]
   const int SZ = (S + 1) & ~1;
@@ -181,6 +187,10 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
       mbar_init(&empty[s], kWarps / 2 + 1);  // the consuming half + the stage's MMAs (or a stand-in)
     }
     mbar_init(dready, 1);
+    if (W > 1) {
+      mbar_init(xready, W - 1);
+      mbar_init(xdone, W - 1);
+    }
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -191,6 +201,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (W > 1) cluster_sync();  // the peers' barriers are initialised before any remote arrival
   pdl_enter();  // the prologue above touches no global memory
 
   // ------------------------------ copy-issuing warp ------------------------------
@@ -359,7 +370,9 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
     const int r = mt * kM + sub * 32 + lane;
     for (int hs = 0; hs < Hs; ++hs) {
       const float ss = r < nrows ? ssbuf[hs * R + r] + ssbuf[(Hs + hs) * R + r] : 0.f;
-      const float rinv = r >= nrows ? 0.f : key_norm ? 1.f / sqrtf(ss / fd + a.eps) : 1.f;
+      // split: raw dot products here; scaled once the cluster's sums are known
+      const float rinv =
+          r >= nrows ? 0.f : (key_norm && W == 1) ? 1.f / sqrtf(ss / fd + a.eps) : 1.f;
       for (int cc = 0; cc < pl.Npad / 16; ++cc) {
         uint32_t v[16];
         tmem_ld16(tmem + (static_cast<uint32_t>(sub * 32) << 16) + (mt * Hs + hs) * pl.Npad +
@@ -379,6 +392,60 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
     }
   }
   named_barrier(1, kCompute);
+
+  // ---------- split: sum the logit numerators and sums of squares over the cluster ----------
+  if (W > 1) {
+    const uint32_t rank = cluster_rank();
+    if (tid == 0)
+      for (int q = 0; q < W; ++q)
+        if (q != static_cast<int>(rank)) mbar_arrive_cluster(mapa_shared(smem_addr(xready), q));
+    if (!*abort_flag && !mbar_wait_cluster(xready, 0)) *abort_flag = 1;
+    // entry i: logit numerator (row i / S, query i % S), then the row sums of squares
+    const int ne = nrows * S + nrows;
+    constexpr int kMaxE = (kM * (kMaxS + 1) + kCompute - 1) / kCompute;  // split: n * 8 <= 128
+    float acc[kMaxE];
+    auto entry = [&](int i) -> float* {
+      return i < nrows * S ? zbuf + (i / S) * ZR + i % S : ssbuf + (i - nrows * S);
+    };
+#pragma unroll
+    for (int k = 0; k < kMaxE; ++k) {
+      const int i = tid + k * kCompute;
+      acc[k] = 0.f;
+      if (i < ne) {
+        float* e = entry(i);
+        const bool ssrow = i >= nrows * S;
+        for (int q = 0; q < W; ++q) {
+          if (q == static_cast<int>(rank)) {
+            acc[k] += e[0] + (ssrow ? e[R] : 0.f);
+          } else {
+            const uint32_t ra = mapa_shared(smem_addr(e), q);
+            acc[k] += ld_cluster_f32(ra) + (ssrow ? ld_cluster_f32(ra + R * 4) : 0.f);
+          }
+        }
+      }
+    }
+    named_barrier(1, kCompute);  // every read of the peers is done
+    if (tid == 0)
+      for (int q = 0; q < W; ++q)
+        if (q != static_cast<int>(rank)) mbar_arrive_cluster(mapa_shared(smem_addr(xdone), q));
+    if (!*abort_flag && !mbar_wait_cluster(xdone, 0)) *abort_flag = 1;  // mine are read
+#pragma unroll
+    for (int k = 0; k < kMaxE; ++k) {
+      const int i = tid + k * kCompute;
+      if (i < ne) {
+        float* e = entry(i);
+        e[0] = acc[k];
+        if (i >= nrows * S) e[R] = 0.f;
+      }
+    }
+    named_barrier(1, kCompute);
+    // z = numerator / r with the row's full sum of squares
+    for (int i = tid; i < nrows * S; i += kCompute) {
+      const int r = i / S;
+      if (key_norm) zbuf[r * ZR + i % S] *= 1.f / sqrtf(ssbuf[r] / fd + a.eps);
+    }
+    named_barrier(1, kCompute);
+  }
 
   // ------------- softmax statistics, one thread per (token, head, query) -------------
   for (int i = tid; i < kTT * Hs * S; i += kCompute) {
@@ -405,9 +472,9 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
       } else {             // in place of the logit, which this thread alone reads
         *zp = al;
       }
-      if (a.alpha != nullptr && tok < T) a.alpha[(sh * T + tok) * n + j] = al;
+      if (a.alpha != nullptr && tok < T && writer) a.alpha[(sh * T + tok) * n + j] = al;
     }
-    if (tok < T) {
+    if (tok < T && writer) {
       if (a.m != nullptr) a.m[sh * T + tok] = m;
       if (a.lse != nullptr && !sigmoid) a.lse[sh * T + tok] = lse;
     }
@@ -522,6 +589,39 @@ cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s) {
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
   if (e != cudaSuccess) return e;
   const int64_t blocks = (a.T + kTT - 1) / kTT;
+  // Few token tiles (decode-sized T, one head, at most 16 sources): a cluster of W CTAs splits
+  // each tile's columns, if W tiles' worth of CTAs still fit one wave and such clusters can be
+  // resident; the CTAs add their partial sums through distributed shared memory.
+  if (a.heads == 1 && a.n * kTT <= kM) {
+    int sms = 0, dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    for (int W = 4; W >= 2; W /= 2) {
+      if (a.d % (W * kKC) != 0 || blocks * W > sms) continue;
+      TcPlan ps = pl;
+      ps.csplit = W;
+      ps.windows = W;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(blocks), static_cast<unsigned>(W));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = ps.smem;
+      cfg.stream = s;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 1;
+      attr[0].val.clusterDim.y = static_cast<unsigned>(W);
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
+        cudaGetLastError();  // not launchable with this cluster size: try the next
+        continue;
+      }
+      return cudaLaunchKernelEx(&cfg, kern, mb, mq, a, ps);
+    }
+  }
   const dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(pl.windows));
   return launch_pdl(kern, grid, kThreads, pl.smem, s, mb, mq, a, pl);
 }
