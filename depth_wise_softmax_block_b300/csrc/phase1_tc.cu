@@ -146,8 +146,9 @@ struct RingPos {
 };
 
 // kSmall: n <= 9 and one head (one M-tile, sweep-2 weights as ready-made pairs, sums of
-// squares in registers), compiled without the paths for larger n.
-template <bool kSmall>
+// squares in registers), compiled without the paths for larger n.  kSplit: the cluster column
+// split for few token tiles (compiled out of the other instantiations).
+template <bool kSmall, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
                  const __grid_constant__ CUtensorMap tm_q, const Phase1Args a, const TcPlan pl) {
@@ -159,7 +160,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   const int64_t T = a.T;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTT;
   const int dh = d / H;                       // columns per head
-  const int W = pl.csplit;                    // > 1: the cluster's CTAs split the columns
+  const int W = kSplit ? pl.csplit : 1;       // > 1: the cluster's CTAs split the columns
   const int wcols = W > 1 ? dh / W : Hs * dh;  // columns of this CTA's window
   const int cw = static_cast<int>(blockIdx.y) * wcols;  // its first column
   const int h0 = W > 1 ? 0 : static_cast<int>(blockIdx.y) * Hs;  // its first head
@@ -585,7 +586,8 @@ cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s) {
   cudaError_t e = encode_source_map(&mb, a.reps, a.src_stride, a.n, a.T, a.d, 2, kKC, kTT);
   if (e == cudaSuccess) e = encode_split_query_map(&mq, a.u_split, a.S, a.d, pl.Npad);
   if (e != cudaSuccess) return e;
-  auto kern = a.heads == 1 && a.n <= kSmallN ? phase1_tc_kernel<true> : phase1_tc_kernel<false>;
+  const bool small = a.heads == 1 && a.n <= kSmallN;
+  auto kern = small ? phase1_tc_kernel<true, false> : phase1_tc_kernel<false, false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
   if (e != cudaSuccess) return e;
   const int64_t blocks = (a.T + kTT - 1) / kTT;
@@ -596,6 +598,9 @@ cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s) {
     int sms = 0, dev = 0;
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    auto ksplit = small ? phase1_tc_kernel<true, true> : phase1_tc_kernel<false, true>;
+    e = cudaFuncSetAttribute(ksplit, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
     if (e != cudaSuccess) return e;
     for (int W = 4; W >= 2; W /= 2) {
       if (a.d % (W * kKC) != 0 || blocks * W > sms) continue;
@@ -615,11 +620,11 @@ cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s) {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int clusters = 0;
-      if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
+      if (cudaOccupancyMaxActiveClusters(&clusters, ksplit, &cfg) != cudaSuccess || clusters < 1) {
         cudaGetLastError();  // not launchable with this cluster size: try the next
         continue;
       }
-      return cudaLaunchKernelEx(&cfg, kern, mb, mq, a, ps);
+      return cudaLaunchKernelEx(&cfg, ksplit, mb, mq, a, ps);
     }
   }
   const dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(pl.windows));
