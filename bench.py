@@ -350,7 +350,7 @@ def run_e2e(step: LongContextStep, iters: int):
         one()
     el = (time.perf_counter() - t0) / iters
     return {"value": wl.T / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": el * 1e3}
+            "d2h_bytes_per_step": d2h, "ms_per_step": el * 1e3, "h2d_gbs": h2d / el / 1e9}
 
 
 def full_grouped_bytes(L: int, S: int, d: int, E: int) -> int:
