@@ -28,6 +28,10 @@
 // the sums of squares, logits and softmax statistics are kept per head, and sweep 2 weights a
 // stage with its head's alpha.  Hs is the largest divisor of H whose columns fit the 512
 // tensor-memory columns (H = 1: one window, the whole row).
+// Few token tiles (decode-sized T, one head, n <= 16): a cluster of 2 or 4 CTAs along grid.y
+// splits each tile's columns; after sweep 1 the CTAs add their partial logit numerators and sums
+// of squares through distributed shared memory (xready / xdone mbarriers), then each runs the
+// softmax and sweep 2 on its own columns (rank 0 alone writes the statistics).
 // Stage hand-off uses mbarriers ("full": copy landed; "empty": all compute warps and the
 // stage's MMAs done); every wait is bounded (tma.cuh).  The tensor-memory allocation is
 // released on every path before the CTA exits.
