@@ -268,7 +268,7 @@ def reference_arm(args, world, rank):
     val = k / step
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
-        "n_gpus": args.gpus, "runs_on": "host cores (the oracle uses no GPU)",
+        "n_gpus": getattr(args, "gpus", 1), "runs_on": "host cores (the oracle uses no GPU)",
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
