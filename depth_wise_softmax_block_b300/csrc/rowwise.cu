@@ -13,10 +13,16 @@
 // Both take the Table 4 variants ("Attention Residuals" note, result 4): the flags (sigmoid
 // weights, no key RMSNorm) and depth-attention heads (H contiguous feature slices, each with its
 // own key RMS, logit and softmax; the input RMSNorm over the whole row).
+//   phase2_heads_kernel, full_heads_kernel
+//                  the same two with H <= 16 heads of at most 128 vectors: one warp per head,
+//                  so every per-head sum is a warp reduction (the other head counts go through
+//                  the generic kernels' per-head reduction in shared memory).
 //   add_kernel     partial-sum update / block close: out = partial + v.
 //   prep_kernel    query preparation u = w ⊙ gamma_key (and its bf16 hi/lo split).
 //
-// Each thread owns VPT 16-byte vectors of the row (vector v = threadIdx.x + k * blockDim.x).
+// In the generic kernels each thread owns VPT 16-byte vectors of the row (vector v =
+// threadIdx.x + k * blockDim.x).  Every kernel is launched with programmatic stream
+// serialisation and enters through pdl_enter() (common.cuh).
 #include <math.h>
 
 #include <algorithm>
