@@ -149,17 +149,20 @@ struct RingPos {
   }
 };
 
-// kSmall: n <= 9 and one head (one M-tile, sweep-2 weights as ready-made pairs, sums of
-// squares in registers), compiled without the paths for larger n.  kSplit: the cluster column
-// split for few token tiles (compiled out of the other instantiations).
-template <bool kSmall, bool kSplit>
+// kN = n in 1 .. 9 with one head: the small layout (one M-tile, sweep-2 weights as ready-made
+// pairs, sums of squares in registers) with the source count known at compile time, so every
+// loop over the sources is unrolled without guards; kN = 0: any n (runtime).  kSplit: the
+// cluster column split for few token tiles (compiled out of the other instantiations).
+template <int kN, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
                  const __grid_constant__ CUtensorMap tm_q, const Phase1Args a, const TcPlan pl) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n = a.n, S = a.S, d = a.d, SB = pl.SB;
+  constexpr bool kSmall = kN > 0;
+  const int n = kSmall ? kN : a.n;
+  const int S = a.S, d = a.d, SB = pl.SB;
   const int H = a.heads, Hs = pl.Hs, R = pl.R;
   const int64_t T = a.T;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTT;
@@ -577,6 +580,26 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
 
 }  // namespace
 
+using Phase1TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const Phase1Args,
+                                const TcPlan);
+
+// The kernel instantiation for kn sources (1 .. 9: compile-time count; 0: any).
+template <bool kSplit>
+Phase1TcKernel phase1_tc_instance(int kn) {
+  switch (kn) {
+    case 1: return phase1_tc_kernel<1, kSplit>;
+    case 2: return phase1_tc_kernel<2, kSplit>;
+    case 3: return phase1_tc_kernel<3, kSplit>;
+    case 4: return phase1_tc_kernel<4, kSplit>;
+    case 5: return phase1_tc_kernel<5, kSplit>;
+    case 6: return phase1_tc_kernel<6, kSplit>;
+    case 7: return phase1_tc_kernel<7, kSplit>;
+    case 8: return phase1_tc_kernel<8, kSplit>;
+    case 9: return phase1_tc_kernel<9, kSplit>;
+    default: return phase1_tc_kernel<0, kSplit>;
+  }
+}
+
 bool phase1_tc_supported(int n, int S, int d, int heads) {
   TcPlan p;
   return make_tc_plan(n, S, d, heads, p);
@@ -590,8 +613,8 @@ cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s) {
   cudaError_t e = encode_source_map(&mb, a.reps, a.src_stride, a.n, a.T, a.d, 2, kKC, kTT);
   if (e == cudaSuccess) e = encode_split_query_map(&mq, a.u_split, a.S, a.d, pl.Npad);
   if (e != cudaSuccess) return e;
-  const bool small = a.heads == 1 && a.n <= kSmallN;
-  auto kern = small ? phase1_tc_kernel<true, false> : phase1_tc_kernel<false, false>;
+  const int kn = a.heads == 1 && a.n <= kSmallN ? a.n : 0;  // compile-time source count
+  auto kern = phase1_tc_instance<false>(kn);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
   if (e != cudaSuccess) return e;
   const int64_t blocks = (a.T + kTT - 1) / kTT;
@@ -603,7 +626,7 @@ cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s) {
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    auto ksplit = small ? phase1_tc_kernel<true, true> : phase1_tc_kernel<false, true>;
+    auto ksplit = phase1_tc_instance<true>(kn);
     e = cudaFuncSetAttribute(ksplit, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
     if (e != cudaSuccess) return e;
     for (int W = 4; W >= 2; W /= 2) {
