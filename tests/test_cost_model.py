@@ -73,3 +73,54 @@ def test_kernel_bytes_hand_counts():
     assert st.close == 3 * d * E
     assert st.final == 11 * d * E
     assert C.phase1_flops(9, 24, d) == 2 * (2 * 24 * 9 * d + 9 * d)
+
+
+def test_head_statistics_bytes():
+    """With H heads every 4-byte statistic is kept per head: phase 1 writes S*H lse values per
+    token, phase 2 reads H."""
+    d, E = 7168, 2
+    assert C.phase1_bytes(9, 24, d, E, heads=16) - C.phase1_bytes(9, 24, d, E) == 4 * 24 * 15
+    assert C.phase2_bytes(d, E, True, True, heads=16) - C.phase2_bytes(d, E, True, True) == 4 * 15
+    assert C.phase2_bytes(d, E, False, False, heads=16) == C.phase2_bytes(d, E, False, False)
+    b1 = C.block_step_bytes(9, 24, d, E, 10)
+    b16 = C.block_step_bytes(9, 24, d, E, 10, heads=16)
+    assert b16.phase1 - b1.phase1 == 4 * 24 * 15
+    assert b16.phase2 - b1.phase2 == 23 * 4 * 15      # 23 calls read the partial's lse
+    assert (b16.close, b16.final) == (b1.close, b1.final)
+
+
+def test_decode_walk_bytes_hand_count():
+    """The decode bench's bytes per depth walk: block n (1-based) runs phase 1 over n sources for
+    its S_n sublayers, S_n phase-2 calls and the close; then the final aggregation over all
+    closed blocks and the embedding."""
+    import bench
+    from synth import inputs as I
+    wl = I.DECODE_BF16
+    d, E, T = wl.d, 2, wl.T
+    want = 0
+    for n, Sn in enumerate([24] * 7 + [18], start=1):
+        want += (n + Sn) * d * E + 4 * Sn                  # phase 1: sources, o; lse
+        want += 2 * d * E                                  # sublayer 1: read o, write y
+        want += 3 * d * E + 4                              # sublayer 2: o, lse, v_1; write y
+        want += (Sn - 2) * (5 * d * E + 4)                 # sublayers 3..: fused update
+        want += 3 * d * E                                  # close
+    want += (9 + 1) * d * E                                # final over 9 slots: read 9, write 1
+    assert bench.decode_walk_bytes(wl) == want * T
+
+
+def test_traffic_lookup_matches_kernel_sources(tmp_path, monkeypatch):
+    """A committed DRAM-traffic capture is used only for the sources it measured: the entry's
+    hash must equal the hash of the kernel's own files."""
+    import json
+    import bench
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    good = {"phase2_fused": {"src_hash": bench.kernel_hash("phase2_fused"),
+                             "bytes_per_launch": 123.0},
+            "phase1": {"src_hash": "0" * 16, "bytes_per_launch": 456.0}}
+    (prof / "dram_traffic_longctx_T4096.json").write_text(json.dumps(good))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_for("phase2_fused") == 123.0
+    assert bench.traffic_for("phase1") is None                 # stale entry
+    assert bench.traffic_for("final") is None                  # no entry
+    assert bench.traffic_for("phase2_fused", heads=16) is None  # no file for 16 heads
