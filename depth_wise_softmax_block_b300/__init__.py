@@ -29,6 +29,7 @@ SIGNATURES = {
     "attnres_status_string": ([_I], ctypes.c_char_p),
     "attnres_last_cuda_error": ([], ctypes.c_char_p),
     "attnres_poll_device_errors": ([], _I),
+    "attnres_selftest_wait_timeout": ([_U, _P], _I),
     "attnres_query_prep": ([_P, _P, _P, _P, _I, _I, _P], _I),
     "attnres_phase1": ([_P, _I64, _I, _I64, _I, _I, _P, _P, _I, _F, _P, _P, _P, _P, _U, _I,
                         _P], _I),
@@ -110,6 +111,13 @@ def _stats(t: torch.Tensor, numel: int, name: str):
 def attnres_poll_device_errors():
     """Raise if a kernel's bounded wait gave up since the previous poll (synchronises)."""
     _check(library().attnres_poll_device_errors(), "attnres_poll_device_errors")
+
+
+def attnres_selftest_wait_timeout(polls=1000, stream=None):
+    """Launch the library's timeout self-test: a kernel whose bounded wait cannot succeed gives
+    up after ``polls`` polls; the next attnres_poll_device_errors raises (ATTNRES_ERR_TIMEOUT)."""
+    _check(library().attnres_selftest_wait_timeout(polls, _stream(stream)),
+           "attnres_selftest_wait_timeout")
 
 
 def attnres_query_prep(w, gamma_key, u_out, u_split_out=None, stream=None):

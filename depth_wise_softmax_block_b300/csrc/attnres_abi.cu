@@ -75,6 +75,11 @@ attnres_status attnres_poll_device_errors(void) {
   return n == 0 ? ATTNRES_OK : ATTNRES_ERR_TIMEOUT;
 }
 
+attnres_status attnres_selftest_wait_timeout(unsigned int polls, void* stream) {
+  if (polls > (1u << 20)) return ATTNRES_ERR_INVALID_ARG;
+  return cuda_status(attnres::launch_wait_selftest(polls, static_cast<cudaStream_t>(stream)));
+}
+
 attnres_status attnres_query_prep(const float* w, const float* gamma_key, float* u_out,
                                   void* u_split_out, int rows, int d, void* stream) {
   if (rows < 0) return ATTNRES_ERR_INVALID_ARG;

@@ -121,6 +121,9 @@ cudaError_t encode_split_query_map(CUtensorMap* map, const void* u_split, int S,
 bool phase1_tc_supported(int n, int S, int d, int heads);
 cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s);
 unsigned int phase1_tc_poll_timeouts();
+// One CTA whose bounded wait cannot succeed: gives up after `polls` polls and counts a timeout
+// (read by phase1_tc_poll_timeouts).
+cudaError_t launch_wait_selftest(unsigned int polls, cudaStream_t s);
 
 // Number of bounded waits in the phase-1 kernel that gave up since the last call (read and
 // cleared; synchronous).  0xffffffff if the device word could not be read.

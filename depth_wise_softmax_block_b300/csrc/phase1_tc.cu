@@ -658,6 +658,30 @@ cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s) {
   return launch_pdl(kern, grid, kThreads, pl.smem, s, mb, mq, a, pl);
 }
 
+namespace {
+// A wait that cannot succeed: an mbarrier that expects one arrival and gets none.  Thread 0 polls
+// it `polls` times, then counts the timeout like any bounded wait of the library and returns.
+__global__ void wait_selftest_kernel(uint32_t polls) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t addr = smem_addr(&bar);
+    bool done = false;
+    for (uint32_t i = 0; i < polls && !done; ++i) done = mbar_try_wait(addr, 0);
+    if (!done) atomicAdd(&g_wait_timeouts, 1u);
+  }
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(unsigned int polls, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(polls);
+  return cudaGetLastError();
+}
+
 unsigned int phase1_tc_poll_timeouts() {
   unsigned int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_wait_timeouts, sizeof(v)) != cudaSuccess) return 0xffffffffu;

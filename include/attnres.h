@@ -86,7 +86,7 @@ typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype;
 #define ATTNRES_MAX_D 16384        /* hidden size (a row stays in registers)               */
 
 /* ABI version of this header; attnres_abi_version() returns the library's. */
-#define ATTNRES_ABI_VERSION 6
+#define ATTNRES_ABI_VERSION 7
 int attnres_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -105,6 +105,17 @@ const char* attnres_last_cuda_error(void);
  * diagnostic, not part of the hot path).
  */
 attnres_status attnres_poll_device_errors(void);
+
+/*
+ * Self-test of the timeout path (a diagnostic, not part of the hot path): launches one small
+ * kernel on `stream` whose bounded wait cannot succeed (an mbarrier that expects an arrival that
+ * never comes).  It polls `polls` times (at most 2^20; 0 gives up at once), then counts the event
+ * like any wait of the library that gives up, and returns; nothing hangs, nothing faults, and the
+ * context stays usable.  After the kernel has run, attnres_poll_device_errors returns
+ * ATTNRES_ERR_TIMEOUT (and clears the word).  Returns ATTNRES_ERR_INVALID_ARG for larger polls,
+ * ATTNRES_ERR_CUDA if the launch fails.
+ */
+attnres_status attnres_selftest_wait_timeout(unsigned int polls, void* stream);
 
 /*
  * Query preparation (row a0): u = w ⊙ gamma_key, row by row.

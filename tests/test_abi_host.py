@@ -45,7 +45,7 @@ def test_header_symbols_exported(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.attnres_abi_version() == 6
+    assert lib.attnres_abi_version() == 7
     for code, name in ar.STATUS.items():
         assert lib.attnres_status_string(code).decode() == name
     assert lib.attnres_status_string(99).decode() == "ATTNRES_ERR_UNKNOWN"
@@ -199,6 +199,10 @@ def test_backward_validation(lib):
     assert err(call(T=4, du=PM)) == MISALIGNED
     bad = (ctypes.c_void_p * 2)(P, PM)
     assert err(call(T=4, dsrcs=bad)) == MISALIGNED
+
+
+def test_selftest_validation(lib):
+    assert lib.attnres_selftest_wait_timeout((1 << 20) + 1, None) == INVALID
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -305,3 +305,63 @@ def test_no_bounded_wait_gave_up(dev, p1path):
     W, G, U = make_queries(S, d, dev, 31)
     run_phase1(reps, U, p1path)
     ar.attnres_poll_device_errors()
+
+
+@pytest.mark.parametrize("flags", [0, ar.SIGMOID_WEIGHTS])
+@pytest.mark.parametrize("n,T", [(9, 256), (9, 520), (12, 256), (9, 1300)])
+def test_phase1_tensor_cores_cluster_split(dev, n, T, flags):
+    """Tensor-core phase 1 at token counts that select the cluster column split (T = 256: four
+    CTAs per 8-token tile; T = 520: two) and at one that does not (T = 1300), d = 7168, S = 24:
+    o, m, alpha (and lse with softmax weights) on sampled rows against the oracle, and every
+    element against the CUDA-core kernel."""
+    d, S = 7168, 24
+    reps = make_reps(n, T, d, torch.bfloat16, dev, 90 + n + T)
+    W, G, U = make_queries(S, d, dev, 90 + T)
+    outs = {}
+    for path in ("tensor_cores", "cuda_cores"):
+        o = torch.empty((S, T, d), dtype=torch.bfloat16, device=dev)
+        m = torch.empty((S, T), device=dev)
+        lse = torch.full((S, T), 5.0, device=dev)
+        alpha = torch.empty((S, T, n), device=dev)
+        ar.attnres_phase1(reps, U, o, m, lse, alpha, eps=EPS,
+                          u_split=split_of(U) if path == "tensor_cores" else None, flags=flags)
+        outs[path] = (o, m, lse, alpha)
+    torch.cuda.synchronize()
+    ar.attnres_poll_device_errors()
+    rows = np.sort(np.random.default_rng(T).choice(T, 12, replace=False))
+    rows[0], rows[-1] = 0, T - 1
+    wk = "sigmoid" if flags else "softmax"
+    oo, om, olse, oa = O.phase1_variant(to64(reps[:, rows]), to64(W), to64(G), EPS, wk, True)
+    o, m, lse, alpha = outs["tensor_cores"]
+    check_outputs(o[:, rows], oo, "bf16", f"o (T={T}, n={n})")
+    check_close(m[:, rows], om, TOL["bf16"]["stat"], "m")
+    check_close(alpha[:, rows], oa, TOL["bf16"]["weight"], "alpha")
+    if flags:
+        assert torch.all(lse == 5.0), "lse is not written with sigmoid weights"
+    else:
+        check_close(lse[:, rows], olse, TOL["bf16"]["stat"], "lse")
+    o2, m2, lse2, alpha2 = outs["cuda_cores"]
+    check_outputs(o, to64(o2), "bf16", "o: tensor cores vs CUDA cores")
+    check_close(alpha, to64(alpha2), TOL["bf16"]["weight"], "alpha: tensor cores vs CUDA cores")
+
+
+@pytest.mark.parametrize("polls", [0, 1000])
+def test_wait_timeout_is_reported_and_context_survives(dev, polls):
+    """The timeout path, made to run out on purpose without a real hang: a kernel whose bounded
+    wait cannot succeed (an mbarrier that nothing arrives on) gives up after `polls` polls and
+    counts the event; the poll reports ATTNRES_ERR_TIMEOUT once, the next poll is clean, and the
+    context still computes phase 1 correctly afterwards."""
+    ar.attnres_poll_device_errors()                       # start from a clean word
+    ar.attnres_selftest_wait_timeout(polls)
+    torch.cuda.synchronize()
+    with pytest.raises(ar.AttnResError, match="ATTNRES_ERR_TIMEOUT"):
+        ar.attnres_poll_device_errors()
+    ar.attnres_poll_device_errors()                       # read and cleared
+    n, S, T, d = 3, 4, 40, 512
+    reps = make_reps(n, T, d, torch.bfloat16, dev, 77)
+    W, G, U = make_queries(S, d, dev, 77)
+    o, m, lse, alpha = run_phase1(reps, U, "tensor_cores")
+    oo, om, olse, oa = O.phase1(to64(reps), to64(W), to64(G), EPS)
+    check_outputs(o, oo, "bf16", "o after the timeout self-test")
+    check_close(lse, olse, TOL["bf16"]["stat"], "lse after the timeout self-test")
+    ar.attnres_poll_device_errors()                       # no wait of phase 1 gave up
