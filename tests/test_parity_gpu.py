@@ -95,6 +95,8 @@ P1_CASES = [
     (17, 24, 12, 128, "bf16"),      # two M-tiles
     (33, 8, 19, 1024, "bf16"),      # three M-tiles
     (49, 16, 9, 2048, "bf16"),      # four M-tiles (the largest Full AttnRes history)
+    (9, 24, 21, 512, "bf16"),       # ring slots in pairs (one copy takes two column stages)
+    (2, 3, 17, 384, "bf16"),        # pairs, odd S, ragged token tile
 ]
 
 
