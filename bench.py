@@ -55,11 +55,12 @@ def csrc_hash(files=None) -> str:
 KERNEL_SOURCES = {
     "phase1": ["phase1_tc.cu", "tc.cuh", "tma.cuh", "tmap.cu", "common.cuh", "kernels.h"],
     "rowwise": ["rowwise.cu", "common.cuh", "kernels.h"],
+    "final": ["rowwise.cu", "fullring.cu", "tma.cuh", "common.cuh", "kernels.h"],
 }
 
 
 def kernel_hash(kind: str) -> str:
-    return csrc_hash(KERNEL_SOURCES["phase1" if kind == "phase1" else "rowwise"])
+    return csrc_hash(KERNEL_SOURCES[kind if kind in ("phase1", "final") else "rowwise"])
 
 
 def peaks():

@@ -1,0 +1,326 @@
+// The direct single-pass aggregation over an explicit source list ("Attention Residuals" note,
+// §7: softmax over the sources of w . RMSNorm(v_i), h = sum_i alpha_i v_i, then the sublayer's
+// input RMSNorm), as a persistent kernel that streams whole source rows through a ring of
+// shared-memory row slots.  Used for one head without a seeded partition, n <= 16 sources and
+// rows of 512 to 1024 16-byte vectors (the final aggregation over the block representations is
+// the case it is built for: n = 10 rows of 14 KB per token).
+//
+// One CTA per SM walks the rows blockIdx.x, blockIdx.x + gridDim.x, ...  A copy warp issues one
+// bulk copy per (row, source) into the next ring slot, as soon as the slot is free, so the copies
+// of the next row stream in while the current one is computed.  The 16 compute warps take a
+// row in two passes over its n resident slots:
+//   pass 1  each thread sums its vectors' squares and query products for every source in
+//           registers (no reduction between sources); one butterfly reduce-scatter over the
+//           warp (31 shuffles) leaves lane L with the warp's total of value L (source L / 2,
+//           square sum or product); one barrier; lane j of every warp then adds the 16 warps'
+//           totals of source j, forms z_j and, with warp shuffles, the softmax statistics, so
+//           each lane holds alpha_j for the sources j = lane;
+//   pass 2  h = sum_j alpha_j v_j from the same slots (alpha_j by one shuffle per source); each
+//           slot is released as soon as the 16 warps are done with it.
+// Against the row-per-CTA kernel (an online softmax whose every source costs a CTA-wide
+// reduction, with two sources in flight in registers) a row costs one barrier (two with the
+// input RMSNorm) and the copy engine keeps the next row's sources in flight.
+// Every wait is bounded (tma.cuh); after a wait gives up the CTA stops issuing copies, skips the
+// remaining waits and exits once its copies in flight have landed.
+#include <math.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tma.cuh"
+
+namespace attnres {
+namespace {
+
+constexpr int kRingCompute = 512;                  // 16 compute warps
+constexpr int kRingWarps = kRingCompute / 32;
+constexpr int kRingThreads = kRingCompute + 32;    // + the copy-issuing warp
+constexpr int kRingVPT = 2;                        // vectors per compute thread: nv <= 1024
+// Shorter rows leave most of the 16 warps idle and the per-row reductions dominate; there the
+// row-per-CTA kernel is faster (measured at 256 vectors: a direct Full AttnRes walk at d = 2048
+// took 21.1 ms through this kernel against 18.0 ms).
+constexpr int kRingMinVectors = 512;
+constexpr int kRingMaxN = 16;                      // 2 sums per source: one lane each
+constexpr int kRingSlotBytes = 216 * 1024;         // shared memory for the slots
+constexpr int kRingMaxSlots = 64;
+
+// Row slots for rows of `rowbytes` bytes; 0 if the ring cannot hold n sources plus two slots.
+int ring_slots(int rowbytes, int n) {
+  const int sb = std::min(kRingMaxSlots, kRingSlotBytes / rowbytes);
+  return sb >= n + 2 ? sb : 0;
+}
+
+int ring_smem(int rowbytes, int SB) {
+  // slots | full, empty barriers | per-warp totals [2 rows][16 warps][32] | y sums [2][16]
+  return 128 + SB * rowbytes + 2 * SB * 8 + 2 * kRingWarps * 32 * 4 + 2 * kRingWarps * 4 + 16;
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRingThreads, 1) full_ring_kernel(const FullArgs a, int SB) {
+  constexpr int VE = Vec<T>::N;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* ring = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
+  const int rowbytes = a.d * static_cast<int>(sizeof(T));
+  const int nv = a.d / VE;
+  const int n = a.n;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + SB * rowbytes);
+  uint64_t* empty = full + SB;
+  float* part = reinterpret_cast<float*>(empty + SB);  // [2][16 warps][32]: value 2j + {ss, dot}
+  float* ysum = part + 2 * kRingWarps * 32;             // [2][16 warps]
+  int* abort_flag = reinterpret_cast<int*>(ysum + 2 * kRingWarps);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < SB; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kRingWarps);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  pdl_enter();  // nothing above touches global memory
+  volatile int* abort_v = abort_flag;
+
+  // ------------------------------ copy-issuing warp ------------------------------
+  if (warp == kRingWarps) {
+    if (lane == 0) {
+      int it = 0, bs = 0, ph = 0;  // copies issued; slot and phase parity of the next one
+      for (int64_t r = blockIdx.x; r < a.T && !*abort_v; r += gridDim.x) {
+        for (int j = 0; j < n; ++j) {
+          if (it >= SB && !mbar_wait(&empty[bs], ph ^ 1)) {
+            *abort_v = 1;
+            break;
+          }
+          if (*abort_v) break;
+          mbar_arrive_expect_tx(&full[bs], static_cast<uint32_t>(rowbytes));
+          bulk_load(ring + bs * rowbytes,
+                    static_cast<const char*>(a.srcs[j]) + r * static_cast<int64_t>(rowbytes),
+                    static_cast<uint32_t>(rowbytes), &full[bs]);
+          ++it;
+          if (++bs == SB) {
+            bs = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      // Drain: the last copy issued into every slot has landed before the CTA may exit.
+      for (int s = 0; s < SB && s < it; ++s) {
+        const int last = it - 1 - ((it - 1 - s) % SB);
+        mbar_wait(&full[s], (last / SB) & 1);
+      }
+    }
+    return;
+  }
+
+  // ------------------------------- compute warps --------------------------------
+  auto wait = [&](uint64_t* bar, int parity) {
+    if (!*abort_v && !mbar_wait(bar, static_cast<uint32_t>(parity))) *abort_v = 1;
+  };
+  const bool sigmoid = (a.flags & kSigmoid) != 0;
+  const bool key_norm = (a.flags & kNoKeyNorm) == 0;
+  const float fd = static_cast<float>(a.d);
+  // The query for this thread's vectors, kept for the CTA's life.
+  float uq[kRingVPT][VE];
+#pragma unroll
+  for (int k = 0; k < kRingVPT; ++k) {
+    const int v = tid + k * kRingCompute;
+#pragma unroll
+    for (int e = 0; e < VE; ++e) uq[k][e] = v < nv ? __ldg(a.u + v * VE + e) : 0.f;
+  }
+
+  int bs = 0, ph = 0;  // ring position of the row's first source
+  int par = 0;         // row parity: which half of the partial buffers
+  for (int64_t r = blockIdx.x; r < a.T; r += gridDim.x, par ^= 1) {
+    float* pw = part + par * (kRingWarps * 32);
+    // ---- pass 1: this thread's sums of squares and query products of every source ----
+    float ps[2 * kRingMaxN];  // value 2j: sum of squares of source j; 2j + 1: query product
+    {
+      int b = bs, p = ph;
+#pragma unroll
+      for (int j = 0; j < kRingMaxN; ++j) {
+        ps[2 * j] = ps[2 * j + 1] = 0.f;
+        if (j < n) {
+          wait(&full[b], p);
+          const uint4* sl = reinterpret_cast<const uint4*>(ring + b * rowbytes);
+#pragma unroll
+          for (int k = 0; k < kRingVPT; ++k) {
+            const int v = tid + k * kRingCompute;
+            if (v < nv) {
+              float x[VE];
+              unpack(sl[v], x);
+#pragma unroll
+              for (int e = 0; e < VE; ++e) {
+                ps[2 * j] = fmaf(x[e], x[e], ps[2 * j]);
+                ps[2 * j + 1] = fmaf(uq[k][e], x[e], ps[2 * j + 1]);
+              }
+            }
+          }
+          if (++b == SB) {
+            b = 0;
+            p ^= 1;
+          }
+        }
+      }
+    }
+    // Butterfly reduce-scatter over the warp: at the step of width o a lane keeps the half of
+    // its values selected by its lane bit o and adds the partner's copy of that half; after the
+    // five steps ps[0] of lane L is the warp's total of value L.
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < o; ++i) {
+        const float send = upper ? ps[i] : ps[i + o];
+        const float keep = upper ? ps[i + o] : ps[i];
+        ps[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+    pw[warp * 32 + lane] = ps[0];
+    named_barrier(1, kRingCompute);
+    // ---- statistics: lane j holds source j (every warp computes the same values) ----
+    float z = -INFINITY;
+    if (lane < n) {
+      float ss = 0.f, dot = 0.f;
+#pragma unroll
+      for (int w = 0; w < kRingWarps; ++w) {
+        ss += pw[w * 32 + 2 * lane];
+        dot += pw[w * 32 + 2 * lane + 1];
+      }
+      z = key_norm ? dot / sqrtf(ss / fd + a.eps_key) : dot;
+    }
+    float m = z;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float al, lse = 0.f;
+    if (sigmoid) {
+      al = lane < n ? 1.f / (1.f + expf(-z)) : 0.f;
+    } else {
+      const float ez = lane < n ? expf(z - m) : 0.f;
+      const float l = warp_sum(ez);
+      al = ez / l;
+      lse = m + logf(l);
+    }
+    if (warp == 0) {
+      if (a.alpha != nullptr && lane < n) a.alpha[r * n + lane] = al;
+      if (lane == 0) {
+        if (a.m != nullptr) a.m[r] = m;
+        if (a.lse != nullptr && !sigmoid) a.lse[r] = lse;
+      }
+    }
+    // ---- pass 2: h = sum_j alpha_j v_j; each slot is released after its use ----
+    float acc[kRingVPT][VE];
+#pragma unroll
+    for (int k = 0; k < kRingVPT; ++k)
+#pragma unroll
+      for (int e = 0; e < VE; ++e) acc[k][e] = 0.f;
+    for (int j = 0; j < n; ++j) {
+      const float aj = __shfl_sync(0xffffffffu, al, j);
+      const uint4* sl = reinterpret_cast<const uint4*>(ring + bs * rowbytes);
+#pragma unroll
+      for (int k = 0; k < kRingVPT; ++k) {
+        const int v = tid + k * kRingCompute;
+        if (v < nv) {
+          float x[VE];
+          unpack(sl[v], x);
+#pragma unroll
+          for (int e = 0; e < VE; ++e) acc[k][e] = fmaf(aj, x[e], acc[k][e]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[bs]);
+      if (++bs == SB) {
+        bs = 0;
+        ph ^= 1;
+      }
+    }
+    // ---- outputs: h, and y = gamma_in * h / r(h) ----
+    const int64_t base = r * a.d;
+    float inv = 0.f;
+    if (a.y != nullptr) {  // uniform over the CTA
+      float s2 = 0.f;
+#pragma unroll
+      for (int k = 0; k < kRingVPT; ++k)
+#pragma unroll
+        for (int e = 0; e < VE; ++e) s2 = fmaf(acc[k][e], acc[k][e], s2);
+      s2 = warp_sum(s2);
+      if (lane == 0) ysum[par * kRingWarps + warp] = s2;
+      named_barrier(1, kRingCompute);
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < kRingWarps; ++w) tot += ysum[par * kRingWarps + w];
+      inv = 1.f / sqrtf(tot / fd + a.eps_in);
+    }
+#pragma unroll
+    for (int k = 0; k < kRingVPT; ++k) {
+      const int v = tid + k * kRingCompute;
+      if (v < nv) {
+        if (a.h != nullptr) st_global(static_cast<T*>(a.h) + base + v * VE, pack(acc[k]));
+        if (a.y != nullptr) {
+          float y[VE];
+#pragma unroll
+          for (int e = 0; e < VE; ++e)
+            y[e] = acc[k][e] * inv * (a.gamma_in != nullptr ? __ldg(a.gamma_in + v * VE + e) : 1.f);
+          st_global(static_cast<T*>(a.y) + base + v * VE, pack(y));
+        }
+      }
+    }
+  }
+}
+
+template <typename T>
+cudaError_t launch_ring(const FullArgs& a, int SB, cudaStream_t s) {
+  const int rowbytes = a.d * static_cast<int>(sizeof(T));
+  const int smem = ring_smem(rowbytes, SB);
+  auto kern = full_ring_kernel<T>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = a.T < sms ? a.T : sms;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kRingThreads),
+                    static_cast<size_t>(smem), s, a, SB);
+}
+
+}  // namespace
+
+bool full_ring_supported(IO io, const FullArgs& a) {
+  const int E = io == IO::BF16 ? 2 : 4;
+  const int VE = 16 / E;
+  if (a.heads != 1 || a.o0 != nullptr || a.n < 1 || a.n > kRingMaxN) return false;
+  if (a.d % VE != 0 || a.d / VE < kRingMinVectors || a.d / VE > kRingVPT * kRingCompute)
+    return false;
+  return ring_slots(a.d * E, a.n) > 0;
+}
+
+cudaError_t launch_full_ring(IO io, const FullArgs& a, cudaStream_t s) {
+  if (!full_ring_supported(io, a)) return cudaErrorInvalidValue;
+  if (a.T == 0) return cudaSuccess;
+  const int E = io == IO::BF16 ? 2 : 4;
+  const int SB = ring_slots(a.d * E, a.n);
+  return io == IO::BF16 ? launch_ring<bf16>(a, SB, s) : launch_ring<float>(a, SB, s);
+}
+
+unsigned int full_ring_poll_timeouts() {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_wait_timeouts, sizeof(v)) != cudaSuccess) return 0xffffffffu;
+  if (v != 0) {
+    const unsigned int z = 0;
+    cudaMemcpyToSymbol(g_wait_timeouts, &z, sizeof(z));
+  }
+  return v;
+}
+
+}  // namespace attnres

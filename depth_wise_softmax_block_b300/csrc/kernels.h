@@ -99,6 +99,11 @@ cudaError_t launch_phase1(IO io, const Phase1Args& a, cudaStream_t s);
 bool phase1_supported(int n, int S);
 cudaError_t launch_phase2(IO io, const Phase2Args& a, cudaStream_t s);
 cudaError_t launch_full(IO io, const FullArgs& a, cudaStream_t s);
+// The same aggregation by the persistent row-ring kernel (fullring.cu): one head, no seeded
+// partition, n <= 16 sources, rows of 512 to 1024 16-byte vectors that fit the ring.
+bool full_ring_supported(IO io, const FullArgs& a);
+cudaError_t launch_full_ring(IO io, const FullArgs& a, cudaStream_t s);
+unsigned int full_ring_poll_timeouts();
 cudaError_t launch_partial_update(IO io, const void* a, const void* b, void* out, int64_t n_elems,
                                   cudaStream_t s);
 // u = w * g (g null: copy); u_split (null: not written) receives rows 2r, 2r + 1 = the bf16

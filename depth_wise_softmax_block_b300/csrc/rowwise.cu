@@ -904,6 +904,7 @@ cudaError_t launch_phase2(IO io, const Phase2Args& a, cudaStream_t s) {
 
 cudaError_t launch_full(IO io, const FullArgs& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
+  if (full_ring_supported(io, a)) return launch_full_ring(io, a, s);
   return io == IO::BF16 ? full_io<bf16>(a, s) : full_io<float>(a, s);
 }
 
