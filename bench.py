@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import queue
 import subprocess
 import sys
 import threading
@@ -228,6 +229,97 @@ def time_oracle(wl: I.Workload, k: int, seed_offset: int = 0):
     return time.perf_counter() - t0
 
 
+def _oracle_worker(wl_name, k, seed_offset, rounds, barrier, out):
+    """One host core's share of the all-cores oracle timing (a spawned process): build the
+    sample once, then for every round wait for all workers and time the oracle on it."""
+    torch.set_num_threads(1)
+    import oracle.attnres_oracle as O
+    wl = I.WORKLOADS[wl_name]
+    args = oracle_sample(wl, k, seed_offset)
+    for r in range(rounds):
+        barrier.wait(timeout=600)
+        t0 = time.perf_counter()
+        O.single_block(args[0], args[1], args[2], args[3], args[4], args[5], args[6], wl.eps,
+                       wl.eps)
+        out.put((r, k, time.perf_counter() - t0))
+
+
+def time_oracle_all_cores(wl: I.Workload, k: int, procs: int, rounds: int = 1):
+    """The oracle on every host core at once: ``procs`` spawned processes (spawn, so nothing
+    is forked from a process that holds a CUDA context), each timing its own k-token sample
+    after a common barrier, ``rounds`` times.  Returns one (tokens, seconds of the slowest
+    worker) pair per round."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(procs)
+    out = ctx.Queue()
+    env_keep = {v: os.environ.get(v) for v in ("OMP_NUM_THREADS", "MKL_NUM_THREADS",
+                                               "OPENBLAS_NUM_THREADS")}
+    for v in env_keep:
+        os.environ[v] = "1"
+    try:
+        ps = [ctx.Process(target=_oracle_worker,
+                          args=(wl.name, k, 500 + i, rounds, barrier, out))
+              for i in range(procs)]
+        for p in ps:
+            p.start()
+        res, deadline = [], time.time() + 900 + 60 * rounds
+        while len(res) < procs * rounds:
+            try:
+                res.append(out.get(timeout=1.0))
+            except queue.Empty:
+                failed = [p.exitcode for p in ps if p.exitcode not in (None, 0)]
+                if failed or time.time() > deadline:
+                    for p in ps:
+                        p.terminate()
+                    raise RuntimeError(f"all-cores oracle timing failed (exit codes {failed})")
+        for p in ps:
+            p.join()
+    finally:
+        for v, old in env_keep.items():
+            if old is None:
+                os.environ.pop(v, None)
+            else:
+                os.environ[v] = old
+    return [(sum(x[1] for x in res if x[0] == r), max(x[2] for x in res if x[0] == r))
+            for r in range(rounds)]
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def host_memory_bytes() -> int:
+    try:
+        return os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError, AttributeError):
+        return 8 << 30
+
+
+def oracle_procs(wl: I.Workload, k: int) -> int:
+    """Host cores to time the oracle on, capped so that the workers' fp64 arrays (about three
+    copies of a k-token sample of 9 sources and 24 sublayer outputs each) fit in half of the
+    free host memory."""
+    per_worker = 3 * k * wl.d * 8 * (9 + 1 + wl.S)
+    return max(1, min(host_cores(), host_memory_bytes() // 2 // per_worker))
+
+
+def cpu_baseline_line(wl: I.Workload, k1: int, k_all: int):
+    """cpu_baseline: the oracle on all host cores (the reported value) and on one core."""
+    secs1 = time_oracle(wl, k1)
+    cores = oracle_procs(wl, k_all)
+    tok, secs = time_oracle_all_cores(wl, k_all, cores)[0]
+    return {"value": tok / secs, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{k_all} tokens per core x {cores} cores (one process each) of one "
+                      f"24-sublayer block over 9 sources + final aggregation, fp64 numpy; "
+                      f"{secs:.1f} s for the slowest core",
+            "single_core": {"value": k1 / secs1, "unit": "tokens/s", "cores": 1,
+                            "sample": f"{k1} tokens, {secs1:.1f} s"}}
+
+
 # --------------------------------------------------------------------------------------------
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -262,22 +354,22 @@ def reference_arm(args, world, rank):
         return None
     wl = I.LONGCTX_PREFILL_BF16
     k = args.ref_tokens
-    for w in range(args.warmup):
-        time_oracle(wl, k, w)
-    secs = [time_oracle(wl, k, 100 + s) for s in range(args.steps)]
-    step = sum(secs) / len(secs)
-    val = k / step
+    cores = oracle_procs(wl, k)
+    rounds = time_oracle_all_cores(wl, k, cores, args.warmup + args.steps)[args.warmup:]
+    step = sum(r[1] for r in rounds) / len(rounds)      # seconds per step (slowest core)
+    val = rounds[0][0] / step
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
         "n_gpus": getattr(args, "gpus", 1), "runs_on": "host cores (the oracle uses no GPU)",
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": wl.name, "tokens_per_step": k, "d": wl.d, "sources": 9,
+        "config": {"workload": wl.name, "tokens_per_step": k * cores, "d": wl.d, "sources": 9,
                    "S": wl.S},
-        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{k} tokens of one 24-sublayer block over 9 sources + "
-                                   "final aggregation, fp64 numpy, 1 thread"},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{k} tokens per core x {cores} cores (one process each) "
+                                   "of one 24-sublayer block over 9 sources + final "
+                                   "aggregation, fp64 numpy, per step"},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -491,10 +583,11 @@ def run_backward(args):
     return 0
 
 
-def decode_walk_bytes(wl: I.Workload) -> int:
-    """Algorithmic bytes of one decode-shaped depth walk: every block's phase 1 over the
+def walk_bytes(wl: I.Workload) -> int:
+    """Algorithmic bytes of one Block AttnRes depth walk: every block's phase 1 over the
     sources before it, its phase-2 calls and close, then the final aggregation."""
-    d, E, T, S, L = wl.d, 2, wl.T, wl.S, wl.L
+    d, T, S, L = wl.d, wl.T, wl.S, wl.L
+    E = 4 if wl.dtype == "f32" else 2
     total = 0
     for n in range(1, wl.n_blocks + 1):
         Sn = min(S, L - (n - 1) * S)
@@ -504,29 +597,29 @@ def decode_walk_bytes(wl: I.Workload) -> int:
     return total * T
 
 
-def run_decode(args):
-    """Decode-shaped Block AttnRes: 256 tokens (one per sequence), d = 7168, the 186-sublayer
-    depth walk in blocks of 24 (phase 1, the phase-2 calls and the close per block, then the
-    final aggregation): 203 launches of a few MB each.  Timed eager (each call launched from
-    Python through the C ABI) and as one CUDA graph of the same calls, captured once and
-    replayed.  Prints one JSON line; ``value`` is tokens/s of the graph replay."""
-    from depth_wise_softmax_block_b300 import attnres_query_prep, build as B
+def run_block_walk(args, wl: I.Workload):
+    """A whole Block AttnRes depth walk of one workload: every block's phase 1 (tensor-core
+    logits for bf16), its phase-2 calls with the fused partial update and input RMSNorm, the
+    block close into the next source slot, then the final aggregation.  Timed eager (each call
+    launched from Python through the C ABI) and as one CUDA graph of the same calls, captured
+    once and replayed.  Prints one JSON line; ``value`` is tokens/s of the faster launch mode."""
+    from depth_wise_softmax_block_b300 import attnres_poll_device_errors, attnres_query_prep
+    from depth_wise_softmax_block_b300 import build as B
     from depth_wise_softmax_block_b300.schedule import BlockRunner, KernelTimer, final_aggregation
     B.build()
     dev = torch.device("cuda", 0)
-    wl = I.DECODE_BF16
     T, d, S, L, N = wl.T, wl.d, wl.S, wl.L, wl.n_blocks
+    bf16 = wl.dtype == "bf16"
     reps = I.make_reps(wl, N + 1, dev)           # slot 0 = b_0; slot n receives block n
     P = I.block_params(wl, dev)
     U = torch.empty_like(P.W)
-    Us = torch.empty((2 * L, d), dtype=torch.bfloat16, device=dev)
+    Us = torch.empty((2 * L, d), dtype=torch.bfloat16, device=dev) if bf16 else None
     uf = torch.empty((1, d), device=dev)
     attnres_query_prep(P.W, P.G_key, U, Us)
     attnres_query_prep(P.w_final.view(1, -1), P.g_final.view(1, -1), uf)
     vbuf = I.make_outputs(wl, 1, S, dev)        # stand-ins for f_i, shared by the blocks
-    runner = BlockRunner(T, d, S, torch.bfloat16, dev)
-    fin = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
-
+    runner = BlockRunner(T, d, S, wl.torch_dtype, dev)
+    fin = torch.empty((T, d), dtype=wl.torch_dtype, device=dev)
     timer = None
 
     def walk():
@@ -535,7 +628,7 @@ def run_decode(args):
             Sn = min(S, L - l0)
             runner.run_block(reps[:n], U[l0:l0 + Sn], P.G_in[l0:l0 + Sn],
                              lambda i, y: vbuf[i - 1], reps[n], wl.eps, wl.eps,
-                             U_split=Us[2 * l0:2 * (l0 + Sn)])
+                             U_split=None if Us is None else Us[2 * l0:2 * (l0 + Sn)])
         final_aggregation(reps[:N + 1], uf[0], fin, wl.eps, timer=timer)
 
     def timed(fn, k):
@@ -577,25 +670,30 @@ def run_decode(args):
         graph_ms = timed(g.replay, args.steps)
     except Exception as e:  # noqa: BLE001 - reported in the JSON line
         graph_err = f"{type(e).__name__}: {e}"
-    from depth_wise_softmax_block_b300 import attnres_poll_device_errors
     attnres_poll_device_errors()
-    byt = decode_walk_bytes(wl)
-    launches = 2 * N + L + 1
+    byt = walk_bytes(wl)
+    E = 4 if wl.dtype == "f32" else 2
+    launches = 2 * N + L + 1 - sum(1 for n in range(1, N + 1) if min(S, L - (n - 1) * S) == 1)
     peak, kind = peaks()
-    best = graph_ms if graph_ms is not None else eager_ms
-    line = {"metric": "Decode-shaped Block AttnRes: tokens/s of the whole 186-sublayer depth walk "
-                      "(256 tokens), 1 GPU",
+    best = eager_ms if graph_ms is None else min(eager_ms, graph_ms)
+    n_last = N                                   # sources of the last block's phase 1
+    line = {"metric": f"Block AttnRes whole-depth walk ({L} sublayers, {T} tokens): tokens/s "
+                      "and achieved HBM GB/s, 1 GPU",
             "value": T / (best / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": best, "higher_is_better": True,
-            "dtype": "bf16", "data": "synthetic",
+            "dtype": wl.dtype, "data": "synthetic",
             "config": {"workload": wl.name, "tokens": T, "d": d, "sublayers": L, "S": S,
-                       "blocks": N, "launch": "cuda_graph" if graph_ms is not None else "eager"},
+                       "blocks": N, "launch": "cuda_graph" if best == graph_ms else "eager",
+                       "l2": "no flush" if byt / L < 126e6 else
+                             "no flush: launches stream more than the 126 MB L2"},
             "eager_ms": eager_ms, "graph_ms": graph_ms,
             "us_per_sublayer": {"eager": eager_ms * 1e3 / L,
                                 "graph": None if graph_ms is None else graph_ms * 1e3 / L},
             "bytes_per_step": byt, "achieved_gbs": byt / (best / 1e3) / 1e9,
             "frac_of_peak": byt / (best / 1e3) / 1e9 / peak, "peak_gbs": peak,
             "peak_source": kind, "gpu_launches": launches * args.steps,
+            "d_elements_per_sublayer": byt / T / L / d / E,
+            "pages_formula_d_elements": {"(N/S + 5) d, last block": n_last / S + 5},
             "kernels_eager_one_walk": per_kernel}
     if graph_err:
         line["graph_error"] = graph_err
@@ -612,17 +710,22 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--cpu-tokens", type=int, default=512,
-                    help="oracle sample for cpu_baseline (about 10 s of one core)")
-    ap.add_argument("--ref-tokens", type=int, default=64,
-                    help="oracle sample per step of the reference arm (about 1 s)")
+                    help="oracle sample for the one-core cpu_baseline (about 10 s)")
+    ap.add_argument("--cpu-tokens-per-core", type=int, default=256,
+                    help="oracle sample per core for the all-cores cpu_baseline")
+    ap.add_argument("--ref-tokens", type=int, default=32,
+                    help="oracle sample per core and step of the reference arm (about 2 s)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the token count (profiling a smaller case)")
     ap.add_argument("--chunk", type=int, default=0, help="override the chunk size")
     ap.add_argument("--workload", default="longctx",
-                    choices=["longctx", "full_grouped", "backward", "decode"],
+                    choices=["longctx", "full_grouped", "backward", "decode", "prefill_chunk",
+                             "tiny"],
                     help="full_grouped: the Full AttnRes depth, grouped two-phase vs direct; "
-                         "backward: one sublayer's aggregation backward; decode: the "
-                         "256-token depth walk, eager and as a CUDA graph")
+                         "backward: one sublayer's aggregation backward; decode, "
+                         "prefill_chunk, tiny: the whole Block AttnRes depth walk of the "
+                         "256-token decode, 16384-token prefill-chunk or tiny fp32 workload, "
+                         "eager and as a CUDA graph")
     ap.add_argument("--group", type=int, default=8, help="group size of --workload full_grouped")
     ap.add_argument("--heads", type=int, default=1,
                     help="depth-attention heads of the longctx step (Table 4 multi-head: 16)")
@@ -633,8 +736,10 @@ def main(argv=None):
         return run_full_grouped(args)
     if args.workload == "backward" and args.impl == "ours":
         return run_backward(args)
-    if args.workload == "decode" and args.impl == "ours":
-        return run_decode(args)
+    walks = {"decode": I.DECODE_BF16, "prefill_chunk": I.PREFILL_CHUNK_BF16,
+             "tiny": I.TINY_BLOCK_F32}
+    if args.workload in walks and args.impl == "ours":
+        return run_block_walk(args, walks[args.workload])
     if args.impl == "reference":
         line = reference_arm(args, world, rank)
         if line is not None:
@@ -722,12 +827,7 @@ def main(argv=None):
     if not args.no_e2e and rank == 0:
         line["e2e"] = run_e2e(step, args.e2e_steps)
     if rank == 0:
-        secs = time_oracle(wl, args.cpu_tokens)
-        line["cpu_baseline"] = {"value": args.cpu_tokens / secs, "unit": "tokens/s", "cores": 1,
-                                "kind": "oracle",
-                                "sample": f"{args.cpu_tokens} tokens of one 24-sublayer block "
-                                          "over 9 sources + final aggregation, fp64 numpy, "
-                                          f"1 thread, {secs:.1f} s"}
+        line["cpu_baseline"] = cpu_baseline_line(wl, args.cpu_tokens, args.cpu_tokens_per_core)
         print(json.dumps(line), flush=True)
     barrier(world)
     return 0

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libattnres.so")
 
 F32, BF16 = 0, 1
 SIGMOID_WEIGHTS, NO_KEY_NORM = 0x1, 0x2   # variant flags (include/attnres.h)
+O_F32 = 0x4                               # phase 1's output o stored in fp32
 _U = ctypes.c_uint
 STATUS = {0: "ATTNRES_OK", 1: "ATTNRES_ERR_INVALID_ARG", 2: "ATTNRES_ERR_UNSUPPORTED",
           3: "ATTNRES_ERR_MISALIGNED", 4: "ATTNRES_ERR_CUDA", 5: "ATTNRES_ERR_TIMEOUT"}
@@ -134,13 +135,22 @@ def attnres_query_prep(w, gamma_key, u_out, u_split_out=None, stream=None):
     return u_out
 
 
+def _o_flag(o, io_dtype) -> int:
+    """ATTNRES_O_F32 when phase 1's output ``o`` is fp32 and the I/O type is not."""
+    if o.dtype == io_dtype:
+        return 0
+    if o.dtype == torch.float32:
+        return O_F32
+    raise TypeError(f"phase-1 output of dtype {o.dtype} with I/O dtype {io_dtype}")
+
+
 def attnres_phase1(reps, u, o_out, m_out=None, lse_out=None, alpha_out=None, eps=1e-6,
                    u_split=None, flags=0, heads=1, stream=None):
     """Phase 1 over ``reps`` [n, T, d] (any source stride, rows of stride d) for the S queries
     ``u`` [S, d]; writes o [S, T, d] and the optional statistics (m, lse [S, heads, T], alpha
     [S, heads, T, n]; with one head the head axis may be left out).  ``u_split`` ([2S, d]
     bf16, from attnres_query_prep) puts the logits on the tensor cores where the shape
-    allows."""
+    allows.  An fp32 ``o_out`` with bf16 sources stores o in fp32 (ATTNRES_O_F32)."""
     n, T, d = reps.shape
     S = u.shape[0]
     if u_split is not None and (tuple(u_split.shape) != (2 * S, d) or not u_split.is_contiguous()
@@ -152,6 +162,7 @@ def attnres_phase1(reps, u, o_out, m_out=None, lse_out=None, alpha_out=None, eps
     src_stride = reps.stride(0) if n > 1 else T * d
     for name, t, per in (("m_out", m_out, 1), ("lse_out", lse_out, 1), ("alpha_out", alpha_out, n)):
         _stats(t, S * heads * T * per, name)
+    flags |= _o_flag(o_out, reps.dtype)
     _check(library().attnres_phase1(_ptr(reps), src_stride, n, T, d, _io(reps), _ptr(u),
                                     _ptr(u_split), S, eps, _ptr(o_out), _ptr(m_out), _ptr(lse_out),
                                     _ptr(alpha_out), flags, heads, _stream(stream)),
@@ -164,15 +175,17 @@ def attnres_phase2_merge(o_l, lse_l, partial, v_prev, partial_out, u_l, gamma_in
                          heads=1, stream=None):
     """Phase 2 for one sublayer: merge the partial-sum source (partial + v_prev) into the
     phase-1 result and apply the input RMSNorm.  Tensors are [T, d]; lse_l and alpha_p_out
-    are [heads, T] (or [T] with one head)."""
+    are [heads, T] (or [T] with one head).  The I/O type is y_out's; an fp32 ``o_l`` with bf16
+    I/O is read as fp32 (ATTNRES_O_F32)."""
     T, d = o_l.shape
     for name, t in (("o_l", o_l), ("partial", partial), ("v_prev", v_prev),
                     ("partial_out", partial_out), ("y_out", y_out), ("h_out", h_out)):
         _rows(t, T, d, name)
     _stats(lse_l, heads * T, "lse_l")
     _stats(alpha_p_out, heads * T, "alpha_p_out")
+    flags |= _o_flag(o_l, y_out.dtype)
     _check(library().attnres_phase2_merge(
-        _ptr(o_l), _ptr(lse_l), _ptr(partial), _ptr(v_prev), _ptr(partial_out), T, d, _io(o_l),
+        _ptr(o_l), _ptr(lse_l), _ptr(partial), _ptr(v_prev), _ptr(partial_out), T, d, _io(y_out),
         _ptr(u_l), eps_key, _ptr(gamma_in), eps_in, _ptr(h_out), _ptr(y_out), _ptr(alpha_p_out),
         flags, heads, _stream(stream)), "attnres_phase2_merge")
     return y_out
@@ -210,8 +223,11 @@ def attnres_phase2_merge_sources(o_l, lse_l, srcs, u_l, gamma_in, h_out=None, y_
                                  stream=None):
     """Grouped Full AttnRes phase 2 for one layer: merge phase 1's (o_l, lse_l) with the
     group's in-group sources ``srcs`` (a list of [T, d] tensors, possibly empty); lse_l is
-    [heads, T] and alpha_out [heads, T, k] (head axis optional with one head)."""
+    [heads, T] and alpha_out [heads, T, k] (head axis optional with one head).  The I/O type is
+    that of the outputs; an fp32 ``o_l`` with bf16 I/O is read as fp32 (ATTNRES_O_F32)."""
     T, d = o_l.shape
+    io_dtype = (y_out if y_out is not None else h_out).dtype
+    flags |= _o_flag(o_l, io_dtype)
     for name, t in [("o_l", o_l), ("h_out", h_out), ("y_out", y_out)] + \
             [("srcs[j]", t) for t in srcs]:
         _rows(t, T, d, name)
@@ -219,9 +235,10 @@ def attnres_phase2_merge_sources(o_l, lse_l, srcs, u_l, gamma_in, h_out=None, y_
     _stats(alpha_out, heads * T * len(srcs), "alpha_out")
     arr = (ctypes.c_void_p * max(1, len(srcs)))(*[t.data_ptr() for t in srcs])
     _check(library().attnres_phase2_merge_sources(
-        _ptr(o_l), _ptr(lse_l), arr if srcs else None, len(srcs), T, d, _io(o_l), _ptr(u_l),
-        eps_key, _ptr(gamma_in), eps_in, _ptr(h_out), _ptr(y_out), _ptr(alpha_out), flags, heads,
-        _stream(stream)), "attnres_phase2_merge_sources")
+        _ptr(o_l), _ptr(lse_l), arr if srcs else None, len(srcs), T, d,
+        BF16 if io_dtype == torch.bfloat16 else F32, _ptr(u_l), eps_key, _ptr(gamma_in), eps_in,
+        _ptr(h_out), _ptr(y_out), _ptr(alpha_out), flags, heads, _stream(stream)),
+        "attnres_phase2_merge_sources")
     return h_out if y_out is None else y_out
 
 

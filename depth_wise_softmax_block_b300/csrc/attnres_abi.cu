@@ -20,6 +20,8 @@ bool valid_io(attnres_dtype io) { return io == ATTNRES_F32 || io == ATTNRES_BF16
 bool valid_flags(unsigned flags) {
   return (flags & ~(ATTNRES_SIGMOID_WEIGHTS | ATTNRES_NO_KEY_NORM)) == 0;
 }
+// The entry points that pass phase 1's output on also take its storage flag.
+bool valid_o_flags(unsigned flags) { return valid_flags(flags & ~ATTNRES_O_F32); }
 
 attnres_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return ATTNRES_OK;
@@ -101,7 +103,7 @@ attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, i
                               attnres_dtype io, const float* u, const void* u_split, int S,
                               float eps, void* o_out, float* m_out, float* lse_out,
                               float* alpha_out, unsigned int flags, int heads, void* stream) {
-  if (!valid_io(io) || !valid_flags(flags)) return ATTNRES_ERR_INVALID_ARG;
+  if (!valid_io(io) || !valid_o_flags(flags)) return ATTNRES_ERR_INVALID_ARG;
   attnres_status sh = check_shape(T, d);
   if (sh == ATTNRES_OK) sh = check_heads(d, heads);
   if (sh != ATTNRES_OK) return sh;
@@ -127,7 +129,7 @@ attnres_status attnres_phase2_merge(const void* o_l, const float* lse_l, const v
                                     const float* gamma_in, float eps_in, void* h_out, void* y_out,
                                     float* alpha_p_out, unsigned int flags, int heads,
                                     void* stream) {
-  if (!valid_io(io) || !valid_flags(flags)) return ATTNRES_ERR_INVALID_ARG;
+  if (!valid_io(io) || !valid_o_flags(flags)) return ATTNRES_ERR_INVALID_ARG;
   attnres_status sh = check_shape(T, d);
   if (sh == ATTNRES_OK) sh = check_heads(d, heads);
   if (sh != ATTNRES_OK) return sh;
@@ -209,7 +211,7 @@ attnres_status attnres_phase2_merge_sources(const void* o_l, const float* lse_l,
                                             const float* gamma_in, float eps_in, void* h_out,
                                             void* y_out, float* alpha_out, unsigned int flags,
                                             int heads, void* stream) {
-  if (!valid_io(io) || !valid_flags(flags)) return ATTNRES_ERR_INVALID_ARG;
+  if (!valid_io(io) || !valid_o_flags(flags)) return ATTNRES_ERR_INVALID_ARG;
   attnres_status sh = check_shape(T, d);
   if (sh == ATTNRES_OK) sh = check_heads(d, heads);
   if (sh != ATTNRES_OK) return sh;
@@ -244,6 +246,7 @@ attnres_status attnres_phase2_merge_sources(const void* o_l, const float* lse_l,
   a.heads = heads;
   a.o0 = o_l;
   a.lse0 = lse_l;
+  a.o0_f32 = io == ATTNRES_BF16 && (flags & ATTNRES_O_F32) != 0;
   return cuda_status(attnres::launch_full(static_cast<IO>(io), a,
                                           static_cast<cudaStream_t>(stream)));
 }

@@ -61,6 +61,48 @@ __device__ __forceinline__ uint4 pack(const float (&f)[4]) {
                     __float_as_uint(f[3]));
 }
 
+// A row vector of VE elements (VE = elements per 16 bytes of the I/O type) stored as TO, which
+// is the I/O type or fp32: NW = VE * sizeof(TO) / 16 words of 16 bytes.
+template <typename TO, int VE> struct OWords {
+  static constexpr int N = VE * int(sizeof(TO)) / 16;
+};
+
+template <typename TO, int VE>
+__device__ __forceinline__ void ld_stream_w(const TO* p, uint4 (&r)[OWords<TO, VE>::N]) {
+#pragma unroll
+  for (int i = 0; i < OWords<TO, VE>::N; ++i)
+    r[i] = ld_stream(reinterpret_cast<const char*>(p) + 16 * i);
+}
+
+template <typename TO, int VE>
+__device__ __forceinline__ void unpack_w(const uint4 (&r)[OWords<TO, VE>::N], float (&f)[VE]) {
+  if constexpr (sizeof(TO) == 2) {
+    unpack(r[0], f);
+  } else {
+#pragma unroll
+    for (int i = 0; i < OWords<TO, VE>::N; ++i) {
+      f[4 * i] = __uint_as_float(r[i].x);
+      f[4 * i + 1] = __uint_as_float(r[i].y);
+      f[4 * i + 2] = __uint_as_float(r[i].z);
+      f[4 * i + 3] = __uint_as_float(r[i].w);
+    }
+  }
+}
+
+// Stores VE elements as TO (bf16 rounded to nearest even, or fp32 as computed).
+template <typename TO, int VE>
+__device__ __forceinline__ void st_vec(TO* p, const float (&f)[VE]) {
+  if constexpr (sizeof(TO) == 2) {
+    st_global(p, pack(f));
+  } else {
+#pragma unroll
+    for (int i = 0; i < VE / 4; ++i)
+      st_global(reinterpret_cast<char*>(p) + 16 * i,
+                make_uint4(__float_as_uint(f[4 * i]), __float_as_uint(f[4 * i + 1]),
+                           __float_as_uint(f[4 * i + 2]), __float_as_uint(f[4 * i + 3])));
+  }
+}
+
 // Eight consecutive elements starting at a 16-byte aligned address (generic or shared).
 template <typename T> __device__ __forceinline__ void load8(const void* p, float (&f)[8]);
 template <> __device__ __forceinline__ void load8<bf16>(const void* p, float (&f)[8]) {

@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) full_ring_kernel(const FullAr
       // Drain: the last copy issued into every slot has landed before the CTA may exit.
       for (int s = 0; s < SB && s < it; ++s) {
         const int last = it - 1 - ((it - 1 - s) % SB);
-        mbar_wait(&full[s], (last / SB) & 1);
+        mbar_wait_drain(&full[s], (last / SB) & 1);
       }
     }
     return;
@@ -265,7 +265,12 @@ __global__ void __launch_bounds__(kRingThreads, 1) full_ring_kernel(const FullAr
     for (int k = 0; k < kRingVPT; ++k) {
       const int v = tid + k * kRingCompute;
       if (v < nv) {
-        if (a.h != nullptr) st_global(static_cast<T*>(a.h) + base + v * VE, pack(acc[k]));
+        if (a.h != nullptr) {
+          if (a.h_f32)
+            st_vec<float, VE>(static_cast<float*>(a.h) + base + v * VE, acc[k]);
+          else
+            st_global(static_cast<T*>(a.h) + base + v * VE, pack(acc[k]));
+        }
         if (a.y != nullptr) {
           float y[VE];
 #pragma unroll
@@ -314,13 +319,7 @@ cudaError_t launch_full_ring(IO io, const FullArgs& a, cudaStream_t s) {
 }
 
 unsigned int full_ring_poll_timeouts() {
-  unsigned int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_wait_timeouts, sizeof(v)) != cudaSuccess) return 0xffffffffu;
-  if (v != 0) {
-    const unsigned int z = 0;
-    cudaMemcpyToSymbol(g_wait_timeouts, &z, sizeof(z));
-  }
-  return v;
+  return take_wait_timeouts();
 }
 
 }  // namespace attnres

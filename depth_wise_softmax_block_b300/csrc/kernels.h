@@ -13,6 +13,9 @@ enum class IO { F32 = 0, BF16 = 1 };
 // Variant flags (values of ATTNRES_SIGMOID_WEIGHTS / ATTNRES_NO_KEY_NORM in attnres.h).
 constexpr unsigned kSigmoid = 1u;    // alpha_i = sigmoid(z_i), no normalisation over sources
 constexpr unsigned kNoKeyNorm = 2u;  // z_i = u . v_i, no RMS division
+// Phase 1's output o is stored in fp32 whatever the I/O type (value of ATTNRES_O_F32); phase 2
+// and the grouped merge then read o_l in fp32.
+constexpr unsigned kOF32 = 4u;
 
 struct Phase1Args {
   const void* reps;
@@ -71,6 +74,8 @@ struct FullArgs {
   const void* o0;   // [T, d] or null: normalised output of an earlier source partition
   const float* lse0;  // [H][T]: its log-sum-exp (required with o0 unless sigmoid weights)
   int heads;          // alpha [H][T][n], m and lse [H][T]
+  bool h_f32;         // h is stored in fp32 (phase 1 with one query and kOF32)
+  bool o0_f32;        // o0 is stored in fp32 (the grouped merge with kOF32)
 };
 
 // Backward of one sublayer's aggregation (backward.cu).

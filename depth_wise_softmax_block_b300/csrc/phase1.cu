@@ -107,6 +107,14 @@ __device__ __forceinline__ void st_stream(void* p, uint4 v) {
 template <typename T> struct Chunk;
 template <> struct Chunk<bf16> {
   static constexpr int PR = 4;
+  // The same pairs stored as fp32 (phase 1's o with kOF32): two 16-byte words.
+  static __device__ __forceinline__ void store_f32(void* p, const float2 (&f)[PR]) {
+    st_stream(p, make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y),
+                            __float_as_uint(f[1].x), __float_as_uint(f[1].y)));
+    st_stream(static_cast<char*>(p) + 16,
+              make_uint4(__float_as_uint(f[2].x), __float_as_uint(f[2].y),
+                         __float_as_uint(f[3].x), __float_as_uint(f[3].y)));
+  }
   static __device__ __forceinline__ void load(const void* p, float2 (&f)[PR]) {
     const uint4 v = *reinterpret_cast<const uint4*>(p);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -121,6 +129,9 @@ template <> struct Chunk<bf16> {
 };
 template <> struct Chunk<float> {
   static constexpr int PR = 2;
+  static __device__ __forceinline__ void store_f32(void* p, const float2 (&f)[PR]) {
+    store(p, f);
+  }
   static __device__ __forceinline__ void load(const void* p, float2 (&f)[PR]) {
     const float4 a = *reinterpret_cast<const float4*>(p);
     f[0] = make_float2(a.x, a.y);
@@ -348,6 +359,7 @@ phase1_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ 
   const int64_t tok2 = t0 + t2;
   const float* at = alph + (t2 * n * QG + g2) * NQ * 2;
   char* o = static_cast<char*>(a.o);
+  const bool of32 = (a.flags & kOF32) != 0;  // o stored in fp32 whatever the I/O type
   for (int c = 0; c < nch; ++c, ++it) {
     const int slot = it % ST;
     acquire(slot);
@@ -392,9 +404,13 @@ phase1_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ 
 #pragma unroll
         for (int qq = 0; qq < NQ; ++qq) {
           const int q = g2 * NQ + qq;
-          if (q < S)
-            Chunk<IOT>::store(o + ((static_cast<int64_t>(q) * T + tok2) * d + cw + k) * E,
-                              acc2[qq]);
+          const int64_t at = (static_cast<int64_t>(q) * T + tok2) * d + cw + k;
+          if (q < S) {
+            if (of32)
+              Chunk<IOT>::store_f32(o + at * 4, acc2[qq]);
+            else
+              Chunk<IOT>::store(o + at * E, acc2[qq]);
+          }
         }
       }
     }
@@ -405,7 +421,7 @@ phase1_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ 
   if (tid == 0) {
     for (int s = 0; s < ST && s < issued; ++s) {
       const int last = issued - 1 - ((issued - 1 - s) % ST);
-      mbar_wait(&full[s], (last / ST) & 1);
+      mbar_wait_drain(&full[s], (last / ST) & 1);
     }
   }
 }
@@ -464,6 +480,7 @@ cudaError_t launch_phase1(IO io, const Phase1Args& a, cudaStream_t s) {
     f.lse = a.lse;
     f.flags = a.flags;
     f.heads = a.heads;
+    f.h_f32 = io == IO::BF16 && (a.flags & kOF32) != 0;
     return launch_full(io, f, s);
   }
   if (io == IO::BF16 && a.u_split != nullptr && phase1_tc_supported(a.n, a.S, a.d, a.heads))
@@ -472,13 +489,7 @@ cudaError_t launch_phase1(IO io, const Phase1Args& a, cudaStream_t s) {
 }
 
 unsigned int phase1_poll_timeouts() {
-  unsigned int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_wait_timeouts, sizeof(v)) != cudaSuccess) return 0xffffffffu;
-  if (v != 0) {
-    const unsigned int z = 0;
-    cudaMemcpyToSymbol(g_wait_timeouts, &z, sizeof(z));
-  }
-  return v;
+  return take_wait_timeouts();
 }
 
 }  // namespace attnres

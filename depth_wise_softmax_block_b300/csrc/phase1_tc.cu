@@ -236,7 +236,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
       // Drain: the last copy issued into every slot has landed before the CTA may exit.
       for (int s = 0; s < SB && s < ib; ++s) {
         const int last = ib - 1 - ((ib - 1 - s) % SB);
-        mbar_wait(&full[s], (last / SB) & 1);
+        mbar_wait_drain(&full[s], (last / SB) & 1);
       }
     }
     return;
@@ -503,6 +503,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   // source j's chunk: row j * 8 + t2, swizzled chunk kg ^ t2 (independent of j)
   const int boff = t2 * 128 + ((kg ^ t2) << 4);
   char* o = static_cast<char*>(a.o);
+  const bool of32 = (a.flags & kOF32) != 0;  // o stored in fp32 instead of bf16
   const int first2 = nch + (((nch & 1) != half) ? 1 : 0);
   RingPos rp2(first2, SB);
   for (int ib = first2; ib < total; ib += 2, rp2.advance(2, SB)) {
@@ -550,7 +551,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
         }
       }
       const int k = c * kKC + kg * 8;  // column in the window
-      if (tok2 < T && k < wcols) {
+      if (tok2 < T && k < wcols && !of32) {
         char* op = o + ((static_cast<int64_t>(grp * 6) * T + tok2) * d + cw + k) * 2;
         const int64_t qstride = T * d * 2;
 #pragma unroll
@@ -562,6 +563,20 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
                               pack_bf16x2(acc[qq][2].x, acc[qq][2].y),
                               pack_bf16x2(acc[qq][3].x, acc[qq][3].y)));
         }
+      } else if (tok2 < T && k < wcols) {  // o in fp32: two 16-byte words per chunk
+        char* op = o + ((static_cast<int64_t>(grp * 6) * T + tok2) * d + cw + k) * 4;
+        const int64_t qstride = T * d * 4;
+#pragma unroll
+        for (int qq = 0; qq < 6; ++qq) {
+          if (grp * 6 + qq < S) {
+            uint4* q4 = reinterpret_cast<uint4*>(op + qq * qstride);
+            __stcs(q4, make_uint4(__float_as_uint(acc[qq][0].x), __float_as_uint(acc[qq][0].y),
+                                  __float_as_uint(acc[qq][1].x), __float_as_uint(acc[qq][1].y)));
+            __stcs(q4 + 1,
+                   make_uint4(__float_as_uint(acc[qq][2].x), __float_as_uint(acc[qq][2].y),
+                              __float_as_uint(acc[qq][3].x), __float_as_uint(acc[qq][3].y)));
+          }
+        }
       }
     }
     release(bs, true);
@@ -572,7 +587,8 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   named_barrier(1, kCompute);
   tc_fence_after();
   if (warp == 0) {
-    if (lane == 0 && *abort_flag) mbar_wait(dready, 0);  // MMAs of an aborted run may still run
+    // the MMAs of an aborted run may still be running
+    if (lane == 0 && *abort_flag) mbar_wait_drain(dready, 0);
     __syncwarp();
     tmem_dealloc(tmem, pl.tcols);
   }
@@ -683,13 +699,7 @@ cudaError_t launch_wait_selftest(unsigned int polls, cudaStream_t s) {
 }
 
 unsigned int phase1_tc_poll_timeouts() {
-  unsigned int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_wait_timeouts, sizeof(v)) != cudaSuccess) return 0xffffffffu;
-  if (v != 0) {
-    const unsigned int z = 0;
-    cudaMemcpyToSymbol(g_wait_timeouts, &z, sizeof(z));
-  }
-  return v;
+  return take_wait_timeouts();
 }
 
 }  // namespace attnres

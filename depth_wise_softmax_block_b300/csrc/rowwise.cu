@@ -77,8 +77,9 @@ __device__ __forceinline__ void head_sum2(const float (&pa)[VPT], const float (&
 // reduction buffer (the block reductions synchronise the CTA).  kHeads: H > 1 depth-attention
 // heads, each merging its slice with its own z_p and lse; `red` is then 2 * nv + 2 * H floats of
 // shared memory.
-template <typename T, int VPT, bool kHeads>
-__device__ __forceinline__ void merge_row(const Phase2Args& a, int64_t row, const uint4 (&ro)[VPT],
+template <typename T, typename TO, int VPT, bool kHeads>
+__device__ __forceinline__ void merge_row(const Phase2Args& a, int64_t row,
+                                          const uint4 (&ro)[VPT][OWords<TO, Vec<T>::N>::N],
                                           const uint4 (&rp)[VPT], const uint4 (&rv)[VPT],
                                           float* scratch, float* red) {
   constexpr int VE = Vec<T>::N;
@@ -186,7 +187,7 @@ __device__ __forceinline__ void merge_row(const Phase2Args& a, int64_t row, cons
   for (int k = 0; k < VPT; ++k) {
     const int v = threadIdx.x + k * blockDim.x;
     if (v < nv) {
-      unpack(ro[k], h[k]);
+      unpack_w<TO, VE>(ro[k], h[k]);
       if (has_p) {
 #pragma unroll
         for (int e = 0; e < VE; ++e) h[k][e] = fmaf(wa[k], h[k][e], wc[k] * p[k][e]);
@@ -223,8 +224,9 @@ __device__ __forceinline__ void merge_row(const Phase2Args& a, int64_t row, cons
   }
 }
 
-// One CTA per row; every load of the row is issued before any arithmetic.
-template <typename T, int VPT, bool kHeads>
+// One CTA per row; every load of the row is issued before any arithmetic.  TO: the type o_l is
+// stored in (the I/O type, or fp32 with kOF32).
+template <typename T, typename TO, int VPT, bool kHeads>
 __global__ void __launch_bounds__(kMergeThreads) phase2_kernel(const Phase2Args a) {
   constexpr int VE = Vec<T>::N;
   __shared__ float scratch[66];
@@ -233,17 +235,17 @@ __global__ void __launch_bounds__(kMergeThreads) phase2_kernel(const Phase2Args 
   const int64_t row = blockIdx.x;
   const int nv = a.d / VE;
   const int64_t base = row * a.d;
-  uint4 ro[VPT], rp[VPT], rv[VPT];
+  uint4 ro[VPT][OWords<TO, VE>::N], rp[VPT], rv[VPT];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     const int v = threadIdx.x + k * blockDim.x;
     if (v < nv) {
-      ro[k] = ld_stream(static_cast<const T*>(a.o) + base + v * VE);
+      ld_stream_w<TO, VE>(static_cast<const TO*>(a.o) + base + v * VE, ro[k]);
       if (a.partial) rp[k] = ld_stream(static_cast<const T*>(a.partial) + base + v * VE);
       if (a.v_prev) rv[k] = ld_stream(static_cast<const T*>(a.v_prev) + base + v * VE);
     }
   }
-  merge_row<T, VPT, kHeads>(a, row, ro, rp, rv, scratch, red);
+  merge_row<T, TO, VPT, kHeads>(a, row, ro, rp, rv, scratch, red);
 }
 
 // Online softmax over the sources, one source per step, with the rows of the next two sources
@@ -294,7 +296,15 @@ __global__ void __launch_bounds__(kRowThreads) full_kernel(const FullArgs a) {
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int v = threadIdx.x + k * blockDim.x;
-      if (v < nv) unpack(ld_stream(static_cast<const T*>(a.o0) + base + v * VE), acc[k]);
+      if (v < nv) {
+        if (a.o0_f32) {
+          uint4 r[OWords<float, VE>::N];
+          ld_stream_w<float, VE>(static_cast<const float*>(a.o0) + base + v * VE, r);
+          unpack_w<float, VE>(r, acc[k]);
+        } else {
+          unpack(ld_stream(static_cast<const T*>(a.o0) + base + v * VE), acc[k]);
+        }
+      }
     }
     if ((a.flags & kSigmoid) == 0) {
 #pragma unroll
@@ -449,7 +459,12 @@ __global__ void __launch_bounds__(kRowThreads) full_kernel(const FullArgs a) {
   for (int k = 0; k < VPT; ++k) {
     const int v = threadIdx.x + k * blockDim.x;
     if (v < nv) {
-      if (a.h) st_global(static_cast<T*>(a.h) + base + v * VE, pack(acc[k]));
+      if (a.h) {
+        if (a.h_f32)
+          st_vec<float, VE>(static_cast<float*>(a.h) + base + v * VE, acc[k]);
+        else
+          st_global(static_cast<T*>(a.h) + base + v * VE, pack(acc[k]));
+      }
       if (a.y) {
         float y[VE];
 #pragma unroll
@@ -480,7 +495,7 @@ constexpr int kHeadWarpsMax = 16;
 // Resident CTAs per SM asked of the compiler (registers), for enough loads in flight.
 template <int VH> constexpr int heads_min_blocks() { return VH <= 2 ? 2 : 1; }
 
-template <typename T, int VH>
+template <typename T, typename TO, int VH>
 __global__ void __launch_bounds__(kHeadWarpsMax * 32, heads_min_blocks<VH>())
     phase2_heads_kernel(const Phase2Args a) {
   constexpr int VE = Vec<T>::N;
@@ -491,12 +506,12 @@ __global__ void __launch_bounds__(kHeadWarpsMax * 32, heads_min_blocks<VH>())
   const int nvh = a.d / VE / a.heads;
   const int64_t base = row * a.d + static_cast<int64_t>(hd) * nvh * VE;  // the head's slice
   const bool has_p = a.partial != nullptr || a.v_prev != nullptr;
-  uint4 ro[VH], rp[VH], rv[VH];
+  uint4 ro[VH][OWords<TO, VE>::N], rp[VH], rv[VH];
 #pragma unroll
   for (int q = 0; q < VH; ++q) {
     const int i = lane + 32 * q;
     if (i < nvh) {
-      ro[q] = ld_stream(static_cast<const T*>(a.o) + base + i * VE);
+      ld_stream_w<TO, VE>(static_cast<const TO*>(a.o) + base + i * VE, ro[q]);
       if (a.partial) rp[q] = ld_stream(static_cast<const T*>(a.partial) + base + i * VE);
       if (a.v_prev) rv[q] = ld_stream(static_cast<const T*>(a.v_prev) + base + i * VE);
     }
@@ -557,7 +572,7 @@ __global__ void __launch_bounds__(kHeadWarpsMax * 32, heads_min_blocks<VH>())
 #pragma unroll
     for (int e = 0; e < VE; ++e) h[q][e] = 0.f;
     if (i < nvh) {
-      unpack(ro[q], h[q]);
+      unpack_w<TO, VE>(ro[q], h[q]);
       if (has_p) {
 #pragma unroll
         for (int e = 0; e < VE; ++e) h[q][e] = fmaf(wa, h[q][e], wc * p[q][e]);
@@ -622,7 +637,15 @@ __global__ void __launch_bounds__(kHeadWarpsMax * 32, VH <= 2 ? 2 : 1)
 #pragma unroll
     for (int q = 0; q < VH; ++q) {
       const int i = lane + 32 * q;
-      if (i < nvh) unpack(ld_stream(static_cast<const T*>(a.o0) + base + i * VE), acc[q]);
+      if (i < nvh) {
+        if (a.o0_f32) {
+          uint4 r[OWords<float, VE>::N];
+          ld_stream_w<float, VE>(static_cast<const float*>(a.o0) + base + i * VE, r);
+          unpack_w<float, VE>(r, acc[q]);
+        } else {
+          unpack(ld_stream(static_cast<const T*>(a.o0) + base + i * VE), acc[q]);
+        }
+      }
     }
     if (!sigmoid) {
       mrun = a.lse0[static_cast<int64_t>(hd) * a.T + row];
@@ -731,7 +754,12 @@ __global__ void __launch_bounds__(kHeadWarpsMax * 32, VH <= 2 ? 2 : 1)
   for (int q = 0; q < VH; ++q) {
     const int i = lane + 32 * q;
     if (i < nvh) {
-      if (a.h) st_global(static_cast<T*>(a.h) + base + i * VE, pack(acc[q]));
+      if (a.h) {
+        if (a.h_f32)
+          st_vec<float, VE>(static_cast<float*>(a.h) + base + i * VE, acc[q]);
+        else
+          st_global(static_cast<T*>(a.h) + base + i * VE, pack(acc[q]));
+      }
       if (a.y) {
         float y[VE];
 #pragma unroll
@@ -814,14 +842,14 @@ inline void row_geometry(int nv, int& vpt, int& threads, int max_threads = kRowT
   threads = ((nv + vpt - 1) / vpt + 31) / 32 * 32;
 }
 
-template <typename T>
+template <typename T, typename TO>
 cudaError_t phase2_heads(const Phase2Args& a, int vh, cudaStream_t s) {
   const unsigned grid = static_cast<unsigned>(a.T);
   const int threads = 32 * a.heads;
   switch (vh) {
-    case 1: return launch_pdl(phase2_heads_kernel<T, 1>, grid, threads, 0, s, a);
-    case 2: return launch_pdl(phase2_heads_kernel<T, 2>, grid, threads, 0, s, a);
-    case 4: return launch_pdl(phase2_heads_kernel<T, 4>, grid, threads, 0, s, a);
+    case 1: return launch_pdl(phase2_heads_kernel<T, TO, 1>, grid, threads, 0, s, a);
+    case 2: return launch_pdl(phase2_heads_kernel<T, TO, 2>, grid, threads, 0, s, a);
+    case 4: return launch_pdl(phase2_heads_kernel<T, TO, 4>, grid, threads, 0, s, a);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -838,26 +866,27 @@ cudaError_t full_heads(const FullArgs& a, int vh, cudaStream_t s) {
   }
 }
 
-template <typename T, int VPT>
+template <typename T, typename TO, int VPT>
 cudaError_t phase2_vpt(const Phase2Args& a, unsigned grid, int threads, cudaStream_t s) {
-  if (a.heads == 1) return launch_pdl(phase2_kernel<T, VPT, false>, grid, threads, 0, s, a);
+  if (a.heads == 1) return launch_pdl(phase2_kernel<T, TO, VPT, false>, grid, threads, 0, s, a);
   const int smem = (2 * (a.d / Vec<T>::N) + 2 * a.heads) * static_cast<int>(sizeof(float));
-  return launch_pdl(phase2_kernel<T, VPT, true>, grid, threads, smem, s, a);
+  return launch_pdl(phase2_kernel<T, TO, VPT, true>, grid, threads, smem, s, a);
 }
 
-template <typename T>
+// TO: the type phase 1's output o_l is stored in (T, or fp32 with kOF32).
+template <typename T, typename TO>
 cudaError_t phase2_io(const Phase2Args& a, cudaStream_t s) {
   const int vh = head_vh(a.d, Vec<T>::N, a.heads);
-  if (vh) return phase2_heads<T>(a, vh, s);
+  if (vh) return phase2_heads<T, TO>(a, vh, s);
   int vpt, threads;
   row_geometry(a.d / Vec<T>::N, vpt, threads, kMergeThreads);
   const unsigned grid = static_cast<unsigned>(a.T);
   switch (vpt) {
-    case 1: return phase2_vpt<T, 1>(a, grid, threads, s);
-    case 2: return phase2_vpt<T, 2>(a, grid, threads, s);
-    case 4: return phase2_vpt<T, 4>(a, grid, threads, s);
-    case 8: return phase2_vpt<T, 8>(a, grid, threads, s);
-    case 16: return phase2_vpt<T, 16>(a, grid, threads, s);
+    case 1: return phase2_vpt<T, TO, 1>(a, grid, threads, s);
+    case 2: return phase2_vpt<T, TO, 2>(a, grid, threads, s);
+    case 4: return phase2_vpt<T, TO, 4>(a, grid, threads, s);
+    case 8: return phase2_vpt<T, TO, 8>(a, grid, threads, s);
+    case 16: return phase2_vpt<T, TO, 16>(a, grid, threads, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -898,7 +927,8 @@ inline unsigned grid_for(int64_t work, int threads) {
 
 cudaError_t launch_phase2(IO io, const Phase2Args& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
-  return io == IO::BF16 ? phase2_io<bf16>(a, s) : phase2_io<float>(a, s);
+  if (io == IO::F32) return phase2_io<float, float>(a, s);
+  return (a.flags & kOF32) ? phase2_io<bf16, float>(a, s) : phase2_io<bf16, bf16>(a, s);
 }
 
 

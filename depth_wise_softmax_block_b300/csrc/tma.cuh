@@ -1,20 +1,48 @@
 // Bulk-tensor (TMA) copies and mbarrier waits for sm_103a, as inline PTX.
 //
-// Every wait on an mbarrier is bounded: after kSpinLimit failed polls the waiting thread gives
-// up, counts the event in the device word `g_wait_timeouts` (read and cleared through
-// attnres_poll_device_errors) and returns false, so a kernel whose copies never land ends
-// instead of spinning forever.
+// Every wait on an mbarrier is bounded in time (the GPU's nanosecond clock %globaltimer): a wait
+// of the pipeline (a stage whose copy or whose consumers are late) gives up after
+// kWaitLimitNs, a drain (a CTA waiting for its own copies in flight before it exits) after
+// kDrainLimitNs.  A wait that gives up counts the event in the device word `g_wait_timeouts`
+// (read and cleared through attnres_poll_device_errors) and returns false, so a kernel whose
+// copies never land ends in well under a second instead of spinning forever.
 #pragma once
 
 #include <cuda.h>  // CUtensorMap (type only; the driver is reached through the runtime)
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace attnres {
 
-// Count of bounded waits that gave up (one copy per translation unit that includes this file).
+// Count of bounded waits that gave up (one copy per translation unit that includes this file),
+// and the value the last read-and-clear took from it.
 static __device__ unsigned int g_wait_timeouts = 0;
+static __device__ unsigned int g_wait_taken = 0;
 
-constexpr uint32_t kSpinLimit = 1u << 24;
+// A legitimate wait lasts microseconds (a copy landing, a stage being consumed).
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;    // 200 ms
+constexpr uint64_t kDrainLimitNs = 2000ull * 1000 * 1000;  // 2 s
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Reads and clears this translation unit's timeout word in one atomic exchange on the device,
+// after every kernel of the device (on every stream) has finished.  Host only; synchronous.
+// 0xffffffff if a CUDA call failed.
+static __global__ void take_wait_timeouts_kernel() {
+  g_wait_taken = atomicExch(&g_wait_timeouts, 0u);
+}
+static inline unsigned int take_wait_timeouts() {
+  if (cudaDeviceSynchronize() != cudaSuccess) return 0xffffffffu;
+  take_wait_timeouts_kernel<<<1, 1>>>();
+  if (cudaGetLastError() != cudaSuccess) return 0xffffffffu;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_wait_taken, sizeof(v)) != cudaSuccess) return 0xffffffffu;
+  return v;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -52,13 +80,45 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits until the phase with the given parity has completed; false after kSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  const uint32_t a = smem_addr(bar);
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(a, parity)) return true;
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Polls until the phase with the given parity has completed (true), or until `limit_ns` have
+// passed since the first failed poll (false, and the event is counted).  kCluster: acquire at
+// cluster scope (arrivals from other CTAs of the cluster).
+template <bool kCluster>
+__device__ __forceinline__ bool mbar_wait_for(uint32_t a, uint32_t parity, uint64_t limit_ns) {
+  auto poll = [&]() {
+    return kCluster ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity);
+  };
+  if (poll()) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 32; ++i)
+      if (poll()) return true;
+    if (global_ns() - t0 > limit_ns) break;
+  }
   atomicAdd(&g_wait_timeouts, 1u);
   return false;
+}
+
+// A wait of the pipeline; false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_for<false>(smem_addr(bar), parity, kWaitLimitNs);
+}
+
+// A CTA waiting for its own copies (or MMAs) in flight before it exits; false after kDrainLimitNs.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_for<false>(smem_addr(bar), parity, kDrainLimitNs);
 }
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
@@ -113,20 +173,7 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
 
 // mbar_wait with acquire at cluster scope (the arrivals come from other CTAs); bounded.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
-  const uint32_t a = smem_addr(bar);
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(a), "r"(parity)
-        : "memory");
-    if (ok) return true;
-  }
-  atomicAdd(&g_wait_timeouts, 1u);
-  return false;
+  return mbar_wait_for<true>(smem_addr(bar), parity, kWaitLimitNs);
 }
 
 // All threads of all CTAs of the cluster (every thread must execute it, convergently).

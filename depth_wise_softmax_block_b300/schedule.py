@@ -53,18 +53,27 @@ def _call(timer, kind, fn, *args, **kw):
 
 class BlockRunner:
     """Work buffers for blocks of up to ``S_max`` sublayers over ``T`` tokens, with ``heads``
-    depth-attention heads (per-head log-sum-exps)."""
+    depth-attention heads (per-head log-sum-exps).
+
+    ``o_dtype``: the type phase 1's output is stored in (the I/O type by default; fp32 removes
+    the rounding between the two phases, ATTNRES_O_F32).  ``extra_outputs``: every phase-2 call
+    also writes h (``self.h``) and the weight of the partial source (``self.alpha_p``), which
+    the caller may read in the sublayer callback."""
 
     def __init__(self, T: int, d: int, S_max: int, dtype, device, keep_y: bool = False,
-                 timer: Optional[KernelTimer] = None, heads: int = 1):
+                 timer: Optional[KernelTimer] = None, heads: int = 1, o_dtype=None,
+                 extra_outputs: bool = False):
         self.timer = timer
         self.T, self.d, self.S_max, self.heads = T, d, S_max, heads
-        self.o = torch.empty((S_max, T, d), dtype=dtype, device=device)
+        self.o = torch.empty((S_max, T, d), dtype=o_dtype or dtype, device=device)
         self.lse = torch.empty((S_max, heads, T), dtype=torch.float32, device=device)
         self.partial = torch.empty((T, d), dtype=dtype, device=device)
         self.keep_y = keep_y
         n_y = S_max if keep_y else 1
         self.y = torch.empty((n_y, T, d), dtype=dtype, device=device)
+        self.h = torch.empty((T, d), dtype=dtype, device=device) if extra_outputs else None
+        self.alpha_p = (torch.empty((heads, T), dtype=torch.float32, device=device)
+                        if extra_outputs else None)
 
     def y_buffer(self, i: int) -> torch.Tensor:
         return self.y[i - 1] if self.keep_y else self.y[0]
@@ -104,7 +113,8 @@ class BlockRunner:
                 on_call(i, args)
             kind = "phase2_first" if i == 1 else ("phase2" if i == 2 else "phase2_fused")
             _call(tm, kind, attnres_phase2_merge, o[i - 1], lse[i - 1], args["partial"],
-                  args["v_prev"], args["partial_out"], U[i - 1], g, y, eps_key=eps_key,
+                  args["v_prev"], args["partial_out"], U[i - 1], g, y, h_out=self.h,
+                  alpha_p_out=self.alpha_p if i > 1 else None, eps_key=eps_key,
                   eps_in=eps_in, flags=flags, heads=self.heads)
             # b^{i-1} now lives in args["partial"] (i == 2) or args["partial_out"] (i >= 3)
             if i == 2:
@@ -146,9 +156,9 @@ class FullGroupedRunner:
     model's attention or MLP; a stand-in for the synthetic workloads)."""
 
     def __init__(self, T: int, d: int, S: int, dtype, device, timer: Optional[KernelTimer] = None,
-                 heads: int = 1):
+                 heads: int = 1, o_dtype=None):
         self.S, self.timer, self.heads = S, timer, heads
-        self.o = torch.empty((S, T, d), dtype=dtype, device=device)
+        self.o = torch.empty((S, T, d), dtype=o_dtype or dtype, device=device)
         self.lse = torch.empty((S, heads, T), dtype=torch.float32, device=device)
 
     def run(self, hist: torch.Tensor, U: torch.Tensor, G_in: Optional[torch.Tensor],

@@ -68,6 +68,20 @@ typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype;
 #define ATTNRES_NO_KEY_NORM 0x2u
 
 /*
+ * Storage flag of phase 1's output (not a variant of the method; accepted by attnres_phase1,
+ * attnres_phase2_merge and attnres_phase2_merge_sources only, ATTNRES_ERR_INVALID_ARG
+ * elsewhere):
+ *   ATTNRES_O_F32            phase 1 writes o in fp32 whatever the I/O type, and phase 2 /
+ *                            the grouped merge read o_l in fp32.  With bf16 I/O this removes
+ *                            the one rounding between the phases: the two-phase result then
+ *                            equals the direct softmax over all sources up to fp32 arithmetic
+ *                            and the final bf16 store ("Attention Residuals" note §10: the
+ *                            merge is exact).  It doubles o's bytes.  With ATTNRES_F32 I/O it
+ *                            changes nothing.
+ */
+#define ATTNRES_O_F32 0x4u
+
+/*
  * Depth-attention heads (`heads` argument; 1 = the method as defined), the multi-head variant
  * of Table 4 ("Attention Residuals" note, result 4: "Block, multi-head H = 16").  The pages
  * give no formula; the reading implemented here: the d features split into H contiguous slices
@@ -86,7 +100,7 @@ typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype;
 #define ATTNRES_MAX_D 16384        /* hidden size (a row stays in registers)               */
 
 /* ABI version of this header; attnres_abi_version() returns the library's. */
-#define ATTNRES_ABI_VERSION 7
+#define ATTNRES_ABI_VERSION 8
 int attnres_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -154,11 +168,12 @@ attnres_status attnres_query_prep(const float* w, const float* gamma_key, float*
  *               computed on the tensor cores as (hi + lo) . b_j[t] with fp32 accumulation;
  *               otherwise the CUDA cores compute them from u in fp32.  Both agree to fp32
  *               rounding plus the split's 2^-16 relative error in u.
- *   o_out       device [S][T][d] (io dtype), required
+ *   o_out       device [S][T][d] (io dtype; fp32 with ATTNRES_O_F32), required
  *   m_out, lse_out  device fp32 [S][T], each optional (NULL = not written); with
  *               ATTNRES_SIGMOID_WEIGHTS, o is the unnormalised sum and lse_out is not written
  *   alpha_out   device fp32 [S][T][n_src], optional
- *   flags       ATTNRES_SIGMOID_WEIGHTS | ATTNRES_NO_KEY_NORM (see above), 0 by default
+ *   flags       ATTNRES_SIGMOID_WEIGHTS | ATTNRES_NO_KEY_NORM | ATTNRES_O_F32 (see above),
+ *               0 by default
  *   heads       depth-attention heads H (see above), 1 by default: m_out and lse_out are then
  *               [S][H][T] and alpha_out [S][H][T][n_src]; the tensor cores take H > 1 when
  *               d / H is a multiple of 64
@@ -181,7 +196,8 @@ attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, i
  * M = max(lse_l, z_p), a = exp(lse_l - M), c = exp(z_p - M):
  *     h = (a o_l + c p) / (a + c)            (h = o_l when there is no partial source)
  *     y = gamma_in ⊙ h / sqrt(mean h^2 + eps_in)
- *   o_l          device [T, d] (io dtype): phase-1 output row block of this sublayer
+ *   o_l          device [T, d] (io dtype; fp32 with ATTNRES_O_F32): phase-1 output row block
+ *                of this sublayer
  *   lse_l        device fp32 [T]; required when there is a partial source
  *   partial      device [T, d] (io dtype) or NULL: b_n^{i-2} (or b_n^{i-1} if v_prev is NULL)
  *   v_prev       device [T, d] (io dtype) or NULL: output of the previous sublayer
@@ -192,7 +208,8 @@ attnres_status attnres_phase1(const void* reps, int64_t src_stride, int n_src, i
  *   h_out        device [T, d] or NULL;  y_out device [T, d], required
  *   alpha_p_out  device fp32 [T] or NULL: weight of the partial source, c / (a + c)
  *   flags        variant flags; with ATTNRES_SIGMOID_WEIGHTS h = o_l + sigmoid(z_p) p, lse_l is
- *                not read (may be NULL) and alpha_p_out receives sigmoid(z_p)
+ *                not read (may be NULL) and alpha_p_out receives sigmoid(z_p); ATTNRES_O_F32:
+ *                o_l is fp32
  *   heads        depth-attention heads H: each head merges its slice with its own r, z_p and
  *                lse (lse_l and alpha_p_out are then [H][T]); y normalises the whole row
  */
@@ -243,7 +260,8 @@ attnres_status attnres_full_reference_path(const void* const* srcs, int n_src, i
  *     y = gamma_in ⊙ h / sqrt(mean h^2 + eps_in)
  * (k = 0 gives h = o_l.)  With ATTNRES_SIGMOID_WEIGHTS, h = o_l + sum_{i in B} sigmoid(z_i) v_i
  * and lse_l is not read.
- *   o_l, lse_l  device [T, d] (io dtype) and fp32 [T]: phase 1's output row block of layer l
+ *   o_l, lse_l  device [T, d] (io dtype; fp32 with ATTNRES_O_F32) and fp32 [T]: phase 1's
+ *               output row block of layer l
  *   srcs        HOST array of k device pointers, each [T, d] (io dtype); may be NULL when k = 0
  *   u_l, gamma_in, eps_key, eps_in: as for attnres_phase2_merge
  *   h_out, y_out  device [T, d] or NULL (at least one required)

@@ -45,7 +45,7 @@ def test_header_symbols_exported(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.attnres_abi_version() == 7
+    assert lib.attnres_abi_version() == 8
     for code, name in ar.STATUS.items():
         assert lib.attnres_status_string(code).decode() == name
     assert lib.attnres_status_string(99).decode() == "ATTNRES_ERR_UNKNOWN"
@@ -86,7 +86,9 @@ def test_phase1_validation(lib):
     assert err(p1(lib, T=4, us=PM)) == MISALIGNED         # split queries misaligned
     assert p1(lib, us=P) == OK
     assert p1(lib, flags=3) == OK                         # both variant flags
-    assert p1(lib, flags=4) == INVALID                    # unknown flag
+    assert p1(lib, flags=4) == OK                         # o stored in fp32
+    assert p1(lib, flags=7) == OK
+    assert p1(lib, flags=8) == INVALID                    # unknown flag
     assert p1(lib, d=128, heads=16) == OK                 # depth-attention heads of 8 columns
     assert p1(lib, d=128, heads=0) == INVALID
     assert p1(lib, d=128, heads=3) == INVALID             # d % heads
@@ -112,6 +114,7 @@ def test_phase2_validation(lib):
     assert err(p2(lib, T=4, part=P, lse=None)) == INVALID  # a partial source needs lse ...
     assert p2(lib, part=P, lse=None, flags=1) == OK       # ... except with sigmoid weights
     assert p2(lib, flags=8) == INVALID
+    assert p2(lib, flags=4) == OK                         # o_l stored in fp32
     assert err(p2(lib, T=4, v=P, u=None)) == INVALID       # ... and the query
     assert err(p2(lib, T=4, pout=P)) == INVALID            # nothing to write without a partial
     assert p2(lib, d=12) == INVALID
@@ -141,6 +144,8 @@ def test_full_and_update_validation(lib):
     assert err(f(nul, 2, 4, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None)) == INVALID
     assert lib.attnres_full_reference_path(arr, 3, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None,
                                            16, 1, None) == INVALID
+    assert lib.attnres_full_reference_path(arr, 3, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None,
+                                           4, 1, None) == INVALID  # no phase-1 output here
     assert f(arr, 3, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None, heads=8) == OK
     assert f(arr, 3, 0, 64, 1, P, 1e-6, None, 1e-6, None, P, None, None, heads=7) == INVALID
     up = lib.attnres_partial_update
@@ -175,7 +180,8 @@ def test_merge_sources_validation(lib):
     assert err(call(T=4, o=PM)) == MISALIGNED
     bad = (ctypes.c_void_p * 2)(P, PM)
     assert err(call(T=4, srcs=bad)) == MISALIGNED
-    assert call(flags=4) == INVALID
+    assert call(flags=4) == OK                            # o_l stored in fp32
+    assert call(flags=8) == INVALID
     assert call(heads=2) == OK
     assert call(heads=128) == UNSUPPORTED
 

@@ -89,23 +89,27 @@ def test_head_statistics_bytes():
     assert (b16.close, b16.final) == (b1.close, b1.final)
 
 
-def test_decode_walk_bytes_hand_count():
-    """The decode bench's bytes per depth walk: block n (1-based) runs phase 1 over n sources for
+def test_walk_bytes_hand_count():
+    """The walk bench's bytes per depth walk: block n (1-based) runs phase 1 over n sources for
     its S_n sublayers, S_n phase-2 calls and the close; then the final aggregation over all
-    closed blocks and the embedding."""
+    closed blocks and the embedding.  The decode and prefill-chunk walks (186 sublayers in
+    7 x 24 + 18, bf16) and the tiny fp32 walk (8 sublayers in 2 x 4)."""
     import bench
     from synth import inputs as I
-    wl = I.DECODE_BF16
-    d, E, T = wl.d, 2, wl.T
-    want = 0
-    for n, Sn in enumerate([24] * 7 + [18], start=1):
-        want += (n + Sn) * d * E + 4 * Sn                  # phase 1: sources, o; lse
-        want += 2 * d * E                                  # sublayer 1: read o, write y
-        want += 3 * d * E + 4                              # sublayer 2: o, lse, v_1; write y
-        want += (Sn - 2) * (5 * d * E + 4)                 # sublayers 3..: fused update
-        want += 3 * d * E                                  # close
-    want += (9 + 1) * d * E                                # final over 9 slots: read 9, write 1
-    assert bench.decode_walk_bytes(wl) == want * T
+    for wl, E, blocks in [(I.DECODE_BF16, 2, [24] * 7 + [18]),
+                          (I.PREFILL_CHUNK_BF16, 2, [24] * 7 + [18]),
+                          (I.TINY_BLOCK_F32, 4, [4, 4])]:
+        d, T = wl.d, wl.T
+        want = 0
+        for n, Sn in enumerate(blocks, start=1):
+            want += (n + Sn) * d * E + 4 * Sn              # phase 1: sources, o; lse
+            want += 2 * d * E                              # sublayer 1: read o, write y
+            want += 3 * d * E + 4                          # sublayer 2: o, lse, v_1; write y
+            want += (Sn - 2) * (5 * d * E + 4)             # sublayers 3..: fused update
+            want += 3 * d * E                              # close
+        nf = len(blocks) + 1
+        want += (nf + 1) * d * E                           # final: read all slots, write 1
+        assert bench.walk_bytes(wl) == want * T, wl.name
 
 
 def test_traffic_lookup_matches_kernel_sources(tmp_path, monkeypatch):

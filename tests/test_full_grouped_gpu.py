@@ -40,9 +40,9 @@ def _setup(T, d, L, dtype, dev, seed):
     return hist, v, W, Gk, Gi, U, Us
 
 
-def _run(hist, v, U, Gi, S, dtype, split, snap=None):
+def _run(hist, v, U, Gi, S, dtype, split, snap=None, o_dtype=None):
     L, T, d = v.shape
-    runner = FullGroupedRunner(T, d, S, dtype, hist.device)
+    runner = FullGroupedRunner(T, d, S, dtype, hist.device, o_dtype=o_dtype)
     ys = torch.empty((L, T, d), dtype=dtype, device=hist.device)
 
     def sub(l, y):
@@ -70,12 +70,16 @@ def test_grouped_full_f32_every_element(dev, S):
 @pytest.mark.parametrize("T,d,L,S,rows_k,split", [(40, 2048, 20, 8, 0, True),
                                                   (8192, 2048, 54, 8, 12, True),
                                                   (8192, 2048, 54, 16, 12, False)])
-def test_grouped_full_bf16(dev, T, d, L, S, rows_k, split):
-    """bf16: every call against the merge of its own stored inputs, every layer against the
-    direct definition with the two-phase storage term (phase 1's o is stored in bf16)."""
+@pytest.mark.parametrize("ostore", ["o_bf16", "o_f32"])
+def test_grouped_full_bf16(dev, T, d, L, S, rows_k, split, ostore):
+    """bf16: every call against the merge of its own stored inputs; every layer against the
+    direct definition, at the output gate when phase 1's o is stored in fp32 (ATTNRES_O_F32)
+    and with the two-phase storage term when it is stored in bf16 (the production path)."""
     hist, v, W, Gk, Gi, U, Us = _setup(T, d, L, torch.bfloat16, dev, 12)
     snap = {}
-    ys = _run(hist, v, U, Gi, S, torch.bfloat16, Us if split else None, snap)
+    o32 = ostore == "o_f32"
+    ys = _run(hist, v, U, Gi, S, torch.bfloat16, Us if split else None, snap,
+              torch.float32 if o32 else None)
     rows = np.arange(T) if rows_k == 0 else np.unique(
         np.concatenate([[0, T - 1], np.random.default_rng(5).integers(0, T, rows_k)]))
     h64 = to64(hist[:, rows])
@@ -91,10 +95,13 @@ def test_grouped_full_bf16(dev, T, d, L, S, rows_k, split):
         # end to end: direct softmax over v_0 .. v_{l-1}
         h_d, y_d, a_d = O.sublayer_input(h64[:l], W64[l - 1], Gk64[l - 1], EPS, Gi64[l - 1],
                                          EPS)
-        oA, _, _, _ = O.partition_stats(h64[:l0 + 1], W64[l - 1], Gk64[l - 1], EPS)
-        wA = np.sum(a_d[:l0 + 1], axis=0)
-        check_two_phase(ys[l - 1][rows], y_d, oA, wA, O.rms(h_d, EPS), Gi64[l - 1], "bf16",
-                        f"y_{l} (two-phase vs direct)")
+        if o32:
+            check_outputs(ys[l - 1][rows], y_d, "bf16", f"y_{l} (vs direct)")
+        else:
+            oA, _, _, _ = O.partition_stats(h64[:l0 + 1], W64[l - 1], Gk64[l - 1], EPS)
+            wA = np.sum(a_d[:l0 + 1], axis=0)
+            check_two_phase(ys[l - 1][rows], y_d, oA, wA, O.rms(h_d, EPS), Gi64[l - 1], "bf16",
+                            f"y_{l} (two-phase vs direct)")
 
 
 def test_merge_sources_weights_and_empty(dev):

@@ -17,6 +17,7 @@ from depth_wise_softmax_block_b300.schedule import BlockRunner, final_aggregatio
 import oracle.attnres_oracle as O
 from parity_util import TOL, check_close, check_outputs, to64
 from synth import inputs as I
+from walk_util import partial_sources
 
 pytestmark = pytest.mark.gpu
 EPS = 1e-6
@@ -148,14 +149,18 @@ ROW_CASES = [(33, 7168, 16, "bf16"), (40, 256, 8, "f32"), (24, 96, 3, "f32"),
 
 @pytest.mark.parametrize("variant", sorted(VARIANTS))
 @pytest.mark.parametrize("mode", ["first", "fused"])
-@pytest.mark.parametrize("T,d,H,dt", ROW_CASES)
-def test_phase2_heads(dev, variant, mode, T, d, H, dt):
+@pytest.mark.parametrize("T,d,H,dt,ostore", [c + ("io",) for c in ROW_CASES] +
+                         [c + ("f32",) for c in ROW_CASES if c[3] == "bf16"])
+def test_phase2_heads(dev, variant, mode, T, d, H, dt, ostore):
+    """Per call against the per-head merge of what the call received; with o stored in fp32
+    (fp32 I/O, or ATTNRES_O_F32 with bf16 I/O) also h, y and the partial's weights end to end
+    against the direct per-head aggregation."""
     flags = VARIANTS[variant]
     n, seed = 4, 8300 + d + H
     dtype = _dt(dt)
     reps = make_reps(n, T, d, dtype, dev, seed)
     W, G, U, _ = queries(1, d, dev, seed, flags)
-    o = torch.empty((1, T, d), dtype=dtype, device=dev)
+    o = torch.empty((1, T, d), dtype=torch.float32 if ostore == "f32" else dtype, device=dev)
     lse = torch.empty((1, H, T), device=dev)
     ar.attnres_phase1(reps, U, o, lse_out=lse, eps=EPS, flags=flags, heads=H)
     G_in = I.gains(1, d, 0.05, seed, "gin", dev)[0]
@@ -180,10 +185,13 @@ def test_phase2_heads(dev, variant, mode, T, d, H, dt):
     check_outputs(y, y_m, dt, f"y ({variant}, {mode}, per call)")
     if fused:
         check_close(ap, a_m, TOL[dt]["weight"], "weights of the partial source")
-    if dt == "f32":   # two-phase against the direct per-head definition
+    if dt == "f32" or ostore == "f32":   # two-phase against the direct per-head definition
         srcs = to64(reps) if p is None else np.concatenate([to64(reps), p[None]])
-        h_d, _, _ = O.multihead_aggregate(srcs, to64(W[0]), _g64(G, 0), EPS, H, **_wk(flags))
+        h_d, a_d, _ = O.multihead_aggregate(srcs, to64(W[0]), _g64(G, 0), EPS, H, **_wk(flags))
         check_outputs(h, h_d, dt, "h (two-phase vs direct)")
+        check_outputs(y, O.rmsnorm(h_d, to64(G_in), EPS), dt, "y (two-phase vs direct)")
+        if fused:
+            check_close(ap, a_d[:, -1], TOL[dt]["weight"], "weights of the partial (vs direct)")
 
 
 @pytest.mark.parametrize("variant", sorted(VARIANTS))
@@ -212,11 +220,12 @@ def test_full_path_heads(dev, variant, n, T, d, H, dt):
 
 @pytest.mark.parametrize("H", [8, 32])
 @pytest.mark.parametrize("k", [0, 1, 3])
-@pytest.mark.parametrize("dt", ["f32", "bf16"])
-def test_merge_sources_heads(dev, k, dt, H):
+@pytest.mark.parametrize("dt,ostore", [("f32", "io"), ("bf16", "io"), ("bf16", "f32")])
+def test_merge_sources_heads(dev, k, dt, ostore, H):
     """Grouped Full AttnRes phase 2 with heads: phase 1 over the history A per head, then the
     merge of k in-group sources; per call against the per-head partition merge of the stored
-    (o, lse), and in fp32 against the direct per-head aggregation over A and B."""
+    (o, lse), and with o stored in fp32 (fp32 I/O, or ATTNRES_O_F32) against the direct
+    per-head aggregation over A and B."""
     T, d, nA = 29, 512, 5
     dtype = _dt(dt)
     seed = 8500 + k
@@ -225,7 +234,7 @@ def test_merge_sources_heads(dev, k, dt, H):
     Bs = [I.normal((T, d), 1.2, seed, f"b{j}", dev, dtype) for j in range(k)]
     W, G, U, us = queries(1, d, dev, seed)
     G_in = I.gains(1, d, 0.05, seed, "gin", dev)[0]
-    o = torch.empty((1, T, d), dtype=dtype, device=dev)
+    o = torch.empty((1, T, d), dtype=torch.float32 if ostore == "f32" else dtype, device=dev)
     lse = torch.empty((1, H, T), device=dev)
     ar.attnres_phase1(A, U, o, lse_out=lse, eps=EPS, heads=H)
     y = torch.empty((T, d), dtype=dtype, device=dev)
@@ -248,10 +257,11 @@ def test_merge_sources_heads(dev, k, dt, H):
     check_outputs(y, O.rmsnorm(hm, to64(G_in), EPS), dt, f"y (k={k}, per call)")
     if k:
         check_close(alpha[..., :k], np.transpose(am, (0, 2, 1)), TOL[dt]["weight"], "alpha")
-    if dt == "f32":
+    if dt == "f32" or ostore == "f32":
         h_d, _, _ = O.multihead_aggregate(np.concatenate([to64(A), B64]), to64(W[0]),
                                           to64(G[0]), EPS, H)
         check_outputs(h, h_d, dt, "h (grouped vs direct)")
+        check_outputs(y, O.rmsnorm(h_d, to64(G_in), EPS), dt, "y (grouped vs direct)")
 
 
 @pytest.mark.parametrize("dt,T,d,H,path", [("f32", 24, 128, 4, "cuda_cores"),
@@ -266,7 +276,7 @@ def test_block_walk_heads(dev, dt, T, d, H, path):
     W, G, U, us = queries(S, d, dev, seed)
     G_in = I.gains(S, d, 0.05, seed, "gin", dev)
     v = torch.stack([I.normal((T, d), 1.0, seed, f"out{i}", dev, dtype) for i in range(S)])
-    runner = BlockRunner(T, d, S, dtype, dev, keep_y=True, heads=H)
+    runner = BlockRunner(T, d, S, dtype, dev, keep_y=True, heads=H, o_dtype=torch.float32)
     ys = torch.empty((S, T, d), dtype=dtype, device=dev)
     close = torch.empty((T, d), dtype=dtype, device=dev)
 
@@ -279,15 +289,15 @@ def test_block_walk_heads(dev, dt, T, d, H, path):
     fin = torch.empty((T, d), dtype=dtype, device=dev)
     final_aggregation(torch.cat([reps, close[None]]), U[0], fin, EPS, heads=H)
     torch.cuda.synchronize()
-    r64, v64 = to64(reps), to64(v)
+    # the partial sums as the GPU stores them (rounded to the I/O type between sublayers);
+    # phase 1's o is stored in fp32 (ATTNRES_O_F32)
+    r64 = to64(reps)
+    ps, close_want = partial_sources(v, dtype)
     for i in range(1, S + 1):
-        if dt == "bf16" and i >= 3:
-            continue      # bf16 partials b^{i-1}, i >= 3, are rounded sums: see fp32 case
-        srcs = r64 if i == 1 else np.concatenate([r64, v64[:i - 1].sum(axis=0)[None]])
+        srcs = r64 if ps[i - 1] is None else np.concatenate([r64, ps[i - 1][None]])
         h_o, _, _ = O.multihead_aggregate(srcs, to64(W[i - 1]), to64(G[i - 1]), EPS, H)
         check_outputs(ys[i - 1], O.rmsnorm(h_o, to64(G_in[i - 1]), EPS), dt, f"y_{i}")
-    if dt == "f32":
-        check_outputs(close, v64.sum(axis=0), dt, "closed block")
+    assert torch.equal(close.cpu(), close_want), "closed block"
     fin_o, _, _ = O.multihead_aggregate(np.concatenate([r64, to64(close)[None]]), to64(W[0]),
                                         to64(G[0]), EPS, H)
     check_outputs(fin, fin_o, dt, "final")

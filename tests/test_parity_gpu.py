@@ -57,10 +57,10 @@ def split_of(U):
     return us
 
 
-def run_phase1(reps, U, path="cuda_cores"):
+def run_phase1(reps, U, path="cuda_cores", o_dtype=None):
     n, T, d = reps.shape
     S = U.shape[0]
-    o = torch.empty((S, T, d), dtype=reps.dtype, device=reps.device)
+    o = torch.empty((S, T, d), dtype=o_dtype or reps.dtype, device=reps.device)
     m = torch.empty((S, T), dtype=torch.float32, device=reps.device)
     lse = torch.empty_like(m)
     alpha = torch.empty((S, T, n), dtype=torch.float32, device=reps.device)
@@ -112,6 +112,29 @@ def test_phase1_matches_oracle(dev, p1path, n, S, T, d, dt):
     check_close(m, om, tol["stat"], "m")
     check_close(lse, olse, tol["stat"], "lse")
     check_close(alpha, oalpha, tol["weight"], "alpha")
+
+
+O_F32_CASES = [(9, 24, 37, 7168), (9, 24, 100, 512), (5, 18, 50, 2048), (8, 24, 16, 200),
+               (10, 1, 33, 7168), (3, 7, 8, 136), (17, 24, 12, 128), (55, 1, 20, 2048)]
+
+
+@pytest.mark.parametrize("n,S,T,d", O_F32_CASES)
+def test_phase1_o_f32(dev, p1path, n, S, T, d):
+    """bf16 sources with phase 1's o stored in fp32 (ATTNRES_O_F32): o against the oracle at
+    the bf16-mode bound without any storage rounding, the statistics as usual, and the fp32 o
+    rounded to bf16 equal, bit for bit, to the o the same kernel stores in bf16 (the store is
+    the only difference)."""
+    seed = 1500 + n * 7 + S
+    reps = make_reps(n, T, d, torch.bfloat16, dev, seed)
+    W, G, U = make_queries(S, d, dev, seed)
+    o32, m, lse, alpha = run_phase1(reps, U, p1path, torch.float32)
+    o16, m2, lse2, alpha2 = run_phase1(reps, U, p1path)
+    oo, om, olse, oalpha = O.phase1(to64(reps), to64(W), to64(G), EPS)
+    check_outputs(o32, oo, "bf16", "o (fp32 store)")
+    check_close(lse, olse, TOL["bf16"]["stat"], "lse")
+    check_close(alpha, oalpha, TOL["bf16"]["weight"], "alpha")
+    assert torch.equal(o32.to(torch.bfloat16), o16), "o: fp32 store rounded != bf16 store"
+    assert torch.equal(lse, lse2) and torch.equal(alpha, alpha2)
 
 
 def test_query_split(dev):
@@ -179,14 +202,21 @@ P2_MODES = ["first", "partial_only", "vprev_only", "fused", "fused_inplace"]
 
 
 @pytest.mark.parametrize("mode", P2_MODES)
-@pytest.mark.parametrize("n,T,d,dt", [(2, 64, 128, "f32"), (9, 45, 7168, "bf16"),
-                                       (3, 17, 2048, "bf16"), (1, 5, 8, "f32")])
-def test_phase2_matches_oracle(dev, mode, n, T, d, dt):
+@pytest.mark.parametrize("n,T,d,dt,ostore", [(2, 64, 128, "f32", "io"), (9, 45, 7168, "bf16", "io"),
+                                              (3, 17, 2048, "bf16", "io"), (1, 5, 8, "f32", "io"),
+                                              (9, 45, 7168, "bf16", "f32"),
+                                              (3, 17, 2048, "bf16", "f32")])
+def test_phase2_matches_oracle(dev, mode, n, T, d, dt, ostore):
+    """Phase 1 then one phase-2 call.  Per call: h, y and the partial's weight against the
+    pages' merge of exactly what the call received.  End to end, against the direct softmax
+    over all the sources: the partial's weight at the weight tolerance; h and y at the output
+    gate when o is stored in fp32 (ostore "f32", or fp32 I/O), and with the derived bound of
+    the bf16 storage of o on the production path (bf16 I/O, ostore "io")."""
     seed = 2000 + n + d
     dtype = _dt(dt)
     reps = make_reps(n, T, d, dtype, dev, seed)
     W, G, U = make_queries(1, d, dev, seed)
-    o, m, lse, _ = run_phase1(reps, U)
+    o, m, lse, _ = run_phase1(reps, U, o_dtype=torch.float32 if ostore == "f32" else None)
     G_in = I.gains(1, d, 0.05, seed, "gin", dev)[0]
     part = I.normal((T, d), 1.5, seed, "part", dev, dtype)
     vprev = I.normal((T, d), 1.0, seed, "vprev", dev, dtype)
@@ -221,10 +251,18 @@ def test_phase2_matches_oracle(dev, mode, n, T, d, dt):
     h_o, y_o, a_o, _ = O.phase2_reference(
         to64(reps), None if partial is None else part_in,
         None if v_prev is None else to64(vprev), to64(W[0]), to64(G[0]), EPS, to64(G_in), EPS)
-    oA, _, _, _ = O.phase1(to64(reps), to64(W[:1]), to64(G[:1]), EPS)
-    wA = 1.0 - (a_o[-1] if has_p else 0.0)
-    rh = O.rms(h_o, EPS)
-    check_two_phase(y, y_o, oA[0], wA, rh, to64(G_in), dt, "y (two-phase vs direct)")
+    if has_p:
+        check_close(ap, a_o[-1], TOL[dt]["weight"], "weight of the partial source (vs direct)")
+    if dt == "f32" or ostore == "f32":
+        check_outputs(h, h_o, dt, "h (vs direct)")
+        check_outputs(y, y_o, dt, "y (vs direct)")
+    else:
+        oA, _, _, _ = O.phase1(to64(reps), to64(W[:1]), to64(G[:1]), EPS)
+        wA = 1.0 - (a_o[-1] if has_p else 0.0)
+        rh = O.rms(h_o, EPS)
+        check_two_phase(y, y_o, oA[0], wA, rh, to64(G_in), dt, "y (two-phase vs direct)")
+        check_two_phase(h, h_o, oA[0], wA, rh, to64(G_in), dt, "h (two-phase vs direct)",
+                        h_only=True)
     if pout is not None:   # the fused update is exactly round(partial + v_prev)
         want = (torch.from_numpy(part_in).float() + vprev.float().cpu()).to(dtype)
         assert torch.equal(pout.cpu(), want)

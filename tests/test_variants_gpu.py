@@ -15,6 +15,7 @@ from depth_wise_softmax_block_b300.schedule import BlockRunner, final_aggregatio
 import oracle.attnres_oracle as O
 from parity_util import TOL, check_close, check_outputs, to64
 from synth import inputs as I
+from walk_util import partial_sources
 
 pytestmark = pytest.mark.gpu
 EPS = 1e-6
@@ -95,14 +96,15 @@ def test_phase1_variant(dev, variant, path, n, S, T, d, dt):
 
 @pytest.mark.parametrize("variant", sorted(VARIANTS))
 @pytest.mark.parametrize("mode", ["first", "partial_only", "fused"])
-@pytest.mark.parametrize("n,T,d,dt", [(9, 33, 7168, "bf16"), (2, 40, 128, "f32")])
-def test_phase2_variant(dev, variant, mode, n, T, d, dt):
+@pytest.mark.parametrize("n,T,d,dt,ostore", [(9, 33, 7168, "bf16", "io"), (2, 40, 128, "f32", "io"),
+                                              (9, 33, 7168, "bf16", "f32")])
+def test_phase2_variant(dev, variant, mode, n, T, d, dt, ostore):
     flags = VARIANTS[variant]
     seed = 5000 + n + d
     dtype = _dt(dt)
     reps = make_reps(n, T, d, dtype, dev, seed)
     W, G, U, us = queries(1, d, dev, seed, flags)
-    o = torch.empty((1, T, d), dtype=dtype, device=dev)
+    o = torch.empty((1, T, d), dtype=torch.float32 if ostore == "f32" else dtype, device=dev)
     lse = torch.empty((1, T), device=dev)
     ar.attnres_phase1(reps, U, o, lse_out=lse, eps=EPS, flags=flags)
     G_in = I.gains(1, d, 0.05, seed, "gin", dev)[0]
@@ -129,12 +131,15 @@ def test_phase2_variant(dev, variant, mode, n, T, d, dt):
     check_outputs(y, y_m, dt, f"y ({variant}, {mode}, per call)")
     if has_p:
         check_close(ap, a_m, TOL[dt]["weight"], "weight of the partial source")
-    # end to end in fp32 mode, where the stored phase-1 output is exact to the tolerance
-    if dt == "f32":
+    # end to end where the stored phase-1 output is fp32 (fp32 I/O, or ATTNRES_O_F32)
+    if dt == "f32" or ostore == "f32":
         srcs = to64(reps) if p_exact is None else np.concatenate([to64(reps), p_exact[None]])
-        h_d, _, _ = O.aggregate_variant(srcs, to64(W[0]), _g64(G, 0), EPS, _weights(flags),
-                                        _kn(flags))
+        h_d, a_d, _ = O.aggregate_variant(srcs, to64(W[0]), _g64(G, 0), EPS, _weights(flags),
+                                          _kn(flags))
         check_outputs(h, h_d, dt, "h (two-phase vs direct)")
+        check_outputs(y, O.rmsnorm(h_d, to64(G_in), EPS), dt, "y (two-phase vs direct)")
+        if has_p:
+            check_close(ap, a_d[-1], TOL[dt]["weight"], "weight of the partial (vs direct)")
 
 
 @pytest.mark.parametrize("variant", sorted(VARIANTS))
@@ -166,7 +171,9 @@ def test_full_path_variant(dev, variant, n, T, d, dt):
 def test_block_walk_variant(dev, variant, dt, T, d, path):
     """One block of S = 4 sublayers over n = 3 given sources through BlockRunner (phase 1,
     phase 2 with the fused partial update, the close) and the final aggregation, every
-    element against the oracle's direct definition."""
+    element against the oracle's direct definition over the partial sums as the GPU stores
+    them; phase 1's o is stored in fp32 (ATTNRES_O_F32), so no rounding sits between the
+    phases."""
     flags = VARIANTS[variant]
     seed, n, S = 7000, 3, 4
     dtype = _dt(dt)
@@ -174,7 +181,7 @@ def test_block_walk_variant(dev, variant, dt, T, d, path):
     W, G, U, us = queries(S, d, dev, seed, flags)
     G_in = I.gains(S, d, 0.05, seed, "gin", dev)
     v = torch.stack([I.normal((T, d), 1.0, seed, f"out{i}", dev, dtype) for i in range(S)])
-    runner = BlockRunner(T, d, S, dtype, dev, keep_y=True)
+    runner = BlockRunner(T, d, S, dtype, dev, keep_y=True, o_dtype=torch.float32)
     ys = torch.empty((S, T, d), dtype=dtype, device=dev)
     close = torch.empty((T, d), dtype=dtype, device=dev)
 
@@ -190,15 +197,15 @@ def test_block_walk_variant(dev, variant, dt, T, d, path):
     torch.cuda.synchronize()
     # the GPU rounds the partial sums to the I/O type between sublayers; feed the oracle the
     # same rounded partials so the comparison is per call, not a drift measurement
-    v64 = to64(v)
-    ys_o, _, closed_o = O.single_block_variant(to64(reps), v64, to64(W), _g64(G), to64(G_in),
-                                               EPS, EPS, _weights(flags), _kn(flags))
-    for i in range(S):
-        if dt == "bf16" and i >= 2:
-            continue      # bf16 partials b^{i-1}, i >= 3, are rounded sums: see fp32 case
-        check_outputs(ys[i], ys_o[i], dt, f"y_{i + 1} ({variant})")
-    if dt == "f32":
-        check_outputs(close, closed_o, dt, "closed block")
+    ps, close_want = partial_sources(v, dtype)
+    r64 = to64(reps)
+    for i in range(1, S + 1):
+        srcs = r64 if ps[i - 1] is None else np.concatenate([r64, ps[i - 1][None]])
+        h_o, _, _ = O.aggregate_variant(srcs, to64(W[i - 1]), _g64(G, i - 1), EPS,
+                                        _weights(flags), _kn(flags))
+        check_outputs(ys[i - 1], O.rmsnorm(h_o, to64(G_in[i - 1]), EPS), dt,
+                      f"y_{i} ({variant})")
+    assert torch.equal(close.cpu(), close_want), "closed block"
     fin_o, _, _ = O.aggregate_variant(np.concatenate([to64(reps), to64(close)[None]]), to64(wf),
                                       _g64(gf), EPS, _weights(flags), _kn(flags))
     check_outputs(fin, fin_o, dt, f"final ({variant})")
