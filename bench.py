@@ -229,12 +229,11 @@ def time_oracle(wl: I.Workload, k: int, seed_offset: int = 0):
     return time.perf_counter() - t0
 
 
-def _oracle_worker(wl_name, k, seed_offset, rounds, barrier, out):
+def _oracle_worker(wl, k, seed_offset, rounds, barrier, out):
     """One host core's share of the all-cores oracle timing (a spawned process): build the
     sample once, then for every round wait for all workers and time the oracle on it."""
     torch.set_num_threads(1)
     import oracle.attnres_oracle as O
-    wl = I.WORKLOADS[wl_name]
     args = oracle_sample(wl, k, seed_offset)
     for r in range(rounds):
         barrier.wait(timeout=600)
@@ -259,7 +258,7 @@ def time_oracle_all_cores(wl: I.Workload, k: int, procs: int, rounds: int = 1):
         os.environ[v] = "1"
     try:
         ps = [ctx.Process(target=_oracle_worker,
-                          args=(wl.name, k, 500 + i, rounds, barrier, out))
+                          args=(wl, k, 500 + i, rounds, barrier, out))
               for i in range(procs)]
         for p in ps:
             p.start()
@@ -583,6 +582,92 @@ def run_backward(args):
     return 0
 
 
+def run_backward_block(args):
+    """Backward of one whole block at the long-context chunk shape: 16384 tokens, d = 7168,
+    bf16, n = 9 completed sources (the embedding and 8 blocks), S = 24 sublayers
+    (attnres_backward_block: phase 1 recomputed for the 24 queries, the merge backward per
+    token, then the sources' and parameters' gradients).  Next to it, in the same run, the same
+    block by the per-sublayer backward (attnres_backward once per sublayer over its explicit
+    sources: the 9 completed ones and, from the second sublayer on, the partial sum).  Prints one
+    JSON line: tokens/s of the block backward and its achieved GB/s against the algorithmic
+    bytes (read the sources, v_1 .. v_{S-1} and the S upstream gradients; write the sources' and
+    the v's gradients)."""
+    from depth_wise_softmax_block_b300 import build as B
+    B.build()
+    import depth_wise_softmax_block_b300 as ar
+    dev = torch.device("cuda", 0)
+    T, d, n, S = args.tokens or 16384, 7168, 9, 24
+    dt = torch.bfloat16
+    reps = torch.empty((n, T, d), dtype=dt, device=dev)
+    for j in range(n):
+        I.fill_block_rep(reps[j], j, 11)
+    v = torch.stack([I.normal((T, d), 1.0, 11, f"v{k}", dev, dt) for k in range(S - 1)])
+    W = I.queries(S, d, 11, "w", dev)
+    Gk = I.gains(S, d, 0.02, 11, "gk", dev)
+    Gi = I.gains(S, d, 0.02, 11, "gi", dev)
+    U = torch.empty_like(W)
+    Us = torch.empty((2 * S, d), dtype=dt, device=dev)
+    ar.attnres_query_prep(W, Gk, U, Us)
+    gy = torch.stack([I.normal((T, d), 1.0, 11, f"gy{i}", dev, dt) for i in range(S)])
+    d_reps = torch.empty_like(reps)
+    d_v = torch.empty_like(v)
+    du = torch.zeros((S, d), device=dev)
+    dgi = torch.zeros((S, d), device=dev)
+    ws = torch.empty((ar.attnres_backward_block_workspace_size(n, S, T, d, dt),),
+                     dtype=torch.uint8, device=dev)
+
+    def block():
+        ar.attnres_backward_block(reps, v, U, Gi, gy, d_reps, d_v, du, dgi, u_split=Us,
+                                  workspace=ws)
+
+    part = v[0].clone()             # stands in for the partial sum of every sublayer
+    dsrcs = [torch.empty((T, d), dtype=dt, device=dev) for _ in range(n + 1)]
+
+    def per_sublayer():
+        for i in range(1, S + 1):
+            srcs = [reps[j] for j in range(n)] + ([part] if i >= 2 else [])
+            ar.attnres_backward(srcs, U[i - 1], Gi[i - 1], gy[i - 1], dsrcs[:len(srcs)],
+                                du[i - 1], dgi[i - 1])
+
+    def timed(fn, k):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(k):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / k
+
+    with ClockSampler(0) as clk:
+        ms = timed(block, args.steps)
+    ms_sub = timed(per_sublayer, max(1, args.steps // 4))
+    ar.attnres_poll_device_errors()
+    byt = (2 * n + 3 * S - 2) * d * 2 * T
+    ws_bytes = ws.numel()
+    sub_bytes = sum((2 * (n + (1 if i >= 2 else 0)) + 1) * d * 2 * T for i in range(1, S + 1))
+    peak, kind = peaks()
+    line = {"metric": "AttnRes block backward (24 sublayers over 9 sources) tokens/s and "
+                      "achieved HBM GB/s, 1 GPU",
+            "value": T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"backward_block_bf16_T{T}_d{d}_n{n}_S{S}", "tokens": T,
+                       "d": d, "sources": n, "sublayers": S,
+                       "l2": "no flush: every launch streams more than the 126 MB L2"},
+            "algorithmic_bytes": byt, "achieved_gbs": byt / (ms / 1e3) / 1e9,
+            "frac_of_peak": byt / (ms / 1e3) / 1e9 / peak, "peak_gbs": peak,
+            "peak_source": kind, "workspace_bytes": ws_bytes,
+            "per_sublayer_backward": {"ms": ms_sub, "algorithmic_bytes": sub_bytes,
+                                      "achieved_gbs": sub_bytes / (ms_sub / 1e3) / 1e9},
+            "speedup_over_per_sublayer": ms_sub / ms,
+            "gpu_launches": 4 * args.steps, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def walk_bytes(wl: I.Workload) -> int:
     """Algorithmic bytes of one Block AttnRes depth walk: every block's phase 1 over the
     sources before it, its phase-2 calls and close, then the final aggregation."""
@@ -719,8 +804,8 @@ def main(argv=None):
                     help="override the token count (profiling a smaller case)")
     ap.add_argument("--chunk", type=int, default=0, help="override the chunk size")
     ap.add_argument("--workload", default="longctx",
-                    choices=["longctx", "full_grouped", "backward", "decode", "prefill_chunk",
-                             "tiny"],
+                    choices=["longctx", "full_grouped", "backward", "backward_block", "decode",
+                             "prefill_chunk", "tiny"],
                     help="full_grouped: the Full AttnRes depth, grouped two-phase vs direct; "
                          "backward: one sublayer's aggregation backward; decode, "
                          "prefill_chunk, tiny: the whole Block AttnRes depth walk of the "
@@ -736,6 +821,8 @@ def main(argv=None):
         return run_full_grouped(args)
     if args.workload == "backward" and args.impl == "ours":
         return run_backward(args)
+    if args.workload == "backward_block" and args.impl == "ours":
+        return run_backward_block(args)
     walks = {"decode": I.DECODE_BF16, "prefill_chunk": I.PREFILL_CHUNK_BF16,
              "tiny": I.TINY_BLOCK_F32}
     if args.workload in walks and args.impl == "ours":

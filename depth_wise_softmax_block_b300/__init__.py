@@ -42,6 +42,9 @@ SIGNATURES = {
     "attnres_phase2_merge_sources": ([_P, _P, _P, _I, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _U,
                                       _I, _P], _I),
     "attnres_backward": ([_P, _I, _I64, _I, _I, _P, _F, _P, _F, _P, _P, _P, _P, _P], _I),
+    "attnres_backward_block_workspace_size": ([_I, _I, _I64, _I, _I, _P], _I),
+    "attnres_backward_block": ([_P, _I64, _I, _P, _I64, _I, _I64, _I, _I, _P, _P, _F, _P, _F, _P,
+                                _P, _P, _I64, _P, _P, _P, ctypes.c_uint64, _P], _I),
 }
 
 
@@ -259,3 +262,45 @@ def attnres_backward(srcs, u, gamma_in, g_y, dsrcs, du, dgamma_in=None, eps_key=
                                       _ptr(dgamma_in), _stream(stream)), "attnres_backward")
     return dsrcs
 
+
+
+def attnres_backward_block_workspace_size(n_src, S, T, d, dtype) -> int:
+    """Bytes of device workspace attnres_backward_block needs for these sizes."""
+    out = ctypes.c_uint64(0)
+    _check(library().attnres_backward_block_workspace_size(
+        n_src, S, T, d, BF16 if dtype == torch.bfloat16 else F32, ctypes.byref(out)),
+        "attnres_backward_block_workspace_size")
+    return int(out.value)
+
+
+def attnres_backward_block(reps, v, u, gamma_in, g_y, d_reps, d_v, du, dgamma_in=None,
+                           u_split=None, eps_key=1e-6, eps_in=1e-6, workspace=None, stream=None):
+    """Backward of one block: ``reps`` [n, T, d] completed sources (any source stride),
+    ``v`` [S-1, T, d] the sublayer outputs v_1 .. v_{S-1} (None when S == 1), ``u`` [S, d] the
+    folded queries, ``g_y`` [S, T, d] = dL/dy_i.  Writes d_reps [n, T, d] (contiguous) and d_v
+    [S-1, T, d]; ADDS du and dgamma_in ([S, d] fp32).  ``workspace``: a uint8 device tensor of
+    at least attnres_backward_block_workspace_size() bytes (made here when None)."""
+    n, T, d = reps.shape
+    S = u.shape[0]
+    _rows(reps[0], T, d, "reps")
+    if g_y.shape != (S, T, d) or not g_y.is_contiguous():
+        raise ValueError("g_y must be a contiguous [S, T, d] tensor")
+    if d_reps.shape != (n, T, d) or not d_reps.is_contiguous():
+        raise ValueError("d_reps must be a contiguous [n, T, d] tensor")
+    if S > 1:
+        for name, t in (("v", v), ("d_v", d_v)):
+            if t is None or t.shape[0] < S - 1 or tuple(t.shape[1:]) != (T, d):
+                raise ValueError(f"{name} must hold S - 1 rows of [T, d]")
+            _rows(t[0], T, d, name)
+    need = attnres_backward_block_workspace_size(n, S, T, d, reps.dtype)
+    if workspace is None:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=reps.device)
+    src_stride = reps.stride(0) if n > 1 else T * d
+    v_stride = v.stride(0) if (v is not None and v.shape[0] > 1) else T * d
+    dv_stride = d_v.stride(0) if (d_v is not None and d_v.shape[0] > 1) else T * d
+    _check(library().attnres_backward_block(
+        _ptr(reps), src_stride, n, _ptr(v), v_stride, S, T, d, _io(reps), _ptr(u), _ptr(u_split),
+        eps_key, _ptr(gamma_in), eps_in, _ptr(g_y), _ptr(d_reps), _ptr(d_v), dv_stride, _ptr(du),
+        _ptr(dgamma_in), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "attnres_backward_block")
+    return d_reps

@@ -290,4 +290,68 @@ attnres_status attnres_backward(const void* const* srcs, int n_src, int64_t T, i
                                               static_cast<cudaStream_t>(stream)));
 }
 
+attnres_status attnres_backward_block_workspace_size(int n_src, int S, int64_t T, int d,
+                                                     attnres_dtype io, uint64_t* bytes) {
+  if (!valid_io(io) || bytes == nullptr) return ATTNRES_ERR_INVALID_ARG;
+  const attnres_status sh = check_shape(T, d);
+  if (sh != ATTNRES_OK) return sh;
+  if (n_src < 1 || S < 1) return ATTNRES_ERR_INVALID_ARG;
+  if (!attnres::backward_block_supported(static_cast<IO>(io), n_src, S, d))
+    return ATTNRES_ERR_UNSUPPORTED;
+  *bytes = static_cast<uint64_t>(
+      attnres::backward_block_workspace_bytes(static_cast<IO>(io), n_src, S, T, d));
+  return ATTNRES_OK;
+}
+
+attnres_status attnres_backward_block(const void* reps, int64_t src_stride, int n_src,
+                                      const void* v, int64_t v_stride, int S, int64_t T, int d,
+                                      attnres_dtype io, const float* u, const void* u_split,
+                                      float eps_key, const float* gamma_in, float eps_in,
+                                      const void* g_y, void* d_reps, void* d_v,
+                                      int64_t dv_stride, float* du, float* dgamma_in,
+                                      void* workspace, uint64_t workspace_bytes, void* stream) {
+  uint64_t need = 0;
+  const attnres_status st = attnres_backward_block_workspace_size(n_src, S, T, d, io, &need);
+  if (st != ATTNRES_OK) return st;
+  if (!(eps_key >= 0.f) || !(eps_in >= 0.f)) return ATTNRES_ERR_INVALID_ARG;
+  if (T == 0) return ATTNRES_OK;
+  if (reps == nullptr || u == nullptr || g_y == nullptr || d_reps == nullptr || du == nullptr ||
+      workspace == nullptr)
+    return ATTNRES_ERR_INVALID_ARG;
+  if (S > 1 && (v == nullptr || d_v == nullptr)) return ATTNRES_ERR_INVALID_ARG;
+  if (workspace_bytes < need) return ATTNRES_ERR_INVALID_ARG;
+  if (n_src > 1 && src_stride < T * d) return ATTNRES_ERR_INVALID_ARG;
+  if (S > 2 && (v_stride < T * d || dv_stride < T * d)) return ATTNRES_ERR_INVALID_ARG;
+  if (src_stride < 0 || v_stride < 0 || dv_stride < 0) return ATTNRES_ERR_INVALID_ARG;
+  if (!aligned16(reps) || !aligned16(u) || !aligned16(g_y) || !aligned16(d_reps) ||
+      !aligned16(du) || !opt_aligned16(v) || !opt_aligned16(d_v) || !opt_aligned16(u_split) ||
+      !opt_aligned16(gamma_in) || !opt_aligned16(dgamma_in) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || src_stride % 8 != 0 ||
+      v_stride % 8 != 0 || dv_stride % 8 != 0)
+    return ATTNRES_ERR_MISALIGNED;
+  attnres::BwdBlockArgs a;
+  memset(&a, 0, sizeof(a));
+  a.reps = reps;
+  a.src_stride = src_stride;
+  a.n = n_src;
+  a.T = T;
+  a.d = d;
+  a.v = v;
+  a.v_stride = v_stride;
+  a.S = S;
+  a.u = u;
+  a.u_split = u_split;
+  a.eps_key = eps_key;
+  a.gamma_in = gamma_in;
+  a.eps_in = eps_in;
+  a.g_y = g_y;
+  a.d_reps = d_reps;
+  a.d_v = d_v;
+  a.dv_stride = dv_stride;
+  a.du = du;
+  a.dgamma_in = dgamma_in;
+  return cuda_status(attnres::launch_backward_block(static_cast<IO>(io), a, workspace,
+                                                    static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -98,6 +98,42 @@ struct BwdArgs {
 constexpr int kBwdMaxVectors = 1024;
 cudaError_t launch_backward(IO io, const BwdArgs& a, cudaStream_t s);
 
+// Backward of one block of Block AttnRes (backward_block.cu).
+constexpr int kBlkMaxN = 16;   // completed sources
+constexpr int kBlkMaxS = 24;   // sublayers of the block
+struct BwdBlockArgs {
+  const void* reps;       // [n][T][d]: source j at reps + j * src_stride elements
+  int64_t src_stride;
+  int n;
+  int64_t T;
+  int d;
+  const void* v;          // v_1 .. v_{S-1}: v_k at v + (k - 1) * v_stride elements ([T, d] each)
+  int64_t v_stride;
+  int S;
+  const float* u;         // [S][d] folded queries
+  const void* u_split;    // [2S][d] bf16 or null (tensor-core phase 1)
+  float eps_key;
+  const float* gamma_in;  // [S][d] or null
+  float eps_in;
+  const void* g_y;        // [S][T][d] dL/dy_i
+  void* d_reps;           // [n][T][d] dL/db_j (written)
+  void* d_v;              // dL/dv_k at d_v + (k - 1) * dv_stride, k = 1 .. S-1 (written)
+  int64_t dv_stride;
+  float* du;              // [S][d] added
+  float* dgamma_in;       // [S][d] added, or null
+  // workspace (set by the launcher)
+  float* o;               // [S][T][d] phase 1 recomputed, fp32
+  float* lse;             // [S][T]
+  float* alpha;           // [S][T][n]
+  float* q;               // [S][T][d] dL/do_i, fp32
+  float* sc2;             // [S][T][4]: c_i, w_A / r_h, w_p / r_h, dz_p / r_p
+  float* rec;             // [T][rec_floats] per-token coefficients of the column kernel
+  int rec_floats;
+};
+int64_t backward_block_workspace_bytes(IO io, int n, int S, int64_t T, int d);
+bool backward_block_supported(IO io, int n, int S, int d);
+cudaError_t launch_backward_block(IO io, BwdBlockArgs a, void* workspace, cudaStream_t s);
+
 // Each launcher returns cudaSuccess or the launch error.
 cudaError_t launch_phase1(IO io, const Phase1Args& a, cudaStream_t s);
 // Returns false when the (n, S) combination does not fit the phase-1 kernel.

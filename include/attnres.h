@@ -100,7 +100,7 @@ typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype;
 #define ATTNRES_MAX_D 16384        /* hidden size (a row stays in registers)               */
 
 /* ABI version of this header; attnres_abi_version() returns the library's. */
-#define ATTNRES_ABI_VERSION 8
+#define ATTNRES_ABI_VERSION 9
 int attnres_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -304,6 +304,53 @@ attnres_status attnres_backward(const void* const* srcs, int n_src, int64_t T, i
                                 attnres_dtype io, const float* u, float eps_key,
                                 const float* gamma_in, float eps_in, const void* g_y,
                                 void* const* dsrcs, float* du, float* dgamma_in, void* stream);
+
+/*
+ * Backward of one whole block of Block AttnRes, structured by the two-phase schedule
+ * ("Attention Residuals" note §8 and §10; the logit gradient of §7; "Attention Residuals
+ * 阅读补充", section "梯度沿切向传播" for both RMSNorm gradients, and the Block AttnRes
+ * training section: the inter-block attention is recomputed in the backward pass).
+ * Forward of the block: sublayer i = 1 .. S reads the completed sources b_0 .. b_{n-1} and,
+ * for i >= 2, the partial sum p_i = v_1 + ... + v_{i-1}; h_i is the depth softmax over those
+ * sources (softmax weights, key RMSNorm, one head) and y_i = gamma_in,i ⊙ h_i / r(h_i).
+ * Given g_i = dL/dy_i for every sublayer, this computes
+ *     dL/db_j = sum over the block's sublayers of each one's gradient of b_j,
+ *     dL/dv_k = sum_{i > k} dL/dp_i  (v_k enters the partial of every later sublayer),
+ *     du_i    += sum over tokens of the query gradient of sublayer i (u = w ⊙ gamma_key; then
+ *                dL/dw_i = gamma_key,i ⊙ du_i and dL/dgamma_key,i = w_i ⊙ du_i),
+ *     dgamma_in,i += sum over tokens of g_i ⊙ h_i / r(h_i).
+ * It recomputes phase 1 for the S queries in one pass over the n sources (o, lse and the
+ * weights go to the workspace), then runs the merge backward of every sublayer per token, then
+ * the sources' and the parameters' gradients; each source row is read three times and written
+ * once per block, however many sublayers the block has.  The partial sums are re-formed in
+ * fp32 from v.
+ *   reps         device [n][T][d] (io dtype): source j at reps + j * src_stride elements
+ *   v            device: v_k (k = 1 .. S-1) at v + (k - 1) * v_stride elements, [T, d] each;
+ *                may be NULL when S == 1.  (v_S enters no sublayer input of the block.)
+ *   u            device fp32 [S][d]: the block's folded queries (attnres_query_prep)
+ *   u_split      device bf16 [2S][d] or NULL: their hi/lo split (tensor-core phase 1)
+ *   gamma_in     device fp32 [S][d] or NULL (ones)
+ *   g_y          device [S][T][d] (io dtype): dL/dy_i
+ *   d_reps       device [n][T][d] (io dtype, contiguous): receives dL/db_j
+ *   d_v          device: dL/dv_k at d_v + (k - 1) * dv_stride elements, k = 1 .. S-1; may be
+ *                NULL when S == 1
+ *   du           device fp32 [S][d]: the gradients are ADDED
+ *   dgamma_in    device fp32 [S][d] or NULL: added, like du
+ *   workspace    device, at least attnres_backward_block_workspace_size() bytes, 256-byte
+ *                aligned; caller-owned scratch, overwritten by every call
+ * The sums over tokens use atomic additions, so their last bits may vary from run to run.
+ * Limits: 1 <= n_src <= 16, 1 <= S <= 24, d / (elements per 16 bytes) <= 1024 (bf16 d <= 8192,
+ * fp32 d <= 4096); otherwise ATTNRES_ERR_UNSUPPORTED.  Strides are multiples of 8 elements.
+ */
+attnres_status attnres_backward_block_workspace_size(int n_src, int S, int64_t T, int d,
+                                                     attnres_dtype io, uint64_t* bytes);
+attnres_status attnres_backward_block(const void* reps, int64_t src_stride, int n_src,
+                                      const void* v, int64_t v_stride, int S, int64_t T, int d,
+                                      attnres_dtype io, const float* u, const void* u_split,
+                                      float eps_key, const float* gamma_in, float eps_in,
+                                      const void* g_y, void* d_reps, void* d_v,
+                                      int64_t dv_stride, float* du, float* dgamma_in,
+                                      void* workspace, uint64_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

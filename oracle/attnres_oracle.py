@@ -419,6 +419,65 @@ def aggregate_backward(sources, w, gamma_key, eps_key: float, gamma_in, eps_in: 
         du=du, dz=dz, g_h=g_h)
 
 
+@dataclass
+class BlockGrads:
+    dcompleted: np.ndarray    # [n, T, d]  dL/db_j of the block's completed sources
+    dv: np.ndarray            # [S, T, d]  dL/dv_k through the block's sublayer inputs (dv_S = 0)
+    dpartial: np.ndarray      # [S, T, d]  dL/dp_i of sublayer i's partial source (dp_1 = 0)
+    du: np.ndarray            # [S, d]     dL/du_i, summed over tokens
+    dw: np.ndarray            # [S, d]
+    dgamma_key: np.ndarray    # [S, d] or None
+    dgamma_in: np.ndarray     # [S, d] or None
+
+
+def block_backward(completed, v, W, G_key, G_in, eps_key: float, eps_in: float, g_y):
+    """Gradients of one block of Block AttnRes (page 2 §8) for the upstream gradients
+    g_y[i] = dL/dy_i of its S sublayer inputs, by the chain rule composed over the block.
+
+    Forward (the direct definition): sublayer i reads the completed sources b_0 .. b_{n-1} and,
+    for i >= 2, the partial sum p_i = b^{i-1} = v_1 + ... + v_{i-1} (page 2 §8: b_n^i =
+    b_n^{i-1} + f_i(h_i)); y_i = RMSNorm_in(h_i) with h_i the depth softmax over those sources.
+    Backward: each sublayer's aggregation backward (``aggregate_backward``) gives the gradient
+    of every source it read; the completed sources collect theirs over all S sublayers, the
+    partial source of sublayer i hands its gradient to every v_k it sums (k < i), and the
+    parameter gradients stay per sublayer.  v_S enters no sublayer input of the block (only
+    the closed block b^S, which later blocks read), so dv_S = 0 here.
+
+    completed [n, T, d]; v [S, T, d]; W, G_key, G_in [S, d] (gains may be None); g_y [S, T, d].
+    """
+    comp = _f64(completed)
+    v = _f64(v)
+    g_y = _f64(g_y)
+    W = _f64(W)
+    S = v.shape[0]
+    n = comp.shape[0]
+    dcomp = np.zeros_like(comp)
+    dv = np.zeros_like(v)
+    dpart = np.zeros_like(v)
+    du = np.zeros((S, comp.shape[-1]))
+    dw = np.zeros_like(du)
+    dgk = None if G_key is None else np.zeros_like(du)
+    dgi = None if G_in is None else np.zeros_like(du)
+    partial = None
+    for i in range(1, S + 1):
+        srcs = block_sources(list(comp), partial)
+        gk = None if G_key is None else _f64(G_key)[i - 1]
+        gi = None if G_in is None else _f64(G_in)[i - 1]
+        G = aggregate_backward(srcs, W[i - 1], gk, eps_key, gi, eps_in, g_y[i - 1])
+        dcomp += G.dsources[:n]
+        if partial is not None:
+            dpart[i - 1] = G.dsources[n]
+            dv[:i - 1] += G.dsources[n][None]
+        du[i - 1], dw[i - 1] = G.du, G.dw
+        if dgk is not None:
+            dgk[i - 1] = G.dgamma_key
+        if dgi is not None:
+            dgi[i - 1] = G.dgamma_in
+        partial = v[i - 1].copy() if partial is None else partial + v[i - 1]
+    return BlockGrads(dcompleted=dcomp, dv=dv, dpartial=dpart, du=du, dw=dw, dgamma_key=dgk,
+                      dgamma_in=dgi)
+
+
 # ---------------------------------------------------------------------------------------------
 # Full AttnRes with the grouped two-phase schedule (page 1, "静态 Query 与两阶段计算": the L
 # layers fall into G scheduling groups of S = L / G; phase 1 scores the S queries of a group

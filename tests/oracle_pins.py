@@ -582,6 +582,37 @@ def pin_backward_scale_invariance(O):
     _close(G.dz.sum(axis=0), np.zeros(T), 1e-12, "sum_i dz_i")
 
 
+def pin_block_backward_fd(O):
+    """The block's backward composed over its S sublayers (every completed source collects the
+    gradients of all S sublayers; the partial source of sublayer i passes its gradient to each
+    v_k it sums, k < i) against central finite differences of L = sum_i g_i ⊙ y_i computed by
+    the forward oracle's block (``single_block``), for the completed sources, the sublayer
+    outputs and every per-sublayer parameter."""
+    r = _rng(53)
+    n, S, T, d = 2, 3, 2, 5
+    comp = _sources(r, n, T, d)
+    v = r.normal(0.0, 1.0, size=(S, T, d))
+    W = r.normal(0.0, 0.7, size=(S, d))
+    Gk = r.normal(1.0, 0.2, size=(S, d))
+    Gi = r.normal(1.0, 0.2, size=(S, d))
+    gy = r.normal(0.0, 1.0, size=(S, T, d))
+    ek, ei = 1e-3, 2e-3
+    G = O.block_backward(comp, v, W, Gk, Gi, ek, ei, gy)
+
+    def loss(cc=comp, vv=v, ww=W, kk=Gk, ii=Gi):
+        b = O.single_block(cc, vv, ww, kk, ii, W[0], None, ek, ei)
+        return float(sum(np.sum(gy[i] * b.y[i]) for i in range(S)))
+    _close(G.dcompleted, _fd_grad(lambda x: loss(cc=x), comp), 1e-7, "dL/db_j")
+    _close(G.dv, _fd_grad(lambda x: loss(vv=x), v), 1e-7, "dL/dv_k")
+    _close(G.dw, _fd_grad(lambda x: loss(ww=x), W), 1e-7, "dL/dw_i")
+    _close(G.dgamma_key, _fd_grad(lambda x: loss(kk=x), Gk), 1e-7, "dL/dgamma_key,i")
+    _close(G.dgamma_in, _fd_grad(lambda x: loss(ii=x), Gi), 1e-7, "dL/dgamma_in,i")
+    _close(G.dw, Gk * G.du, 1e-13, "dw_i = gamma_key,i ⊙ du_i")
+    assert np.all(G.dv[-1] == 0.0) and np.all(G.dpartial[0] == 0.0)
+    # dv_k is the sum of the partial gradients of the sublayers after k
+    _close(G.dv[:-1], np.cumsum(G.dpartial[::-1], axis=0)[::-1][1:], 1e-13, "dv = suffix sums")
+
+
 # --- grouped two-phase Full AttnRes (page 1, "静态 Query 与两阶段计算") ------------------------
 def pin_grouped_full_equals_direct(O):
     """The grouped two-phase schedule reproduces the direct Full AttnRes walk for every group

@@ -45,7 +45,7 @@ def test_header_symbols_exported(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.attnres_abi_version() == 8
+    assert lib.attnres_abi_version() == 9
     for code, name in ar.STATUS.items():
         assert lib.attnres_status_string(code).decode() == name
     assert lib.attnres_status_string(99).decode() == "ATTNRES_ERR_UNKNOWN"
@@ -205,6 +205,40 @@ def test_backward_validation(lib):
     assert err(call(T=4, du=PM)) == MISALIGNED
     bad = (ctypes.c_void_p * 2)(P, PM)
     assert err(call(T=4, dsrcs=bad)) == MISALIGNED
+
+
+def test_backward_block_validation(lib):
+    import ctypes
+    ws = lib.attnres_backward_block_workspace_size
+    out = ctypes.c_uint64(0)
+    assert ws(9, 24, 16, 7168, 1, ctypes.byref(out)) == OK
+    n, S, T, d = 9, 24, 16, 7168
+    R = (S * n + 3 * S + 3) // 4 * 4
+    a256 = lambda x: (x + 255) // 256 * 256              # noqa: E731
+    want = (a256(S * T * d * 4) + a256(S * T * 4) + a256(S * T * n * 4) + a256(S * T * d * 4)
+            + a256(S * T * 16) + a256(T * R * 4))
+    assert out.value == want                              # o, lse, alpha, q, scalars, records
+    assert ws(17, 24, 16, 64, 1, ctypes.byref(out)) == UNSUPPORTED
+    assert ws(9, 25, 16, 64, 1, ctypes.byref(out)) == UNSUPPORTED
+    assert ws(9, 24, 16, 8192 + 8, 1, ctypes.byref(out)) == UNSUPPORTED
+    assert ws(9, 24, 16, 4096 + 8, 0, ctypes.byref(out)) == UNSUPPORTED
+    assert ws(0, 24, 16, 64, 1, ctypes.byref(out)) == INVALID
+    assert ws(9, 24, 16, 64, 1, None) == INVALID
+    bb = lib.attnres_backward_block
+
+    def call(reps=P, n=2, v=P, S=3, T=0, d=64, u=P, gy=P, dr=P, dv=P, du=P, ws=P + 8192,
+             wsb=1 << 40, vst=1 << 20, sst=1 << 20):
+        return bb(reps, sst, n, v, vst, S, T, d, 1, u, None, 1e-6, None, 1e-6, gy, dr, dv, vst,
+                  du, None, ws, wsb, None)
+    assert call() == OK                                   # T = 0: nothing to do
+    assert call(n=17) == UNSUPPORTED
+    assert err(call(T=4, v=None)) == INVALID              # S > 1 needs v and d_v
+    assert err(call(T=4, du=None)) == INVALID
+    assert err(call(T=4, ws=None)) == INVALID
+    assert err(call(T=4, wsb=16)) == INVALID              # workspace too small
+    assert err(call(T=4, ws=P + 16)) == MISALIGNED        # workspace not 256-byte aligned
+    assert err(call(T=4, reps=PM)) == MISALIGNED
+    assert call(S=1, v=None, dv=None) == OK
 
 
 def test_selftest_validation(lib):

@@ -157,6 +157,15 @@ def _multihead_row_norm(sources, w, gamma_key, eps, H, weights="softmax", key_no
     return h, np.stack(al), np.stack(zz)
 
 
+def _block_backward_partial_off_by_one(completed, v, W, G_key, G_in, eps_key, eps_in, g_y):
+    # hands the partial gradient of sublayer i to v_1 .. v_i instead of v_1 .. v_{i-1}
+    G = _ORIG_BLOCK_BACKWARD(completed, v, W, G_key, G_in, eps_key, eps_in, g_y)
+    S = G.dv.shape[0]
+    G.dv = np.stack([G.dpartial[k:].sum(axis=0) for k in range(S)])
+    return G
+
+
+_ORIG_BLOCK_BACKWARD = O.block_backward
 _ORIG_PARTITION = O.partition_stats
 _ORIG_BACKWARD = O.aggregate_backward
 _ORIG_MERGE_S = O.merge_sources_reference
@@ -185,6 +194,7 @@ MUTATIONS = {
     "merge_sources_drops_history": ("merge_sources_reference", _merge_sources_drops_history),
     "rmsnorm_backward_no_radial": ("rmsnorm_backward", _rmsnorm_backward_no_radial),
     "logit_gradient_without_h": ("aggregate_backward", _aggregate_backward_no_minus_h),
+    "block_backward_partial_off_by_one": ("block_backward", _block_backward_partial_off_by_one),
     "heads_interleaved": ("head_slices", _head_slices_interleaved),
     "head_key_norm_over_row": ("multihead_aggregate", _multihead_row_norm),
 }
