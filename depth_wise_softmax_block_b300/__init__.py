@@ -45,6 +45,8 @@ SIGNATURES = {
     "attnres_backward_block_workspace_size": ([_I, _I, _I64, _I, _I, _P], _I),
     "attnres_backward_block": ([_P, _I64, _I, _P, _I64, _I, _I64, _I, _I, _P, _P, _F, _P, _F, _P,
                                 _P, _P, _I64, _P, _P, _P, ctypes.c_uint64, _P], _I),
+    "attnres_backward_block_noalloc": ([_P, _I64, _I, _P, _I64, _I, _I64, _I, _I, _P, _P, _F, _P,
+                                        _F, _P, _P, _P, _I64, _P, _P, _P], _I),
 }
 
 
@@ -303,4 +305,34 @@ def attnres_backward_block(reps, v, u, gamma_in, g_y, d_reps, d_v, du, dgamma_in
         eps_key, _ptr(gamma_in), eps_in, _ptr(g_y), _ptr(d_reps), _ptr(d_v), dv_stride, _ptr(du),
         _ptr(dgamma_in), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)), "attnres_backward_block")
+    return d_reps
+
+
+def attnres_backward_block_noalloc(reps, v, u, gamma_in, g_y, d_reps, d_v, du, dgamma_in=None,
+                                   u_split=None, eps_key=1e-6, eps_in=1e-6, stream=None):
+    """attnres_backward_block for callers that cannot allocate device memory while it runs: the
+    scratch is the library's own fixed device array (ATTNRES_NOALLOC_SCRATCH_BYTES), so nothing
+    is allocated here or in the library.  Blocks whose scratch would not fit raise
+    (ATTNRES_ERR_UNSUPPORTED).  Calls whose work overlaps on the GPU share that array and race:
+    order them.  The first call on a device looks up the array's address; make it before any
+    stream capture."""
+    n, T, d = reps.shape
+    S = u.shape[0]
+    _rows(reps[0], T, d, "reps")
+    if g_y.shape != (S, T, d) or not g_y.is_contiguous():
+        raise ValueError("g_y must be a contiguous [S, T, d] tensor")
+    if d_reps.shape != (n, T, d) or not d_reps.is_contiguous():
+        raise ValueError("d_reps must be a contiguous [n, T, d] tensor")
+    if S > 1:
+        for name, t in (("v", v), ("d_v", d_v)):
+            if t is None or t.shape[0] < S - 1 or tuple(t.shape[1:]) != (T, d):
+                raise ValueError(f"{name} must hold S - 1 rows of [T, d]")
+            _rows(t[0], T, d, name)
+    src_stride = reps.stride(0) if n > 1 else T * d
+    v_stride = v.stride(0) if (v is not None and v.shape[0] > 1) else T * d
+    dv_stride = d_v.stride(0) if (d_v is not None and d_v.shape[0] > 1) else T * d
+    _check(library().attnres_backward_block_noalloc(
+        _ptr(reps), src_stride, n, _ptr(v), v_stride, S, T, d, _io(reps), _ptr(u), _ptr(u_split),
+        eps_key, _ptr(gamma_in), eps_in, _ptr(g_y), _ptr(d_reps), _ptr(d_v), dv_stride, _ptr(du),
+        _ptr(dgamma_in), _stream(stream)), "attnres_backward_block_noalloc")
     return d_reps

@@ -15,8 +15,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libattnres.so")
-SOURCES = ["attnres_abi.cu", "backward.cu", "backward_block.cu", "fullring.cu", "phase1.cu",
-           "phase1_tc.cu", "rowwise.cu", "tmap.cu"]
+SOURCES = ["attnres_abi.cu", "backward.cu", "backward_block.cu", "fullring.cu", "noalloc.cu",
+           "phase1.cu", "phase1_tc.cu", "rowwise.cu", "tmap.cu"]
 HEADERS = ["common.cuh", "kernels.h", "tma.cuh", "tc.cuh"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -352,6 +352,36 @@ attnres_status attnres_backward_block(const void* reps, int64_t src_stride, int 
                                       int64_t dv_stride, float* du, float* dgamma_in,
                                       void* workspace, uint64_t workspace_bytes, void* stream);
 
+/*
+ * The same block backward for callers that cannot allocate device memory while they run it:
+ * code inside a framework whose allocator owns every device byte and hands out no extra buffer
+ * during execution, or code on a latency-critical path that cannot afford cudaMalloc's
+ * implicit synchronisation.  (The pages have no counterpart: this is a property of the
+ * library, not of the method.)
+ * Arguments and results are those of attnres_backward_block, without the workspace: the
+ * scratch comes from a fixed array of ATTNRES_NOALLOC_SCRATCH_BYTES in this library's own
+ * device memory, which every GPU that loads the library keeps until the process exits.  Nothing
+ * is allocated by this call: no cudaMalloc, no cudaFree, no allocating library routine.
+ *   - Size: if attnres_backward_block_workspace_size() for these sizes exceeds
+ *     ATTNRES_NOALLOC_SCRATCH_BYTES (about 48 tokens at n = 9, S = 24, d = 7168), the call
+ *     returns ATTNRES_ERR_UNSUPPORTED and nothing runs.
+ *   - Set-up: the first call on a device, with that device current, looks up the array's device
+ *     address (cudaGetSymbolAddress) and keeps it for later calls on that device; make that first
+ *     call before any stream capture.
+ *   - Sharing: every call uses the same array and leaves its contents behind.  Nothing in it
+ *     needs to start at zero (each call writes every part before reading it), but calls whose
+ *     work overlaps on the GPU (other streams, or other host threads) race on it: order them.
+ */
+#define ATTNRES_NOALLOC_SCRATCH_BYTES (64u << 20)
+attnres_status attnres_backward_block_noalloc(const void* reps, int64_t src_stride, int n_src,
+                                              const void* v, int64_t v_stride, int S, int64_t T,
+                                              int d, attnres_dtype io, const float* u,
+                                              const void* u_split, float eps_key,
+                                              const float* gamma_in, float eps_in,
+                                              const void* g_y, void* d_reps, void* d_v,
+                                              int64_t dv_stride, float* du, float* dgamma_in,
+                                              void* stream);
+
 #ifdef __cplusplus
 }
 #endif
