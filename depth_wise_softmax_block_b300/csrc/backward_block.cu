@@ -20,20 +20,23 @@
 //                dgamma_in,i = sum_t g_i ⊙ h_i / r(h_i)
 //   outputs      dL/dv_k = sum_{i > k} dL/dp_i   (v_k enters the partial of every later sublayer)
 //
-// Four launches, each source row of the block read a bounded number of times (not once per
+// Five launches, each source row of the block read a bounded number of times (not once per
 // sublayer):
 //   1. phase 1 recomputed (the forward's own kernel) over the n sources for the S queries:
 //      o_i (fp32), lse_i, alpha_ij into the workspace;
 //   2. bwd_merge_kernel, one CTA per token row, the S sublayers in reverse order with the
-//      partial sum and the dL/dv running sums in registers: per sublayer one CTA reduction of
+//      partial sum and the dL/dv running sums in shared memory: per sublayer one CTA reduction of
 //      six sums (|p|^2, u.p, |o|^2, o.p, gamma g.o, gamma g.p) gives every scalar of the merge
 //      and of both norms' backward; writes q_i (fp32) and dL/dv_{i-1};
 //   3. bwd_sources_kernel, one CTA per token row: q_i . b_j for all (i, j) and |b_j|^2 (eight
 //      warps, three queries each), the coefficients dz_ij / r_j and sum_i dz_ij z_ij / (d r_j^2),
 //      then dL/db_j per element in a second pass (q_i again, from L2); the coefficients the
 //      parameter sums need go to a per-token record;
-//   4. bwd_params_kernel, one thread per column and a range of tokens: du_i and dgamma_in,i
-//      summed over the CTA's tokens in registers (one atomic per element and CTA at the end).
+//   4. bwd_params_kernel, two columns per thread and 32 tokens per CTA: the partial sums' part
+//      of du_i and dgamma_in,i, summed over the CTA's tokens (one atomic per element, CTA and
+//      sublayer);
+//   5. bwd_du_kernel: the sources' part of du_i, sum over tokens and sources of E_ij b_j, as a
+//      register-blocked product (six sublayers x four columns per thread).
 // Softmax weights, key RMSNorm, one head (the method as defined).
 #include <math.h>
 
@@ -45,12 +48,10 @@
 namespace attnres {
 namespace {
 
-constexpr int kRowThreads = 512;    // merge kernel: at most 512 threads per row
+constexpr int kRowThreads = 256;    // merge kernel: at most 256 threads per row
 constexpr int kDotThreads = 256;    // sources kernel: 8 warps
 constexpr int kDotQ = 3;            // queries per warp in the sources kernel's dots (8 x 3 = 24)
 constexpr int kDbGroup = 8;         // sources whose gradients a thread accumulates at once
-constexpr int kColThreads = 256;    // columns per CTA of the parameter kernel
-constexpr int kColBatch = 16;       // token records staged in shared memory at a time
 
 inline int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
 
@@ -72,65 +73,61 @@ __device__ __forceinline__ void ldg_f32(const float* p, float (&f)[VE]) {
 }
 
 // ------------------------------------------------------------------------------------------
-// 2. merge backward: one CTA per token row, sublayers S .. 1; the rows of sublayer i - 1 (o, g)
-// and v_{i-1} are loaded while sublayer i is reduced and written.
+// 2. merge backward: one CTA per token row, sublayers S .. 1.  The running partial sum p_i and
+// the running sum of dL/dp live in shared memory (element (v, e) of the row at e * nv + v, so
+// the threads of a warp touch consecutive words), which keeps the registers low enough for
+// three rows per SM; the rows of o_i, g_i and v_{i-1} are all requested at the start of a
+// sublayer.
 template <typename IOT, int VPT>
-__global__ void __launch_bounds__(kRowThreads) bwd_merge_kernel(const BwdBlockArgs a) {
+__global__ void __launch_bounds__(kRowThreads, 2) bwd_merge_kernel(const BwdBlockArgs a) {
   constexpr int VE = Vec<IOT>::N;
   constexpr int NW = OWords<float, VE>::N;
   __shared__ float scratch[6 * 33];
+  extern __shared__ float pa[];   // P [VE][nv], then A [VE][nv]
   pdl_enter();
   const int64_t t = blockIdx.x, T = a.T;
   const int d = a.d, nv = d / VE, S = a.S;
   const float fd = static_cast<float>(d);
   const int64_t row = t * d;
+  float* Ps = pa;
+  float* As = pa + d;
 
-  float P[VPT][VE], A[VPT][VE];  // running partial sum p_i and running sum of dL/dp
 #pragma unroll
-  for (int k = 0; k < VPT; ++k)
+  for (int k = 0; k < VPT; ++k) {  // p_S = v_1 + ... + v_{S-1}, and A = 0
+    const int v = threadIdx.x + k * blockDim.x;
+    if (v < nv) {
+      float acc[VE];
 #pragma unroll
-    for (int e = 0; e < VE; ++e) P[k][e] = A[k][e] = 0.f;
+      for (int e = 0; e < VE; ++e) acc[e] = 0.f;
 #pragma unroll 4
-  for (int kv = 1; kv < S; ++kv) {  // p_S = v_1 + ... + v_{S-1}
-    const IOT* vk = static_cast<const IOT*>(a.v) + (kv - 1) * a.v_stride + row;
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int v = threadIdx.x + k * blockDim.x;
-      if (v < nv) {
+      for (int kv = 1; kv < S; ++kv) {
         float x[VE];
-        unpack(ld_stream(vk + v * VE), x);
+        unpack(ld_stream(static_cast<const IOT*>(a.v) + (kv - 1) * a.v_stride + row + v * VE), x);
 #pragma unroll
-        for (int e = 0; e < VE; ++e) P[k][e] += x[e];
+        for (int e = 0; e < VE; ++e) acc[e] += x[e];
+      }
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        Ps[e * nv + v] = acc[e];
+        As[e * nv + v] = 0.f;
       }
     }
   }
-  auto load_og = [&](int i, uint4 (&ro)[VPT][NW], uint4 (&rg)[VPT]) {
-    const int64_t ri = static_cast<int64_t>(i - 1) * T + t;
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int v = threadIdx.x + k * blockDim.x;
-      if (v < nv) {
-        ld_stream_w<float, VE>(a.o + ri * d + v * VE, ro[k]);
-        rg[k] = ld_stream(static_cast<const IOT*>(a.g_y) + ri * d + v * VE);
-      }
-    }
-  };
-  uint4 ro[VPT][NW], rg[VPT];
-  load_og(S, ro, rg);
 
   for (int i = S; i >= 1; --i) {
     const bool has_p = i >= 2;
     const int64_t ri = static_cast<int64_t>(i - 1) * T + t;
     const float* ui = a.u + static_cast<int64_t>(i - 1) * d;
     const float* gam = a.gamma_in ? a.gamma_in + static_cast<int64_t>(i - 1) * d : nullptr;
-    uint4 no[VPT][NW], ng[VPT], rv[VPT];  // sublayer i - 1 and v_{i-1}, in flight
-    if (has_p) {
-      load_og(i - 1, no, ng);
-      const IOT* vk = static_cast<const IOT*>(a.v) + (i - 2) * a.v_stride + row;
+    uint4 ro[VPT][NW], rg[VPT], rv[VPT];
 #pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        const int v = threadIdx.x + k * blockDim.x;
-        if (v < nv) rv[k] = ld_stream(vk + v * VE);
+    for (int k = 0; k < VPT; ++k) {
+      const int v = threadIdx.x + k * blockDim.x;
+      if (v < nv) {
+        ld_stream_w<float, VE>(a.o + ri * d + v * VE, ro[k]);
+        rg[k] = ld_stream(static_cast<const IOT*>(a.g_y) + ri * d + v * VE);
+        if (has_p)
+          rv[k] = ld_stream(static_cast<const IOT*>(a.v) + (i - 2) * a.v_stride + row + v * VE);
       }
     }
     // |p|^2, u.p, |o|^2, o.p, (gamma g).o, (gamma g).p
@@ -152,7 +149,7 @@ __global__ void __launch_bounds__(kRowThreads) bwd_merge_kernel(const BwdBlockAr
 #pragma unroll
         for (int e = 0; e < VE; ++e) {
           const float ge = gg[e] * g[e];
-          const float p = P[k][e];
+          const float p = Ps[e * nv + v];
           s[0] = fmaf(p, p, s[0]);
           s[1] = fmaf(uu[e], p, s[1]);
           s[2] = fmaf(o[e], o[e], s[2]);
@@ -194,7 +191,7 @@ __global__ void __launch_bounds__(kRowThreads) bwd_merge_kernel(const BwdBlockAr
     for (int k = 0; k < VPT; ++k) {
       const int v = threadIdx.x + k * blockDim.x;
       if (v < nv) {
-        float o[VE], g[VE], q[VE], uu[VE], gg[VE];
+        float o[VE], g[VE], q[VE], uu[VE], gg[VE], dv[VE], x[VE];
         unpack_w<float, VE>(ro[k], o);
         unpack(rg[k], g);
         ldg_f32<VE>(ui + v * VE, uu);
@@ -204,34 +201,25 @@ __global__ void __launch_bounds__(kRowThreads) bwd_merge_kernel(const BwdBlockAr
 #pragma unroll
           for (int e = 0; e < VE; ++e) gg[e] = 1.f;
         }
+        if (has_p) unpack(rv[k], x);
 #pragma unroll
         for (int e = 0; e < VE; ++e) {
-          const float h = wA * o[e] + wP * P[k][e];
+          const float p = Ps[e * nv + v];
+          const float h = wA * o[e] + wP * p;
           const float gh = gg[e] * g[e] * inv_rh - kap * h;
           q[e] = wA * gh;
-          if (has_p) A[k][e] += wP * gh + coefu * uu[e] - coefp * P[k][e];
+          if (has_p) {
+            dv[e] = As[e * nv + v] + wP * gh + coefu * uu[e] - coefp * p;
+            As[e * nv + v] = dv[e];
+            Ps[e * nv + v] = p - x[e];   // p_{i-1} = p_i - v_{i-1}
+          }
         }
         st_vec<float, VE>(qi + v * VE, q);
-        if (has_p) st_vec<IOT, VE>(dvi + v * VE, A[k]);
+        if (has_p) st_vec<IOT, VE>(dvi + v * VE, dv);
       }
     }
     if (threadIdx.x == 0)
       *reinterpret_cast<float4*>(a.sc2 + ri * 4) = make_float4(c, wA * inv_rh, wP * inv_rh, coefu);
-    if (has_p) {  // p_{i-1} = p_i - v_{i-1}; the next sublayer's rows are already loaded
-#pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        const int v = threadIdx.x + k * blockDim.x;
-        if (v < nv) {
-          float x[VE];
-          unpack(rv[k], x);
-#pragma unroll
-          for (int e = 0; e < VE; ++e) P[k][e] -= x[e];
-#pragma unroll
-          for (int w = 0; w < NW; ++w) ro[k][w] = no[k][w];
-          rg[k] = ng[k];
-        }
-      }
-    }
   }
 }
 
@@ -240,7 +228,7 @@ __global__ void __launch_bounds__(kRowThreads) bwd_merge_kernel(const BwdBlockAr
 // dL/db_j = sum_i alpha_ij q_i + sum_i E_ij u_i - F_j b_j per element (pass 2, q_i again from
 // L2), with E_ij = dz_ij / r_j and F_j = sum_i dz_ij z_ij / (d r_j^2).
 template <typename IOT>
-__global__ void __launch_bounds__(kDotThreads) bwd_sources_kernel(const BwdBlockArgs a) {
+__global__ void __launch_bounds__(kDotThreads, 3) bwd_sources_kernel(const BwdBlockArgs a) {
   constexpr int VE = Vec<IOT>::N;
   constexpr int NJ = kBlkMaxN;
   constexpr int NW = OWords<float, VE>::N;
@@ -392,68 +380,179 @@ __device__ __forceinline__ float ld1(const IOT* p) {
 }
 
 template <typename IOT>
-__global__ void __launch_bounds__(kColThreads) bwd_params_kernel(const BwdBlockArgs a,
-                                                                 int tokens_per_cta) {
-  constexpr int NJ = kBlkMaxN, NS = kBlkMaxS;
-  extern __shared__ float srec[];  // [kColBatch][R]
+__device__ __forceinline__ void ld2(const IOT* p, float& x, float& y) {
+  if constexpr (sizeof(IOT) == 2) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+    x = __uint_as_float(w << 16);
+    y = __uint_as_float(w & 0xffff0000u);
+  } else {
+    const float2 f = *reinterpret_cast<const float2*>(p);
+    x = f.x;
+    y = f.y;
+  }
+}
+
+// The CTA owns kParCols columns (two per thread) and kParTok consecutive tokens.  Sublayers run
+// in the outer loop, tokens in the inner one, so all loads of a sublayer over the CTA's tokens
+// are independent: the partial sums p_i of the CTA's tokens live in shared memory
+// ([token][column], updated with v_{i-1} before sublayer i), and the per-token scalars
+// (w_A / r_h, w_p / r_h, dz_p / r_p of every sublayer) are staged once.
+constexpr int kParThreads = 128;
+constexpr int kParCols = 2 * kParThreads;
+constexpr int kParTok = 32;
+
+template <typename IOT>
+__global__ void __launch_bounds__(kParThreads) bwd_params_kernel(const BwdBlockArgs a) {
+  extern __shared__ float psm[];   // P [kParTok][kParCols], then scalars [kParTok][3S]
   pdl_enter();
   const int d = a.d, S = a.S, n = a.n, R = a.rec_floats;
   const int64_t T = a.T;
-  const int c = blockIdx.x * kColThreads + threadIdx.x;
-  const bool valid = c < d;
+  const int cl = 2 * threadIdx.x;                 // local column pair
+  const int c = blockIdx.x * kParCols + cl;
+  const bool valid = c < d;                       // d is even
+  const int64_t t0 = static_cast<int64_t>(blockIdx.y) * kParTok;
+  const int nt = static_cast<int>(T - t0 < kParTok ? T - t0 : kParTok);
+  float* Ps = psm;
+  float* sc = psm + kParTok * kParCols;
+  for (int k = threadIdx.x; k < nt * 3 * S; k += blockDim.x) {
+    const int tt = k / (3 * S), r = k - tt * 3 * S;
+    sc[k] = a.rec[(t0 + tt) * R + S * n + r];      // a [S], b [S], e [S] of token t0 + tt
+  }
+  for (int tt = 0; tt < nt; ++tt) {
+    Ps[tt * kParCols + cl] = 0.f;
+    Ps[tt * kParCols + cl + 1] = 0.f;
+  }
+  __syncthreads();
+  if (!valid) return;
+  const IOT* vb = static_cast<const IOT*>(a.v);
+  const IOT* gb = static_cast<const IOT*>(a.g_y);
+  for (int i = 0; i < S; ++i) {                   // sublayer i + 1
+    float du0 = 0.f, du1 = 0.f, dg0 = 0.f, dg1 = 0.f;
+#pragma unroll 8
+    for (int tt = 0; tt < nt; ++tt) {
+      const int64_t t = t0 + tt;
+      float p0 = Ps[tt * kParCols + cl], p1 = Ps[tt * kParCols + cl + 1];
+      if (i >= 1) {
+        float x0, x1;
+        ld2(vb + (i - 1) * a.v_stride + t * d + c, x0, x1);
+        p0 += x0;
+        p1 += x1;
+        Ps[tt * kParCols + cl] = p0;
+        Ps[tt * kParCols + cl + 1] = p1;
+      }
+      const int64_t at = (static_cast<int64_t>(i) * T + t) * d + c;
+      const float2 o = *reinterpret_cast<const float2*>(a.o + at);
+      float g0, g1;
+      ld2(gb + at, g0, g1);
+      const float* st = sc + tt * 3 * S;
+      const float wa = st[i], wb = st[S + i], we = st[2 * S + i];
+      dg0 = fmaf(g0, wa * o.x + wb * p0, dg0);
+      dg1 = fmaf(g1, wa * o.y + wb * p1, dg1);
+      du0 = fmaf(we, p0, du0);
+      du1 = fmaf(we, p1, du1);
+    }
+    atomicAdd(a.du + static_cast<int64_t>(i) * d + c, du0);
+    atomicAdd(a.du + static_cast<int64_t>(i) * d + c + 1, du1);
+    if (a.dgamma_in != nullptr) {
+      atomicAdd(a.dgamma_in + static_cast<int64_t>(i) * d + c, dg0);
+      atomicAdd(a.dgamma_in + static_cast<int64_t>(i) * d + c + 1, dg1);
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// 5. the sources' part of the query gradients, du_i += sum_t sum_j E_ij(t) b_j(t): a product of
+// the [S x (tokens x sources)] coefficients and the [(tokens x sources) x d] source rows, summed
+// over a range of tokens per CTA.  Warp w owns sublayers 6w .. 6w + 5, lane l four columns; the
+// CTA stages its tokens' coefficients in shared memory as [token][source][sublayer].
+constexpr int kDuThreads = 128;   // 4 warps x 6 sublayers = 24
+constexpr int kDuCols = 128;      // columns per CTA (4 per lane)
+constexpr int kDuRows = 6;        // sublayers per warp
+constexpr int kDuBatch = 32;      // tokens staged at a time
+
+template <typename IOT>
+__device__ __forceinline__ void ld4(const IOT* p, float (&f)[4]) {
+  if constexpr (sizeof(IOT) == 2) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    f[0] = __uint_as_float(w.x << 16);
+    f[1] = __uint_as_float(w.x & 0xffff0000u);
+    f[2] = __uint_as_float(w.y << 16);
+    f[3] = __uint_as_float(w.y & 0xffff0000u);
+  } else {
+    const float4 x = *reinterpret_cast<const float4*>(p);
+    f[0] = x.x;
+    f[1] = x.y;
+    f[2] = x.z;
+    f[3] = x.w;
+  }
+}
+
+template <typename IOT>
+__global__ void __launch_bounds__(kDuThreads) bwd_du_kernel(const BwdBlockArgs a,
+                                                            int tokens_per_cta) {
+  constexpr int SP = 24;                      // padded sublayer stride of the staged tile
+  extern __shared__ float ce[];               // [kDuBatch][n][SP]
+  pdl_enter();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.d, S = a.S, n = a.n, R = a.rec_floats;
+  const int64_t T = a.T;
+  const int c = blockIdx.x * kDuCols + 4 * lane;
+  const bool valid = c < d;                   // d is a multiple of 4
+  const int i0 = warp * kDuRows;
   const int64_t t0 = static_cast<int64_t>(blockIdx.y) * tokens_per_cta;
   const int64_t t1 = t0 + tokens_per_cta < T ? t0 + tokens_per_cta : T;
   const IOT* reps = static_cast<const IOT*>(a.reps);
-  const IOT* vb = static_cast<const IOT*>(a.v);
-  const IOT* gb = static_cast<const IOT*>(a.g_y);
-
-  float du[NS], dg[NS];
+  float acc[kDuRows][4];
 #pragma unroll
-  for (int i = 0; i < NS; ++i) du[i] = dg[i] = 0.f;
-  const int oE = 0, oa = S * n, ob = oa + S, oe = ob + S;
-
-  for (int64_t tb0 = t0; tb0 < t1; tb0 += kColBatch) {
-    const int nb = static_cast<int>(t1 - tb0 < kColBatch ? t1 - tb0 : kColBatch);
-    __syncthreads();  // the previous batch's records are no longer read
-    for (int k = threadIdx.x; k < nb * R / 4; k += blockDim.x)
-      reinterpret_cast<float4*>(srec)[k] = reinterpret_cast<const float4*>(a.rec + tb0 * R)[k];
+  for (int r = 0; r < kDuRows; ++r)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
+  for (int64_t tb0 = t0; tb0 < t1; tb0 += kDuBatch) {
+    const int nb = static_cast<int>(t1 - tb0 < kDuBatch ? t1 - tb0 : kDuBatch);
     __syncthreads();
-    if (!valid) continue;
+    for (int k = threadIdx.x; k < nb * S * n; k += blockDim.x) {  // record [i][j] -> [j][i]
+      const int tb = k / (S * n), rem = k - tb * S * n, i = rem / n, j = rem - i * n;
+      ce[(tb * n + j) * SP + i] = a.rec[(tb0 + tb) * R + rem];
+    }
+    __syncthreads();
+    if (!valid || i0 >= S) continue;
     for (int tb = 0; tb < nb; ++tb) {
-      const int64_t t = tb0 + tb;
-      const float* rr = srec + tb * R;
-      float b[NJ];
+      const IOT* bt = reps + (tb0 + tb) * d + c;
+#pragma unroll 3
+      for (int j = 0; j < n; ++j) {
+        float b[4];
+        ld4(bt + j * a.src_stride, b);
+        const float* e = ce + (tb * n + j) * SP + i0;
 #pragma unroll
-      for (int j = 0; j < NJ; ++j) b[j] = j < n ? ld1(reps + j * a.src_stride + t * d + c) : 0.f;
-      float P = 0.f;  // partial sum of sublayer i + 1
+        for (int r = 0; r < kDuRows; ++r) {
+          const float er = e[r];
 #pragma unroll
-      for (int i = 0; i < NS; ++i) {
-        if (i < S) {
-          if (i >= 1) P += ld1(vb + (i - 1) * a.v_stride + t * d + c);
-          const int64_t at = (static_cast<int64_t>(i) * T + t) * d + c;
-          const float o = a.o[at], g = ld1(gb + at);
-          dg[i] = fmaf(g, rr[oa + i] * o + rr[ob + i] * P, dg[i]);
-          float dui = rr[oe + i] * P;
-#pragma unroll
-          for (int j = 0; j < NJ; ++j)
-            if (j < n) dui = fmaf(rr[oE + i * n + j], b[j], dui);
-          du[i] += dui;
+          for (int q = 0; q < 4; ++q) acc[r][q] = fmaf(er, b[q], acc[r][q]);
         }
       }
     }
   }
   if (valid) {
 #pragma unroll
-    for (int i = 0; i < NS; ++i) {
-      if (i < S) {
-        atomicAdd(a.du + static_cast<int64_t>(i) * d + c, du[i]);
-        if (a.dgamma_in != nullptr) atomicAdd(a.dgamma_in + static_cast<int64_t>(i) * d + c, dg[i]);
-      }
-    }
+    for (int r = 0; r < kDuRows; ++r)
+      if (i0 + r < S)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          atomicAdd(a.du + static_cast<int64_t>(i0 + r) * d + c + q, acc[r][q]);
   }
 }
 
 // ------------------------------------------------------------------------------------------
+template <typename IOT, int VPT>
+cudaError_t launch_merge_vpt(const BwdBlockArgs& a, int threads, cudaStream_t s) {
+  const size_t smem = 2 * static_cast<size_t>(a.d) * sizeof(float);
+  auto kern = bwd_merge_kernel<IOT, VPT>;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(a.T)), dim3(threads), smem, s, a);
+}
+
 template <typename IOT>
 cudaError_t launch_merge(const BwdBlockArgs& a, cudaStream_t s) {
   constexpr int VE = Vec<IOT>::N;
@@ -461,10 +560,10 @@ cudaError_t launch_merge(const BwdBlockArgs& a, cudaStream_t s) {
   int vpt = 1;
   while ((nv + vpt - 1) / vpt > kRowThreads) vpt *= 2;
   const int threads = ((nv + vpt - 1) / vpt + 31) / 32 * 32;
-  const unsigned grid = static_cast<unsigned>(a.T);
   switch (vpt) {
-    case 1: return launch_pdl(bwd_merge_kernel<IOT, 1>, grid, threads, 0, s, a);
-    case 2: return launch_pdl(bwd_merge_kernel<IOT, 2>, grid, threads, 0, s, a);
+    case 1: return launch_merge_vpt<IOT, 1>(a, threads, s);
+    case 2: return launch_merge_vpt<IOT, 2>(a, threads, s);
+    case 4: return launch_merge_vpt<IOT, 4>(a, threads, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -478,18 +577,29 @@ cudaError_t launch_rest(const BwdBlockArgs& a, cudaStream_t s) {
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int gx = (a.d + kColThreads - 1) / kColThreads;
-  int64_t gy = (8LL * sms + gx - 1) / gx;   // about eight CTAs per SM
-  if (gy > a.T) gy = a.T;
-  const int tpc = static_cast<int>((a.T + gy - 1) / gy);
-  gy = (a.T + tpc - 1) / tpc;
-  const size_t smem = static_cast<size_t>(kColBatch) * a.rec_floats * sizeof(float);
+  const int gx = (a.d + kParCols - 1) / kParCols;
+  const int64_t gy = (a.T + kParTok - 1) / kParTok;
+  const size_t smem = (static_cast<size_t>(kParTok) * kParCols + kParTok * 3 * a.S) * sizeof(float);
   auto kern = bwd_params_kernel<IOT>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)),
-                    dim3(kColThreads), smem, s, a, tpc);
+  e = launch_pdl(kern, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)),
+                 dim3(kParThreads), smem, s, a);
+  if (e != cudaSuccess) return e;
+  // the sources' part of du
+  const int dx = (a.d + kDuCols - 1) / kDuCols;
+  int64_t dy = (6LL * sms + dx - 1) / dx;
+  if (dy > a.T) dy = a.T;
+  const int dtpc = static_cast<int>((a.T + dy - 1) / dy);
+  dy = (a.T + dtpc - 1) / dtpc;
+  const size_t dsmem = static_cast<size_t>(kDuBatch) * a.n * 24 * sizeof(float);
+  auto dkern = bwd_du_kernel<IOT>;
+  e = cudaFuncSetAttribute(dkern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(dsmem));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(dkern, dim3(static_cast<unsigned>(dx), static_cast<unsigned>(dy)),
+                    dim3(kDuThreads), dsmem, s, a, dtpc);
 }
 
 }  // namespace
@@ -504,7 +614,7 @@ int64_t backward_block_workspace_bytes(IO io, int n, int S, int64_t T, int d) {
 bool backward_block_supported(IO io, int n, int S, int d) {
   const int VE = io == IO::BF16 ? 8 : 4;
   return n >= 1 && n <= kBlkMaxN && S >= 1 && S <= kBlkMaxS && d % VE == 0 &&
-         d / VE <= 2 * kRowThreads;   // the merge kernel keeps two vectors per thread
+         d / VE <= 4 * kRowThreads;   // the merge kernel keeps four vectors per thread
 }
 
 cudaError_t launch_backward_block(IO io, BwdBlockArgs a, void* workspace, cudaStream_t s) {
