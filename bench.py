@@ -388,6 +388,63 @@ def traffic_for(kernel: str, heads: int = 1):
     return e.get("bytes_per_launch")
 
 
+def import_traffic(csv_path: str, tokens: int, heads: int = 1, scale_to: int = 16384):
+    """Turn an ncu capture of the step at ``tokens`` tokens (one chunk; metrics
+    dram__bytes_read.sum and dram__bytes_write.sum of this library's kernels, in launch order)
+    into the per-kernel DRAM traffic that ``traffic_for`` reads: bytes per launch scaled to a
+    ``scale_to``-token launch (traffic grows with the tokens), stamped with the hash of each
+    kernel's source files.  The launches of a chunk come in the step's order: phase 1, the S
+    phase-2 calls (the first, the one with the partial given, then the fused ones), the close,
+    the final aggregation."""
+    import csv
+    import collections
+    rows = list(csv.reader(open(csv_path)))
+    hdr = None
+    launches = collections.OrderedDict()
+    for r in rows:
+        if "Kernel Name" in r:
+            hdr = r
+            continue
+        if hdr is None or len(r) != len(hdr):
+            continue
+        rec = dict(zip(hdr, r))
+        lid = int(rec["ID"])
+        e = launches.setdefault(lid, {"name": rec["Kernel Name"]})
+        e[rec["Metric Name"]] = float(rec["Metric Value"].replace(",", ""))
+    step_kernels = ("phase1_tc_kernel", "phase1_kernel", "phase2_kernel", "phase2_heads_kernel",
+                    "add_kernel", "full_ring_kernel", "full_kernel", "full_heads_kernel")
+    ours = [e for e in launches.values()
+            if any(k + "<" in e["name"] for k in step_kernels)]
+    S = I.LONGCTX_PREFILL_BF16.S
+    per_chunk = ["phase1"] + ["phase2_first", "phase2"] + ["phase2_fused"] * (S - 2) + ["close",
+                                                                                      "final"]
+    assert len(ours) % len(per_chunk) == 0, (len(ours), len(per_chunk))
+    acc = collections.defaultdict(lambda: [0, 0.0, 0.0, 0.0, ""])
+    for k, e in enumerate(ours):
+        kind = per_chunk[k % len(per_chunk)]
+        a = acc[kind]
+        a[0] += 1
+        a[1] += e.get("dram__bytes_read.sum", 0.0)
+        a[2] += e.get("dram__bytes_write.sum", 0.0)
+        a[3] += e.get("gpu__time_duration.sum", 0.0)
+        a[4] = e["name"]
+    tag = "" if heads == 1 else f"_heads{heads}"
+    out_path = os.path.join(ROOT, "profiles", f"dram_traffic_longctx{tag}_T{tokens}.json")
+    out = {}
+    for kind, (cnt, rd, wr, dur, name) in acc.items():
+        files = KERNEL_SOURCES[kind if kind in ("phase1", "final") else "rowwise"]
+        out[kind] = {"src_hash": kernel_hash(kind), "src_files": files, "kernel": name[:120],
+                     "heads": heads, "captured_tokens": tokens, "scaled_to_tokens": scale_to,
+                     "launches_captured": cnt, "read_bytes_captured": rd,
+                     "write_bytes_captured": wr,
+                     "bytes_per_launch": (rd + wr) / cnt * scale_to / tokens,
+                     "ncu_duration_ns_captured": dur / cnt}
+    with open(out_path, "w") as f:
+        json.dump(out, f, indent=1)
+    print(json.dumps({k: round(v["bytes_per_launch"] / 1e9, 4) for k, v in out.items()}))
+    return 0
+
+
 def run_e2e(step: LongContextStep, iters: int):
     """The same step through the public API from pinned HOST buffers: per step, copy the
     block-representation cache (slots 0..8), the sublayer stand-ins and the parameters to the
@@ -511,11 +568,32 @@ def run_full_grouped(args):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / args.steps
 
-    ms_g = timed(grouped)
+    ms_g_eager = timed(grouped)
     kern = {k: {"launches_per_step": c // args.steps, "avg_ms": t / c}
             for k, (t, c) in timer.totals_ms().items()}
     runner.timer = None
-    ms_d = timed(direct)
+    ms_d_eager = timed(direct)
+
+    def graphed(fn):
+        """The same calls captured once as a CUDA graph and replayed (the library launches on the
+        caller's stream and allocates nothing); None if the capture fails."""
+        try:
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                fn()
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g):
+                fn()
+            return timed(g.replay)
+        except Exception:  # noqa: BLE001 - the eager time stands
+            return None
+
+    ms_g_graph, ms_d_graph = graphed(grouped), graphed(direct)
+    ms_g = min(x for x in (ms_g_eager, ms_g_graph) if x is not None)
+    ms_d = min(x for x in (ms_d_eager, ms_d_graph) if x is not None)
     bg, bd = full_grouped_bytes(L, S, d, 2) * T, full_direct_bytes(L, d, 2) * T
     peak, kind = peaks()
     line = {
@@ -526,6 +604,10 @@ def run_full_grouped(args):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name + f"_grouped_S{S}", "tokens": T, "d": d, "layers": L,
                    "group": S},
+        "launch": {"grouped": "cuda_graph" if ms_g == ms_g_graph else "eager",
+                   "direct": "cuda_graph" if ms_d == ms_d_graph else "eager",
+                   "eager_ms": {"grouped": ms_g_eager, "direct": ms_d_eager},
+                   "graph_ms": {"grouped": ms_g_graph, "direct": ms_d_graph}},
         "grouped": {"ms": ms_g, "bytes": bg, "achieved_gbs": bg / (ms_g / 1e3) / 1e9,
                     "frac_of_peak": bg / (ms_g / 1e3) / 1e9 / peak,
                     "d_elements_per_layer": bg / T / L / d / 2, "kernels": kern},
@@ -814,7 +896,12 @@ def main(argv=None):
     ap.add_argument("--group", type=int, default=8, help="group size of --workload full_grouped")
     ap.add_argument("--heads", type=int, default=1,
                     help="depth-attention heads of the longctx step (Table 4 multi-head: 16)")
+    ap.add_argument("--import-traffic", default="",
+                    help="write profiles/dram_traffic_longctx_T<tokens>.json from an ncu CSV of "
+                         "dram__bytes_read.sum / dram__bytes_write.sum of the step at --tokens")
     args = ap.parse_args(argv)
+    if args.import_traffic:
+        return import_traffic(args.import_traffic, args.tokens or 4096, args.heads)
     world, rank, local = dist_setup()
 
     if args.workload == "full_grouped" and args.impl == "ours":
