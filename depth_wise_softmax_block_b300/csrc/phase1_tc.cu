@@ -61,6 +61,9 @@ constexpr int kSmallN = 9;          // up to here the sweep-2 weights are stored
 constexpr int kTmemMax = 512;       // tensor-memory columns of an SM
 constexpr int kMaxSlots = 12;       // ring slots
 constexpr int kMaxSmem = 227 * 1024;
+constexpr int kTc2Col0 = 128;       // first tensor-memory column of the sweep-2 accumulators
+constexpr int kGrpQ = 6;                          // sweep 2: queries per group of 4 warps
+constexpr int kStgWarp = kGrpQ * kTT * 32 * 2;    // a warp's staged o tile [6][8][32] bf16
 
 struct TcPlan {
   int Hs, windows;    // heads per CTA window, windows (= H / Hs, or csplit)
@@ -72,29 +75,44 @@ struct TcPlan {
   int bBytes;         // source box bytes as copied (rows * 128)
   int bSpan;          // rounded up to 1024
   int qBytes;         // split-query box bytes (Npad rows x 128 bytes, rows >= 2S zero-filled)
-  int slot, SB;       // ring slot bytes ([sources][split queries]), slots
-  int offZ, offAlph, offSs, offBar, offTmem;
+  int qOff;           // offset of the split-query box in a slot
+  int slot, SB;       // ring slot bytes ([sources][split queries]), slots (even: see below)
+  // sweep 2 on the tensor cores (tc2) has a ring of its own over the same memory: SB2 slots of
+  // two 64-column source boxes `region` bytes apart (rows padded to a multiple of 16 with
+  // zeros), then the weights as the MMA's B operand, [Nb / 8 row groups][KC chunks of 8 rows]
+  // core matrices, once as hi and once as lo halves
+  int tc2, region, KC, Nb, abBytes, slot2, SB2;
+  int offAB, offZ, offAlph, offSs, offBar, offTmem;
   int smem;
 };
 
 inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-// Layout for n sources, S queries and a window of Hs heads; false if it does not fit.
-bool make_tc_window(int n, int S, int H, int Hs, TcPlan& p) {
+// Layout for n sources, S queries and a window of Hs heads, with sweep 2 on the tensor cores
+// (tc2: one head, n <= 9) or on the CUDA cores; false if it does not fit.
+bool make_tc_window(int n, int S, int H, int Hs, bool tc2, TcPlan& p) {
   p.Hs = Hs;
   p.windows = H / Hs;
   p.csplit = 1;
+  p.tc2 = tc2 ? 1 : 0;
   p.Npad = align_up(2 * S, 16);
   p.rows = n * kTT;
   p.nMT = (p.rows + kM - 1) / kM;
   p.R = p.nMT * kM;
-  const int cols = p.nMT * Hs * p.Npad;
+  int cols = p.nMT * Hs * p.Npad;
+  if (tc2) {
+    if (H != 1 || n > kSmallN || cols > kTc2Col0) return false;
+    p.Nb = align_up(kTT * S, 16);            // sweep-2 MMA N: (query, token) pairs
+    p.KC = align_up(p.rows, 16) / 8;         // sweep-2 K chunks: (source, token) rows / 8
+    cols = kTc2Col0 + 2 * p.Nb;              // two accumulators, alternate 128-column stages
+  }
   if (cols > kTmemMax) return false;
   for (p.tcols = 32; p.tcols < cols; p.tcols *= 2) {
   }
   p.bBytes = p.rows * 128;
-  p.bSpan = align_up(p.bBytes, 1024);
   p.qBytes = p.Npad * 128;
+  p.bSpan = align_up(p.bBytes, 1024);
+  p.qOff = p.bSpan;
   p.slot = p.bSpan + align_up(p.qBytes, 1024);
   // The MMAs read nMT * 128 rows from a slot's base; rows past the tile's n * 8 are ignored but
   // must lie inside the allocation, hence the slack after the last slot.
@@ -103,28 +121,50 @@ bool make_tc_window(int n, int S, int H, int Hs, TcPlan& p) {
   // small layout) the weights in their place; 8 floats of padding for the last query group's
   // 6-wide read
   const int zb = (p.rows * Hs * ((S + 1) & ~1) + 8) * 4;
-  const bool small = H == 1 && n <= kSmallN;
+  const bool small = H == 1 && n <= kSmallN && !tc2;
   const int ab = small ? kTT * n * 4 * 12 * 4 : 0;  // [token][source][4][6 pairs][2]
   const int sb = 2 * Hs * p.R * 4;                  // per-half, per-head row sums of squares
-  const int fixed = slack + align_up(zb, 16) + align_up(ab, 16) + sb +
-                    (2 * kMaxSlots + 4) * 8 + 16;
-  p.SB = std::min(kMaxSlots, (kMaxSmem - 1024 - fixed) / p.slot);
+  // tc2: sweep 2 stages its output tiles where the logits and sums of squares were (dead by then)
+  const int zone = std::max(align_up(zb, 16) + align_up(ab, 16) + sb,
+                            tc2 ? kWarps * kStgWarp : 0);
+  const int avail = kMaxSmem - 1024 - zone - (4 * kMaxSlots + 10) * 8 - 16;
+  // The two halves of the compute warps take alternate stages of the sweep-1 ring, each
+  // waiting on the "full" barriers of its own stages only.  With an odd number of slots
+  // consecutive users of a slot belong to different halves, and a half running a ring ahead
+  // could see the completion two phases back (same parity) as its own stage's: the slot count
+  // is even, so a slot's successive stages always belong to the same half.
+  if (tc2) {
+    p.region = p.KC * 8 * 128;  // a multiple of 2048: both boxes stay 1024-byte aligned
+    p.slot2 = 2 * p.region;
+    p.abBytes = (p.Nb / 8) * p.KC * 128;
+    p.SB2 = std::min(kMaxSlots, (avail - 2 * p.abBytes) / p.slot2);  // one in-order consumer
+    if (p.SB2 < 2) return false;
+    p.offAB = p.SB2 * p.slot2;
+    p.offZ = p.offAB + 2 * p.abBytes;  // the sweep-1 ring spans [0, offZ): both rings, weights
+    p.SB = std::min(kMaxSlots, (p.offZ - slack) / p.slot) & ~1;
+  } else {
+    p.region = p.KC = p.Nb = p.abBytes = p.slot2 = p.SB2 = 0;
+    p.SB = std::min(kMaxSlots, (avail - slack) / p.slot) & ~1;
+    p.offAB = p.SB * p.slot + slack;
+    p.offZ = p.offAB;
+  }
   if (p.SB < 2) return false;
-  p.offZ = p.SB * p.slot + slack;
   p.offAlph = p.offZ + align_up(zb, 16);
   p.offSs = p.offAlph + align_up(ab, 16);
-  p.offBar = p.offSs + sb;
-  p.offTmem = p.offBar + (2 * p.SB + 4) * 8;  // full, empty, dready, abort, xready, xdone
+  p.offBar = p.offZ + zone;
+  // full[SB], empty[SB], dready, abort, xready, xdone, dfull[2], dempty[2], aready, mdone,
+  // full2[SB2], empty2[SB2]
+  p.offTmem = p.offBar + (2 * p.SB + 10 + 2 * p.SB2) * 8;
   p.smem = 1024 + p.offTmem + 16;
   return true;
 }
 
 // The widest window (most heads per CTA) that fits; false if none does.
-bool make_tc_plan(int n, int S, int d, int H, TcPlan& p) {
+bool make_tc_plan(int n, int S, int d, int H, bool tc2, TcPlan& p) {
   if (n < 1 || n > kMaxN || S < 2 || S > kMaxS || H < 1 || d % H != 0) return false;
   if (H > 1 && (d / H) % kKC != 0) return false;
   for (int Hs = H; Hs >= 1; --Hs)
-    if (H % Hs == 0 && make_tc_window(n, S, H, Hs, p)) return true;
+    if (H % Hs == 0 && make_tc_window(n, S, H, Hs, tc2, p)) return true;
   return false;
 }
 
@@ -156,13 +196,16 @@ struct RingPos {
 template <int kN, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
-                 const __grid_constant__ CUtensorMap tm_q, const Phase1Args a, const TcPlan pl) {
+                 const __grid_constant__ CUtensorMap tm_q,
+                 const __grid_constant__ CUtensorMap tm_o, const Phase1Args a, const TcPlan pl) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr bool kSmall = kN > 0;
+  // sweep 2 on the tensor cores: the one-head layout with a compile-time source count
+  constexpr bool kTc2 = kSmall && !kSplit;
   const int n = kSmall ? kN : a.n;
-  const int S = a.S, d = a.d, SB = pl.SB;
+  const int S = a.S, d = a.d, SB = pl.SB, SB2 = pl.SB2;
   const int H = a.heads, Hs = pl.Hs, R = pl.R;
   const int64_t T = a.T;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTT;
@@ -174,7 +217,8 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   const int cph = (W > 1 ? wcols : dh) / kKC + ((W > 1 ? wcols : dh) % kKC != 0);  // stages per head
   const bool writer = W == 1 || blockIdx.y == 0;  // writes the statistics of the tile
   const int nch = (wcols + kKC - 1) / kKC;
-  const int total = 2 * nch;  // source-ring iterations: sweep 1, then sweep 2
+  const int nch2 = kTc2 ? (wcols + 2 * kKC - 1) / (2 * kKC) : nch;  // sweep-2 stages
+  const int total = nch + nch2;  // source-ring iterations: sweep 1, then sweep 2
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + pl.offBar);
   uint64_t* empty = full + SB;
@@ -182,6 +226,13 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   volatile int* abort_flag = reinterpret_cast<volatile int*>(dready + 1);
   uint64_t* xready = dready + 2;  // split: the peers' partial sums are ready to be read
   uint64_t* xdone = dready + 3;   // split: the peers have read this CTA's partial sums
+  uint64_t* dfull = dready + 4;   // tc2: accumulator b holds a finished stage
+  uint64_t* dempty = dready + 6;  // tc2: every compute warp has read accumulator b
+  uint64_t* aready = dready + 8;  // tc2: the weights are in place as the B operand
+  uint64_t* mdone = dready + 9;   // tc2: every MMA has completed
+  uint64_t* full2 = dready + 10;  // tc2: the sweep-2 ring's barriers
+  uint64_t* empty2 = full2 + SB2;
+  unsigned char* abuf = smem + pl.offAB;  // tc2: weights, hi halves then lo halves
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + pl.offTmem);
   float* zbuf = reinterpret_cast<float*>(smem + pl.offZ);     // [n * 8 rows][Hs][SZ]
   const int SZ = (S + 1) & ~1;
@@ -199,8 +250,34 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
       mbar_init(xready, W - 1);
       mbar_init(xdone, W - 1);
     }
+    if (kTc2) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&dfull[b], 1);
+        mbar_init(&dempty[b], kWarps);
+      }
+      mbar_init(aready, kWarps);
+      mbar_init(mdone, 1);
+      for (int s = 0; s < SB2; ++s) {
+        mbar_init(&full2[s], 1);
+        mbar_init(&empty2[s], 1);  // the stage's MMAs
+      }
+    }
     *abort_flag = 0;
     mbar_fence_init();
+  }
+  if (kTc2) {
+    // Zeros in the rows that pad each sweep-2 box to a multiple of 16 (the weights there are
+    // zero too, but a stale non-finite value times zero would not be).  Sweep 1's copies may
+    // overwrite some of them with source rows, which are finite as well.  Made visible to the
+    // async proxy before the barrier below.
+    const int pad16 = (pl.region - pl.bBytes) / 16;  // 16-byte words of padding per box
+    if (pad16 > 0)
+      for (int i = tid; i < SB2 * 2 * pad16; i += kThreads) {
+        const int box = i / pad16, k = i - box * pad16;
+        *reinterpret_cast<uint4*>(smem + (box >> 1) * pl.slot2 + (box & 1) * pl.region +
+                                  pl.bBytes + k * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    fence_async_smem();
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, pl.tcols);
@@ -217,8 +294,9 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
     if (lane == 0) {
       tma_prefetch_map(&tm_b);
       tma_prefetch_map(&tm_q);
+      const int n1 = kTc2 ? nch : total;  // iterations of the first ring
       int ib = 0;  // ring iterations issued
-      for (RingPos rp(0, SB); ib < total; ++ib, rp.advance(1, SB)) {
+      for (RingPos rp(0, SB); ib < n1; ++ib, rp.advance(1, SB)) {
         const int bs = rp.bs;
         if (ib >= SB && !mbar_wait(&empty[bs], rp.ph ^ 1)) {
           *abort_flag = 1;
@@ -227,16 +305,49 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
         if (*abort_flag) break;
         // sweep 2 walks the columns backwards: the chunks read last come back first, from L2
         const bool first = ib < nch;
-        const int c = first ? ib : total - 1 - ib;
         unsigned char* st = smem + bs * pl.slot;
-        mbar_arrive_expect_tx(&full[bs], pl.bBytes + (first ? pl.qBytes : 0));
-        tma_load_3d(st, &tm_b, cw + c * kKC, static_cast<int>(t0), 0, &full[bs]);
-        if (first) tma_load_2d(st + pl.bSpan, &tm_q, cw + c * kKC, 0, &full[bs]);
+        if (first) {
+          mbar_arrive_expect_tx(&full[bs], pl.bBytes + pl.qBytes);
+          tma_load_3d(st, &tm_b, cw + ib * kKC, static_cast<int>(t0), 0, &full[bs]);
+          tma_load_2d(st + pl.qOff, &tm_q, cw + ib * kKC, 0, &full[bs]);
+        } else {
+          const int c = total - 1 - ib;
+          mbar_arrive_expect_tx(&full[bs], pl.bBytes);
+          tma_load_3d(st, &tm_b, cw + c * kKC, static_cast<int>(t0), 0, &full[bs]);
+        }
       }
       // Drain: the last copy issued into every slot has landed before the CTA may exit.
       for (int s = 0; s < SB && s < ib; ++s) {
         const int last = ib - 1 - ((ib - 1 - s) % SB);
         mbar_wait_drain(&full[s], (last / SB) & 1);
+      }
+      if (kTc2 && !*abort_flag) {
+        // Sweep 2's ring reuses the first ring's memory: every sweep-1 stage is consumed first.
+        for (int s = 0; s < SB && s < nch; ++s) {
+          const int last = nch - 1 - ((nch - 1 - s) % SB);
+          if (!*abort_flag && !mbar_wait(&empty[s], (last / SB) & 1)) *abort_flag = 1;
+        }
+        // 128-column stages, columns in reverse (the chunks read last in sweep 1 come back
+        // first, from L2): two boxes, the second only if it starts in the row.
+        int q = 0;
+        for (RingPos r2(0, SB2); q < nch2 && !*abort_flag; ++q, r2.advance(1, SB2)) {
+          if (q >= SB2 && !mbar_wait(&empty2[r2.bs], r2.ph ^ 1)) {
+            *abort_flag = 1;
+            break;
+          }
+          unsigned char* st = smem + r2.bs * pl.slot2;
+          const int c2 = (nch2 - 1 - q) * 2 * kKC;
+          const bool second = c2 + kKC < wcols;
+          mbar_arrive_expect_tx(&full2[r2.bs], pl.bBytes * (second ? 2 : 1));
+          tma_load_3d(st, &tm_b, cw + c2, static_cast<int>(t0), 0, &full2[r2.bs]);
+          if (second)
+            tma_load_3d(st + pl.region, &tm_b, cw + c2 + kKC, static_cast<int>(t0), 0,
+                        &full2[r2.bs]);
+        }
+        for (int s = 0; s < SB2 && s < q; ++s) {
+          const int last = q - 1 - ((q - 1 - s) % SB2);
+          mbar_wait_drain(&full2[s], (last / SB2) & 1);
+        }
       }
     }
     return;
@@ -258,7 +369,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
       tc_fence_after();
       if (lane == 0) {
         const unsigned char* st = smem + bs * pl.slot;
-        const uint32_t b0 = smem_addr(st + pl.bSpan);
+        const uint32_t b0 = smem_addr(st + pl.qOff);
         for (int mt = 0; mt < (kSmall ? 1 : pl.nMT); ++mt) {  // M-tile mt: rows mt * 128 ..
           const uint32_t a0 = smem_addr(st + mt * kM * 128);
 #pragma unroll
@@ -274,6 +385,39 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
         ch = 0;
         ++hs;
       }
+    }
+    if constexpr (kTc2) {
+      // Sweep 2: o^T of a 128-column stage, D[column][query * 8 + token] =
+      // sum over (source, token') of b[source, token'][column] * w[(query, token), (source,
+      // token')], with w zero unless token' = token (alpha on the diagonal of every 8 x 8 core
+      // matrix), once with the weights' bf16 hi halves and once with their lo halves.  A is the
+      // stage's two boxes as copied (MN-major); the accumulators alternate between two blocks
+      // of tensor-memory columns.
+      const uint32_t idesc2 = idesc_bf16_f32_amn(kM, pl.Nb);
+      const uint32_t ab0 = smem_addr(abuf);
+      if (!*abort_flag && !mbar_wait(aready, 0)) *abort_flag = 1;
+      tc_fence_after();
+      RingPos r2(0, SB2);
+      for (int q = 0; q < nch2; ++q, r2.advance(1, SB2)) {
+        const int bs = r2.bs, b = q & 1, use = q >> 1;
+        if (!*abort_flag && !mbar_wait(&full2[bs], r2.ph)) *abort_flag = 1;
+        if (use > 0 && !*abort_flag && !mbar_wait(&dempty[b], (use - 1) & 1)) *abort_flag = 1;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = smem_addr(smem + bs * pl.slot2);
+          const uint32_t dcol = tmem + kTc2Col0 + b * pl.Nb;
+          for (int kk = 0; kk < pl.KC / 2; ++kk)
+#pragma unroll
+            for (int hl = 0; hl < 2; ++hl)
+              tc_mma_bf16(dcol, desc_mnmajor_sw128(a0 + 2048 * kk, pl.region),
+                          desc_kmajor_plain(ab0 + hl * pl.abBytes + 256 * kk, 128, pl.KC * 128),
+                          idesc2, (kk | hl) != 0 ? 1u : 0u);
+          tc_commit(&empty2[bs]);  // the slot may be refilled
+          tc_commit(&dfull[b]);
+        }
+        __syncwarp();
+      }
+      if (lane == 0) tc_commit(mdone);
     }
     return;
   }
@@ -455,6 +599,15 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
     named_barrier(1, kCompute);
   }
 
+  if (kTc2) {
+    // The weight operand lies in the sweep-1 ring's memory, free now (every sweep-1 copy has
+    // been consumed and every sweep-1 MMA has completed): zero it, then the softmax below
+    // writes the diagonals.
+    for (int i = tid; i < 2 * pl.abBytes / 16; i += kCompute)
+      *reinterpret_cast<uint4*>(abuf + i * 16) = make_uint4(0u, 0u, 0u, 0u);
+    named_barrier(1, kCompute);
+  }
+
   // ------------- softmax statistics, one thread per (token, head, query) -------------
   for (int i = tid; i < kTT * Hs * S; i += kCompute) {
     const int t = i / (Hs * S), hs = (i / S) % Hs, s = i % S;
@@ -473,7 +626,13 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
       float* zp = zbuf + (j * kTT + t) * ZR + hs * SZ + s;
       const float zj = *zp;
       const float al = sigmoid ? 1.f / (1.f + expf(-zj)) : expf(zj - m) * rl;
-      if (kSmall) {  // ready-made (a, a) pairs
+      if (kTc2) {  // diagonal entry (t, t) of core matrix (query s, source j), hi and lo halves
+        const __nv_bfloat16 hi = __float2bfloat16_rn(al);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(al - __bfloat162float(hi));
+        const int off = (s * pl.KC + j) * 128 + t * 18;
+        *reinterpret_cast<__nv_bfloat16*>(abuf + off) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(abuf + pl.abBytes + off) = lo;
+      } else if (kSmall) {  // ready-made (a, a) pairs
         float* ap = alph + (((t * n + j) * 4 + g) * 6 + pp) * 2;
         ap[0] = al;
         ap[1] = al;
@@ -487,9 +646,93 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
       if (a.lse != nullptr && !sigmoid) a.lse[sh * T + tok] = lse;
     }
   }
+  if (kTc2) {  // the weights, written through the generic proxy, go to the tensor core
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(aready);
+  }
   named_barrier(1, kCompute);
 
   // ------------------------------------ sweep 2 ------------------------------------
+  if constexpr (kTc2) {
+    // The MMA warp leaves o^T of 128 columns in accumulator b = stage & 1: tensor-memory lane
+    // = column, column query * 8 + token.  Warp w reads lanes 32 (w % 4) .. + 31 (its columns)
+    // of the queries s = 6 (w / 4) .. 6 (w / 4) + 5 and frees the accumulator.  bf16 o: each
+    // 16-lane x 8-token block comes in the accumulator-fragment layout (16x256b loads), is packed
+    // to bf16 and written transposed (stmatrix) into the warp's [6 queries][8 tokens][32 columns]
+    // tile, which one tensor store writes out (rows past T, columns past d and queries past S
+    // clipped).  fp32 o: 32x32b loads (lane = column) and direct stores, 128-byte row pieces.
+    const int quarter = warp & 3, grp = warp >> 2;
+    const int sg = grp * kGrpQ;                         // the group's first query
+    const int nq = min(kGrpQ, S - sg);                  // its queries (<= 0: none)
+    const bool of32 = (a.flags & kOF32) != 0;
+    char* o = static_cast<char*>(a.o);
+    unsigned char* stg = smem + pl.offZ + warp * kStgWarp;
+    // stmatrix row address of thread `lane` for query 0: row lane % 8, columns 8 (lane / 8)
+    const uint32_t stg_row = smem_addr(stg) + ((lane & 7) * 32 + (lane >> 3) * 8) * 2;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kTc2Col0;
+    for (int q = 0; q < nch2; ++q) {
+      const int b = q & 1;
+      wait(&dfull[b], (q >> 1) & 1);
+      tc_fence_after();
+      const int c2 = (nch2 - 1 - q) * 2 * kKC;  // the stage's first column in the window
+      uint32_t v[kGrpQ][8];
+      if (!of32) {
+#pragma unroll
+        for (int k = 0; k < kGrpQ; ++k)
+          if (k < nq) {
+            uint32_t(&lo)[4] = *reinterpret_cast<uint32_t(*)[4]>(&v[k][0]);
+            uint32_t(&hi)[4] = *reinterpret_cast<uint32_t(*)[4]>(&v[k][4]);
+            const uint32_t col = b * pl.Nb + (sg + k) * kTT;
+            tmem_ld_16x256b(tq + col, lo);
+            tmem_ld_16x256b(tq + (16u << 16) + col, hi);
+          }
+      } else {
+#pragma unroll
+        for (int k = 0; k < kGrpQ; ++k)
+          if (k < nq) tmem_ld8(tq + b * pl.Nb + (sg + k) * kTT, v[k]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&dempty[b]);
+      if (nq <= 0) continue;
+      if (!of32) {
+        if (lane == 0) bulk_wait_read<0>();  // the previous stage's store has read the tile
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < kGrpQ; ++k)
+          if (k < nq)
+            stmatrix_x4_trans(stg_row + k * kTT * 32 * 2,
+                              pack_bf16x2(__uint_as_float(v[k][0]), __uint_as_float(v[k][1])),
+                              pack_bf16x2(__uint_as_float(v[k][2]), __uint_as_float(v[k][3])),
+                              pack_bf16x2(__uint_as_float(v[k][4]), __uint_as_float(v[k][5])),
+                              pack_bf16x2(__uint_as_float(v[k][6]), __uint_as_float(v[k][7])));
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tm_o, stg, cw + c2 + quarter * 32, static_cast<int>(t0), sg);
+          bulk_commit();
+        }
+      } else {
+        const int tc = quarter * 32 + lane;  // this thread's column in the stage
+        if (c2 + tc < wcols) {
+#pragma unroll
+          for (int k = 0; k < kGrpQ; ++k)
+            if (k < nq)
+#pragma unroll
+              for (int t = 0; t < kTT; ++t) {
+                const int64_t tok = t0 + t;
+                if (tok < T)
+                  __stcs(reinterpret_cast<float*>(
+                             o + ((static_cast<int64_t>(sg + k) * T + tok) * d + cw + c2 + tc) * 4),
+                         __uint_as_float(v[k][t]));
+              }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all();  // o written before the CTA exits
+  } else {
   // Half h takes the ring's stages of parity h.  Within a half, warp hw is token hw; lane:
   // group of 6 queries (lane / 8) and 16-byte chunk (lane % 8).  The weights come from shared
   // memory as ready-made (a, a) pairs, 3 x 16 bytes per source.
@@ -581,6 +824,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
     }
     release(bs, true);
   }
+  }
 
   // ------------------------------------ teardown ------------------------------------
   tc_fence_before();
@@ -589,6 +833,8 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   if (warp == 0) {
     // the MMAs of an aborted run may still be running
     if (lane == 0 && *abort_flag) mbar_wait_drain(dready, 0);
+    // every MMA (and its completion signals) done before the columns are freed
+    if (kTc2 && lane == 0) mbar_wait_drain(mdone, 0);
     __syncwarp();
     tmem_dealloc(tmem, pl.tcols);
   }
@@ -596,8 +842,8 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
 
 }  // namespace
 
-using Phase1TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const Phase1Args,
-                                const TcPlan);
+using Phase1TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                                const Phase1Args, const TcPlan);
 
 // The kernel instantiation for kn sources (1 .. 9: compile-time count; 0: any).
 template <bool kSplit>
@@ -618,18 +864,25 @@ Phase1TcKernel phase1_tc_instance(int kn) {
 
 bool phase1_tc_supported(int n, int S, int d, int heads) {
   TcPlan p;
-  return make_tc_plan(n, S, d, heads, p);
+  return make_tc_plan(n, S, d, heads, heads == 1 && n <= kSmallN, p);
 }
 
 cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s) {
   TcPlan pl;
-  if (a.u_split == nullptr || !make_tc_plan(a.n, a.S, a.d, a.heads, pl))
+  // one head and at most 9 sources: compile-time source count and sweep 2 on the tensor cores
+  const bool small = a.heads == 1 && a.n <= kSmallN;
+  if (a.u_split == nullptr || !make_tc_plan(a.n, a.S, a.d, a.heads, small, pl))
     return cudaErrorInvalidValue;
-  CUtensorMap mb, mq;
+  CUtensorMap mb, mq, mo;
   cudaError_t e = encode_source_map(&mb, a.reps, a.src_stride, a.n, a.T, a.d, 2, kKC, kTT);
   if (e == cudaSuccess) e = encode_split_query_map(&mq, a.u_split, a.S, a.d, pl.Npad);
+  // bf16 o of the tensor-core sweep 2 leaves through tensor stores; otherwise unused
+  if (e == cudaSuccess)
+    e = small && (a.flags & kOF32) == 0
+            ? encode_output_map(&mo, a.o, a.S, a.T, a.d, 32, kTT, kGrpQ)
+            : (mo = mb, cudaSuccess);
   if (e != cudaSuccess) return e;
-  const int kn = a.heads == 1 && a.n <= kSmallN ? a.n : 0;  // compile-time source count
+  const int kn = small ? a.n : 0;  // compile-time source count
   auto kern = phase1_tc_instance<false>(kn);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
   if (e != cudaSuccess) return e;
@@ -637,17 +890,18 @@ cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s) {
   // Few token tiles (decode-sized T, one head, at most 16 sources): a cluster of W CTAs splits
   // each tile's columns, if W tiles' worth of CTAs still fit one wave and such clusters can be
   // resident; the CTAs add their partial sums through distributed shared memory.
-  if (a.heads == 1 && a.n * kTT <= kM) {
+  TcPlan psplit;  // the split kernels keep sweep 2 on the CUDA cores
+  if (a.heads == 1 && a.n * kTT <= kM && make_tc_plan(a.n, a.S, a.d, 1, false, psplit)) {
     int sms = 0, dev = 0;
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     auto ksplit = phase1_tc_instance<true>(kn);
-    e = cudaFuncSetAttribute(ksplit, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
+    e = cudaFuncSetAttribute(ksplit, cudaFuncAttributeMaxDynamicSharedMemorySize, psplit.smem);
     if (e != cudaSuccess) return e;
     for (int W = 4; W >= 2; W /= 2) {
       if (a.d % (W * kKC) != 0 || blocks * W > sms) continue;
-      TcPlan ps = pl;
+      TcPlan ps = psplit;
       ps.csplit = W;
       ps.windows = W;
       cudaLaunchConfig_t cfg = {};
@@ -667,11 +921,11 @@ cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s) {
         cudaGetLastError();  // not launchable with this cluster size: try the next
         continue;
       }
-      return cudaLaunchKernelEx(&cfg, ksplit, mb, mq, a, ps);
+      return cudaLaunchKernelEx(&cfg, ksplit, mb, mq, mo, a, ps);
     }
   }
   const dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(pl.windows));
-  return launch_pdl(kern, grid, kThreads, pl.smem, s, mb, mq, a, pl);
+  return launch_pdl(kern, grid, kThreads, pl.smem, s, mb, mq, mo, a, pl);
 }
 
 namespace {
