@@ -37,7 +37,10 @@ def _rel_check(got, want, rel, what):
 
 @pytest.mark.parametrize("n,T,d,dt", [(3, 24, 128, "f32"), (1, 5, 64, "f32"),
                                       (10, 37, 7168, "bf16"), (16, 20, 2048, "bf16"),
-                                      (9, 300, 1024, "bf16")])
+                                      (9, 300, 1024, "bf16"),
+                                      (10, 700, 7168, "bf16"),   # several rows per CTA
+                                      (1, 9, 4096, "bf16"), (13, 160, 6144, "bf16"),
+                                      (4, 45, 4096, "f32")])     # 1024 vectors of fp32
 def test_backward_matches_oracle(dev, n, T, d, dt):
     dtype = torch.float32 if dt == "f32" else torch.bfloat16
     seed = 8000 + n + d
