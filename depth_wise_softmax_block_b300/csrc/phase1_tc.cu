@@ -62,6 +62,10 @@ constexpr int kTmemMax = 512;       // tensor-memory columns of an SM
 constexpr int kMaxSlots = 12;       // ring slots
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kTc2Col0 = 128;       // first tensor-memory column of the sweep-2 accumulators
+// The tensor-core weighted sum writes o at the same cost whatever n is; with fewer sources the
+// CUDA-core sum is cheaper (16384 tokens, S = 24: 1.37 against 1.67 ms at n = 1, 1.76 against
+// 1.77 ms at n = 6, 1.86 against 1.79 ms at n = 7, 2.02 against 1.90 ms at n = 9).
+constexpr int kTc2MinN = 7;
 constexpr int kGrpQ = 6;                          // sweep 2: queries per group of 4 warps
 constexpr int kStgWarp = kGrpQ * kTT * 32 * 2;    // a warp's staged o tile [6][8][32] bf16
 
@@ -192,8 +196,9 @@ struct RingPos {
 // kN = n in 1 .. 9 with one head: the small layout (one M-tile, sweep-2 weights as ready-made
 // pairs, sums of squares in registers) with the source count known at compile time, so every
 // loop over the sources is unrolled without guards; kN = 0: any n (runtime).  kSplit: the
-// cluster column split for few token tiles (compiled out of the other instantiations).
-template <int kN, bool kSplit>
+// cluster column split for few token tiles (compiled out of the other instantiations).  kTc:
+// sweep 2 on the tensor cores (one head, kN >= kTc2MinN, no split).
+template <int kN, bool kSplit, bool kTc>
 __global__ void __launch_bounds__(kThreads, 1)
 phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
                  const __grid_constant__ CUtensorMap tm_q,
@@ -202,8 +207,8 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr bool kSmall = kN > 0;
-  // sweep 2 on the tensor cores: the one-head layout with a compile-time source count
-  constexpr bool kTc2 = kSmall && !kSplit;
+  constexpr bool kTc2 = kTc;
+  static_assert(!kTc || (kN >= kTc2MinN && !kSplit), "tensor-core sweep 2: 7 to 9 sources");
   const int n = kSmall ? kN : a.n;
   const int S = a.S, d = a.d, SB = pl.SB, SB2 = pl.SB2;
   const int H = a.heads, Hs = pl.Hs, R = pl.R;
@@ -845,45 +850,58 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
 using Phase1TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
                                 const Phase1Args, const TcPlan);
 
-// The kernel instantiation for kn sources (1 .. 9: compile-time count; 0: any).
+// The kernel instantiation for kn sources (1 .. 9: compile-time count; 0: any), sweep 2 on the
+// CUDA cores.
 template <bool kSplit>
 Phase1TcKernel phase1_tc_instance(int kn) {
   switch (kn) {
-    case 1: return phase1_tc_kernel<1, kSplit>;
-    case 2: return phase1_tc_kernel<2, kSplit>;
-    case 3: return phase1_tc_kernel<3, kSplit>;
-    case 4: return phase1_tc_kernel<4, kSplit>;
-    case 5: return phase1_tc_kernel<5, kSplit>;
-    case 6: return phase1_tc_kernel<6, kSplit>;
-    case 7: return phase1_tc_kernel<7, kSplit>;
-    case 8: return phase1_tc_kernel<8, kSplit>;
-    case 9: return phase1_tc_kernel<9, kSplit>;
-    default: return phase1_tc_kernel<0, kSplit>;
+    case 1: return phase1_tc_kernel<1, kSplit, false>;
+    case 2: return phase1_tc_kernel<2, kSplit, false>;
+    case 3: return phase1_tc_kernel<3, kSplit, false>;
+    case 4: return phase1_tc_kernel<4, kSplit, false>;
+    case 5: return phase1_tc_kernel<5, kSplit, false>;
+    case 6: return phase1_tc_kernel<6, kSplit, false>;
+    case 7: return phase1_tc_kernel<7, kSplit, false>;
+    case 8: return phase1_tc_kernel<8, kSplit, false>;
+    case 9: return phase1_tc_kernel<9, kSplit, false>;
+    default: return phase1_tc_kernel<0, kSplit, false>;
   }
 }
 
+// Sweep 2 on the tensor cores, kn in kTc2MinN .. 9.
+Phase1TcKernel phase1_tc2_instance(int kn) {
+  switch (kn) {
+    case 7: return phase1_tc_kernel<7, false, true>;
+    case 8: return phase1_tc_kernel<8, false, true>;
+    default: return phase1_tc_kernel<9, false, true>;
+  }
+}
+
+// One head and kTc2MinN .. 9 sources: the weighted sum on the tensor cores.
+bool use_tc2(int n, int heads) { return heads == 1 && n >= kTc2MinN && n <= kSmallN; }
+
 bool phase1_tc_supported(int n, int S, int d, int heads) {
   TcPlan p;
-  return make_tc_plan(n, S, d, heads, heads == 1 && n <= kSmallN, p);
+  return make_tc_plan(n, S, d, heads, use_tc2(n, heads), p);
 }
 
 cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s) {
   TcPlan pl;
-  // one head and at most 9 sources: compile-time source count and sweep 2 on the tensor cores
-  const bool small = a.heads == 1 && a.n <= kSmallN;
-  if (a.u_split == nullptr || !make_tc_plan(a.n, a.S, a.d, a.heads, small, pl))
+  const bool small = a.heads == 1 && a.n <= kSmallN;  // compile-time source count
+  const bool tc2 = use_tc2(a.n, a.heads);
+  if (a.u_split == nullptr || !make_tc_plan(a.n, a.S, a.d, a.heads, tc2, pl))
     return cudaErrorInvalidValue;
   CUtensorMap mb, mq, mo;
   cudaError_t e = encode_source_map(&mb, a.reps, a.src_stride, a.n, a.T, a.d, 2, kKC, kTT);
   if (e == cudaSuccess) e = encode_split_query_map(&mq, a.u_split, a.S, a.d, pl.Npad);
   // bf16 o of the tensor-core sweep 2 leaves through tensor stores; otherwise unused
   if (e == cudaSuccess)
-    e = small && (a.flags & kOF32) == 0
+    e = tc2 && (a.flags & kOF32) == 0
             ? encode_output_map(&mo, a.o, a.S, a.T, a.d, 32, kTT, kGrpQ)
             : (mo = mb, cudaSuccess);
   if (e != cudaSuccess) return e;
   const int kn = small ? a.n : 0;  // compile-time source count
-  auto kern = phase1_tc_instance<false>(kn);
+  auto kern = tc2 ? phase1_tc2_instance(kn) : phase1_tc_instance<false>(kn);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
   if (e != cudaSuccess) return e;
   const int64_t blocks = (a.T + kTT - 1) / kTT;
