@@ -8,19 +8,26 @@
 // kernel computes it with tcgen05 MMAs (bf16 x bf16 -> fp32 in tensor memory).  U is fp32; the
 // caller passes it also as split bf16 rows (attnres_query_prep): row 2s = hi(u_s), row 2s + 1 =
 // lo(u_s), with |u - hi - lo| <= 2^-16 |u|, so the logits keep fp32-level accuracy (the sources
-// are bf16 already).  Everything else runs on the CUDA cores:
+// are bf16 already).
 //   sweep 1  a copy-issuing warp streams 64-column stages of the tile (n sources x 8 tokens,
-//            128-byte swizzled rows) and of the split queries through a ring of up to 12 slots;
-//            an MMA-issuing warp issues the stage's four K=16 MMAs, D[row, 2s + {hi,lo}] +=
-//            b_row . u_s, with the tile's n*8 rows as M (= 128, unused rows ignored), while the
-//            16 compute warps accumulate each source row's sum of squares;
+//            128-byte swizzled rows) and of the split queries through a ring of up to 12 slots
+//            (an even number); an MMA-issuing warp issues the stage's four K=16 MMAs,
+//            D[row, 2s + {hi,lo}] += b_row . u_s, with the tile's n*8 rows as M (= 128, unused
+//            rows ignored), while the 16 compute warps, in two halves that take alternate
+//            stages, accumulate each source row's sum of squares;
 //   softmax  warps 0-3 read D from tensor memory (one row per thread), form
 //            z = (hi + lo) / r_j, and one thread per (token, query) computes m, lse, alpha;
-//   sweep 2  the tile streams through the ring again, columns in reverse order so that the
-//            chunks read last in sweep 1 are still in L2, and the compute warps write
-//            o[s,t,:] = sum_j alpha_j b_j[t,:] (packed fp32 FMAs, 16-byte streaming stores).
-// The compute warps work in two halves of 8 that take alternate stages of the ring, so one
-// half's loads and stores overlap the other half's arithmetic.
+//   sweep 2  the tile streams again, columns in reverse order so that the chunks read last in
+//            sweep 1 are still in L2, and o[s,t,:] = sum_j alpha_j b_j[t,:] is formed
+//            - with one head and 7 to 9 sources, on the tensor cores: per 128-column stage
+//              D[column][s*8 + t] = sum over (j, t') of b[j,t'][column] W[(j,t'), (s,t)], W
+//              zero off the token diagonal and alpha on it (bf16 hi and lo halves, two MMAs per
+//              K step), through a ring of its own; the compute warps read D in the fragment
+//              layout, write it transposed to shared memory (stmatrix) and store it with
+//              tensor stores;
+//            - otherwise on the CUDA cores: the two halves of the compute warps take alternate
+//              stages of the ring (one half's loads and stores overlap the other half's
+//              arithmetic), packed fp32 FMAs and 16-byte streaming stores.
 // Depth-attention heads (the multi-head variant of Table 4, "Attention Residuals" note,
 // result 4): head k owns the contiguous columns k*dh .. k*dh + dh - 1 (dh = d / H, a multiple of
 // 64 so that every stage lies in one head).  A CTA covers a window of Hs whole heads (grid.y
@@ -33,8 +40,9 @@
 // of squares through distributed shared memory (xready / xdone mbarriers), then each runs the
 // softmax and sweep 2 on its own columns (rank 0 alone writes the statistics).
 // Stage hand-off uses mbarriers ("full": copy landed; "empty": all compute warps and the
-// stage's MMAs done); every wait is bounded (tma.cuh).  The tensor-memory allocation is
-// released on every path before the CTA exits.
+// stage's MMAs done; on the tensor-core sweep 2 also "dfull" / "dempty" for its two tensor-memory
+// accumulators); every wait is bounded (tma.cuh).  The tensor-memory allocation is released on
+// every path before the CTA exits.
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
