@@ -385,6 +385,56 @@ def test_phase1_tensor_cores_cluster_split(dev, n, T, flags):
     check_close(alpha, to64(alpha2), TOL["bf16"]["weight"], "alpha: tensor cores vs CUDA cores")
 
 
+TC2_CASES = [
+    # n, S, T, d, weights, o stored in; T >= 600 keeps the cluster split (which keeps the
+    # CUDA-core weighted sum) out
+    (7, 2, 601, 1024, "softmax", "bf16"),    # the fewest sources of the path, the fewest queries
+    (8, 13, 603, 2112, "softmax", "bf16"),   # odd S; the last 128-column stage has one box
+    (9, 23, 605, 704, "sigmoid", "bf16"),    # odd S, sigmoid weights, half a last stage
+    (7, 24, 604, 960, "softmax", "f32"),     # o stored in fp32 (direct stores), half a stage
+    (9, 24, 600, 7168, "softmax", "f32"),    # the block shape, o in fp32 (sampled rows)
+]
+
+
+@pytest.mark.parametrize("n,S,T,d,wk,ost", TC2_CASES)
+def test_phase1_tensor_core_weighted_sum(dev, n, S, T, d, wk, ost):
+    """The weighted sum of phase 1 on the tensor cores (one head, 7 to 9 sources, no cluster
+    split): o, m, alpha and lse against the oracle, on every row (sampled rows at d = 7168), and
+    every element of o against the CUDA-core kernel at the same gate."""
+    flags = ar.SIGMOID_WEIGHTS if wk == "sigmoid" else 0
+    odt = torch.float32 if ost == "f32" else torch.bfloat16
+    seed = 7000 + n * 31 + S
+    reps = make_reps(n, T, d, torch.bfloat16, dev, seed)
+    W, G, U = make_queries(S, d, dev, seed)
+    outs = {}
+    for path in ("tensor_cores", "cuda_cores"):
+        o = torch.empty((S, T, d), dtype=odt, device=dev)
+        m = torch.empty((S, T), device=dev)
+        lse = torch.full((S, T), 5.0, device=dev)
+        alpha = torch.empty((S, T, n), device=dev)
+        ar.attnres_phase1(reps, U, o, m, lse, alpha, eps=EPS,
+                          u_split=split_of(U) if path == "tensor_cores" else None, flags=flags)
+        outs[path] = (o, m, lse, alpha)
+    torch.cuda.synchronize()
+    ar.attnres_poll_device_errors()
+    if d > 4096:
+        rows = np.sort(np.random.default_rng(T).choice(T, 16, replace=False))
+        rows[0], rows[-1] = 0, T - 1
+    else:
+        rows = np.arange(T)
+    oo, om, olse, oa = O.phase1_variant(to64(reps[:, rows]), to64(W), to64(G), EPS, wk, True)
+    o, m, lse, alpha = outs["tensor_cores"]
+    check_outputs(o[:, rows], oo, "bf16", f"o (n={n}, S={S}, d={d}, {wk}, o {ost})")
+    check_close(m[:, rows], om, TOL["bf16"]["stat"], "m")
+    check_close(alpha[:, rows], oa, TOL["bf16"]["weight"], "alpha")
+    if flags:
+        assert torch.all(lse == 5.0), "lse is not written with sigmoid weights"
+    else:
+        check_close(lse[:, rows], olse, TOL["bf16"]["stat"], "lse")
+    o2 = outs["cuda_cores"][0]
+    check_outputs(o, to64(o2), "bf16", "o: tensor cores vs CUDA cores")
+
+
 @pytest.mark.parametrize("polls", [0, 1000])
 def test_wait_timeout_is_reported_and_context_survives(dev, polls):
     """The timeout path, made to run out on purpose without a real hang: a kernel whose bounded
