@@ -162,9 +162,9 @@ cudaError_t encode_query_map(CUtensorMap* map, const float* u, int S, int d);
 cudaError_t encode_split_query_map(CUtensorMap* map, const void* u_split, int S, int d,
                                    int rows_box);
 // bf16 [S][T][d] output (phase 1's o) for tensor stores of [box_s queries][box_t rows][box_k
-// columns] tiles, unswizzled.
+// columns] tiles, unswizzled or with the 128-byte swizzle (box_k = 64).
 cudaError_t encode_output_map(CUtensorMap* map, void* o, int S, int64_t T, int d, int box_k,
-                              int box_t, int box_s);
+                              int box_t, int box_s, bool swizzle128);
 
 // Tensor-core phase 1 (phase1_tc.cu): bf16 I/O, 2 <= S <= 24, n <= 64, split queries given;
 // with H > 1 heads, d / H a multiple of 64.

@@ -19,12 +19,12 @@
 //            z = (hi + lo) / r_j, and one thread per (token, query) computes m, lse, alpha;
 //   sweep 2  the tile streams again, columns in reverse order so that the chunks read last in
 //            sweep 1 are still in L2, and o[s,t,:] = sum_j alpha_j b_j[t,:] is formed
-//            - with one head and 7 to 9 sources, on the tensor cores: per 128-column stage
+//            - with one head and 3 to 9 sources, on the tensor cores: per 128-column stage
 //              D[column][s*8 + t] = sum over (j, t') of b[j,t'][column] W[(j,t'), (s,t)], W
 //              zero off the token diagonal and alpha on it (bf16 hi and lo halves, two MMAs per
 //              K step), through a ring of its own; the compute warps read D in the fragment
-//              layout, write it transposed to shared memory (stmatrix) and store it with
-//              tensor stores;
+//              layout, write it transposed to shared memory (stmatrix, 128-byte swizzle) and
+//              store it with tensor stores of [6 queries][8 tokens][64 columns] tiles;
 //            - otherwise on the CUDA cores: the two halves of the compute warps take alternate
 //              stages of the ring (one half's loads and stores overlap the other half's
 //              arithmetic), packed fp32 FMAs and 16-byte streaming stores.
@@ -70,12 +70,15 @@ constexpr int kTmemMax = 512;       // tensor-memory columns of an SM
 constexpr int kMaxSlots = 12;       // ring slots
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kTc2Col0 = 128;       // first tensor-memory column of the sweep-2 accumulators
-// The tensor-core weighted sum writes o at the same cost whatever n is; with fewer sources the
-// CUDA-core sum is cheaper (16384 tokens, S = 24: 1.37 against 1.67 ms at n = 1, 1.76 against
-// 1.77 ms at n = 6, 1.86 against 1.79 ms at n = 7, 2.02 against 1.90 ms at n = 9).
-constexpr int kTc2MinN = 7;
+// The tensor-core weighted sum writes o at about the same cost whatever n is; with one or two
+// sources the CUDA-core sum is cheaper (16384 tokens, S = 24, CUDA cores against tensor cores:
+// 1.37 / 1.46 ms at n = 1, 1.43 / 1.46 at n = 2, 1.46 / 1.44 at n = 3, 1.74 / 1.54 at n = 6,
+// 2.02 / 1.60 at n = 9).
+constexpr int kTc2MinN = 3;
 constexpr int kGrpQ = 6;                          // sweep 2: queries per group of 4 warps
-constexpr int kStgWarp = kGrpQ * kTT * 32 * 2;    // a warp's staged o tile [6][8][32] bf16
+// A group's staged o tile: two halves [6 queries][8 tokens][64 columns] bf16 with the 128-byte
+// swizzle, each 1024-byte aligned (6 KB)
+constexpr int kStgHalf = kGrpQ * kTT * 64 * 2;
 
 struct TcPlan {
   int Hs, windows;    // heads per CTA window, windows (= H / Hs, or csplit)
@@ -138,7 +141,7 @@ bool make_tc_window(int n, int S, int H, int Hs, bool tc2, TcPlan& p) {
   const int sb = 2 * Hs * p.R * 4;                  // per-half, per-head row sums of squares
   // tc2: sweep 2 stages its output tiles where the logits and sums of squares were (dead by then)
   const int zone = std::max(align_up(zb, 16) + align_up(ab, 16) + sb,
-                            tc2 ? kWarps * kStgWarp : 0);
+                            tc2 ? 4 * 2 * kStgHalf : 0);
   const int avail = kMaxSmem - 1024 - zone - (4 * kMaxSlots + 10) * 8 - 16;
   // The two halves of the compute warps take alternate stages of the sweep-1 ring, each
   // waiting on the "full" barriers of its own stages only.  With an odd number of slots
@@ -216,7 +219,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr bool kSmall = kN > 0;
   constexpr bool kTc2 = kTc;
-  static_assert(!kTc || (kN >= kTc2MinN && !kSplit), "tensor-core sweep 2: 7 to 9 sources");
+  static_assert(!kTc || (kN >= kTc2MinN && !kSplit), "tensor-core sweep 2: 3 to 9 sources");
   const int n = kSmall ? kN : a.n;
   const int S = a.S, d = a.d, SB = pl.SB, SB2 = pl.SB2;
   const int H = a.heads, Hs = pl.Hs, R = pl.R;
@@ -672,17 +675,23 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
     // = column, column query * 8 + token.  Warp w reads lanes 32 (w % 4) .. + 31 (its columns)
     // of the queries s = 6 (w / 4) .. 6 (w / 4) + 5 and frees the accumulator.  bf16 o: each
     // 16-lane x 8-token block comes in the accumulator-fragment layout (16x256b loads), is packed
-    // to bf16 and written transposed (stmatrix) into the warp's [6 queries][8 tokens][32 columns]
-    // tile, which one tensor store writes out (rows past T, columns past d and queries past S
-    // clipped).  fp32 o: 32x32b loads (lane = column) and direct stores, 128-byte row pieces.
+    // to bf16 and written transposed (stmatrix) into the group's [6 queries][8 tokens][128
+    // columns] tile, as two 64-column halves with the 128-byte swizzle (16-byte chunk c of row r
+    // at c ^ (r % 8): conflict-free); after a group barrier one thread writes the halves out with
+    // two tensor stores (rows past T, columns past d and queries past S clipped).  fp32 o: 32x32b
+    // loads (lane = column) and direct stores, 128-byte row pieces.
     const int quarter = warp & 3, grp = warp >> 2;
     const int sg = grp * kGrpQ;                         // the group's first query
     const int nq = min(kGrpQ, S - sg);                  // its queries (<= 0: none)
     const bool of32 = (a.flags & kOF32) != 0;
     char* o = static_cast<char*>(a.o);
-    unsigned char* stg = smem + pl.offZ + warp * kStgWarp;
-    // stmatrix row address of thread `lane` for query 0: row lane % 8, columns 8 (lane / 8)
-    const uint32_t stg_row = smem_addr(stg) + ((lane & 7) * 32 + (lane >> 3) * 8) * 2;
+    unsigned char* gstg = smem + pl.offZ + grp * 2 * kStgHalf;
+    const bool issuer = quarter == 0 && lane == 0;
+    // stmatrix row address of thread `lane` for query 0: row t = lane % 8 of the half holding
+    // this warp's columns, 16-byte chunk (quarter % 2) * 4 + lane / 8, swizzled by t
+    const int t8 = lane & 7;
+    const uint32_t stg_row = smem_addr(gstg) + (quarter >> 1) * kStgHalf + t8 * 128 +
+                             ((((quarter & 1) * 4 + (lane >> 3)) ^ t8) << 4);
     const uint32_t tq = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kTc2Col0;
     for (int q = 0; q < nch2; ++q) {
       const int b = q & 1;
@@ -711,20 +720,22 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
       if (lane == 0) mbar_arrive(&dempty[b]);
       if (nq <= 0) continue;
       if (!of32) {
-        if (lane == 0) bulk_wait_read<0>();  // the previous stage's store has read the tile
-        __syncwarp();
+        if (issuer) bulk_wait_read<0>();  // the previous stage's stores have read the tile
+        named_barrier(2 + grp, 128);
 #pragma unroll
         for (int k = 0; k < kGrpQ; ++k)
           if (k < nq)
-            stmatrix_x4_trans(stg_row + k * kTT * 32 * 2,
+            stmatrix_x4_trans(stg_row + k * kTT * 128,
                               pack_bf16x2(__uint_as_float(v[k][0]), __uint_as_float(v[k][1])),
                               pack_bf16x2(__uint_as_float(v[k][2]), __uint_as_float(v[k][3])),
                               pack_bf16x2(__uint_as_float(v[k][4]), __uint_as_float(v[k][5])),
                               pack_bf16x2(__uint_as_float(v[k][6]), __uint_as_float(v[k][7])));
         fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(&tm_o, stg, cw + c2 + quarter * 32, static_cast<int>(t0), sg);
+        named_barrier(2 + grp, 128);
+        if (issuer) {
+          tma_store_3d(&tm_o, gstg, cw + c2, static_cast<int>(t0), sg);
+          if (c2 + kKC < wcols)
+            tma_store_3d(&tm_o, gstg + kStgHalf, cw + c2 + kKC, static_cast<int>(t0), sg);
           bulk_commit();
         }
       } else {
@@ -744,7 +755,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
         }
       }
     }
-    if (lane == 0) bulk_wait_all();  // o written before the CTA exits
+    if (issuer) bulk_wait_all();  // o written before the CTA exits
   } else {
   // Half h takes the ring's stages of parity h.  Within a half, warp hw is token hw; lane:
   // group of 6 queries (lane / 8) and 16-byte chunk (lane % 8).  The weights come from shared
@@ -879,6 +890,10 @@ Phase1TcKernel phase1_tc_instance(int kn) {
 // Sweep 2 on the tensor cores, kn in kTc2MinN .. 9.
 Phase1TcKernel phase1_tc2_instance(int kn) {
   switch (kn) {
+    case 3: return phase1_tc_kernel<3, false, true>;
+    case 4: return phase1_tc_kernel<4, false, true>;
+    case 5: return phase1_tc_kernel<5, false, true>;
+    case 6: return phase1_tc_kernel<6, false, true>;
     case 7: return phase1_tc_kernel<7, false, true>;
     case 8: return phase1_tc_kernel<8, false, true>;
     default: return phase1_tc_kernel<9, false, true>;
@@ -905,7 +920,7 @@ cudaError_t launch_phase1_tc(const Phase1Args& a, cudaStream_t s) {
   // bf16 o of the tensor-core sweep 2 leaves through tensor stores; otherwise unused
   if (e == cudaSuccess)
     e = tc2 && (a.flags & kOF32) == 0
-            ? encode_output_map(&mo, a.o, a.S, a.T, a.d, 32, kTT, kGrpQ)
+            ? encode_output_map(&mo, a.o, a.S, a.T, a.d, kKC, kTT, kGrpQ, true)
             : (mo = mb, cudaSuccess);
   if (e != cudaSuccess) return e;
   const int kn = small ? a.n : 0;  // compile-time source count

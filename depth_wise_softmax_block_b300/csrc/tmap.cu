@@ -44,7 +44,7 @@ cudaError_t encode_source_map(CUtensorMap* map, const void* reps, int64_t src_st
 }
 
 cudaError_t encode_output_map(CUtensorMap* map, void* o, int S, int64_t T, int d, int box_k,
-                              int box_t, int box_s) {
+                              int box_t, int box_s, bool swizzle128) {
   const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
   const cuuint32_t unit[3] = {1, 1, 1};
@@ -55,7 +55,8 @@ cudaError_t encode_output_map(CUtensorMap* map, void* o, int S, int64_t T, int d
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_k), static_cast<cuuint32_t>(box_t),
                              static_cast<cuuint32_t>(box_s)};
   if (enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, o, dims, strides, box, unit,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+          CU_TENSOR_MAP_INTERLEAVE_NONE,
+          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   return cudaSuccess;

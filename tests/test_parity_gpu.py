@@ -388,7 +388,8 @@ def test_phase1_tensor_cores_cluster_split(dev, n, T, flags):
 TC2_CASES = [
     # n, S, T, d, weights, o stored in; T >= 600 keeps the cluster split (which keeps the
     # CUDA-core weighted sum) out
-    (7, 2, 601, 1024, "softmax", "bf16"),    # the fewest sources of the path, the fewest queries
+    (3, 5, 602, 640, "softmax", "bf16"),     # the fewest sources of the path, half a stage
+    (7, 2, 601, 1024, "softmax", "bf16"),    # the fewest queries
     (8, 13, 603, 2112, "softmax", "bf16"),   # odd S; the last 128-column stage has one box
     (9, 23, 605, 704, "sigmoid", "bf16"),    # odd S, sigmoid weights, half a last stage
     (7, 24, 604, 960, "softmax", "f32"),     # o stored in fp32 (direct stores), half a stage
@@ -398,7 +399,7 @@ TC2_CASES = [
 
 @pytest.mark.parametrize("n,S,T,d,wk,ost", TC2_CASES)
 def test_phase1_tensor_core_weighted_sum(dev, n, S, T, d, wk, ost):
-    """The weighted sum of phase 1 on the tensor cores (one head, 7 to 9 sources, no cluster
+    """The weighted sum of phase 1 on the tensor cores (one head, 3 to 9 sources, no cluster
     split): o, m, alpha and lse against the oracle, on every row (sampled rows at d = 7168), and
     every element of o against the CUDA-core kernel at the same gate."""
     flags = ar.SIGMOID_WEIGHTS if wk == "sigmoid" else 0
