@@ -152,6 +152,12 @@ __device__ __forceinline__ void pdl_enter() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
+// Only the wait: the kernel's successor is scheduled when this grid's CTAs have exited.  For a
+// kernel whose CTAs fill the SMs for many waves, an early-scheduled successor's CTAs sit on the
+// SMs beside the last waves for nothing.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 // Launch `kern` on stream `s` with programmatic stream serialisation allowed.
 template <typename... KArgs, typename... Args>

@@ -303,7 +303,7 @@ phase1_tc_kernel(const __grid_constant__ CUtensorMap tm_b,
   __syncthreads();
   tc_fence_after();
   if (W > 1) cluster_sync();  // the peers' barriers are initialised before any remote arrival
-  pdl_enter();  // the prologue above touches no global memory
+  pdl_wait();  // the prologue above touches no global memory; the successor waits for the exit
 
   // ------------------------------ copy-issuing warp ------------------------------
   if (warp == kWarps) {
