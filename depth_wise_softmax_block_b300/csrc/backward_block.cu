@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) bwd_merge_kernel(const BwdBloc
   constexpr int NW = OWords<float, VE>::N;
   __shared__ float scratch[6 * 33];
   extern __shared__ float pa[];   // P [VE][nv], then A [VE][nv]
-  pdl_enter();
+  pdl_wait();
   const int64_t t = blockIdx.x, T = a.T;
   const int d = a.d, nv = d / VE, S = a.S;
   const float fd = static_cast<float>(d);
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kDotThreads, 3) bwd_sources_kernel(const BwdBl
   __shared__ float As[kBlkMaxS * NJ];   // alpha_ij
   __shared__ float dzz[kBlkMaxS * NJ];
   __shared__ float ssj[NJ], Fs[NJ];
-  pdl_enter();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t = blockIdx.x, T = a.T;
   const int d = a.d, nv = d / VE, S = a.S, n = a.n;
@@ -404,7 +404,7 @@ constexpr int kParTok = 32;
 template <typename IOT>
 __global__ void __launch_bounds__(kParThreads) bwd_params_kernel(const BwdBlockArgs a) {
   extern __shared__ float psm[];   // P [kParTok][kParCols], then scalars [kParTok][3S]
-  pdl_enter();
+  pdl_wait();
   const int d = a.d, S = a.S, n = a.n, R = a.rec_floats;
   const int64_t T = a.T;
   const int cl = 2 * threadIdx.x;                 // local column pair
@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(kDuThreads) bwd_du_kernel(const BwdBlockArgs a
                                                             int tokens_per_cta) {
   constexpr int SP = 24;                      // padded sublayer stride of the staged tile
   extern __shared__ float ce[];               // [kDuBatch][n][SP]
-  pdl_enter();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = a.d, S = a.S, n = a.n, R = a.rec_floats;
   const int64_t T = a.T;

@@ -152,9 +152,11 @@ __device__ __forceinline__ void pdl_enter() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
-// Only the wait: the kernel's successor is scheduled when this grid's CTAs have exited.  For a
-// kernel whose CTAs fill the SMs for many waves, an early-scheduled successor's CTAs sit on the
-// SMs beside the last waves for nothing.
+// Only the wait: the kernel's successor is scheduled when this grid's CTAs have exited.  Used by
+// the kernels whose CTAs fill the SMs for many waves and whose successor gains nothing from
+// waiting beside their last waves: with the tensor-core phase 1 entering through pdl_enter(),
+// the long-context step (8 chunks of 16384 tokens, no events between the launches) took 71.0
+// instead of 58.5 ms; the block backward's kernels gain 1 %.
 __device__ __forceinline__ void pdl_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }

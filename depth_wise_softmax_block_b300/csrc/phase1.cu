@@ -176,7 +176,7 @@ phase1_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ 
     mbar_fence_init();
   }
   __syncthreads();
-  pdl_enter();  // the prologue above touches no global memory
+  pdl_wait();  // the prologue above touches no global memory; the successor waits for the exit
 
   // The ring runs 2 * nch iterations: sweep 1 (sources + queries), then sweep 2 (sources).
   // Thread 0 issues the copies: the first ST iterations up front, then, at every iteration,
