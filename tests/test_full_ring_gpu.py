@@ -23,9 +23,17 @@ SIG, NOKN = ar.SIGMOID_WEIGHTS, ar.NO_KEY_NORM
 # n, T, d, dtype, flags: T well above the 148 CTAs (several rows each, so the ring wraps);
 # d = 7168 at n = 10 is the final aggregation's shape (15 slots); 512-vector rows (bf16 d = 4096,
 # fp32 d = 2048) are the shortest the kernel takes, 1024 (bf16 d = 8192, fp32 d = 4096) the
-# longest; n = 11 at d = 8192 leaves the ring its minimum of n + 2 slots.
-CASES = [(10, 400, 7168, "bf16", 0), (16, 700, 4096, "bf16", SIG), (3, 2000, 2048, "f32", NOKN),
-         (11, 333, 8192, "bf16", SIG | NOKN), (5, 1500, 4096, "f32", 0)]
+# longest; n = 11 at d = 8192 leaves the ring its minimum of n + 2 slots.  bf16 rows of at most
+# 896 vectors over at most 10 sources take the register-held kernel (the first six cases: it
+# keeps eight sources in registers and the ninth and tenth in their slots, so n = 10, 9 and
+# n <= 8 each take a different path through it), the rest the kernel that keeps a row's slots
+# through both passes (n = 16, n = 11, 1024-vector bf16 rows at n = 4, and fp32).
+CASES = [(10, 400, 7168, "bf16", 0), (10, 1200, 7168, "bf16", SIG | NOKN),
+         (9, 640, 7168, "bf16", NOKN), (1, 300, 4096, "bf16", NOKN), (7, 1000, 6144, "bf16", SIG),
+         (2, 777, 4096, "bf16", 0),
+         (16, 700, 4096, "bf16", SIG), (3, 2000, 2048, "f32", NOKN),
+         (11, 333, 8192, "bf16", SIG | NOKN), (4, 500, 8192, "bf16", 0),
+         (5, 1500, 4096, "f32", 0)]
 
 
 @pytest.fixture(scope="module")
