@@ -412,9 +412,10 @@ def import_traffic(csv_path: str, tokens: int, heads: int = 1, scale_to: int = 1
         e = launches.setdefault(lid, {"name": rec["Kernel Name"]})
         e[rec["Metric Name"]] = float(rec["Metric Value"].replace(",", ""))
     step_kernels = ("phase1_tc_kernel", "phase1_kernel", "phase2_kernel", "phase2_heads_kernel",
-                    "add_kernel", "full_ring_kernel", "full_kernel", "full_heads_kernel")
-    ours = [e for e in launches.values()
-            if any(k + "<" in e["name"] for k in step_kernels)]
+                    "add_kernel", "full_ring_kernel", "full_hold_kernel", "full_kernel",
+                    "full_heads_kernel")
+    ours = [e for e in launches.values()  # a template's name is followed by '<', others by '('
+            if any(k + "<" in e["name"] or k + "(" in e["name"] for k in step_kernels)]
     S = I.LONGCTX_PREFILL_BF16.S
     per_chunk = ["phase1"] + ["phase2_first", "phase2"] + ["phase2_fused"] * (S - 2) + ["close",
                                                                                       "final"]
