@@ -388,14 +388,21 @@ def traffic_for(kernel: str, heads: int = 1):
     return e.get("bytes_per_launch")
 
 
-def import_traffic(csv_path: str, tokens: int, heads: int = 1, scale_to: int = 16384):
+# ncu metric units -> bytes or nanoseconds
+_NCU_UNITS = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12,
+              "ns": 1.0, "nsecond": 1.0, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6}
+
+
+def import_traffic(csv_path: str, tokens: int, heads: int = 1, scale_to: int = 16384,
+                   out_dir: str = ""):
     """Turn an ncu capture of the step at ``tokens`` tokens (one chunk; metrics
     dram__bytes_read.sum and dram__bytes_write.sum of this library's kernels, in launch order)
     into the per-kernel DRAM traffic that ``traffic_for`` reads: bytes per launch scaled to a
     ``scale_to``-token launch (traffic grows with the tokens), stamped with the hash of each
     kernel's source files.  The launches of a chunk come in the step's order: phase 1, the S
     phase-2 calls (the first, the one with the partial given, then the fused ones), the close,
-    the final aggregation."""
+    the final aggregation.  Values are converted from the unit ncu printed them in; the JSON
+    goes to ``out_dir`` (default: profiles/)."""
     import csv
     import collections
     rows = list(csv.reader(open(csv_path)))
@@ -410,7 +417,10 @@ def import_traffic(csv_path: str, tokens: int, heads: int = 1, scale_to: int = 1
         rec = dict(zip(hdr, r))
         lid = int(rec["ID"])
         e = launches.setdefault(lid, {"name": rec["Kernel Name"]})
-        e[rec["Metric Name"]] = float(rec["Metric Value"].replace(",", ""))
+        unit = rec.get("Metric Unit", "byte") or "byte"
+        if unit not in _NCU_UNITS:
+            raise ValueError(f"unknown ncu unit {unit!r} for {rec['Metric Name']}")
+        e[rec["Metric Name"]] = float(rec["Metric Value"].replace(",", "")) * _NCU_UNITS[unit]
     step_kernels = ("phase1_tc_kernel", "phase1_kernel", "phase2_kernel", "phase2_heads_kernel",
                     "add_kernel", "full_ring_kernel", "full_hold_kernel", "full_kernel",
                     "full_heads_kernel")
@@ -430,7 +440,8 @@ def import_traffic(csv_path: str, tokens: int, heads: int = 1, scale_to: int = 1
         a[3] += e.get("gpu__time_duration.sum", 0.0)
         a[4] = e["name"]
     tag = "" if heads == 1 else f"_heads{heads}"
-    out_path = os.path.join(ROOT, "profiles", f"dram_traffic_longctx{tag}_T{tokens}.json")
+    out_path = os.path.join(out_dir or os.path.join(ROOT, "profiles"),
+                            f"dram_traffic_longctx{tag}_T{tokens}.json")
     out = {}
     for kind, (cnt, rd, wr, dur, name) in acc.items():
         files = KERNEL_SOURCES[kind if kind in ("phase1", "final") else "rowwise"]
