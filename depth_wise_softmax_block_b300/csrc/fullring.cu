@@ -55,8 +55,9 @@ constexpr int kRingMinVectors = 512;
 constexpr int kRingMaxN = 16;                      // 2 sums per source: one lane each
 constexpr int kRingSlotBytes = 216 * 1024;         // shared memory for the slots
 constexpr int kRingMaxSlots = 64;
-// Rows held in registers: 14 compute warps + the copy warp = 480 threads, so a thread may keep
-// 136 registers; a row of n <= 10 sources takes 2 x 4 x n of them.
+// Rows held in registers: 14 compute warps + the copy warp = 480 threads.  Four of the 15 warps
+// share one of the SM's four register-file partitions, so a thread may keep 128 registers (a
+// 136-register build is refused at launch); the sources held take 2 x 4 of them each.
 constexpr int kHoldWarps = 14;
 constexpr int kHoldCompute = kHoldWarps * 32;
 constexpr int kHoldThreads = kHoldCompute + 32;
