@@ -70,9 +70,11 @@ attnres_status attnres_poll_device_errors(void) {
   const unsigned int n1 = attnres::phase1_poll_timeouts();
   const unsigned int n2 = attnres::phase1_tc_poll_timeouts();
   const unsigned int n3 = attnres::full_ring_poll_timeouts();
-  const unsigned int n = (n1 == 0xffffffffu || n2 == 0xffffffffu || n3 == 0xffffffffu)
-                             ? 0xffffffffu
-                             : n1 + n2 + n3;
+  const unsigned int n4 = attnres::backward_poll_timeouts();
+  const unsigned int n =
+      (n1 == 0xffffffffu || n2 == 0xffffffffu || n3 == 0xffffffffu || n4 == 0xffffffffu)
+          ? 0xffffffffu
+          : n1 + n2 + n3 + n4;
   if (n == 0xffffffffu) {
     g_last_cuda_error = "could not read the device wait-timeout counter";
     return ATTNRES_ERR_CUDA;

@@ -97,6 +97,8 @@ struct BwdArgs {
 // Row-vector limit of the backward kernel: d / (elements per 16 bytes) <= 4 * 256.
 constexpr int kBwdMaxVectors = 1024;
 cudaError_t launch_backward(IO io, const BwdArgs& a, cudaStream_t s);
+// Bounded waits of the ring backward that gave up since the last call (synchronises the device).
+unsigned int backward_poll_timeouts();
 
 // Backward of one block of Block AttnRes (backward_block.cu).
 constexpr int kBlkMaxN = 16;   // completed sources
